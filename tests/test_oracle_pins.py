@@ -1,0 +1,314 @@
+"""Pins of the CPU oracle to facts outside itself: the pages' worked examples, format
+definitions, library-routine reductions, brute force and invariants."""
+import math
+
+import numpy as np
+import pytest
+from scipy.special import expit, softmax
+
+import oracle
+import synth
+from conftest import golden_kv, golden_rows
+
+
+def bf16_bits(vals):
+    """Exact bf16 bit patterns of values that bf16 represents exactly."""
+    f = np.asarray(vals, dtype=np.float32)
+    b = f.view(np.uint32)
+    assert np.all(b & 0xFFFF == 0), "value not exactly representable in bf16"
+    return (b >> 16).astype(np.uint16)
+
+
+def rand_bf16(rng, shape, sigma=1.0):
+    return synth.double_to_bf16(rng.normal(0.0, sigma, size=shape))
+
+
+# ---- worked example: "第 6 章 超節點", 6.2.2 ----------------------------------------------------
+
+def test_worked_example_matvec_and_splits():
+    g = golden_kv("matmul_split_2x2.txt")
+    x = np.array([float(v) for v in g["x"].split()])
+    W = np.array([[float(v) for v in g["W_row0"].split()], [float(v) for v in g["W_row1"].split()]])
+    Wt = bf16_bits(W.T.copy())  # stored [out, in]
+    np.testing.assert_array_equal(oracle.matvec(Wt, x), [float(v) for v in g["xW"].split()])
+    # column split: each device computes its own output features
+    assert oracle.matvec(Wt, x, row0=0, nrows=1)[0] == float(g["col_split_0"])
+    assert oracle.matvec(Wt, x, row0=1, nrows=1)[0] == float(g["col_split_1"])
+    # row split: each device sees part of the input features, outputs are partial sums
+    p0 = oracle.matvec(Wt, np.array([x[0], 0.0]))
+    p1 = oracle.matvec(Wt, np.array([0.0, x[1]]))
+    np.testing.assert_array_equal(p0, [float(v) for v in g["row_split_0"].split()])
+    np.testing.assert_array_equal(p1, [float(v) for v in g["row_split_1"].split()])
+    np.testing.assert_array_equal(p0 + p1, [float(v) for v in g["xW"].split()])
+
+
+def test_fp8_block_scales_index_by_row_and_column_block():
+    # 256 x 256 E4M3 matrix of code 0x38 (1.0) with a different scale in each 128x128 block:
+    # with a one-hot x, W x picks out column c, whose entries are 1.0 * s[r//128][c//128].
+    q = np.full((256, 256), 0x38, dtype=np.uint8)
+    s = np.array([[2.0, 3.0], [5.0, 7.0]], dtype=np.float32)
+    for c, expect in ((0, [2.0, 5.0]), (200, [3.0, 7.0])):
+        x = np.zeros(256)
+        x[c] = 1.0
+        y = oracle.matvec(q, x, wdtype="fp8", s=s)
+        np.testing.assert_array_equal(y[:128], expect[0])
+        np.testing.assert_array_equal(y[128:], expect[1])
+
+
+# ---- number formats -----------------------------------------------------------------------
+
+def test_e4m3_decode_golden_codes():
+    for row in golden_rows("e4m3_codes.txt"):
+        code, val = row.split()
+        v = oracle.e4m3_value(int(code, 16))
+        if val == "nan":
+            assert math.isnan(v)
+        else:
+            assert v == float(val) and math.copysign(1.0, v) == math.copysign(1.0, float(val))
+
+
+def test_e4m3_decode_roundtrips_through_the_independent_encoder():
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    vals = np.array([oracle.e4m3_value(int(c)) for c in codes], dtype=np.float32)
+    back = synth.f32_to_e4m3(vals)
+    # +0 and -0 both decode to zero; everything else must map back to its own code
+    np.testing.assert_array_equal(back, codes)
+    assert np.all(np.diff(vals[(codes < 0x80)]) > 0)  # positive codes are strictly increasing
+
+
+def test_bf16_decode():
+    assert oracle.bf16_value(0x3F80) == 1.0
+    assert oracle.bf16_value(0xC000) == -2.0
+    assert oracle.bf16_value(0x3B80) == 2.0 ** -8
+    assert oracle.bf16_value(0x0001) == 2.0 ** -133  # smallest subnormal
+    assert oracle.bf16_value(0x7F7F) == (2 - 2 ** -7) * 2.0 ** 127
+
+
+# ---- a1: router ---------------------------------------------------------------------------
+
+def _parse(v):
+    v = v.strip()
+    if v == "1+2^-23":
+        return 1.0 + 2.0 ** -23
+    if v.startswith("2^"):
+        return 2.0 ** float(v[2:])
+    return float(v)
+
+
+def test_router_logit_fixed_order_cases():
+    for row in golden_rows("router_logit_order.txt"):
+        name, d, prods, expect = (c.strip() for c in row.split("|"))
+        d = int(d)
+        x, w = np.zeros(d, np.float32), np.zeros(d, np.float32)
+        for p in prods.split():
+            i, xv, wv = p.split(":")
+            x[int(i)], w[int(i)] = _parse(xv), _parse(wv)
+        l = oracle.router_logits(bf16_bits(x)[None, :], bf16_bits(w)[None, :])
+        assert l[0, 0] == np.float32(_parse(expect)), name
+
+
+def test_router_logit_bias_is_added_after_the_dot_product():
+    x = bf16_bits(np.array([1.0] + [0.0] * 255))[None, :]
+    w = bf16_bits(np.array([[0.5] + [0.0] * 255, [0.25] + [0.0] * 255]))
+    l = oracle.router_logits(x, w, np.array([1.0, -3.0], np.float32))
+    np.testing.assert_array_equal(l, [[1.5, -2.75]])
+
+
+def test_router_logits_within_fp32_error_bound_of_exact_sum():
+    rng = np.random.default_rng(1)
+    T, d, E = 3, 7168, 5
+    x, wg = rand_bf16(rng, (T, d)), rand_bf16(rng, (E, d), 0.02)
+    l = oracle.router_logits(x, wg)
+    xf, wf = oracle.bf16_to_f64(x), oracle.bf16_to_f64(wg)
+    n = d // 32 + 5
+    gamma = n * 2.0 ** -24 / (1 - n * 2.0 ** -24)
+    for t in range(T):
+        for e in range(E):
+            prods = xf[t] * wf[e]                 # exact in fp64
+            exact = math.fsum(prods)
+            assert abs(float(l[t, e]) - exact) <= gamma * np.abs(prods).sum()
+
+
+def _routing_case(seed=2, T=40, E=24, d=256):
+    rng = np.random.default_rng(seed)
+    return oracle.router_logits(rand_bf16(rng, (T, d)), rand_bf16(rng, (E, d), 0.02))
+
+
+@pytest.mark.parametrize("k", [1, 3, 8, 24])
+def test_topk_matches_full_sort(k):
+    l = _routing_case()
+    idx, w, w64 = oracle.route(l, k)
+    T, E = l.shape
+    for t in range(T):
+        order = np.lexsort((np.arange(E), -l[t].astype(np.float64)))  # logit desc, index asc
+        np.testing.assert_array_equal(idx[t], order[:k])
+
+
+def test_topk_weights_k_equals_E_is_full_softmax_and_k1_is_one():
+    l = _routing_case()
+    T, E = l.shape
+    idx, _, w64 = oracle.route(l, E)
+    for t in range(T):
+        full = softmax(l[t].astype(np.float64))
+        np.testing.assert_allclose(w64[t], full[idx[t]], rtol=1e-13, atol=0)
+    _, w1, w164 = oracle.route(l, 1)
+    assert np.all(w1 == 1.0) and np.all(w164 == 1.0)
+
+
+def test_topk_weights_sum_to_one_and_equal_softmax_over_chosen():
+    l = _routing_case()
+    idx, w, w64 = oracle.route(l, 6)
+    np.testing.assert_allclose(w64.sum(1), 1.0, atol=1e-14)
+    assert np.all(np.abs(w.astype(np.float64).sum(1) - 1.0) <= 1e-6)
+    for t in range(l.shape[0]):
+        np.testing.assert_allclose(w64[t], softmax(l[t, idx[t]].astype(np.float64)), rtol=1e-13)
+
+
+def test_topk_ties_go_to_lower_index():
+    x = rand_bf16(np.random.default_rng(3), (4, 256))
+    row = rand_bf16(np.random.default_rng(4), (1, 256), 0.02)
+    wg = np.repeat(row, 8, axis=0)                 # eight identical experts -> equal logits
+    idx, w, _ = oracle.route(oracle.router_logits(x, wg), 3)
+    np.testing.assert_array_equal(idx, np.tile([0, 1, 2], (4, 1)))
+    np.testing.assert_allclose(w, 1.0 / 3.0, rtol=1e-7)
+
+
+def test_distinct_experts_hit_matches_eq_6_8_within_5_percent():
+    # plain router on the V3 shape: E=256, k=8, m=64 tokens -> eq. 6-8 expects 222.6 experts
+    cfg = synth.get_config("v3_decode", T=64)
+    l = oracle.router_logits(synth.host_x(cfg), synth.host_wg(cfg))
+    idx, _, _ = oracle.route(l, cfg.k)
+    expect = cfg.E * (1 - (1 - cfg.k / cfg.E) ** cfg.T)
+    assert abs(len(np.unique(idx)) - expect) <= 0.05 * expect
+
+
+# ---- a2: permutation ------------------------------------------------------------------------
+
+def _random_topk(rng, T, E, k):
+    return np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+
+
+@pytest.mark.parametrize("T,E,k,S", [(37, 8, 2, 1), (64, 16, 16, 1), (5, 1, 1, 0), (0, 4, 2, 1),
+                                     (100, 33, 3, 0)])
+def test_permutation_is_stable_counting_sort(T, E, k, S):
+    rng = np.random.default_rng(T + E)
+    idx = _random_topk(rng, T, E, k) if T else np.zeros((0, k), np.int32)
+    off, perm, inv = oracle.permute(idx, E, S)
+    counts = np.bincount(idx.ravel(), minlength=E)
+    np.testing.assert_array_equal(np.diff(off[: E + 1]), counts)
+    assert off[0] == 0 and off[E] == T * k and off[E + 1] == T * k + S * T
+    # brute force: stable sort of (expert, token) pairs
+    tok = np.repeat(np.arange(T), k)
+    order = np.lexsort((tok, idx.ravel()))
+    np.testing.assert_array_equal(perm, tok[order])
+    pos = np.empty(T * k, np.int64)
+    pos[order] = np.arange(T * k)
+    np.testing.assert_array_equal(inv, pos)
+    # invariants
+    if T:
+        np.testing.assert_array_equal(perm[inv], tok)
+        np.testing.assert_array_equal(np.bincount(perm, minlength=T), np.full(T, k))
+
+
+# ---- a3 + a4: SwiGLU expert ------------------------------------------------------------------
+
+def test_swiglu_known_values_gate_then_up_then_down():
+    # x = one-hot, gate/up weights hold chosen scalars in column 0, W_d routes h_r to y_r:
+    # then y_r = SiLU(g_r) * u_r with SiLU(z) = z * logistic(z).
+    d, f = 128, 128
+    g = np.array([0.0, 2.0, -2.0, 8.0, 0.5, -0.25] + [1.0] * (f - 6))
+    u = np.array([3.0, 1.0, 1.0, 0.5, -2.0, 4.0] + [0.0] * (f - 6))
+    w13 = np.zeros((2 * f, d), np.float32)
+    w13[:f, 0], w13[f:, 0] = g, u
+    w2 = np.eye(d, f, dtype=np.float32)
+    x = np.zeros((1, d), np.float32)
+    x[0, 0] = 1.0
+    y, h = oracle.expert_rows(bf16_bits(x), bf16_bits(w13), bf16_bits(w2), want_h=True)
+    np.testing.assert_allclose(h[0], g * expit(g) * u, rtol=1e-15, atol=1e-300)
+    np.testing.assert_allclose(y[0], h[0], rtol=0, atol=0)
+
+
+def test_swiglu_split_intermediate_sums_eq_6_3():
+    # Y = Z0 Wd0 + Z1 Wd1 when the intermediate width f is split in two halves.
+    rng = np.random.default_rng(5)
+    d, f = 128, 256
+    x = rand_bf16(rng, (3, d))
+    w13, w2 = rand_bf16(rng, (2 * f, d), 0.02), rand_bf16(rng, (d, f), 0.02)
+    full = oracle.expert_rows(x, w13, w2)
+    half = f // 2
+    parts = []
+    for s in (slice(0, half), slice(half, f)):
+        w13_s = np.concatenate([w13[:f][s], w13[f:][s]])
+        parts.append(oracle.expert_rows(x, w13_s, np.ascontiguousarray(w2[:, s])))
+    np.testing.assert_allclose(parts[0] + parts[1], full, rtol=1e-12, atol=1e-15)
+
+
+def test_single_expert_layer_is_a_dense_swiglu_ffn():
+    # E = 1, k = 1, no shared expert: the layer is Y = [SiLU(X Wg) (.) (X Wu)] Wd (numpy matmul).
+    cfg = synth.get_config("tiny", E=1, k=1, n_shared=0, T=9)
+    inp = synth.host_inputs(cfg)
+    out = oracle.moe_layer(cfg, inp)
+    X = oracle.bf16_to_f64(inp.x)
+    W13 = oracle.bf16_to_f64(inp.experts[0].w13)
+    Wd = oracle.bf16_to_f64(inp.experts[0].w2)
+    G, U = X @ W13[: cfg.f].T, X @ W13[cfg.f:].T
+    Y = (G * expit(G) * U) @ Wd.T
+    np.testing.assert_allclose(out["y"], Y, rtol=1e-11, atol=1e-13)
+    assert np.all(out["topk_idx"] == 0) and np.all(out["topk_w"] == 1.0)
+
+
+@pytest.mark.parametrize("name,over", [("tiny", {}), ("tiny", {"wdtype": "fp8"}),
+                                       ("tiny", {"n_shared": 0, "k": 3}),
+                                       ("tiny", {"router": "zipf", "T": 21})])
+def test_layer_equals_dense_masked_evaluation(name, over):
+    # every expert evaluated on every token with numpy, non-chosen ones weighted 0
+    cfg = synth.get_config(name, **over)
+    inp = synth.host_inputs(cfg)
+    out = oracle.moe_layer(cfg, inp)
+    X = oracle.bf16_to_f64(inp.x)
+
+    def dense_w(ew, which):
+        if cfg.wdtype == "bf16":
+            return oracle.bf16_to_f64(getattr(ew, which))
+        q = getattr(ew, which)
+        s = getattr(ew, "s" + which[1:])
+        vals = np.array([oracle.e4m3_value(c) for c in range(256)])[q]
+        return vals * np.kron(s.astype(np.float64), np.ones((128, 128)))
+
+    Ys = []
+    for ew in inp.experts:
+        W13, Wd = dense_w(ew, "w13"), dense_w(ew, "w2")
+        G, U = X @ W13[: cfg.f].T, X @ W13[cfg.f:].T
+        Ys.append((G * expit(G) * U) @ Wd.T)
+    mask = np.zeros((cfg.T, cfg.E))
+    for t in range(cfg.T):
+        mask[t, out["topk_idx"][t]] = out["topk_w64"][t]
+    y = np.einsum("te,etd->td", mask, np.stack(Ys[: cfg.E]))
+    if cfg.n_shared:
+        y += Ys[cfg.E]
+    np.testing.assert_allclose(out["y"], y, rtol=1e-10, atol=1e-14)
+
+
+# ---- a5: combine ----------------------------------------------------------------------------
+
+def test_combine_four_contributions_sum_to_ten():
+    g = golden_kv("combine_sum.txt")
+    w = np.array([[float(v) for v in g["weights"].split()]])
+    idx = np.array([[0, 1, 2, 3]], np.int32)
+    off, perm, inv = oracle.permute(idx, 4, 0)
+    y_perm = np.full((4, 3), float(g["expert_output"]))
+    y = oracle.combine(y_perm, inv, w, 1, 4, n_shared=0)
+    np.testing.assert_allclose(y, float(g["expected"]), rtol=1e-15)
+
+
+def test_combine_is_a1_y1_plus_a6_y6_plus_shared():
+    rng = np.random.default_rng(7)
+    idx = np.array([[6, 1], [3, 6]], np.int32)          # token A -> experts 6 and 1
+    w = np.array([[0.7, 0.3], [0.55, 0.45]])
+    off, perm, inv = oracle.permute(idx, 8, 1)
+    y_perm = rng.normal(size=(off[-1], 5))
+    y = oracle.combine(y_perm, inv, w, 2, 2, n_shared=1)
+    slot = {(int(perm[s]), e): s for e in range(8) for s in range(off[e], off[e + 1])}
+    a6, a1 = w[0]
+    y1, y6, shared = y_perm[slot[(0, 1)]], y_perm[slot[(0, 6)]], y_perm[4 + 0]
+    np.testing.assert_allclose(y[0], a1 * y1 + a6 * y6 + shared, rtol=1e-15)
