@@ -1,0 +1,148 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) routed-expert MoE FFN layer, inference hot path.
+ *
+ * The layer, as the pages state it:
+ *   router     -- score every routed expert for each token, keep the top-k
+ *                 ("DeepSeek-V4-Pro on NVIDIA H200", section 0.2.2, step D4);
+ *   permute    -- reorder the token rows by expert ("第 6 章 超節點", section 6.2.6: the receiver
+ *                 reorders rows by expert, multiplies, then restores token order);
+ *   expert FFN -- per expert Y = [SiLU(X W_g) (.) (X W_u)] W_d ("第 6 章 超節點", section 6.2.2),
+ *                 three GEMMs per expert ("DeepSeek V3/R1 Inference Efficiency (1)", Parameters);
+ *   combine    -- routing-weighted sum of the experts' outputs, a1*y1 + a6*y6, plus the
+ *                 always-on shared expert ("第 6 章 超節點", sections 6.2.6 and 6.4.1;
+ *                 "DeepSeek-V4-Pro on NVIDIA H200", section 0.1.2 and step D7).
+ * On one GPU the dispatch and combine exchanges become in-HBM gathers.
+ *
+ * Conventions shared by every entry point
+ *   - Pointers named x, wg, bias, topk_*, expert_offsets, perm_token, inv_slot, w13, s13, w2,
+ *     s2, y_perm, y and ws are DEVICE pointers, allocated and owned by the caller. The library
+ *     never allocates, frees or synchronises in these calls; work is enqueued on `stream`
+ *     (a cudaStream_t, NULL = legacy default stream) and the call returns immediately.
+ *   - `shape` is a host pointer read during the call only.
+ *   - Arguments are validated on the host first: a negative status is returned before any
+ *     launch and nothing is written (no side effects).
+ *   - Device-side checks (an index out of range, a duplicated expert in a token's top-k row, a
+ *     bounded wait that gave up) never fault: the kernel skips the bad access and records the
+ *     first error code in the workspace; moe_check_device_status() reports it.
+ *   - Tensors are dense row-major; "bf16" is IEEE-style bfloat16, "E4M3" is OCP FP8 E4M3.
+ *   - Every pointer must be 16-byte aligned (256-byte for ws).
+ *   - Shapes: 1 <= E <= 1024, 1 <= k <= min(E, 32), n_shared in {0, 1}, d and f multiples of
+ *     128 with 128 <= d <= 16384 and 128 <= f <= 16384, 0 <= T and T*(k+1) <= 2^30.
+ *   - Not thread-safe per workspace: calls that share a workspace must be ordered on one stream.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,     /* bad pointer, shape or alignment (host check)             */
+  MOE_ERR_UNSUPPORTED = -2,     /* valid request this build does not serve (e.g. no GPU)    */
+  MOE_ERR_WORKSPACE = -3,       /* ws_bytes < moe_workspace_size(shape)                     */
+  MOE_ERR_CUDA = -4,            /* a CUDA runtime/driver call or a launch failed            */
+  MOE_ERR_DEVICE_TIMEOUT = -5,  /* a bounded device wait gave up (reported by the check)    */
+  MOE_ERR_DEVICE_BOUNDS = -6    /* a device-side index check failed (reported by the check) */
+} moe_status;
+
+typedef enum {
+  MOE_W_BF16 = 0,            /* expert weights bf16                                          */
+  MOE_W_FP8_E4M3_B128 = 1    /* expert weights E4M3 with one fp32 scale per 128x128 block    */
+} moe_wdtype;
+
+typedef struct {
+  int32_t T;         /* tokens in the batch                                                   */
+  int32_t d;         /* hidden size                                                           */
+  int32_t E;         /* routed experts                                                        */
+  int32_t k;         /* routed experts chosen per token                                       */
+  int32_t f;         /* expert intermediate size                                              */
+  int32_t n_shared;  /* shared (always-on) experts, 0 or 1; the shared expert is index E      */
+  int32_t wdtype;    /* moe_wdtype of w13/w2                                                  */
+} moe_shape;
+
+/* Bytes of scratch (`ws`) the four calls need for this shape; 0 for an invalid shape. One
+ * workspace serves all four calls of a layer. Its first 4 bytes are the device status word:
+ * moe_route clears it (a layer starts there); a caller that skips moe_route must zero those
+ * 4 bytes once before its first call. Nothing else in it needs initialisation. */
+MOE_API size_t moe_workspace_size(const moe_shape* shape);
+
+/* Router ("DeepSeek-V4-Pro on NVIDIA H200", 0.2.2 D4; "CANN DeepSeek-V4推理优化", MoE
+ * 专家模型规格, soft routing).
+ *   x        [T, d] bf16 tokens.        wg [E, d] bf16 router weight (one row per expert).
+ *   bias     [E] fp32 added to the logits, or NULL.
+ *   topk_idx [T, k] int32 out: the k experts with the largest logits, by descending logit,
+ *            ties to the lower expert index.
+ *   topk_w   [T, k] fp32 out: softmax over all E logits, renormalised over the k chosen
+ *            (= softmax over the k chosen logits).
+ * The logit l[t,e] = x[t].wg[e] (+ bias[e]) is formed in fp32 in one fixed order, so the
+ * choice is reproducible bit for bit: d is cut into 8-element chunks, lane j of 32 accumulates
+ * chunks j, j+32, ... element by element with fused multiply-add from +0, the 32 lane sums
+ * are combined by an xor butterfly (offsets 16, 8, 4, 2, 1), then the bias is added.
+ * Inputs must be finite. */
+MOE_API moe_status moe_route(const moe_shape* shape, const void* x, const void* wg, const float* bias,
+                     int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes, void* stream);
+
+/* Token -> expert permutation ("第 6 章 超節點", 6.2.6).
+ *   topk_idx       [T, k] int32, each row k distinct experts in [0, E).
+ *   expert_offsets [E+2] int32 out: expert e (< E) owns slots [offsets[e], offsets[e+1]);
+ *                  offsets[E] = T*k starts the shared expert's segment and
+ *                  offsets[E+1] = T*k + n_shared*T ends it.
+ *   perm_token     [T*k] int32 out: token of each routed slot; slots are expert-major and,
+ *                  within an expert, in ascending token order (a stable counting sort).
+ *   inv_slot       [T*k] int32 out: inv_slot[t*k + j] = slot of token t's j-th choice.
+ * The shared segment is implicit: slot T*k + t belongs to token t. Deterministic (no atomics
+ * decide any order). */
+MOE_API moe_status moe_permute(const moe_shape* shape, const int32_t* topk_idx, int32_t* expert_offsets,
+                       int32_t* perm_token, int32_t* inv_slot, void* ws, size_t ws_bytes,
+                       void* stream);
+
+/* Per-expert SwiGLU FFN over every slot ("第 6 章 超節點", 6.2.2: Y = [SiLU(X W_g) (.) (X W_u)] W_d).
+ *   x              [T, d] bf16 tokens; perm_token and expert_offsets as made by moe_permute.
+ *   w13            [E+n_shared, 2f, d]: rows 0..f-1 of expert e are its gate projection, rows
+ *                  f..2f-1 its up projection (one row per output feature, d contiguous).
+ *   w2             [E+n_shared, d, f]: the down projection (one row per output feature).
+ *                  bf16, or E4M3 codes (one byte each) for MOE_W_FP8_E4M3_B128.
+ *   s13, s2        fp32 block scales [E+n_shared, 2f/128, d/128] and [E+n_shared, d/128, f/128]
+ *                  for E4M3 weights (weight = code value * scale of its 128x128 block); NULL
+ *                  for bf16.
+ *   y_perm         [T*k + n_shared*T, d] fp32 out: row s = expert output for slot s, i.e.
+ *                  W_d^T (SiLU(W_g^T x) * (W_u^T x)) for the slot's token and expert.
+ * The intermediate h = SiLU(G) * U is kept in bf16; accumulation is fp32. */
+MOE_API moe_status moe_expert_ffn(const moe_shape* shape, const void* x, const int32_t* perm_token,
+                          const int32_t* expert_offsets, const void* w13, const float* s13,
+                          const void* w2, const float* s2, float* y_perm, void* ws,
+                          size_t ws_bytes, void* stream);
+
+/* Combine ("第 6 章 超節點", 6.2.6 and 6.4.1: send back, restore token order, sum with the
+ * routing weights).
+ *   y[t] = y_perm[T*k + t] (if n_shared) + sum_j topk_w[t, j] * y_perm[inv_slot[t*k + j]],
+ *   accumulated in fp32 in that order and rounded once to bf16 (nearest even).
+ *   y [T, d] bf16 out. ws is used only to record device-side index errors. */
+MOE_API moe_status moe_combine(const moe_shape* shape, const float* y_perm, const int32_t* inv_slot,
+                       const float* topk_w, void* y, void* ws, size_t ws_bytes, void* stream);
+
+/* Reads (and clears) the first device-side error recorded in `ws` since the last check.
+ * Synchronises `stream`. Returns MOE_OK, MOE_ERR_DEVICE_BOUNDS or MOE_ERR_DEVICE_TIMEOUT (or
+ * MOE_ERR_CUDA if the read itself fails). */
+MOE_API moe_status moe_check_device_status(void* ws, void* stream);
+
+/* Message for the last non-OK status returned on the calling thread (thread-local storage;
+ * valid until the next call on that thread). */
+MOE_API const char* moe_last_error_string(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -177,6 +177,7 @@ void oracle_permute(const int32_t* topk_idx, int T, int E, int k, int n_shared, 
  * is). */
 void oracle_matvec(int wdtype, const void* w, const float* s, int64_t cols, int64_t row0,
                    int64_t nrows, const double* x, double* y) {
+#pragma omp parallel for schedule(static)
   for (int64_t r = 0; r < nrows; ++r) {
     double acc = 0.0;
     for (int64_t c = 0; c < cols; ++c) acc += weight(wdtype, w, s, cols, row0 + r, c) * x[c];
@@ -190,7 +191,6 @@ void oracle_matvec(int wdtype, const void* w, const float* s, int64_t cols, int6
 void oracle_expert_rows(const uint16_t* xrows, int n, int d, int f, int wdtype, const void* w13,
                         const float* s13, const void* w2, const float* s2, double* y,
                         double* h_out) {
-#pragma omp parallel for schedule(dynamic)
   for (int i = 0; i < n; ++i) {
     double* xv = (double*)malloc(sizeof(double) * (size_t)d);
     double* g = (double*)malloc(sizeof(double) * (size_t)f);

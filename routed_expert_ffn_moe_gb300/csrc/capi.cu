@@ -1,0 +1,194 @@
+// The C ABI (include/moe.h): host-side validation, workspace carving, kernel dispatch.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+thread_local char g_err[512] = "";
+
+moe_status fail(moe_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+moe_status fail(moe_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof g_err, fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+moe_status cuda_fail(cudaError_t e, const char* where) {
+  return fail(MOE_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+moe_status check_shape(const moe_shape* s) {
+  if (!s) return fail(MOE_ERR_INVALID_ARG, "shape is NULL");
+  if (s->E < 1 || s->E > 1024) return fail(MOE_ERR_INVALID_ARG, "E=%d not in [1, 1024]", s->E);
+  if (s->k < 1 || s->k > s->E || s->k > 32)
+    return fail(MOE_ERR_INVALID_ARG, "k=%d not in [1, min(E, 32)]", s->k);
+  if (s->n_shared != 0 && s->n_shared != 1)
+    return fail(MOE_ERR_INVALID_ARG, "n_shared=%d not 0 or 1", s->n_shared);
+  if (s->d < 128 || s->d > 16384 || s->d % 128)
+    return fail(MOE_ERR_INVALID_ARG, "d=%d not a multiple of 128 in [128, 16384]", s->d);
+  if (s->f < 128 || s->f > 16384 || s->f % 128)
+    return fail(MOE_ERR_INVALID_ARG, "f=%d not a multiple of 128 in [128, 16384]", s->f);
+  if (s->T < 0 || (long long)s->T * (s->k + 1) > (1LL << 30))
+    return fail(MOE_ERR_INVALID_ARG, "T=%d out of range (need 0 <= T, T*(k+1) <= 2^30)", s->T);
+  if (s->wdtype != MOE_W_BF16 && s->wdtype != MOE_W_FP8_E4M3_B128)
+    return fail(MOE_ERR_INVALID_ARG, "wdtype=%d unknown", s->wdtype);
+  return MOE_OK;
+}
+
+#define REQUIRE_PTR(p, align)                                                          \
+  do {                                                                                  \
+    if (!(p)) return fail(MOE_ERR_INVALID_ARG, "%s is NULL", #p);                       \
+    if (!aligned((p), (align)))                                                         \
+      return fail(MOE_ERR_INVALID_ARG, "%s not %d-byte aligned", #p, (int)(align));     \
+  } while (0)
+
+moe_status check_ws(const moe_shape* s, const void* ws, size_t ws_bytes, WsLayout* L) {
+  REQUIRE_PTR(ws, 256);
+  *L = ws_layout(*s);
+  if (ws_bytes < L->total)
+    return fail(MOE_ERR_WORKSPACE, "workspace %zu bytes < %zu required", ws_bytes, L->total);
+  return MOE_OK;
+}
+
+}  // namespace
+
+int num_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (!cached[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 1;
+  }
+  return cached[dev];
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+size_t moe_workspace_size(const moe_shape* shape) {
+  if (check_shape(shape) != MOE_OK) return 0;
+  return ws_layout(*shape).total;
+}
+
+moe_status moe_route(const moe_shape* shape, const void* x, const void* wg, const float* bias,
+                     int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes, void* stream) {
+  moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (shape->T > 0) {
+    REQUIRE_PTR(x, 16);
+    REQUIRE_PTR(topk_idx, 16);
+    REQUIRE_PTR(topk_w, 16);
+  }
+  REQUIRE_PTR(wg, 16);
+  if (bias && !aligned(bias, 16)) return fail(MOE_ERR_INVALID_ARG, "bias not 16-byte aligned");
+  WsLayout L;
+  if ((st = check_ws(shape, ws, ws_bytes, &L)) != MOE_OK) return st;
+  // A layer starts here: clear the device status word.
+  cudaError_t e = cudaMemsetAsync(static_cast<char*>(ws) + L.status, 0, sizeof(int),
+                                  static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "moe_route status reset");
+  e = launch_route(*shape, static_cast<const uint16_t*>(x),
+                               static_cast<const uint16_t*>(wg), bias, topk_idx, topk_w,
+                               static_cast<char*>(ws), L, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_route launch");
+}
+
+moe_status moe_permute(const moe_shape* shape, const int32_t* topk_idx, int32_t* expert_offsets,
+                       int32_t* perm_token, int32_t* inv_slot, void* ws, size_t ws_bytes,
+                       void* stream) {
+  moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (shape->T > 0) {
+    REQUIRE_PTR(topk_idx, 16);
+    REQUIRE_PTR(perm_token, 16);
+    REQUIRE_PTR(inv_slot, 16);
+  }
+  REQUIRE_PTR(expert_offsets, 16);
+  WsLayout L;
+  if ((st = check_ws(shape, ws, ws_bytes, &L)) != MOE_OK) return st;
+  cudaError_t e = launch_permute(*shape, topk_idx, expert_offsets, perm_token, inv_slot,
+                                 static_cast<char*>(ws), L, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_permute launch");
+}
+
+moe_status moe_expert_ffn(const moe_shape* shape, const void* x, const int32_t* perm_token,
+                          const int32_t* expert_offsets, const void* w13, const float* s13,
+                          const void* w2, const float* s2, float* y_perm, void* ws,
+                          size_t ws_bytes, void* stream) {
+  moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (shape->T > 0) {
+    REQUIRE_PTR(x, 16);
+    REQUIRE_PTR(perm_token, 16);
+    REQUIRE_PTR(y_perm, 16);
+  }
+  REQUIRE_PTR(expert_offsets, 16);
+  REQUIRE_PTR(w13, 16);
+  REQUIRE_PTR(w2, 16);
+  if (shape->wdtype == MOE_W_FP8_E4M3_B128) {
+    REQUIRE_PTR(s13, 16);
+    REQUIRE_PTR(s2, 16);
+  } else if (s13 || s2) {
+    return fail(MOE_ERR_INVALID_ARG, "s13/s2 must be NULL for bf16 weights");
+  }
+  WsLayout L;
+  if ((st = check_ws(shape, ws, ws_bytes, &L)) != MOE_OK) return st;
+  cudaError_t e = launch_expert_ffn(*shape, static_cast<const uint16_t*>(x), perm_token,
+                                    expert_offsets, w13, s13, w2, s2, y_perm,
+                                    static_cast<char*>(ws), L, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_expert_ffn launch");
+}
+
+moe_status moe_combine(const moe_shape* shape, const float* y_perm, const int32_t* inv_slot,
+                       const float* topk_w, void* y, void* ws, size_t ws_bytes, void* stream) {
+  moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (shape->T > 0) {
+    REQUIRE_PTR(y_perm, 16);
+    REQUIRE_PTR(inv_slot, 16);
+    REQUIRE_PTR(topk_w, 16);
+    REQUIRE_PTR(y, 16);
+  }
+  WsLayout L;
+  if ((st = check_ws(shape, ws, ws_bytes, &L)) != MOE_OK) return st;
+  int* status = reinterpret_cast<int*>(static_cast<char*>(ws) + L.status);
+  cudaError_t e = launch_combine(*shape, y_perm, inv_slot, topk_w, static_cast<uint16_t*>(y),
+                                 status, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_combine launch");
+}
+
+moe_status moe_check_device_status(void* ws, void* stream) {
+  REQUIRE_PTR(ws, 256);
+  int code = 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(&code, ws, sizeof(int), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess && code != 0) e = cudaMemsetAsync(ws, 0, sizeof(int), st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "moe_check_device_status");
+  if (code == MOE_ERR_DEVICE_BOUNDS)
+    return fail(MOE_ERR_DEVICE_BOUNDS, "a device-side index check failed");
+  if (code == MOE_ERR_DEVICE_TIMEOUT)
+    return fail(MOE_ERR_DEVICE_TIMEOUT, "a bounded device wait gave up");
+  if (code != 0) return fail(MOE_ERR_CUDA, "unknown device status %d", code);
+  return MOE_OK;
+}
+
+const char* moe_last_error_string(void) { return g_err; }
+
+}  // extern "C"

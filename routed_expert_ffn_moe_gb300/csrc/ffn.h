@@ -1,0 +1,29 @@
+// Internal interface of the expert-FFN kernels (weight-streaming and tensor-core paths).
+#pragma once
+
+#include "internal.h"
+
+namespace moe {
+
+struct FfnArgs {
+  int T, d, E, k, f, n_shared, wdtype;
+  const uint16_t* x;           // [T, d] bf16
+  const int32_t* perm_token;   // [T*k]
+  const int32_t* offsets;      // [E+2]
+  const void* w13;             // [E+S, 2f, d]
+  const float* s13;            // FP8 scales or null
+  const void* w2;              // [E+S, d, f]
+  const float* s2;
+  uint16_t* h;                 // [slots, f] bf16 (workspace)
+  uint16_t* x_perm;            // [T*k, d] bf16 (workspace)
+  float* y_perm;               // [slots, d] fp32
+  int* status;                 // device error word
+};
+
+// weight-streaming path (ffn_gemv.cu)
+int gemv_items_per_group(bool gateup, int d, int f);
+int gemv_group_tokens();
+cudaError_t launch_gemv(const FfnArgs& a, const int32_t* prefix_up, const int32_t* prefix_down,
+                        bool gateup, int max_items, cudaStream_t st);
+
+}  // namespace moe

@@ -1,0 +1,130 @@
+// Internal interface of the MoE library: workspace layout, launch entry points of each kernel
+// family, and small device helpers shared by the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// ---- workspace -----------------------------------------------------------------------------
+// One scratch buffer serves the four calls of a layer:
+//   status   int32[64]            device error code (first error wins) + details
+//   logits   f32 [T, E]           router logits
+//   hist     i32 [E, nchunk]      per (expert, 32-token chunk) counts
+//   base     i32 [E, nchunk]      exclusive scan of hist: first slot of each (expert, chunk)
+//   plan     i32 [kPlanRows, E+2] per-expert work prefixes of the FFN kernels + counters
+//   x_perm   bf16 [T*k, d]        token rows gathered in slot order (tensor-core path input)
+//   h        bf16 [T*k + S*T, f]  SiLU(gate) * up for every slot
+constexpr int kChunkTokens = 32;
+constexpr int kPlanRows = 8;
+
+struct WsLayout {
+  size_t status, logits, hist, base, plan, x_perm, h, total;
+  int nchunk;
+};
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+inline WsLayout ws_layout(const moe_shape& s) {
+  WsLayout L{};
+  const size_t T = (size_t)s.T, E = (size_t)s.E, k = (size_t)s.k;
+  L.nchunk = (int)((T + kChunkTokens - 1) / kChunkTokens);
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t at = off; off = align_up(off + bytes, 256); return at; };
+  L.status = take(256);
+  L.logits = take(T * E * 4);
+  L.hist = take(E * (size_t)L.nchunk * 4);
+  L.base = take(E * (size_t)L.nchunk * 4);
+  L.plan = take((size_t)kPlanRows * (E + 2) * 4 + 256);
+  L.x_perm = take(T * k * (size_t)s.d * 2);
+  L.h = take((T * k + (size_t)s.n_shared * T) * (size_t)s.f * 2);
+  L.total = off;
+  return L;
+}
+
+// plan rows (each E+2 int32 entries, see ffn kernels)
+enum PlanRow { kPlanGemvUp = 0, kPlanGemvDown = 1, kPlanTcUp = 2, kPlanTcDown = 3 };
+
+// ---- launchers (each returns cudaGetLastError() of its launches) ---------------------------
+cudaError_t launch_route(const moe_shape& s, const uint16_t* x, const uint16_t* wg,
+                         const float* bias, int32_t* topk_idx, float* topk_w, char* ws,
+                         const WsLayout& L, cudaStream_t st);
+cudaError_t launch_permute(const moe_shape& s, const int32_t* topk_idx, int32_t* offsets,
+                           int32_t* perm_token, int32_t* inv_slot, char* ws, const WsLayout& L,
+                           cudaStream_t st);
+cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32_t* perm_token,
+                              const int32_t* offsets, const void* w13, const float* s13,
+                              const void* w2, const float* s2, float* y_perm, char* ws,
+                              const WsLayout& L, cudaStream_t st);
+cudaError_t launch_combine(const moe_shape& s, const float* y_perm, const int32_t* inv_slot,
+                           const float* topk_w, uint16_t* y, int* status, cudaStream_t st);
+
+int num_sms();
+
+// ---- device helpers ------------------------------------------------------------------------
+#ifdef __CUDACC__
+__device__ __forceinline__ void record_error(int* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+// element i (0..7) of eight packed bf16 values, as fp32 (exact)
+__device__ __forceinline__ float bf16x8_elem(const uint4& v, int i) {
+  const uint32_t w = i < 2 ? v.x : i < 4 ? v.y : i < 6 ? v.z : v.w;
+  return __uint_as_float((i & 1) ? (w & 0xFFFF0000u) : (w << 16));
+}
+
+__device__ __forceinline__ uint4 ldg_u4(const void* p) {
+  return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+// streamed once: do not keep in L1
+__device__ __forceinline__ uint4 ld_stream_u4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) {
+  // round to nearest even via the hardware conversion
+  uint16_t r;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(v));
+  return r;
+}
+
+// Exclusive scan of one int per thread over a block of up to 1024 threads; returns the
+// thread's exclusive prefix and writes the block total to *total.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* total) {
+  __shared__ int warp_tot[32];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) warp_tot[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    const int nw = (blockDim.x + 31) >> 5;
+    int w = lane < nw ? warp_tot[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += n;
+    }
+    warp_tot[lane] = w;  // inclusive prefix of warp totals
+  }
+  __syncthreads();
+  const int warp_prefix = wid ? warp_tot[wid - 1] : 0;
+  *total = warp_tot[((blockDim.x + 31) >> 5) - 1];
+  __syncthreads();
+  return warp_prefix + incl - v;
+}
+#endif
+
+}  // namespace moe

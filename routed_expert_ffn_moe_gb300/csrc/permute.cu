@@ -1,0 +1,134 @@
+// Token -> expert permutation: a deterministic, stable counting sort of the T*k (token, choice)
+// pairs by expert ("第 6 章 超節點", 6.2.6: the receiver reorders its input rows by expert before
+// the matrix multiply and restores token order afterwards).
+//
+// Tokens are cut into 32-token chunks, one warp each. For its chunk a warp builds, in shared
+// memory, one 32-bit mask per expert of the lanes (tokens) that chose it; the popcount of a
+// mask is the chunk's count for that expert, and the popcount of the mask below a lane is that
+// token's rank among the chunk's tokens of the same expert. An exclusive scan over
+// (expert, chunk) in expert-major order then gives every pair its slot. No atomic decides an
+// order: the OR of bits is order-independent.
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kWarpsPerBlock = 8;
+
+// Valid choice: in range and not a repeat of an earlier choice of the same token.
+__device__ __forceinline__ bool valid_choice(const int32_t* row, int j, int E) {
+  const int e = row[j];
+  if ((unsigned)e >= (unsigned)E) return false;
+  for (int j2 = 0; j2 < j; ++j2)
+    if (row[j2] == e) return false;
+  return true;
+}
+
+// Builds this warp's expert -> lane mask table for its chunk.
+__device__ __forceinline__ void build_masks(uint32_t* sel, const int32_t* topk_idx, int T, int E,
+                                            int k, int chunk, int nchunk, int* status) {
+  const int lane = threadIdx.x & 31;
+  for (int e = lane; e < E; e += 32) sel[e] = 0;
+  __syncwarp();
+  const int t = chunk * kChunkTokens + lane;
+  if (chunk < nchunk && t < T) {
+    const int32_t* row = topk_idx + (size_t)t * k;
+    for (int j = 0; j < k; ++j) {
+      if (valid_choice(row, j, E))
+        atomicOr(&sel[row[j]], 1u << lane);
+      else
+        record_error(status, MOE_ERR_DEVICE_BOUNDS);
+    }
+  }
+  __syncwarp();
+}
+
+__global__ void __launch_bounds__(256) k_perm_count(const int32_t* __restrict__ topk_idx, int T,
+                                                    int E, int k, int nchunk,
+                                                    int32_t* __restrict__ hist, int* status) {
+  extern __shared__ uint32_t sel_all[];
+  const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int chunk = blockIdx.x * kWarpsPerBlock + wid;
+  uint32_t* sel = sel_all + (size_t)wid * E;
+  build_masks(sel, topk_idx, T, E, k, chunk, nchunk, status);
+  if (chunk < nchunk)
+    for (int e = lane; e < E; e += 32) hist[(size_t)e * nchunk + chunk] = __popc(sel[e]);
+}
+
+// One block: exclusive scan of hist (expert-major) into base; expert offsets from it.
+__global__ void __launch_bounds__(1024) k_perm_scan(const int32_t* __restrict__ hist, int E,
+                                                    int nchunk, int T, int k, int n_shared,
+                                                    int32_t* __restrict__ base,
+                                                    int32_t* __restrict__ offsets) {
+  const long n = (long)E * nchunk;
+  const long per = (n + blockDim.x - 1) / blockDim.x;
+  const long beg = per * threadIdx.x, end = beg + per < n ? beg + per : n;
+  int s = 0;
+  for (long i = beg; i < end; ++i) s += hist[i];
+  int total;
+  int run = block_exclusive_scan(s, &total);
+  for (long i = beg; i < end; ++i) {
+    base[i] = run;
+    run += hist[i];
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    offsets[e] = nchunk ? base[(size_t)e * nchunk] : 0;
+  if (threadIdx.x == 0) {
+    offsets[E] = T * k;
+    offsets[E + 1] = T * k + n_shared * T;
+  }
+}
+
+__global__ void __launch_bounds__(256) k_perm_scatter(const int32_t* __restrict__ topk_idx, int T,
+                                                      int E, int k, int nchunk,
+                                                      const int32_t* __restrict__ base,
+                                                      int32_t* __restrict__ perm_token,
+                                                      int32_t* __restrict__ inv_slot) {
+  extern __shared__ uint32_t sel_all[];
+  const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int chunk = blockIdx.x * kWarpsPerBlock + wid;
+  uint32_t* sel = sel_all + (size_t)wid * E;
+  build_masks(sel, topk_idx, T, E, k, chunk, nchunk, nullptr);
+  const int t = chunk * kChunkTokens + lane;
+  if (chunk >= nchunk || t >= T) return;
+  const int32_t* row = topk_idx + (size_t)t * k;
+  const uint32_t below = (1u << lane) - 1u;
+  for (int j = 0; j < k; ++j) {
+    if (!valid_choice(row, j, E)) {
+      inv_slot[(size_t)t * k + j] = -1;
+      continue;
+    }
+    const int e = row[j];
+    const int slot = base[(size_t)e * nchunk + chunk] + __popc(sel[e] & below);
+    perm_token[slot] = t;
+    inv_slot[(size_t)t * k + j] = slot;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_permute(const moe_shape& s, const int32_t* topk_idx, int32_t* offsets,
+                           int32_t* perm_token, int32_t* inv_slot, char* ws, const WsLayout& L,
+                           cudaStream_t st) {
+  int* status = reinterpret_cast<int*>(ws + L.status);
+  int32_t* hist = reinterpret_cast<int32_t*>(ws + L.hist);
+  int32_t* base = reinterpret_cast<int32_t*>(ws + L.base);
+  const int nchunk = L.nchunk;
+  const unsigned blocks = (unsigned)((nchunk + kWarpsPerBlock - 1) / kWarpsPerBlock);
+  const size_t smem = (size_t)kWarpsPerBlock * s.E * sizeof(uint32_t);
+  if (blocks) {
+    k_perm_count<<<blocks, 32 * kWarpsPerBlock, smem, st>>>(topk_idx, s.T, s.E, s.k, nchunk, hist,
+                                                            status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  k_perm_scan<<<1, 1024, 0, st>>>(hist, s.E, nchunk, s.T, s.k, s.n_shared, base, offsets);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || !blocks) return e;
+  k_perm_scatter<<<blocks, 32 * kWarpsPerBlock, smem, st>>>(topk_idx, s.T, s.E, s.k, nchunk, base,
+                                                            perm_token, inv_slot);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

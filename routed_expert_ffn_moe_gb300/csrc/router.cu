@@ -1,0 +1,156 @@
+// Router: logits in a fixed fp32 order, top-k selection, gate weights.
+//
+// The pages: the router scores every routed expert for each token and keeps the top-k, its
+// compute is small and its product is the sparse metadata for dispatch ("DeepSeek-V4-Pro on
+// NVIDIA H200", 0.2.2 step D4); V4 uses learned soft routing ("CANN DeepSeek-V4推理优化", MoE
+// 专家模型规格). Ascend fuses the gate into one "GatingTopK" kernel (same page, 融合Kernel);
+// here the logits GEMM and the selection are two kernels so the selection can see all E
+// logits of a token at once.
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+// One warp computes TT tokens x TE experts. Lane j owns the 8-element chunks j, j+32, ... of
+// the hidden dimension and accumulates them element by element with fused multiply-add; the
+// 32 lane sums are then combined by an xor butterfly. This is the library's defined order for
+// the logit, so the top-k choice is reproducible bit for bit.
+template <int TT, int TE>
+__global__ void __launch_bounds__(128) k_router_logits(const uint16_t* __restrict__ x,
+                                                       const uint16_t* __restrict__ wg,
+                                                       const float* __restrict__ bias, int T,
+                                                       int d, int E, float* __restrict__ logits) {
+  const int lane = threadIdx.x & 31;
+  const int warp = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int n_et = (E + TE - 1) / TE;
+  const int t0 = (warp / n_et) * TT, e0 = (warp % n_et) * TE;
+  if (t0 >= T) return;
+  float acc[TT][TE];
+#pragma unroll
+  for (int t = 0; t < TT; ++t)
+#pragma unroll
+    for (int e = 0; e < TE; ++e) acc[t][e] = 0.f;
+  const int chunks = d >> 3;
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  for (int c = lane; c < chunks; c += 32) {
+    uint4 xv[TT], wv[TE];
+#pragma unroll
+    for (int t = 0; t < TT; ++t)
+      xv[t] = (t0 + t < T) ? ldg_u4(x + (size_t)(t0 + t) * d + 8 * c) : zero;
+#pragma unroll
+    for (int e = 0; e < TE; ++e)
+      wv[e] = (e0 + e < E) ? ldg_u4(wg + (size_t)(e0 + e) * d + 8 * c) : zero;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float xf[TT], wf[TE];
+#pragma unroll
+      for (int t = 0; t < TT; ++t) xf[t] = bf16x8_elem(xv[t], i);
+#pragma unroll
+      for (int e = 0; e < TE; ++e) wf[e] = bf16x8_elem(wv[e], i);
+#pragma unroll
+      for (int t = 0; t < TT; ++t)
+#pragma unroll
+        for (int e = 0; e < TE; ++e) acc[t][e] = __fmaf_rn(xf[t], wf[e], acc[t][e]);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1)
+#pragma unroll
+    for (int t = 0; t < TT; ++t)
+#pragma unroll
+      for (int e = 0; e < TE; ++e)
+        acc[t][e] = __fadd_rn(acc[t][e], __shfl_xor_sync(0xffffffffu, acc[t][e], off));
+#pragma unroll
+  for (int t = 0; t < TT; ++t)
+#pragma unroll
+    for (int e = 0; e < TE; ++e)
+      if (((t * TE + e) & 31) == lane && t0 + t < T && e0 + e < E) {
+        const float l = bias ? __fadd_rn(acc[t][e], bias[e0 + e]) : acc[t][e];
+        logits[(size_t)(t0 + t) * E + e0 + e] = l;
+      }
+}
+
+// (value desc, index asc): is (la, ea) ranked before (lb, eb)?
+__device__ __forceinline__ bool ranks_before(float la, int ea, float lb, int eb) {
+  return la > lb || (la == lb && ea < eb);
+}
+
+// One warp per token: k rounds of warp-wide arg-max over the E logits (lane j holds experts
+// j, j+32, ...), then the gate weights softmax(l_chosen) = exp(l_j - l_max) / sum.
+__global__ void __launch_bounds__(256) k_router_topk(const float* __restrict__ logits, int T,
+                                                     int E, int k, int32_t* __restrict__ topk_idx,
+                                                     float* __restrict__ topk_w) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const float* lt = logits + (size_t)t * E;
+  float l[32];
+#pragma unroll
+  for (int m = 0; m < 32; ++m) l[m] = (lane + 32 * m < E) ? lt[lane + 32 * m] : -INFINITY;
+  uint32_t taken = 0;
+  float my_l = -INFINITY;
+  int my_e = 0;
+  for (int j = 0; j < k; ++j) {
+    float bl = -INFINITY;
+    int be = 0x7FFFFFFF;
+#pragma unroll
+    for (int m = 0; m < 32; ++m) {
+      const int e = lane + 32 * m;
+      if (e < E && !((taken >> m) & 1u) && ranks_before(l[m], e, bl, be)) {
+        bl = l[m];
+        be = e;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+      const float ol = __shfl_xor_sync(0xffffffffu, bl, off);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+      if (ranks_before(ol, oe, bl, be)) {
+        bl = ol;
+        be = oe;
+      }
+    }
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    if (lane == j) {
+      my_l = bl;
+      my_e = be;
+    }
+  }
+  const float lmax = __shfl_sync(0xffffffffu, my_l, 0);
+  const float ex = lane < k ? expf(my_l - lmax) : 0.f;
+  float sum = ex;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  if (lane < k) {
+    topk_idx[(size_t)t * k + lane] = my_e;
+    topk_w[(size_t)t * k + lane] = ex / sum;
+  }
+}
+
+template <int TT, int TE>
+cudaError_t launch_logits(const uint16_t* x, const uint16_t* wg, const float* bias, int T, int d,
+                          int E, float* logits, cudaStream_t st) {
+  const long warps = (long)((T + TT - 1) / TT) * ((E + TE - 1) / TE);
+  const long blocks = (warps + 3) / 4;
+  k_router_logits<TT, TE><<<(unsigned)blocks, 128, 0, st>>>(x, wg, bias, T, d, E, logits);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_route(const moe_shape& s, const uint16_t* x, const uint16_t* wg,
+                         const float* bias, int32_t* topk_idx, float* topk_w, char* ws,
+                         const WsLayout& L, cudaStream_t st) {
+  if (s.T == 0) return cudaSuccess;
+  float* logits = reinterpret_cast<float*>(ws + L.logits);
+  cudaError_t e;
+  if (s.T < 64)
+    e = launch_logits<1, 8>(x, wg, bias, s.T, s.d, s.E, logits, st);
+  else
+    e = launch_logits<4, 8>(x, wg, bias, s.T, s.d, s.E, logits, st);
+  if (e != cudaSuccess) return e;
+  k_router_topk<<<(unsigned)((s.T + 7) / 8), 256, 0, st>>>(logits, s.T, s.E, s.k, topk_idx, topk_w);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,64 @@
+"""Shared helpers of the GPU tests: move seeded inputs to the device, run the layer through the C
+ABI one call at a time, and compare with the oracle."""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+import synth
+
+# Acceptance bars of the layer output y (bf16) against the fp64 oracle.
+TOL_MAX_ABS_BF16 = 2e-2
+TOL_REL_L2_BF16 = 1e-2
+TOL_REL_L2_FP8 = 3e-2
+# gate weights: fp32 softmax over the k chosen logits vs the fp64 renormalised softmax
+TOL_TOPK_W = 2e-6
+
+
+def torch():
+    import torch as _t
+    return _t
+
+
+def bf16_dev(a: np.ndarray):
+    t = torch()
+    return t.from_numpy(np.ascontiguousarray(a).view(np.int16)).to("cuda").view(t.bfloat16)
+
+
+def bf16_host(t) -> np.ndarray:
+    return t.detach().view(torch().int16).cpu().numpy().view(np.uint16)
+
+
+def to_dev(a):
+    return None if a is None else torch().from_numpy(np.ascontiguousarray(a)).to("cuda")
+
+
+def device_weights(cfg, inp: synth.HostInputs) -> dict:
+    """Stacked [E+S, ...] device weights from host-drawn per-expert weights (small configs)."""
+    w13 = np.ascontiguousarray(np.stack([e.w13 for e in inp.experts]))
+    w2 = np.ascontiguousarray(np.stack([e.w2 for e in inp.experts]))
+    out = {"wg": bf16_dev(inp.wg), "bias": to_dev(inp.bias)}
+    if cfg.wdtype == "bf16":
+        out.update(w13=bf16_dev(w13), w2=bf16_dev(w2), s13=None, s2=None)
+    else:
+        out.update(w13=to_dev(w13), w2=to_dev(w2),
+                   s13=to_dev(np.stack([e.s13 for e in inp.experts])),
+                   s2=to_dev(np.stack([e.s2 for e in inp.experts])))
+    return out
+
+
+def rel_l2(a, b) -> float:
+    a, b = np.asarray(a, np.float64), np.asarray(b, np.float64)
+    den = np.linalg.norm(b)
+    return float(np.linalg.norm(a - b) / den) if den > 0 else float(np.linalg.norm(a - b))
+
+
+def assert_y_close(y_gpu_bits, y_ref, wdtype, what="y"):
+    y = oracle.bf16_to_f64(y_gpu_bits)
+    ma = float(np.abs(y - y_ref).max()) if y.size else 0.0
+    rl = rel_l2(y, y_ref) if y.size else 0.0
+    if wdtype == "bf16":
+        assert ma <= TOL_MAX_ABS_BF16 and rl <= TOL_REL_L2_BF16, (what, ma, rl)
+    else:
+        assert rl <= TOL_REL_L2_FP8, (what, ma, rl)
+    return ma, rl

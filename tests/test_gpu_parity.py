@@ -1,0 +1,215 @@
+"""GPU parity: each C-ABI call and the whole layer against the CPU oracle, on seeded inputs.
+
+Routing indices and the permutation must match bit for bit; gate weights within 2e-6; the
+layer output within max-abs 2e-2 and relative-L2 1e-2 (bf16 weights) or relative-L2 3e-2 (FP8
+weights) of the fp64 oracle."""
+import numpy as np
+import pytest
+
+import oracle
+import routed_expert_ffn_moe_gb300 as moe
+import synth
+from gpu_helpers import (TOL_TOPK_W, assert_y_close, bf16_dev, bf16_host, device_weights,
+                         rel_l2, to_dev, torch)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from routed_expert_ffn_moe_gb300 import build
+    build.build()
+    moe.load()
+
+
+def run_layer(cfg, x_dev, w):
+    """The four calls in order; returns the MoeLayer with every intermediate on the device."""
+    layer = moe.MoeLayer(cfg.T, cfg.d, cfg.E, cfg.k, cfg.f, cfg.n_shared, cfg.wdtype, w)
+    layer.forward(x_dev)
+    torch().cuda.synchronize()
+    moe.moe_check_device_status(layer.ws)
+    return layer
+
+
+def check_small(cfg, bias_override=None):
+    inp = synth.host_inputs(cfg)
+    if bias_override is not None:
+        inp.bias = bias_override
+    ref = oracle.moe_layer(cfg, inp)
+    w = device_weights(cfg, inp)
+    layer = run_layer(cfg, bf16_dev(inp.x), w)
+    T, k = cfg.T, cfg.k
+    idx = layer.topk_idx.cpu().numpy()
+    np.testing.assert_array_equal(idx, ref["topk_idx"])
+    np.testing.assert_allclose(layer.topk_w.cpu().numpy(), ref["topk_w64"], rtol=0, atol=TOL_TOPK_W)
+    np.testing.assert_array_equal(layer.expert_offsets.cpu().numpy(), ref["expert_offsets"])
+    np.testing.assert_array_equal(layer.perm_token.cpu().numpy()[: T * k], ref["perm_token"])
+    np.testing.assert_array_equal(layer.inv_slot.cpu().numpy()[: T * k], ref["inv_slot"])
+    yp = layer.y_perm.cpu().numpy()[: cfg.slots]
+    if cfg.slots:
+        assert rel_l2(yp, ref["y_perm"]) <= 1e-2
+    assert_y_close(bf16_host(layer.y), ref["y"], cfg.wdtype)
+    return layer, ref
+
+
+SMALL = [
+    ("tiny", {}),
+    ("tiny", {"wdtype": "fp8"}),
+    ("tiny", {"router": "zipf", "T": 45}),
+    ("tiny", {"n_shared": 0}),
+    ("tiny", {"k": 8}),                        # k = E: every expert
+    ("tiny", {"E": 1, "k": 1}),                # a single expert
+    ("tiny", {"T": 1}),
+    ("tiny", {"T": 37}),                       # ragged: not a multiple of 32 or 4
+    ("tiny", {"T": 0}),
+    ("tiny", {"d": 512, "f": 384, "T": 70, "E": 12, "k": 3}),
+    ("tiny", {"d": 512, "f": 384, "T": 70, "E": 12, "k": 3, "wdtype": "fp8"}),
+    ("tiny", {"T": 300, "E": 40, "k": 5}),     # several permute chunks, uneven segments
+]
+
+
+@pytest.mark.parametrize("name,over", SMALL, ids=[str(o) for _, o in SMALL])
+def test_small_layer_matches_oracle(name, over):
+    check_small(synth.get_config(name, **over))
+
+
+def test_all_tokens_to_one_expert():
+    cfg = synth.get_config("tiny", T=40, k=1, router="zipf")
+    bias = np.zeros(cfg.E, np.float32)
+    bias[5] = 100.0
+    layer, ref = check_small(cfg, bias_override=bias)
+    off = layer.expert_offsets.cpu().numpy()
+    assert off[6] - off[5] == 40 and off[5] == 0
+
+
+def test_permute_direct_random_rows():
+    rng = np.random.default_rng(11)
+    for T, E, k, S in ((1, 1, 1, 1), (33, 7, 7, 0), (257, 64, 6, 1), (1000, 384, 6, 1)):
+        idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+        s = moe.shape_of(T, 256, E, k, 128, S)
+        ws = torch().empty(moe.moe_workspace_size(s), dtype=torch().uint8, device="cuda")
+        ws[:4].zero_()
+        off = torch().empty(E + 2, dtype=torch().int32, device="cuda")
+        perm = torch().empty(T * k, dtype=torch().int32, device="cuda")
+        inv = torch().empty(T * k, dtype=torch().int32, device="cuda")
+        moe.moe_permute(s, to_dev(idx), off, perm, inv, ws)
+        torch().cuda.synchronize()
+        moe.moe_check_device_status(ws)
+        r_off, r_perm, r_inv = oracle.permute(idx, E, S)
+        np.testing.assert_array_equal(off.cpu().numpy(), r_off)
+        np.testing.assert_array_equal(perm.cpu().numpy(), r_perm)
+        np.testing.assert_array_equal(inv.cpu().numpy(), r_inv)
+
+
+def test_permute_flags_out_of_range_expert_without_faulting():
+    T, E, k = 8, 4, 2
+    idx = np.tile(np.array([[0, 1]], np.int32), (T, 1))
+    idx[3, 1] = E          # out of range
+    idx[5, 1] = 0          # repeats the row's first choice
+    s = moe.shape_of(T, 256, E, k, 128, 1)
+    ws = torch().zeros(moe.moe_workspace_size(s), dtype=torch().uint8, device="cuda")
+    off = torch().empty(E + 2, dtype=torch().int32, device="cuda")
+    perm = torch().zeros(T * k, dtype=torch().int32, device="cuda")
+    inv = torch().empty(T * k, dtype=torch().int32, device="cuda")
+    moe.moe_permute(s, to_dev(idx), off, perm, inv, ws)
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_check_device_status(ws)
+    assert ei.value.status == -6
+    inv_h = inv.cpu().numpy().reshape(T, k)
+    assert inv_h[3, 1] == -1 and inv_h[5, 1] == -1
+    moe.moe_check_device_status(ws)  # the check cleared the flag
+
+
+def test_combine_direct():
+    rng = np.random.default_rng(12)
+    T, k, d, S = 50, 4, 384, 1
+    idx = np.stack([rng.permutation(16)[:k] for _ in range(T)]).astype(np.int32)
+    _, _, inv = oracle.permute(idx, 16, S)
+    yp = rng.normal(size=(T * k + S * T, d)).astype(np.float32)
+    w = rng.dirichlet(np.ones(k), size=T).astype(np.float32)
+    s = moe.shape_of(T, d, 16, k, 128, S)
+    ws = torch().zeros(moe.moe_workspace_size(s), dtype=torch().uint8, device="cuda")
+    y = torch().empty(T, d, dtype=torch().bfloat16, device="cuda")
+    moe.moe_combine(s, to_dev(yp), to_dev(inv), to_dev(w), y, ws)
+    torch().cuda.synchronize()
+    ref = oracle.combine(yp.astype(np.float64), inv, w.astype(np.float64), T, k, S)
+    got = oracle.bf16_to_f64(bf16_host(y))
+    # one bf16 rounding of the fp32 sum: |err| <= 2^-8 |y| + fp32 accumulation error
+    assert np.all(np.abs(got - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-5)
+
+
+def test_layer_is_deterministic():
+    cfg = synth.get_config("tiny", T=200, E=16, k=4, d=512, f=256)
+    inp = synth.host_inputs(cfg)
+    w = device_weights(cfg, inp)
+    x = bf16_dev(inp.x)
+    a = run_layer(cfg, x, w)
+    ya, ia, pa = a.y.clone(), a.topk_idx.clone(), a.perm_token.clone()
+    b = run_layer(cfg, x, w)
+    assert torch().equal(ya.view(torch().int16), b.y.view(torch().int16))
+    assert torch().equal(ia, b.topk_idx) and torch().equal(pa, b.perm_token)
+
+
+# ---- full-size workloads --------------------------------------------------------------------
+
+def test_device_generator_matches_host_generator():
+    cfg = synth.get_config("v3_decode")
+    t = torch()
+    n = 1 << 16
+    buf = t.empty(n, dtype=t.bfloat16, device="cuda")
+    for stream, sigma, off in ((synth.STREAM_X, 1.0, 12345), (synth.STREAM_W13, 0.02, 3 << 30)):
+        synth._dev_normal(buf, cfg.seed, stream, sigma, offset=off)
+        np.testing.assert_array_equal(bf16_host(buf), synth.normal_bf16(cfg.seed, stream, sigma, off, n))
+    w = synth.normal_bf16(0, 4, 0.02, 777, 256 * 384).reshape(256, 384)
+    q_h, s_h = synth.quantize_e4m3(w)
+    q = t.empty(256, 384, dtype=t.uint8, device="cuda")
+    s = t.empty(2, 3, dtype=t.float32, device="cuda")
+    import ctypes
+    rc = synth.lib().synth_quant_e4m3_device(bf16_dev(w).data_ptr(), q.data_ptr(), s.data_ptr(),
+                                             256, 384, ctypes.c_void_p(t.cuda.current_stream().cuda_stream))
+    assert rc == 0
+    np.testing.assert_array_equal(q.cpu().numpy(), q_h)
+    np.testing.assert_array_equal(s.cpu().numpy(), s_h)
+
+
+def sample_tokens(cfg, idx, n_even=6):
+    """Evenly spaced tokens plus tokens of the hottest and the coldest non-empty experts."""
+    T = cfg.T
+    picks = set(np.linspace(0, T - 1, min(n_even, T)).astype(int).tolist())
+    counts = np.bincount(idx.ravel(), minlength=cfg.E)
+    hot = int(np.argmax(counts))
+    cold = int(np.argmin(np.where(counts > 0, counts, 1 << 30)))
+    for e in (hot, cold):
+        rows = np.nonzero((idx == e).any(1))[0]
+        picks.update(rows[:2].tolist())
+    return sorted(picks)
+
+
+FULL = ["v3_decode", "v4pro_decode", "skewed_prefill", "sweep_fp8_T1", "sweep_fp8_T64",
+        "sweep_fp8_T1024"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_routing_exact_and_sampled_outputs(name):
+    cfg = synth.get_config(name)
+    dev = synth.device_inputs(cfg)
+    w = {k: dev[k] for k in ("wg", "bias", "w13", "w2", "s13", "s2")}
+    layer = run_layer(cfg, dev["x"], w)
+    idx = layer.topk_idx.cpu().numpy()
+    # routing and permutation: every token, bit for bit
+    x_h = synth.host_x(cfg)
+    logits = oracle.router_logits(x_h, synth.host_wg(cfg), synth.host_bias(cfg))
+    r_idx, _, r_w64 = oracle.route(logits, cfg.k)
+    np.testing.assert_array_equal(idx, r_idx)
+    np.testing.assert_allclose(layer.topk_w.cpu().numpy(), r_w64, rtol=0, atol=TOL_TOPK_W)
+    r_off, r_perm, r_inv = oracle.permute(r_idx, cfg.E, cfg.n_shared)
+    np.testing.assert_array_equal(layer.expert_offsets.cpu().numpy(), r_off)
+    np.testing.assert_array_equal(layer.perm_token.cpu().numpy(), r_perm)
+    np.testing.assert_array_equal(layer.inv_slot.cpu().numpy(), r_inv)
+    # outputs of sampled tokens, each straight from the definition
+    toks = sample_tokens(cfg, r_idx)
+    experts = {int(e): synth.host_expert(cfg, int(e)) for e in np.unique(r_idx[toks])}
+    shared = synth.host_expert(cfg, cfg.E) if cfg.n_shared else None
+    y_ref = oracle.token_outputs(x_h[toks], r_idx[toks], r_w64[toks], experts, shared, cfg.wdtype)
+    y_gpu = bf16_host(layer.y)[toks]
+    assert_y_close(y_gpu, y_ref, cfg.wdtype, what=name)
