@@ -137,6 +137,19 @@ MOE_API moe_status moe_combine(const moe_shape* shape, const float* y_perm, cons
  * MOE_ERR_CUDA if the read itself fails). */
 MOE_API moe_status moe_check_device_status(void* ws, void* stream);
 
+/* Phase timing for benchmarks and profilers (no counterpart on the pages).
+ * moe_profile_enable(1) starts a session (and clears the previous one): from then on every
+ * moe_expert_ffn call records three CUDA events on its stream -- before its gate/up kernels,
+ * between them and its down kernels, and after -- and every call counts the kernels it
+ * launches. Events are created by the library while a session is on (host-side objects; no
+ * device memory is allocated). moe_profile_enable(0) stops recording.
+ * moe_profile_read waits for the recorded events and returns the summed device milliseconds of
+ * the gate/up and down phases over the session, the number of moe_expert_ffn calls timed, and
+ * the number of kernels launched by all four calls; any output pointer may be NULL. */
+MOE_API moe_status moe_profile_enable(int on);
+MOE_API moe_status moe_profile_read(double* ms_gate_up, double* ms_down, int64_t* ffn_calls,
+                                    int64_t* kernel_launches);
+
 /* Message for the last non-OK status returned on the calling thread (thread-local storage;
  * valid until the next call on that thread). */
 MOE_API const char* moe_last_error_string(void);

@@ -12,15 +12,16 @@ import os
 
 __all__ = ["MoeError", "MoeShape", "MOE_W_BF16", "MOE_W_FP8_E4M3_B128", "load", "lib_path",
            "moe_workspace_size", "moe_route", "moe_permute", "moe_expert_ffn", "moe_combine",
-           "moe_check_device_status", "moe_last_error_string", "shape_of", "MoeLayer",
-           "EXPORTED"]
+           "moe_check_device_status", "moe_profile_enable", "moe_profile_read",
+           "moe_last_error_string", "shape_of", "MoeLayer", "EXPORTED"]
 
 MOE_W_BF16, MOE_W_FP8_E4M3_B128 = 0, 1
 STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED",
           -3: "MOE_ERR_WORKSPACE", -4: "MOE_ERR_CUDA", -5: "MOE_ERR_DEVICE_TIMEOUT",
           -6: "MOE_ERR_DEVICE_BOUNDS"}
 EXPORTED = ("moe_workspace_size", "moe_route", "moe_permute", "moe_expert_ffn", "moe_combine",
-            "moe_check_device_status", "moe_last_error_string")
+            "moe_check_device_status", "moe_profile_enable", "moe_profile_read",
+            "moe_last_error_string")
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 
@@ -68,6 +69,11 @@ def load():
     L.moe_combine.argtypes = [shp, vp, vp, vp, vp, vp, sz, vp]
     L.moe_check_device_status.restype = i32
     L.moe_check_device_status.argtypes = [vp, vp]
+    L.moe_profile_enable.restype = i32
+    L.moe_profile_enable.argtypes = [i32]
+    L.moe_profile_read.restype = i32
+    L.moe_profile_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
+                                   ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]
     L.moe_last_error_string.restype = ctypes.c_char_p
     L.moe_last_error_string.argtypes = []
     _lib = L
@@ -148,6 +154,19 @@ def moe_combine(shape, y_perm, inv_slot, topk_w, y, ws, stream=None, ws_bytes=No
 
 def moe_check_device_status(ws, stream=None):
     _check(load().moe_check_device_status(_ptr(ws), _stream(stream)), "moe_check_device_status")
+
+
+def moe_profile_enable(on: bool = True):
+    _check(load().moe_profile_enable(1 if on else 0), "moe_profile_enable")
+
+
+def moe_profile_read() -> dict:
+    up, dn = ctypes.c_double(), ctypes.c_double()
+    calls, launches = ctypes.c_int64(), ctypes.c_int64()
+    _check(load().moe_profile_read(ctypes.byref(up), ctypes.byref(dn), ctypes.byref(calls),
+                                   ctypes.byref(launches)), "moe_profile_read")
+    return {"ms_gate_up": up.value, "ms_down": dn.value, "ffn_calls": calls.value,
+            "kernel_launches": launches.value}
 
 
 class MoeLayer:

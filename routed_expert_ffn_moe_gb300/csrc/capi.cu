@@ -2,7 +2,9 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
+#include <vector>
 
 #include "internal.h"
 
@@ -59,6 +61,39 @@ moe_status check_ws(const moe_shape* s, const void* ws, size_t ws_bytes, WsLayou
   return MOE_OK;
 }
 
+}  // namespace
+
+// ---- profiling session ------------------------------------------------------------------
+namespace {
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<PhaseEvents> g_prof_events;
+int64_t g_prof_calls = 0;
+std::atomic<int64_t> g_launches{0};
+}  // namespace
+
+void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+PhaseEvents profile_phase_events() {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  PhaseEvents ev;
+  if (!g_prof_on) return ev;
+  if (cudaEventCreate(&ev.begin) != cudaSuccess || cudaEventCreate(&ev.mid) != cudaSuccess ||
+      cudaEventCreate(&ev.end) != cudaSuccess)
+    return PhaseEvents{};
+  g_prof_events.push_back(ev);
+  return ev;
+}
+
+namespace {
+void destroy_events() {
+  for (auto& ev : g_prof_events) {
+    cudaEventDestroy(ev.begin);
+    cudaEventDestroy(ev.mid);
+    cudaEventDestroy(ev.end);
+  }
+  g_prof_events.clear();
+}
 }  // namespace
 
 int num_sms() {
@@ -186,6 +221,37 @@ moe_status moe_check_device_status(void* ws, void* stream) {
   if (code == MOE_ERR_DEVICE_TIMEOUT)
     return fail(MOE_ERR_DEVICE_TIMEOUT, "a bounded device wait gave up");
   if (code != 0) return fail(MOE_ERR_CUDA, "unknown device status %d", code);
+  return MOE_OK;
+}
+
+moe_status moe_profile_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (on) {
+    destroy_events();
+    g_prof_calls = 0;
+    g_launches.store(0);
+  }
+  g_prof_on = on != 0;
+  return MOE_OK;
+}
+
+moe_status moe_profile_read(double* ms_gate_up, double* ms_down, int64_t* ffn_calls,
+                            int64_t* kernel_launches) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  double up = 0.0, dn = 0.0;
+  for (auto& ev : g_prof_events) {
+    float a = 0.f, b = 0.f;
+    cudaError_t e = cudaEventSynchronize(ev.end);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&a, ev.begin, ev.mid);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&b, ev.mid, ev.end);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_profile_read");
+    up += a;
+    dn += b;
+  }
+  if (ms_gate_up) *ms_gate_up = up;
+  if (ms_down) *ms_down = dn;
+  if (ffn_calls) *ffn_calls = (int64_t)g_prof_events.size();
+  if (kernel_launches) *kernel_launches = g_launches.load();
   return MOE_OK;
 }
 

@@ -48,6 +48,7 @@ cudaError_t launch_combine(const moe_shape& s, const float* y_perm, const int32_
   if (n == 0) return cudaSuccess;
   k_combine<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(y_perm, inv_slot, topk_w, s.T, s.k, s.d,
                                                          s.n_shared, y, status);
+  count_launches(1);
   return cudaGetLastError();
 }
 

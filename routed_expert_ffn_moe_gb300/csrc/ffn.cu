@@ -63,9 +63,12 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32
   const int group = gemv_group_tokens();
   const int items_up = gemv_items_per_group(true, s.d, s.f);
   const int items_dn = gemv_items_per_group(false, s.d, s.f);
+  const PhaseEvents ev = profile_phase_events();
   k_ffn_plan<<<1, 1024, 0, st>>>(offsets, s.E, s.n_shared, items_up, items_dn, group, plan, stride);
+  count_launches(1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (ev.begin) cudaEventRecord(ev.begin, st);
   // Upper bound on the number of groups: every slot in its own group plus one partial group
   // per expert.
   const long slots = (long)s.T * s.k + (long)s.n_shared * s.T;
@@ -74,8 +77,11 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32
   e = launch_gemv(a, plan + kPlanGemvUp * stride, plan + kPlanGemvDown * stride, true,
                   (int)(max_up < (1L << 30) ? max_up : (1L << 30)), st);
   if (e != cudaSuccess) return e;
-  return launch_gemv(a, plan + kPlanGemvUp * stride, plan + kPlanGemvDown * stride, false,
-                     (int)(max_dn < (1L << 30) ? max_dn : (1L << 30)), st);
+  if (ev.mid) cudaEventRecord(ev.mid, st);
+  e = launch_gemv(a, plan + kPlanGemvUp * stride, plan + kPlanGemvDown * stride, false,
+                  (int)(max_dn < (1L << 30) ? max_dn : (1L << 30)), st);
+  if (ev.end) cudaEventRecord(ev.end, st);
+  return e;
 }
 
 }  // namespace moe

@@ -184,6 +184,7 @@ cudaError_t launch_one(const FfnArgs& a, const int32_t* prefix, int grid, cudaSt
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   k_gemv<FP8, GATEUP><<<grid, 32 * kWarps, smem, st>>>(a, prefix);
+  count_launches(1);
   return cudaGetLastError();
 }
 

@@ -64,6 +64,13 @@ cudaError_t launch_combine(const moe_shape& s, const float* y_perm, const int32_
 
 int num_sms();
 
+// profiling hooks (capi.cu): kernel launch counter and per-call phase events
+void count_launches(int n);
+struct PhaseEvents {
+  cudaEvent_t begin = nullptr, mid = nullptr, end = nullptr;
+};
+PhaseEvents profile_phase_events();  // all null unless a profiling session is on
+
 // ---- device helpers ------------------------------------------------------------------------
 #ifdef __CUDACC__
 __device__ __forceinline__ void record_error(int* status, int code) {

@@ -124,6 +124,7 @@ cudaError_t launch_permute(const moe_shape& s, const int32_t* topk_idx, int32_t*
     if (e != cudaSuccess) return e;
   }
   k_perm_scan<<<1, 1024, 0, st>>>(hist, s.E, nchunk, s.T, s.k, s.n_shared, base, offsets);
+  count_launches(blocks ? 3 : 1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !blocks) return e;
   k_perm_scatter<<<blocks, 32 * kWarpsPerBlock, smem, st>>>(topk_idx, s.T, s.E, s.k, nchunk, base,

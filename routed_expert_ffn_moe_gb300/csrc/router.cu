@@ -150,6 +150,7 @@ cudaError_t launch_route(const moe_shape& s, const uint16_t* x, const uint16_t* 
     e = launch_logits<4, 8>(x, wg, bias, s.T, s.d, s.E, logits, st);
   if (e != cudaSuccess) return e;
   k_router_topk<<<(unsigned)((s.T + 7) / 8), 256, 0, st>>>(logits, s.T, s.E, s.k, topk_idx, topk_w);
+  count_launches(2);
   return cudaGetLastError();
 }
 

@@ -53,12 +53,25 @@ def rel_l2(a, b) -> float:
     return float(np.linalg.norm(a - b) / den) if den > 0 else float(np.linalg.norm(a - b))
 
 
+def bf16_half_ulp(v):
+    """Half the spacing of bf16 numbers at |v|: the largest error of rounding v to bf16."""
+    a = np.maximum(np.abs(np.asarray(v, np.float64)), 2.0 ** -126)
+    return 2.0 ** (np.floor(np.log2(a)) - 8)
+
+
 def assert_y_close(y_gpu_bits, y_ref, wdtype, what="y"):
+    """The layer output is bf16, so each element carries the format's own rounding on top of
+    the computation error: the max-abs bar is 2e-2 for the computation plus that half-ulp
+    (|y| reaches ~10 at the V3 shapes, where a bf16 half-ulp is 0.031)."""
     y = oracle.bf16_to_f64(y_gpu_bits)
-    ma = float(np.abs(y - y_ref).max()) if y.size else 0.0
-    rl = rel_l2(y, y_ref) if y.size else 0.0
+    if not y.size:
+        return 0.0, 0.0
+    err = np.abs(y - y_ref)
+    ma = float(err.max())
+    excess = float((err - bf16_half_ulp(y_ref)).max())
+    rl = rel_l2(y, y_ref)
     if wdtype == "bf16":
-        assert ma <= TOL_MAX_ABS_BF16 and rl <= TOL_REL_L2_BF16, (what, ma, rl)
+        assert excess <= TOL_MAX_ABS_BF16 and rl <= TOL_REL_L2_BF16, (what, ma, excess, rl)
     else:
         assert rl <= TOL_REL_L2_FP8, (what, ma, rl)
     return ma, rl
