@@ -233,8 +233,8 @@ def main():
     over = {k: v for k, v in (("T", args.T), ("E", args.E)) if v is not None}
     cfg = synth.get_config(args.config, **over)
     if over:
-        cfg = synth.get_config(args.config, name=cfg.name + "".join(f"_{k}{v}" for k, v in over.items()),
-                               **over)
+        import dataclasses
+        cfg = dataclasses.replace(cfg, name=cfg.name + "".join(f"_{k}{v}" for k, v in over.items()))
     if args.impl == "reference":
         run_reference(args, cfg, rank)
         return
