@@ -1,45 +1,73 @@
 // Expert FFN orchestration: a device-side work plan from the expert segment sizes, then the
-// gate/up pass and the down pass.
+// gate/up pass and the down pass, each split between the tensor-core grouped GEMM (experts with
+// at least tc_min tokens) and the weight-streaming GEMV (experts with fewer).
 //
 // Expert segment sizes exist only on the device (they come from the router), so the host never
 // waits for them: a one-block plan kernel turns expert_offsets into per-expert prefix sums of
-// work items, and the persistent FFN kernels walk those items.
+// work items for each kernel, and the persistent FFN kernels walk those lists.
+#include <climits>
+
 #include "ffn.h"
 
 namespace moe {
 namespace {
 
-// plan[kPlanGemvUp][e] / plan[kPlanGemvDown][e]: exclusive prefix over experts of the number of
-// weight-streaming work items; entry E1 is the total.
-__global__ void __launch_bounds__(1024) k_ffn_plan(const int32_t* __restrict__ offsets, int E,
-                                                   int n_shared, int items_up, int items_down,
-                                                   int group, int32_t* __restrict__ plan,
-                                                   int plan_stride) {
-  const int E1 = E + n_shared;
-  int run_up = 0, run_dn = 0;
+struct PlanArgs {
+  int E, n_shared, tc_min;
+  int group, items_up, items_dn;   // weight-streaming: tokens per item, items per group
+  int nt_up, nt_dn, mt_up, mt_dn;  // tensor-core: tokens per tile, weight tiles per expert
+  int stride;
+};
+
+// plan[row][e]: exclusive prefix over experts of the work of each kernel; entry E1 = total.
+__global__ void __launch_bounds__(1024) k_ffn_plan(const int32_t* __restrict__ offsets,
+                                                   PlanArgs a, int32_t* __restrict__ plan) {
+  const int E1 = a.E + a.n_shared;
+  int run[4] = {0, 0, 0, 0};
   for (int b = 0; b < E1; b += blockDim.x) {
     const int e = b + threadIdx.x;
-    int n_up = 0, n_dn = 0;
+    int n[4] = {0, 0, 0, 0};
     if (e < E1) {
       const int cnt = offsets[e + 1] - offsets[e];
-      const int groups = cnt > 0 ? (cnt + group - 1) / group : 0;
-      n_up = groups * items_up;
-      n_dn = groups * items_down;
+      if (cnt >= a.tc_min) {
+        n[kPlanTcUp] = (cnt + a.nt_up - 1) / a.nt_up * a.mt_up;
+        n[kPlanTcDown] = (cnt + a.nt_dn - 1) / a.nt_dn * a.mt_dn;
+      } else if (cnt > 0) {
+        const int groups = (cnt + a.group - 1) / a.group;
+        n[kPlanGemvUp] = groups * a.items_up;
+        n[kPlanGemvDown] = groups * a.items_dn;
+      }
     }
-    int tot_up, tot_dn;
-    const int p_up = block_exclusive_scan(n_up, &tot_up);
-    const int p_dn = block_exclusive_scan(n_dn, &tot_dn);
-    if (e < E1) {
-      plan[kPlanGemvUp * plan_stride + e] = run_up + p_up;
-      plan[kPlanGemvDown * plan_stride + e] = run_dn + p_dn;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      int tot;
+      const int pre = block_exclusive_scan(n[r], &tot);
+      if (e < E1) plan[r * a.stride + e] = run[r] + pre;
+      run[r] += tot;
     }
-    run_up += tot_up;
-    run_dn += tot_dn;
   }
-  if (threadIdx.x == 0) {
-    plan[kPlanGemvUp * plan_stride + E1] = run_up;
-    plan[kPlanGemvDown * plan_stride + E1] = run_dn;
+  if (threadIdx.x == 0)
+    for (int r = 0; r < 4; ++r) plan[r * a.stride + E1] = run[r];
+}
+
+// x_perm[s] = x[perm_token[s]] for every routed slot: the tensor-core path's token tiles are
+// contiguous rows for TMA.
+__global__ void __launch_bounds__(256) k_gather_rows(const uint16_t* __restrict__ x,
+                                                     const int32_t* __restrict__ perm_token,
+                                                     int T, long routed, int d,
+                                                     uint16_t* __restrict__ x_perm, int* status) {
+  const int d8 = d >> 3;
+  const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= routed * d8) return;
+  const long s = i / d8;
+  const int c = (int)(i - s * d8);
+  int t = __ldg(perm_token + s);
+  if (t < 0 || t >= T) {
+    record_error(status, MOE_ERR_DEVICE_BOUNDS);
+    t = 0;
   }
+  reinterpret_cast<uint4*>(x_perm + s * d)[c] =
+      __ldg(reinterpret_cast<const uint4*>(x + (long)t * d) + c);
 }
 
 }  // namespace
@@ -59,27 +87,54 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32
   a.y_perm = y_perm;
   a.status = reinterpret_cast<int*>(ws + L.status);
   int32_t* plan = reinterpret_cast<int32_t*>(ws + L.plan);
-  const int stride = s.E + 2;
-  const int group = gemv_group_tokens();
-  const int items_up = gemv_items_per_group(true, s.d, s.f);
-  const int items_dn = gemv_items_per_group(false, s.d, s.f);
+
+  // Tensor cores take every bf16 expert; FP8 experts use the weight-streaming path.
+  const bool use_tc = s.wdtype == MOE_W_BF16;
+  const long routed = (long)s.T * s.k;
+  const bool decode = routed <= 32L * s.E;  // at most ~32 tokens per routed expert on average
+  PlanArgs pa{};
+  pa.E = s.E; pa.n_shared = s.n_shared;
+  pa.tc_min = use_tc ? 1 : INT_MAX;
+  pa.group = gemv_group_tokens();
+  pa.items_up = gemv_items_per_group(true, s.d, s.f);
+  pa.items_dn = gemv_items_per_group(false, s.d, s.f);
+  pa.nt_up = tc_tile_tokens(true, decode);
+  pa.nt_dn = tc_tile_tokens(false, decode);
+  pa.mt_up = s.f / 128;
+  pa.mt_dn = s.d / 128;
+  pa.stride = s.E + 2;
+  const int stride = pa.stride;
+
   const PhaseEvents ev = profile_phase_events();
-  k_ffn_plan<<<1, 1024, 0, st>>>(offsets, s.E, s.n_shared, items_up, items_dn, group, plan, stride);
+  k_ffn_plan<<<1, 1024, 0, st>>>(offsets, pa, plan);
   count_launches(1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (use_tc && routed > 0) {
+    const long n = routed * (s.d / 8);
+    k_gather_rows<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(x, perm_token, s.T, routed, s.d,
+                                                                a.x_perm, a.status);
+    count_launches(1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   if (ev.begin) cudaEventRecord(ev.begin, st);
-  // Upper bound on the number of groups: every slot in its own group plus one partial group
-  // per expert.
-  const long slots = (long)s.T * s.k + (long)s.n_shared * s.T;
-  const long max_groups = (slots + group - 1) / group + s.E + s.n_shared;
-  const long max_up = max_groups * items_up, max_dn = max_groups * items_dn;
-  e = launch_gemv(a, plan + kPlanGemvUp * stride, plan + kPlanGemvDown * stride, true,
-                  (int)(max_up < (1L << 30) ? max_up : (1L << 30)), st);
+
+  // Upper bound on the weight-streaming work: every slot in its own group plus one partial
+  // group per expert (the device-side totals are usually far smaller).
+  const long slots = routed + (long)s.n_shared * s.T;
+  const long max_groups = (slots + pa.group - 1) / pa.group + s.E + s.n_shared;
+  const auto cap = [](long v) { return (int)(v < (1L << 30) ? v : (1L << 30)); };
+  const int max_up = use_tc ? 0 : cap(max_groups * pa.items_up);
+  const int max_dn = use_tc ? 0 : cap(max_groups * pa.items_dn);
+
+  if (use_tc) e = launch_tc(a, plan + kPlanTcUp * stride, true, decode, st);
+  if (e == cudaSuccess)
+    e = launch_gemv(a, plan + kPlanGemvUp * stride, plan + kPlanGemvDown * stride, true, max_up, st);
   if (e != cudaSuccess) return e;
   if (ev.mid) cudaEventRecord(ev.mid, st);
-  e = launch_gemv(a, plan + kPlanGemvUp * stride, plan + kPlanGemvDown * stride, false,
-                  (int)(max_dn < (1L << 30) ? max_dn : (1L << 30)), st);
+  if (use_tc) e = launch_tc(a, plan + kPlanTcDown * stride, false, decode, st);
+  if (e == cudaSuccess)
+    e = launch_gemv(a, plan + kPlanGemvUp * stride, plan + kPlanGemvDown * stride, false, max_dn, st);
   if (ev.end) cudaEventRecord(ev.end, st);
   return e;
 }

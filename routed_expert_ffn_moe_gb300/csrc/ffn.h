@@ -26,4 +26,9 @@ int gemv_group_tokens();
 cudaError_t launch_gemv(const FfnArgs& a, const int32_t* prefix_up, const int32_t* prefix_down,
                         bool gateup, int max_items, cudaStream_t st);
 
+// tensor-core path (ffn_tc.cu): bf16 weights
+int tc_tile_tokens(bool gateup, bool decode);
+cudaError_t launch_tc(const FfnArgs& a, const int32_t* prefix, bool gateup, bool decode,
+                      cudaStream_t st);
+
 }  // namespace moe

@@ -1,0 +1,382 @@
+// Expert FFN, tensor-core path: a persistent grouped GEMM on tcgen05 with TMEM accumulators,
+// fed by TMA, for bf16 expert weights.
+//
+// The pages: once an expert receives enough tokens its weights are reused across rows and the
+// work becomes a real matrix multiply ("第 6 章 超節點", 6.1.3 and 6.3.2: batch reuse moves the
+// limit from weight reads to math; "DeepSeek V3/R1 Inference Efficiency (1)": DeepGEMM's
+// grouped expert GEMMs). Y = [SiLU(X W_g) (.) (X W_u)] W_d ("第 6 章 超節點", 6.2.2) is computed in
+// two passes, gate/up (with SiLU x up fused into the epilogue) and down.
+//
+// Shape of one tile (swap-AB): M = 128 rows of one expert's weight matrix (output features),
+// N = the expert's tokens in this tile (16..NT, a multiple of 16), K streamed in 64-wide
+// stages. Weights are the M side so that a decode expert with a handful of tokens still reads
+// each weight byte exactly once per call, at full tile width. Gate/up tiles issue two MMAs per
+// K step (gate rows and up rows of the same output features) into two accumulators.
+//
+// Warp roles (6 warps, one CTA per SM, persistent over a device-built tile list):
+//   warp 0     TMA producer (one thread): weight tile + token tile per stage
+//   warp 1     TMEM owner and MMA issuer (one thread)
+//   warps 2-5  epilogue: TMEM -> registers -> SiLU(gate)*up -> bf16 h, or fp32 expert output
+// Accumulators are double-buffered in TMEM so the epilogue of tile i overlaps the mainloop of
+// tile i+1. Every wait is bounded: a wait that gives up records MOE_ERR_DEVICE_TIMEOUT and the
+// CTA winds down, frees its TMEM and exits.
+#include "ffn.h"
+#include "sm100_ptx.cuh"
+
+namespace moe {
+namespace {
+
+using namespace ptx;
+
+constexpr int kBM = 128;               // weight rows per tile (MMA M)
+constexpr int kBK = 64;                // K per stage: one 128-byte swizzle row of bf16
+constexpr int kBoxRows = 16;           // token rows per TMA box
+constexpr uint32_t kATileBytes = kBM * kBK * 2;     // 16 KB
+constexpr uint32_t kBBoxBytes = kBoxRows * kBK * 2; // 2 KB
+constexpr uint64_t kWaitLimitNs = 2000000000ull;    // 2 s
+constexpr int kThreads = 192;
+
+struct TcParams {
+  int T, k, E, n_shared;
+  int K;                 // reduction width: d (gate/up) or f (down)
+  int mtiles;            // 128-row weight tiles per expert
+  int rows_per_expert;   // rows of the weight map per expert: 2f (gate/up) or d (down)
+  int f, d;
+  const int32_t* offsets;
+  const int32_t* prefix;  // [E1 + 1] tile prefix over experts
+  uint16_t* h;
+  float* y_perm;
+  int* status;
+};
+
+struct Tile {
+  int e, mt, slot0, ntok, brow0;
+  bool shared;
+};
+
+// Token rows of the gate/up pass come from the gathered rows (routed experts) or straight from
+// x (the shared expert, whose slot T*k + t is token t); the down pass reads h in slot order.
+template <bool GATEUP, int NT>
+__device__ __forceinline__ void decode_tile(const TcParams& p, int tile, Tile& t) {
+  const int E1 = p.E + p.n_shared;
+  int lo = 0, hi = E1;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(p.prefix + mid) <= tile) lo = mid; else hi = mid;
+  }
+  const int e = lo;
+  const int seg0 = __ldg(p.offsets + e);
+  const int cnt = __ldg(p.offsets + e + 1) - seg0;
+  const int ntn = (cnt + NT - 1) / NT;
+  const int local = tile - __ldg(p.prefix + e);
+  const int mt = local / ntn, nt = local - mt * ntn;
+  t.e = e;
+  t.mt = mt;
+  t.slot0 = seg0 + nt * NT;
+  t.ntok = min(NT, cnt - nt * NT);
+  t.shared = (e == p.E);
+  t.brow0 = (GATEUP && t.shared) ? t.slot0 - p.T * p.k : t.slot0;
+}
+
+// Bounded wait on an mbarrier phase. Returns false (after recording a timeout) if it gave up
+// or if another role already gave up.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                         int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > kWaitLimitNs) {
+        record_error(status, MOE_ERR_DEVICE_TIMEOUT);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// Bounded wait that ignores the abort flag: used to drain this CTA's own copies in flight
+// before it exits.
+__device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity, int* status) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      record_error(status, MOE_ERR_DEVICE_TIMEOUT);
+      return;
+    }
+  }
+}
+
+template <bool GATEUP, int NT, int STAGES>
+struct Smem {
+  static constexpr int kA = GATEUP ? 2 : 1;  // weight tiles per stage
+  static constexpr uint32_t kStageBytes = kA * kATileBytes + (uint32_t)NT * kBK * 2;
+  static constexpr uint32_t kTilesBytes = STAGES * kStageBytes;
+  static constexpr uint32_t kBarBytes = 8 * (2 * STAGES + 4) + 16;
+  static constexpr uint32_t kTotal = kTilesBytes + kBarBytes + 1024;  // + alignment slack
+  static constexpr uint32_t kAccCols = GATEUP ? 2 * NT : NT;          // per accumulator buffer
+  static constexpr uint32_t kTmemCols = 2 * kAccCols;                 // double-buffered
+};
+
+template <bool GATEUP, int NT, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_tc_ffn(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b0,
+             const __grid_constant__ CUtensorMap tm_b1, const TcParams p) {
+  using S = Smem<GATEUP, NT, STAGES>;
+  static_assert(S::kTmemCols <= 512 && (S::kTmemCols & (S::kTmemCols - 1)) == 0, "TMEM cols");
+  static_assert(NT % 16 == 0 && NT >= 16 && NT <= 256, "MMA N");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kTilesBytes);
+  uint64_t* empty = full + STAGES;
+  uint64_t* acc_full = empty + STAGES;
+  uint64_t* acc_empty = acc_full + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E1 = p.E + p.n_shared;
+  const int total = __ldg(p.prefix + E1);
+  const int kblocks = p.K / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);  // one arrival per epilogue warp
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tm_w);
+    prefetch_tmap(&tm_b0);
+    prefetch_tmap(&tm_b1);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, S::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();  // weights: streamed once per call
+      const uint64_t pol_b = policy_evict_last();   // token rows: reused by every weight tile
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        Tile t;
+        decode_tile<GATEUP, NT>(p, tile, t);
+        const int nbox = (t.ntok + kBoxRows - 1) / kBoxRows;
+        const uint32_t bytes = S::kA * kATileBytes + (uint32_t)nbox * kBBoxBytes;
+        const int wrow = t.e * p.rows_per_expert + t.mt * kBM;
+        const CUtensorMap* bmap = (GATEUP && t.shared) ? &tm_b1 : &tm_b0;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!wait_bar(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+          uint8_t* st = smem + stage * S::kStageBytes;
+          mbar_arrive_expect_tx(&full[stage], bytes);
+          tma_load_2d(st, &tm_w, &full[stage], kb * kBK, wrow, pol_w);
+          if (GATEUP) tma_load_2d(st + kATileBytes, &tm_w, &full[stage], kb * kBK, wrow + p.f, pol_w);
+          uint8_t* bt = st + S::kA * kATileBytes;
+          for (int i = 0; i < nbox; ++i)
+            tma_load_2d(bt + i * kBBoxBytes, bmap, &full[stage], kb * kBK, t.brow0 + i * kBoxRows,
+                        pol_b);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      // Every load this thread issued has landed before the CTA may exit.
+      for (int s = 0; s < STAGES; ++s) {
+        const uint32_t issued_phase = (s < (int)stage) ? phase : (phase ^ 1u);
+        drain_bar(&full[s], issued_phase, p.status);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      uint32_t acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        Tile t;
+        decode_tile<GATEUP, NT>(p, tile, t);
+        const int npad = (t.ntok + 15) & ~15;
+        const uint32_t idesc = idesc_bf16(kBM, npad);
+        if (!wait_bar(&acc_empty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t d0 = tmem_base + acc * S::kAccCols;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!wait_bar(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t st = smem_u32(smem + stage * S::kStageBytes);
+          const uint64_t da = sw128_desc(st);
+          const uint64_t du = sw128_desc(st + kATileBytes);
+          const uint64_t db = sw128_desc(st + S::kA * kATileBytes);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint32_t accum = (kb | kk) ? 1u : 0u;
+            mma_bf16_ss(d0, da + 2 * kk, db + 2 * kk, idesc, accum);
+            if (GATEUP) mma_bf16_ss(d0 + NT, du + 2 * kk, db + 2 * kk, idesc, accum);
+          }
+          mma_commit(&empty[stage]);  // frees the stage once these MMAs have read it
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        mma_commit(&acc_full[acc]);   // accumulator ready for the epilogue
+        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int q = warp & 3;                 // TMEM lane quadrant this warp may access
+    const int row = q * 32 + lane;          // weight row within the tile
+    uint32_t acc = 0, acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      Tile t;
+      decode_tile<GATEUP, NT>(p, tile, t);
+      const int npad = (t.ntok + 15) & ~15;
+      if (!wait_bar(&acc_full[acc], acc_phase, abort_flag, p.status)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * S::kAccCols;
+      const int orow = t.mt * kBM + row;    // output feature
+      for (int c0 = 0; c0 < npad; c0 += 16) {
+        uint32_t g[16];
+        tmem_ld16(tbase + c0, g);
+        if (GATEUP) {
+          uint32_t u[16];
+          tmem_ld16(tbase + NT + c0, u);
+          tmem_ld_wait2(g, u);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int n = c0 + j;
+            if (n < t.ntok) {
+              const float gv = __uint_as_float(g[j]), uv = __uint_as_float(u[j]);
+              const float silu = gv / (1.0f + __expf(-gv));
+              p.h[(size_t)(t.slot0 + n) * p.f + orow] = f32_to_bf16_rn(silu * uv);
+            }
+          }
+        } else {
+          tmem_ld_wait(g);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int n = c0 + j;
+            if (n < t.ntok) p.y_perm[(size_t)(t.slot0 + n) * p.d + orow] = __uint_as_float(g[j]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, S::kTmemCols);
+  }
+}
+
+// ---- host side -------------------------------------------------------------------------------
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// Row-major [rows, cols] bf16 matrix, box of box_rows x 64 columns, 128-byte swizzle.
+cudaError_t encode_bf16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                           uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <bool GATEUP, int NT, int STAGES>
+cudaError_t launch_variant(const CUtensorMap& w, const CUtensorMap& b0, const CUtensorMap& b1,
+                           const TcParams& p, cudaStream_t st) {
+  using S = Smem<GATEUP, NT, STAGES>;
+  static_assert(S::kTotal <= 227 * 1024, "shared memory");
+  auto kern = k_tc_ffn<GATEUP, NT, STAGES>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)S::kTotal);
+  if (e != cudaSuccess) return e;
+  kern<<<num_sms(), kThreads, S::kTotal, st>>>(w, b0, b1, p);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int tc_tile_tokens(bool gateup, bool decode) {
+  if (decode) return 64;
+  return gateup ? 128 : 256;
+}
+
+cudaError_t launch_tc(const FfnArgs& a, const int32_t* prefix, bool gateup, bool decode,
+                      cudaStream_t st) {
+  TcParams p{};
+  p.T = a.T; p.k = a.k; p.E = a.E; p.n_shared = a.n_shared;
+  p.f = a.f; p.d = a.d;
+  p.K = gateup ? a.d : a.f;
+  p.mtiles = (gateup ? a.f : a.d) / kBM;
+  p.rows_per_expert = gateup ? 2 * a.f : a.d;
+  p.offsets = a.offsets;
+  p.prefix = prefix;
+  p.h = a.h;
+  p.y_perm = a.y_perm;
+  p.status = a.status;
+  const uint64_t E1 = (uint64_t)a.E + a.n_shared;
+  const uint64_t routed = (uint64_t)a.T * a.k;
+  const uint64_t slots = routed + (uint64_t)a.n_shared * a.T;
+  CUtensorMap w, b0, b1;
+  cudaError_t e;
+  if (gateup) {
+    e = encode_bf16_2d(&w, a.w13, E1 * 2 * a.f, a.d, kBM);
+    if (e == cudaSuccess) e = encode_bf16_2d(&b0, a.x_perm, routed ? routed : 1, a.d, kBoxRows);
+    if (e == cudaSuccess) e = encode_bf16_2d(&b1, a.x, a.T, a.d, kBoxRows);
+  } else {
+    e = encode_bf16_2d(&w, a.w2, E1 * a.d, a.f, kBM);
+    if (e == cudaSuccess) e = encode_bf16_2d(&b0, a.h, slots, a.f, kBoxRows);
+    b1 = b0;
+  }
+  if (e != cudaSuccess) return e;
+  if (gateup)
+    return decode ? launch_variant<true, 64, 5>(w, b0, b1, p, st)
+                  : launch_variant<true, 128, 4>(w, b0, b1, p, st);
+  return decode ? launch_variant<false, 64, 8>(w, b0, b1, p, st)
+                : launch_variant<false, 256, 4>(w, b0, b1, p, st);
+}
+
+}  // namespace moe
