@@ -93,6 +93,23 @@ MOE_API size_t moe_workspace_size(const moe_shape* shape);
 MOE_API moe_status moe_route(const moe_shape* shape, const void* x, const void* wg, const float* bias,
                      int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes, void* stream);
 
+/* The router of moe_route without a workspace, for callers that cannot allocate device memory
+ * themselves -- for instance a plugin whose host process owns every device allocation through
+ * its own pool and lends it no scratch, or a deployment that fixes its device memory budget at
+ * start-up and forbids allocations afterwards. The pages have no counterpart of this entry point.
+ * Same arguments, results and validation as moe_route, minus ws/ws_bytes; it allocates nothing
+ * and calls no allocating routine. Its logits scratch is a fixed 4 MiB device array inside the
+ * library (one copy per GPU that loads the library, kept until the process exits), so it serves
+ * shapes with T*E <= 1,048,576 (e.g. T <= 4096 at E = 256) and rejects larger ones with
+ * MOE_ERR_INVALID_ARG. The first call on each device looks up that array's device address:
+ * make that first call before any stream capture. Every call shares the one array, so calls
+ * that overlap on the GPU (different streams, or different host threads on the same device)
+ * race on it; order them on one stream. Nothing in the array needs to start at zero: each call
+ * overwrites the logits it reads. It records no device status. */
+MOE_API moe_status moe_route_noalloc(const moe_shape* shape, const void* x, const void* wg,
+                                     const float* bias, int32_t* topk_idx, float* topk_w,
+                                     void* stream);
+
 /* Token -> expert permutation ("第 6 章 超節點", 6.2.6).
  *   topk_idx       [T, k] int32, each row k distinct experts in [0, E).
  *   expert_offsets [E+2] int32 out: expert e (< E) owns slots [offsets[e], offsets[e+1]);

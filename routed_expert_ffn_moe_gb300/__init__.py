@@ -11,7 +11,8 @@ import ctypes
 import os
 
 __all__ = ["MoeError", "MoeShape", "MOE_W_BF16", "MOE_W_FP8_E4M3_B128", "load", "lib_path",
-           "moe_workspace_size", "moe_route", "moe_permute", "moe_expert_ffn", "moe_combine",
+           "moe_workspace_size", "moe_route", "moe_route_noalloc", "moe_permute",
+           "moe_expert_ffn", "moe_combine",
            "moe_check_device_status", "moe_profile_enable", "moe_profile_read",
            "moe_last_error_string", "shape_of", "MoeLayer", "EXPORTED"]
 
@@ -19,7 +20,7 @@ MOE_W_BF16, MOE_W_FP8_E4M3_B128 = 0, 1
 STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED",
           -3: "MOE_ERR_WORKSPACE", -4: "MOE_ERR_CUDA", -5: "MOE_ERR_DEVICE_TIMEOUT",
           -6: "MOE_ERR_DEVICE_BOUNDS"}
-EXPORTED = ("moe_workspace_size", "moe_route", "moe_permute", "moe_expert_ffn", "moe_combine",
+EXPORTED = ("moe_workspace_size", "moe_route", "moe_route_noalloc", "moe_permute", "moe_expert_ffn", "moe_combine",
             "moe_check_device_status", "moe_profile_enable", "moe_profile_read",
             "moe_last_error_string")
 
@@ -61,6 +62,8 @@ def load():
     L.moe_workspace_size.argtypes = [shp]
     L.moe_route.restype = i32
     L.moe_route.argtypes = [shp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.moe_route_noalloc.restype = i32
+    L.moe_route_noalloc.argtypes = [shp, vp, vp, vp, vp, vp, vp]
     L.moe_permute.restype = i32
     L.moe_permute.argtypes = [shp, vp, vp, vp, vp, vp, sz, vp]
     L.moe_expert_ffn.restype = i32
@@ -126,6 +129,14 @@ def moe_route(shape, x, wg, bias, topk_idx, topk_w, ws, stream=None, ws_bytes=No
     _check(load().moe_route(ctypes.byref(shape), _ptr(x), _ptr(wg), _ptr(bias), _ptr(topk_idx),
                             _ptr(topk_w), wp, wb if ws_bytes is None else ws_bytes,
                             _stream(stream)), "moe_route")
+
+
+def moe_route_noalloc(shape, x, wg, bias, topk_idx, topk_w, stream=None):
+    """moe_route without a workspace (for callers that cannot allocate device memory): the
+    library keeps the logits in a fixed 4 MiB device array, so T*E must be <= 2^20."""
+    _check(load().moe_route_noalloc(ctypes.byref(shape), _ptr(x), _ptr(wg), _ptr(bias),
+                                    _ptr(topk_idx), _ptr(topk_w), _stream(stream)),
+           "moe_route_noalloc")
 
 
 def moe_permute(shape, topk_idx, expert_offsets, perm_token, inv_slot, ws, stream=None,

@@ -143,6 +143,29 @@ moe_status moe_route(const moe_shape* shape, const void* x, const void* wg, cons
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_route launch");
 }
 
+moe_status moe_route_noalloc(const moe_shape* shape, const void* x, const void* wg,
+                             const float* bias, int32_t* topk_idx, float* topk_w, void* stream) {
+  moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (shape->T > 0) {
+    REQUIRE_PTR(x, 16);
+    REQUIRE_PTR(topk_idx, 16);
+    REQUIRE_PTR(topk_w, 16);
+  }
+  REQUIRE_PTR(wg, 16);
+  if (bias && !aligned(bias, 16)) return fail(MOE_ERR_INVALID_ARG, "bias not 16-byte aligned");
+  const size_t need = (size_t)shape->T * (size_t)shape->E;
+  if (need > route_noalloc_max_logits())
+    return fail(MOE_ERR_INVALID_ARG,
+                "moe_route_noalloc: T*E = %zu logits exceed its built-in scratch of %zu fp32 "
+                "values (4 MiB); use moe_route with a workspace for this shape",
+                need, route_noalloc_max_logits());
+  cudaError_t e = launch_route_noalloc(*shape, static_cast<const uint16_t*>(x),
+                                       static_cast<const uint16_t*>(wg), bias, topk_idx, topk_w,
+                                       static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_route_noalloc");
+}
+
 moe_status moe_permute(const moe_shape* shape, const int32_t* topk_idx, int32_t* expert_offsets,
                        int32_t* perm_token, int32_t* inv_slot, void* ws, size_t ws_bytes,
                        void* stream) {

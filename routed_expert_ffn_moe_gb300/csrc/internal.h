@@ -64,6 +64,12 @@ cudaError_t launch_combine(const moe_shape& s, const float* y_perm, const int32_
 
 int num_sms();
 
+// router with its logits scratch in a fixed device array (router.cu)
+size_t route_noalloc_max_logits();
+cudaError_t launch_route_noalloc(const moe_shape& s, const uint16_t* x, const uint16_t* wg,
+                                 const float* bias, int32_t* topk_idx, float* topk_w,
+                                 cudaStream_t st);
+
 // profiling hooks (capi.cu): kernel launch counter and per-call phase events
 void count_launches(int n);
 struct PhaseEvents {

@@ -6,6 +6,8 @@
 // 专家模型规格). Ascend fuses the gate into one "GatingTopK" kernel (same page, 融合Kernel);
 // here the logits GEMM and the selection are two kernels so the selection can see all E
 // logits of a token at once.
+#include <mutex>
+
 #include "internal.h"
 
 namespace moe {
@@ -137,6 +139,52 @@ cudaError_t launch_logits(const uint16_t* x, const uint16_t* wg, const float* bi
 }
 
 }  // namespace
+
+// ---- router without a caller-provided workspace ------------------------------------------
+// The logits scratch of moe_route_noalloc lives in this fixed device array, one copy per GPU
+// that loads the library, held until the process exits. Every call shares it: each call
+// overwrites the first T*E entries before reading them (nothing in it must start at zero), and
+// calls that overlap on the GPU race on it.
+constexpr size_t kNoAllocLogits = size_t(1) << 20;  // fp32 logits: 4 MiB
+static __device__ __align__(256) float g_noalloc_logits[kNoAllocLogits];
+
+size_t route_noalloc_max_logits() { return kNoAllocLogits; }
+
+// Device address of the array for the current device, looked up once per device (the first
+// call on a device does this set-up).
+static cudaError_t noalloc_logits_ptr(float** out) {
+  static std::mutex mu;
+  static float* ptrs[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_logits);
+    if (e != cudaSuccess) return e;
+    ptrs[dev] = static_cast<float*>(p);
+  }
+  *out = ptrs[dev];
+  return cudaSuccess;
+}
+
+cudaError_t launch_route_noalloc(const moe_shape& s, const uint16_t* x, const uint16_t* wg,
+                                 const float* bias, int32_t* topk_idx, float* topk_w,
+                                 cudaStream_t st) {
+  float* logits = nullptr;
+  cudaError_t e = noalloc_logits_ptr(&logits);
+  if (e != cudaSuccess || s.T == 0) return e;
+  if (s.T < 64)
+    e = launch_logits<1, 8>(x, wg, bias, s.T, s.d, s.E, logits, st);
+  else
+    e = launch_logits<4, 8>(x, wg, bias, s.T, s.d, s.E, logits, st);
+  if (e != cudaSuccess) return e;
+  k_router_topk<<<(unsigned)((s.T + 7) / 8), 256, 0, st>>>(logits, s.T, s.E, s.k, topk_idx, topk_w);
+  count_launches(2);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_route(const moe_shape& s, const uint16_t* x, const uint16_t* wg,
                          const float* bias, int32_t* topk_idx, float* topk_w, char* ws,
