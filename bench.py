@@ -64,29 +64,26 @@ def measured_peaks():
                 "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def kernel_sources_sha() -> str:
+def kernel_sources_sha(files) -> str:
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "routed_expert_ffn_moe_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
-        if fn.endswith((".cu", ".h", ".cuh")):
-            with open(os.path.join(csrc, fn), "rb") as fh:
-                h.update(fn.encode() + fh.read())
+    for fn in files:
+        with open(os.path.join(ROOT, fn), "rb") as fh:
+            h.update(os.path.basename(fn).encode() + fh.read())
     return h.hexdigest()[:16]
 
 
 def ncu_traffic(config_name: str):
     """DRAM bytes per launch of the gate/up kernel from a committed ncu capture, if it was taken
-    on the current kernel sources; else None."""
+    on the kernel's current sources; else None."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as fh:
-            d = json.load(fh)
-    except (OSError, ValueError):
-        return None
-    ent = d.get(config_name)
-    if not ent or ent.get("kernel_sources_sha") != kernel_sources_sha():
-        return None
-    return ent.get("dram_bytes_per_launch")
+            ent = json.load(fh).get(config_name)
+        if ent and ent.get("kernel_sources_sha") == kernel_sources_sha(ent["kernel_sources"]):
+            return ent.get("dram_bytes_per_launch")
+    except (OSError, ValueError, KeyError):
+        pass
+    return None
 
 
 class ClockSampler:
