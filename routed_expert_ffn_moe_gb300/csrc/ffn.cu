@@ -6,6 +6,7 @@
 // waits for them: a one-block plan kernel turns expert_offsets into per-expert prefix sums of
 // work items for each kernel, and the persistent FFN kernels walk those lists.
 #include <climits>
+#include <cstdlib>
 
 #include "ffn.h"
 
@@ -70,6 +71,14 @@ __global__ void __launch_bounds__(256) k_gather_rows(const uint16_t* __restrict_
       __ldg(reinterpret_cast<const uint4*>(x + (long)t * d) + c);
 }
 
+// Token count from which an expert runs on the tensor cores (default 1: all of them).
+int tc_min_tokens() {
+  const char* v = getenv("MOE_TC_MIN_TOKENS");
+  if (!v || !*v) return 1;
+  const long n = strtol(v, nullptr, 10);
+  return n < 1 ? 1 : (n > INT_MAX ? INT_MAX : (int)n);
+}
+
 }  // namespace
 
 cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32_t* perm_token,
@@ -88,18 +97,24 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32
   a.status = reinterpret_cast<int*>(ws + L.status);
   int32_t* plan = reinterpret_cast<int32_t*>(ws + L.plan);
 
-  // Tensor cores take every bf16 expert; FP8 experts use the weight-streaming path.
-  const bool use_tc = s.wdtype == MOE_W_BF16;
+  // Experts with at least tc_min tokens go to the tensor-core GEMM, the rest to the
+  // weight-streaming GEMV. Both stream each weight byte once; the tensor-core kernel does so at
+  // full HBM rate from one token up, so by default it takes every expert. MOE_TC_MIN_TOKENS
+  // moves the split (a tuning and testing knob; results agree within rounding either way).
+  const int tc_min = tc_min_tokens();
+  const bool fp8 = s.wdtype == MOE_W_FP8_E4M3_B128;
   const long routed = (long)s.T * s.k;
   const bool decode = routed <= 32L * s.E;  // at most ~32 tokens per routed expert on average
+  const bool use_tc = tc_min < INT_MAX;
+  const bool use_gemv = tc_min > 1;
   PlanArgs pa{};
   pa.E = s.E; pa.n_shared = s.n_shared;
-  pa.tc_min = use_tc ? 1 : INT_MAX;
+  pa.tc_min = tc_min;
   pa.group = gemv_group_tokens();
   pa.items_up = gemv_items_per_group(true, s.d, s.f);
   pa.items_dn = gemv_items_per_group(false, s.d, s.f);
-  pa.nt_up = tc_tile_tokens(true, decode);
-  pa.nt_dn = tc_tile_tokens(false, decode);
+  pa.nt_up = fp8 ? tc_fp8_tile_tokens(true, decode) : tc_tile_tokens(true, decode);
+  pa.nt_dn = fp8 ? tc_fp8_tile_tokens(false, decode) : tc_tile_tokens(false, decode);
   pa.mt_up = s.f / 128;
   pa.mt_dn = s.d / 128;
   pa.stride = s.E + 2;
@@ -124,15 +139,19 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32
   const long slots = routed + (long)s.n_shared * s.T;
   const long max_groups = (slots + pa.group - 1) / pa.group + s.E + s.n_shared;
   const auto cap = [](long v) { return (int)(v < (1L << 30) ? v : (1L << 30)); };
-  const int max_up = use_tc ? 0 : cap(max_groups * pa.items_up);
-  const int max_dn = use_tc ? 0 : cap(max_groups * pa.items_dn);
+  const int max_up = use_gemv ? cap(max_groups * pa.items_up) : 0;
+  const int max_dn = use_gemv ? cap(max_groups * pa.items_dn) : 0;
+  const auto tc = [&](bool gateup, const int32_t* prefix) {
+    return fp8 ? launch_tc_fp8(a, prefix, gateup, decode, st)
+               : launch_tc(a, prefix, gateup, decode, st);
+  };
 
-  if (use_tc) e = launch_tc(a, plan + kPlanTcUp * stride, true, decode, st);
+  if (use_tc) e = tc(true, plan + kPlanTcUp * stride);
   if (e == cudaSuccess)
     e = launch_gemv(a, plan + kPlanGemvUp * stride, plan + kPlanGemvDown * stride, true, max_up, st);
   if (e != cudaSuccess) return e;
   if (ev.mid) cudaEventRecord(ev.mid, st);
-  if (use_tc) e = launch_tc(a, plan + kPlanTcDown * stride, false, decode, st);
+  if (use_tc) e = tc(false, plan + kPlanTcDown * stride);
   if (e == cudaSuccess)
     e = launch_gemv(a, plan + kPlanGemvUp * stride, plan + kPlanGemvDown * stride, false, max_dn, st);
   if (ev.end) cudaEventRecord(ev.end, st);

@@ -31,4 +31,9 @@ int tc_tile_tokens(bool gateup, bool decode);
 cudaError_t launch_tc(const FfnArgs& a, const int32_t* prefix, bool gateup, bool decode,
                       cudaStream_t st);
 
+// tensor-core path (ffn_tc_fp8.cu): E4M3 weights dequantised into TMEM
+int tc_fp8_tile_tokens(bool gateup, bool decode);
+cudaError_t launch_tc_fp8(const FfnArgs& a, const int32_t* prefix, bool gateup, bool decode,
+                          cudaStream_t st);
+
 }  // namespace moe

@@ -20,94 +20,13 @@
 // Accumulators are double-buffered in TMEM so the epilogue of tile i overlaps the mainloop of
 // tile i+1. Every wait is bounded: a wait that gives up records MOE_ERR_DEVICE_TIMEOUT and the
 // CTA winds down, frees its TMEM and exits.
-#include "ffn.h"
-#include "sm100_ptx.cuh"
+#include "tc_common.cuh"
 
 namespace moe {
 namespace {
 
 using namespace ptx;
-
-constexpr int kBM = 128;               // weight rows per tile (MMA M)
-constexpr int kBK = 64;                // K per stage: one 128-byte swizzle row of bf16
-constexpr int kBoxRows = 16;           // token rows per TMA box
-constexpr uint32_t kATileBytes = kBM * kBK * 2;     // 16 KB
-constexpr uint32_t kBBoxBytes = kBoxRows * kBK * 2; // 2 KB
-constexpr uint64_t kWaitLimitNs = 2000000000ull;    // 2 s
-constexpr int kThreads = 192;
-
-struct TcParams {
-  int T, k, E, n_shared;
-  int K;                 // reduction width: d (gate/up) or f (down)
-  int mtiles;            // 128-row weight tiles per expert
-  int rows_per_expert;   // rows of the weight map per expert: 2f (gate/up) or d (down)
-  int f, d;
-  const int32_t* offsets;
-  const int32_t* prefix;  // [E1 + 1] tile prefix over experts
-  uint16_t* h;
-  float* y_perm;
-  int* status;
-};
-
-struct Tile {
-  int e, mt, slot0, ntok, brow0;
-  bool shared;
-};
-
-// Token rows of the gate/up pass come from the gathered rows (routed experts) or straight from
-// x (the shared expert, whose slot T*k + t is token t); the down pass reads h in slot order.
-template <bool GATEUP, int NT>
-__device__ __forceinline__ void decode_tile(const TcParams& p, int tile, Tile& t) {
-  const int E1 = p.E + p.n_shared;
-  int lo = 0, hi = E1;
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (__ldg(p.prefix + mid) <= tile) lo = mid; else hi = mid;
-  }
-  const int e = lo;
-  const int seg0 = __ldg(p.offsets + e);
-  const int cnt = __ldg(p.offsets + e + 1) - seg0;
-  const int ntn = (cnt + NT - 1) / NT;
-  const int local = tile - __ldg(p.prefix + e);
-  const int mt = local / ntn, nt = local - mt * ntn;
-  t.e = e;
-  t.mt = mt;
-  t.slot0 = seg0 + nt * NT;
-  t.ntok = min(NT, cnt - nt * NT);
-  t.shared = (e == p.E);
-  t.brow0 = (GATEUP && t.shared) ? t.slot0 - p.T * p.k : t.slot0;
-}
-
-// Bounded wait on an mbarrier phase. Returns false (after recording a timeout) if it gave up
-// or if another role already gave up.
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                         int* status) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
-        record_error(status, MOE_ERR_DEVICE_TIMEOUT);
-        *abort_flag = 1;
-        return false;
-      }
-    }
-  }
-}
-
-// Bounded wait that ignores the abort flag: used to drain this CTA's own copies in flight
-// before it exits.
-__device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity, int* status) {
-  const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer() - t0 > kWaitLimitNs) {
-      record_error(status, MOE_ERR_DEVICE_TIMEOUT);
-      return;
-    }
-  }
-}
+using namespace tc;
 
 template <bool GATEUP, int NT, int STAGES>
 struct Smem {
@@ -236,47 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
-    const int q = warp & 3;                 // TMEM lane quadrant this warp may access
-    const int row = q * 32 + lane;          // weight row within the tile
-    uint32_t acc = 0, acc_phase = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      Tile t;
-      decode_tile<GATEUP, NT>(p, tile, t);
-      const int npad = (t.ntok + 15) & ~15;
-      if (!wait_bar(&acc_full[acc], acc_phase, abort_flag, p.status)) break;
-      tc_fence_after();
-      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * S::kAccCols;
-      const int orow = t.mt * kBM + row;    // output feature
-      for (int c0 = 0; c0 < npad; c0 += 16) {
-        uint32_t g[16];
-        tmem_ld16(tbase + c0, g);
-        if (GATEUP) {
-          uint32_t u[16];
-          tmem_ld16(tbase + NT + c0, u);
-          tmem_ld_wait2(g, u);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int n = c0 + j;
-            if (n < t.ntok) {
-              const float gv = __uint_as_float(g[j]), uv = __uint_as_float(u[j]);
-              const float silu = gv / (1.0f + __expf(-gv));
-              p.h[(size_t)(t.slot0 + n) * p.f + orow] = f32_to_bf16_rn(silu * uv);
-            }
-          }
-        } else {
-          tmem_ld_wait(g);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int n = c0 + j;
-            if (n < t.ntok) p.y_perm[(size_t)(t.slot0 + n) * p.d + orow] = __uint_as_float(g[j]);
-          }
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[acc]);
-      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
-    }
+    run_epilogue<GATEUP, NT, S::kAccCols>(p, total, tmem_base, acc_full, acc_empty, abort_flag);
   }
 
   tc_fence_before();
@@ -285,42 +164,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, S::kTmemCols);
   }
-}
-
-// ---- host side -------------------------------------------------------------------------------
-
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  }
-  return fn;
-}
-
-// Row-major [rows, cols] bf16 matrix, box of box_rows x 64 columns, 128-byte swizzle.
-cudaError_t encode_bf16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
-                           uint32_t box_rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return cudaErrorNotSupported;
-  const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 template <bool GATEUP, int NT, int STAGES>

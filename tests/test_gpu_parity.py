@@ -73,6 +73,16 @@ def test_small_layer_matches_oracle(name, over):
     check_small(synth.get_config(name, **over))
 
 
+@pytest.mark.parametrize("tc_min", ["3", "1000000000"])
+@pytest.mark.parametrize("over", [{}, {"wdtype": "fp8"}, {"T": 70, "d": 512, "f": 384, "E": 12, "k": 3},
+                                  {"T": 70, "d": 512, "f": 384, "E": 12, "k": 3, "wdtype": "fp8"}],
+                         ids=["bf16", "fp8", "bf16_big", "fp8_big"])
+def test_weight_streaming_path_and_mixed_split(monkeypatch, tc_min, over):
+    # experts below tc_min tokens run on the weight-streaming GEMV, the rest on tensor cores
+    monkeypatch.setenv("MOE_TC_MIN_TOKENS", tc_min)
+    check_small(synth.get_config("tiny", **over))
+
+
 def test_all_tokens_to_one_expert():
     cfg = synth.get_config("tiny", T=40, k=1, router="zipf")
     bias = np.zeros(cfg.E, np.float32)
@@ -185,8 +195,9 @@ def sample_tokens(cfg, idx, n_even=6):
     return sorted(picks)
 
 
-FULL = ["v3_decode", "v4pro_decode", "skewed_prefill", "sweep_fp8_T1", "sweep_fp8_T64",
-        "sweep_fp8_T1024"]
+FULL = ["v3_decode", "v4pro_decode", "skewed_prefill", "sweep_fp8_T1", "sweep_fp8_T8",
+        "sweep_fp8_T64", "sweep_fp8_T256", "sweep_fp8_T1024", "sweep_fp8_T4096",
+        "sweep_fp8_T16384"]
 
 
 @pytest.mark.parametrize("name", FULL)
