@@ -35,5 +35,8 @@ cudaError_t launch_tc(const FfnArgs& a, const int32_t* prefix, bool gateup, bool
 int tc_fp8_tile_tokens(bool gateup, bool decode);
 cudaError_t launch_tc_fp8(const FfnArgs& a, const int32_t* prefix, bool gateup, bool decode,
                           cudaStream_t st);
+// wide-tile variant (ffn_tc_fp8_wide.cu): E4M3 weights dequantised to bf16 into TMEM
+cudaError_t launch_tc_fp8_wide(const FfnArgs& a, const int32_t* prefix, bool gateup,
+                               cudaStream_t st);
 
 }  // namespace moe

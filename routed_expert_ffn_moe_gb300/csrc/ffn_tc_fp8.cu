@@ -1,19 +1,31 @@
 // Expert FFN, tensor-core path for FP8 E4M3 expert weights with one fp32 scale per 128x128
-// block (W8A16: weights dequantised on chip, activations stay bf16).
+// block (W8A16: weights dequantised on chip, activations arrive as bf16).
 //
 // The pages: FP8/FP4 expert weights cut the bytes streamed from HBM, at the price of "scale
 // reading, unpacking and tile alignment" work on chip ("DeepSeek-V4-Pro on NVIDIA H200",
 // 0.1.3; "CANN DeepSeek-V4推理优化", 量化策略). Here that work is a warp-specialised stage of
-// the grouped GEMM:
+// the grouped GEMM, arranged so the per-weight work is as small as possible.
 //
-//   TMA       E4M3 weight tiles (128 rows x 128 K = one scale block) and bf16 token tiles -> smem
-//   convert   8 warps: code -> fp32 -> x block scale -> bf16, written straight into TMEM with
-//             tcgen05.st (one weight row per TMEM lane)
-//   MMA       tcgen05.mma.kind::f16 with A (weights) read from TMEM and B (tokens) from smem
+// A tile covers 128 weight rows (one row block) and K in 128-wide stages (one column block), so
+// one stage of one weight matrix has a single scale s, and
+//     sum_k (q[m,k] * s) * x[n,k]  ==  sum_k q[m,k] * (s * x[n,k]).
+// The weights therefore go to the tensor cores as their exact code values, and the scale is
+// applied to the (few) token rows instead:
+//
+//   TMA       E4M3 weight tiles (128 rows x 128 K) and bf16 token tiles -> smem ring
+//   convert   8 warps: codes -> f16 (exact; one cvt per two codes) written straight into TMEM
+//             with tcgen05.st, one weight row per TMEM lane; token rows -> f16(s * x) written
+//             into a smem tile per weight matrix (gate and up have their own scale)
+//   MMA       tcgen05.mma.kind::f16 (f16 x f16 -> fp32) with A (codes) read from TMEM and B
+//             (scaled tokens) from smem
 //   epilogue  as in the bf16 kernel: TMEM accumulators -> SiLU(gate) * up -> bf16 h, or fp32
 //
-// Keeping the dequantised operand in TMEM leaves shared memory carrying only the E4M3 bytes and
-// the token rows. Same tile list, swap-AB tile shape and bounded waits as the bf16 kernel.
+// Numerics: codes are exact in f16; s * x is rounded once to f16 (11-bit significand, better
+// than bf16) and saturates at +-65504, so the product of a block scale and an activation must
+// stay below that (block scales are amax/448, far below 1 for expert weights).
+//
+// This variant serves decode-sized tiles (up to 32 tokens); wide tiles go to ffn_tc_fp8_wide.cu,
+// where dequantising the weights costs less than scaling 64-128 token rows.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -28,49 +40,68 @@ using namespace tc;
 constexpr int kQK = 128;                          // K per stage = one scale block
 constexpr uint32_t kQTileBytes = kBM * kQK;       // 16 KB of E4M3 codes
 constexpr int kConvWarps = 8;                     // two per TMEM lane quadrant
-constexpr int kThreadsQ = 32 * (6 + kConvWarps);  // producer, MMA, 4 epilogue, converters
-constexpr uint32_t kACols = kQK / 2;              // TMEM columns of one 128 x 128 bf16 tile
+constexpr int kConvThreads = 32 * kConvWarps;
+constexpr int kThreadsQ = 32 * 6 + kConvThreads;  // producer, MMA, 4 epilogue, converters
+constexpr uint32_t kACols = kQK / 2;              // TMEM columns of one 128 x 128 f16 tile
 
-template <bool GATEUP, int NT, int STAGES, int ASTAGES>
+template <bool GATEUP, int NT, int STAGES, int CSTAGES>
 struct SmemQ {
   static constexpr int kA = GATEUP ? 2 : 1;
-  static constexpr uint32_t kBHalf = (uint32_t)NT * kBK * 2;   // NT rows x 64 K bf16
-  static constexpr uint32_t kStageBytes = kA * kQTileBytes + 2 * kBHalf;
-  static constexpr uint32_t kTilesBytes = STAGES * kStageBytes;
-  static constexpr uint32_t kBarBytes = 8 * (2 * STAGES + 2 * ASTAGES + 4) + 16;
+  static constexpr uint32_t kBHalf = (uint32_t)NT * kBK * 2;   // NT rows x 64 K of 16-bit
+  static constexpr uint32_t kStageBytes = kA * kQTileBytes + 2 * kBHalf;   // TMA ring
+  static constexpr uint32_t kCSlotBytes = kA * 2 * kBHalf;                 // scaled token tiles
+  static constexpr uint32_t kTilesBytes = STAGES * kStageBytes + CSTAGES * kCSlotBytes;
+  static constexpr uint32_t kBarBytes = 8 * (2 * STAGES + 2 * CSTAGES + 4) + 16;
   static constexpr uint32_t kTotal = kTilesBytes + kBarBytes + 1024;
   static constexpr uint32_t kAccCols = GATEUP ? 2 * NT : NT;
   static constexpr uint32_t kAStageCols = kA * kACols;
-  static constexpr uint32_t kUsedCols = 2 * kAccCols + ASTAGES * kAStageCols;
+  static constexpr uint32_t kUsedCols = 2 * kAccCols + CSTAGES * kAStageCols;
   static constexpr uint32_t kTmemCols =
       kUsedCols <= 32 ? 32 : kUsedCols <= 64 ? 64 : kUsedCols <= 128 ? 128
       : kUsedCols <= 256 ? 256 : 512;
 };
 
-// Two E4M3 codes (low byte first) times the block scale, as a bf16 pair (low element first).
-__device__ __forceinline__ uint32_t dequant2(uint32_t two, float s) {
-  const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xFFFFu), __NV_E4M3);
-  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
-  const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * s, f.y * s);
-  return *reinterpret_cast<const uint32_t*>(&b);
+// Instruction descriptor of kind::f16 with f16 A and B, fp32 accumulator, both K-major.
+__device__ __forceinline__ uint32_t idesc_f16(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-template <bool GATEUP, int NT, int STAGES, int ASTAGES>
+// Two E4M3 codes (low byte first) as an exact f16 pair (low element first).
+__device__ __forceinline__ uint32_t codes_to_f16x2(uint32_t two) {
+  const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xFFFFu), __NV_E4M3);
+  return *reinterpret_cast<const uint32_t*>(&hr);
+}
+
+// f16 pair (lo, hi) = (round(lo), round(hi)), saturating to the largest finite f16.
+__device__ __forceinline__ uint32_t f32x2_to_f16x2_sat(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+__device__ __forceinline__ void sts_u4(uint32_t addr, const uint4& v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+template <bool GATEUP, int NT, int STAGES, int CSTAGES>
 __global__ void __launch_bounds__(kThreadsQ, 1)
     k_tc_ffn_fp8(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b0,
                  const __grid_constant__ CUtensorMap tm_b1, const TcParams p,
                  const float* __restrict__ scales) {
-  using S = SmemQ<GATEUP, NT, STAGES, ASTAGES>;
+  using S = SmemQ<GATEUP, NT, STAGES, CSTAGES>;
   static_assert(S::kUsedCols <= 512, "TMEM columns");
   static_assert(NT % 16 == 0 && NT >= 16 && NT <= 256, "MMA N");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
+  uint8_t* cslots = smem + STAGES * S::kStageBytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kTilesBytes);
   uint64_t* empty = full + STAGES;
-  uint64_t* a_full = empty + STAGES;
-  uint64_t* a_empty = a_full + ASTAGES;
-  uint64_t* acc_full = a_empty + ASTAGES;
+  uint64_t* c_full = empty + STAGES;
+  uint64_t* c_empty = c_full + CSTAGES;
+  uint64_t* acc_full = c_empty + CSTAGES;
   uint64_t* acc_empty = acc_full + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
@@ -79,16 +110,15 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
   const int E1 = p.E + p.n_shared;
   const int total = __ldg(p.prefix + E1);
   const int kblocks = p.K / kQK;
-  constexpr uint32_t kConvThreads = 32 * kConvWarps;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConvThreads + 1);  // every converter thread + the MMA commit
+      mbar_init(&empty[s], kConvThreads);    // every converter thread has read the stage
     }
-    for (int s = 0; s < ASTAGES; ++s) {
-      mbar_init(&a_full[s], kConvThreads);
-      mbar_init(&a_empty[s], 1);
+    for (int s = 0; s < CSTAGES; ++s) {
+      mbar_init(&c_full[s], kConvThreads);   // converted operands written
+      mbar_init(&c_empty[s], 1);             // MMA commit: converted operands consumed
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -108,7 +138,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-  const uint32_t acol0 = 2 * S::kAccCols;  // first TMEM column of the A ring
+  const uint32_t acol0 = 2 * S::kAccCols;  // first TMEM column of the converted-weights ring
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -146,34 +176,33 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      uint32_t stage = 0, phase = 0, astage = 0, aphase = 0;
+      uint32_t cs = 0, cphase = 0;
       uint32_t acc = 0, acc_phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
         Tile t;
         decode_tile<GATEUP, NT>(p, tile, t);
         const int npad = (t.ntok + 15) & ~15;
-        const uint32_t idesc = idesc_bf16(kBM, npad);
+        const uint32_t idesc = idesc_f16(kBM, npad);
         if (!wait_bar(&acc_empty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t d0 = tmem_base + acc * S::kAccCols;
         for (int kb = 0; kb < kblocks; ++kb) {
-          if (!wait_bar(&full[stage], phase, abort_flag, p.status) ||
-              !wait_bar(&a_full[astage], aphase, abort_flag, p.status)) { ok = false; break; }
+          if (!wait_bar(&c_full[cs], cphase, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t a0 = tmem_base + acol0 + astage * S::kAStageCols;
-          const uint32_t bst = smem_u32(smem + stage * S::kStageBytes + S::kA * kQTileBytes);
+          const uint32_t a0 = tmem_base + acol0 + cs * S::kAStageCols;
+          const uint32_t bp = smem_u32(cslots + cs * S::kCSlotBytes);
 #pragma unroll
           for (int kk = 0; kk < kQK / 16; ++kk) {
-            const uint64_t bd = sw128_desc(bst + (kk >> 2) * S::kBHalf) + 2 * (kk & 3);
             const uint32_t accum = (kb | kk) ? 1u : 0u;
-            mma_bf16_ts(d0, a0 + kk * 8, bd, idesc, accum);
-            if (GATEUP) mma_bf16_ts(d0 + NT, a0 + kACols + kk * 8, bd, idesc, accum);
+            const uint32_t boff = (kk >> 2) * S::kBHalf;
+            mma_ts(d0, a0 + kk * 8, sw128_desc(bp + boff) + 2 * (kk & 3), idesc, accum);
+            if (GATEUP)
+              mma_ts(d0 + NT, a0 + kACols + kk * 8,
+                          sw128_desc(bp + 2 * S::kBHalf + boff) + 2 * (kk & 3), idesc, accum);
           }
-          mma_commit(&empty[stage]);    // token rows consumed
-          mma_commit(&a_empty[astage]); // dequantised weights consumed
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-          if (++astage == ASTAGES) { astage = 0; aphase ^= 1u; }
+          mma_commit(&c_empty[cs]);
+          if (++cs == CSTAGES) { cs = 0; cphase ^= 1u; }
         }
         if (!ok) break;
         mma_commit(&acc_full[acc]);
@@ -184,23 +213,31 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
     // ---------------- epilogue (warps 2..5) ----------------
     run_epilogue<GATEUP, NT, S::kAccCols>(p, total, tmem_base, acc_full, acc_empty, abort_flag);
   } else {
-    // ---------------- dequantisers (warps 6..13) ----------------
+    // ---------------- converters (warps 6..13) ----------------
+    const int ct = threadIdx.x - 192;         // 0..255
     const int q = warp & 3;                   // TMEM lane quadrant
     const int hk = (warp - 6) >> 2;           // which 64-wide half of the stage's K
     const int row = q * 32 + lane;            // weight row within the tile = TMEM lane
     const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
     const int kbl = p.K / 128;                // scale blocks along K
-    uint32_t stage = 0, phase = 0, astage = 0, aphase = 0;
+    uint32_t stage = 0, phase = 0, cs = 0, cphase = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
       Tile t;
       decode_tile<GATEUP, NT>(p, tile, t);
+      const int npad = (t.ntok + 15) & ~15;
       const float* sc = scales + (size_t)t.e * (p.rows_per_expert / 128) * kbl;
       const int rb_g = t.mt, rb_u = p.f / 128 + t.mt;
       for (int kb = 0; kb < kblocks; ++kb) {
         if (!wait_bar(&full[stage], phase, abort_flag, p.status) ||
-            !wait_bar(&a_empty[astage], aphase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+            !wait_bar(&c_empty[cs], cphase ^ 1u, abort_flag, p.status)) { ok = false; break; }
         const uint32_t st = smem_u32(smem + stage * S::kStageBytes);
+        const uint32_t bsrc = st + S::kA * kQTileBytes;
+        const uint32_t bdst = smem_u32(cslots + cs * S::kCSlotBytes);
+        float s_o[2];
+        s_o[0] = __ldg(sc + rb_g * kbl + kb);
+        s_o[1] = GATEUP ? __ldg(sc + rb_u * kbl + kb) : 0.f;
+        // weight codes of this thread's row and K half -> exact f16 in TMEM
         uint4 raw[S::kA][4];
 #pragma unroll
         for (int o = 0; o < S::kA; ++o)
@@ -209,10 +246,24 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
             const uint32_t chunk = (uint32_t)(4 * hk + j) ^ (uint32_t)(row & 7);  // 128B swizzle
             raw[o][j] = lds_u4(st + o * kQTileBytes + row * 128 + (chunk << 4));
           }
-        mbar_arrive(&empty[stage]);           // this thread is done with the E4M3 bytes
-        float s_o[2];
-        s_o[0] = __ldg(sc + rb_g * kbl + kb);
-        s_o[1] = GATEUP ? __ldg(sc + rb_u * kbl + kb) : 0.f;
+        // token rows -> f16(s * x), same 128-byte-swizzled K-major layout as the TMA source
+        const int units = S::kA * npad * 16;  // (operand, row, 16-byte chunk)
+        for (int u = ct; u < units; u += kConvThreads) {
+          const int o = u / (npad * 16);
+          const int rem = u - o * npad * 16;
+          const int n = rem >> 4, c = rem & 15;
+          const uint32_t off = (uint32_t)(c >> 3) * S::kBHalf + (uint32_t)n * 128 +
+                               ((uint32_t)((c & 7) ^ (n & 7)) << 4);
+          const uint4 xv = lds_u4(bsrc + off);
+          const float s = o ? s_o[1] : s_o[0];
+          uint4 r;
+          r.x = f32x2_to_f16x2_sat(__uint_as_float(xv.x << 16) * s, __uint_as_float(xv.x & 0xFFFF0000u) * s);
+          r.y = f32x2_to_f16x2_sat(__uint_as_float(xv.y << 16) * s, __uint_as_float(xv.y & 0xFFFF0000u) * s);
+          r.z = f32x2_to_f16x2_sat(__uint_as_float(xv.z << 16) * s, __uint_as_float(xv.z & 0xFFFF0000u) * s);
+          r.w = f32x2_to_f16x2_sat(__uint_as_float(xv.w << 16) * s, __uint_as_float(xv.w & 0xFFFF0000u) * s);
+          sts_u4(bdst + o * 2 * S::kBHalf + off, r);
+        }
+        mbar_arrive(&empty[stage]);           // this thread is done reading the TMA stage
 #pragma unroll
         for (int o = 0; o < S::kA; ++o) {
           uint32_t out[32];
@@ -221,17 +272,18 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
             const uint32_t w[4] = {raw[o][j].x, raw[o][j].y, raw[o][j].z, raw[o][j].w};
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
-              out[j * 8 + 2 * m] = dequant2(w[m] & 0xFFFFu, s_o[o]);
-              out[j * 8 + 2 * m + 1] = dequant2(w[m] >> 16, s_o[o]);
+              out[j * 8 + 2 * m] = codes_to_f16x2(w[m] & 0xFFFFu);
+              out[j * 8 + 2 * m + 1] = codes_to_f16x2(w[m] >> 16);
             }
           }
-          tmem_st32(lane_base + acol0 + astage * S::kAStageCols + o * kACols + hk * 32, out);
+          tmem_st32(lane_base + acol0 + cs * S::kAStageCols + o * kACols + hk * 32, out);
         }
+        fence_proxy_async_smem();             // scaled token tiles -> visible to the MMA
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&a_full[astage]);
+        mbar_arrive(&c_full[cs]);
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-        if (++astage == ASTAGES) { astage = 0; aphase ^= 1u; }
+        if (++cs == CSTAGES) { cs = 0; cphase ^= 1u; }
       }
     }
   }
@@ -244,12 +296,12 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
   }
 }
 
-template <bool GATEUP, int NT, int STAGES, int ASTAGES>
+template <bool GATEUP, int NT, int STAGES, int CSTAGES>
 cudaError_t launch_variant(const CUtensorMap& w, const CUtensorMap& b0, const CUtensorMap& b1,
                            const TcParams& p, const float* scales, cudaStream_t st) {
-  using S = SmemQ<GATEUP, NT, STAGES, ASTAGES>;
+  using S = SmemQ<GATEUP, NT, STAGES, CSTAGES>;
   static_assert(S::kTotal <= 227 * 1024, "shared memory");
-  auto kern = k_tc_ffn_fp8<GATEUP, NT, STAGES, ASTAGES>;
+  auto kern = k_tc_ffn_fp8<GATEUP, NT, STAGES, CSTAGES>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)S::kTotal);
   if (e != cudaSuccess) return e;
@@ -267,6 +319,7 @@ int tc_fp8_tile_tokens(bool gateup, bool decode) {
 
 cudaError_t launch_tc_fp8(const FfnArgs& a, const int32_t* prefix, bool gateup, bool decode,
                           cudaStream_t st) {
+  if (!decode) return launch_tc_fp8_wide(a, prefix, gateup, st);
   TcParams p{};
   p.T = a.T; p.k = a.k; p.E = a.E; p.n_shared = a.n_shared;
   p.f = a.f; p.d = a.d;
@@ -294,11 +347,8 @@ cudaError_t launch_tc_fp8(const FfnArgs& a, const int32_t* prefix, bool gateup, 
   }
   if (e != cudaSuccess) return e;
   const float* sc = gateup ? a.s13 : a.s2;
-  if (gateup)
-    return decode ? launch_variant<true, 32, 5, 3>(w, b0, b1, p, sc, st)
-                  : launch_variant<true, 64, 4, 2>(w, b0, b1, p, sc, st);
-  return decode ? launch_variant<false, 32, 8, 4>(w, b0, b1, p, sc, st)
-                : launch_variant<false, 128, 4, 4>(w, b0, b1, p, sc, st);
+  if (gateup) return launch_variant<true, 32, 4, 3>(w, b0, b1, p, sc, st);
+  return launch_variant<false, 32, 6, 4>(w, b0, b1, p, sc, st);
 }
 
 }  // namespace moe

@@ -138,7 +138,7 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t adesc, uin
 
 // D[tmem] (+)= A[tmem] * B[smem]^T: A is 128 lanes (one row of M per lane) x K/2 columns, two
 // 16-bit elements per 32-bit column in increasing K order.
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
                                             uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n"
