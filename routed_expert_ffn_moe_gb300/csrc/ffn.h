@@ -28,6 +28,7 @@ cudaError_t launch_gemv(const FfnArgs& a, const int32_t* prefix_up, const int32_
 
 // tensor-core path (ffn_tc.cu): bf16 weights
 int tc_tile_tokens(bool gateup, bool decode);
+int tc_tile_rows(bool gateup, bool decode, int d);  // weight rows per tile
 cudaError_t launch_tc(const FfnArgs& a, const int32_t* prefix, bool gateup, bool decode,
                       cudaStream_t st);
 

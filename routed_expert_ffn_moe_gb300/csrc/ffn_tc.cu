@@ -28,24 +28,29 @@ namespace {
 using namespace ptx;
 using namespace tc;
 
-template <bool GATEUP, int NT, int STAGES>
+// KA weight tiles of 128 rows share each token tile: gate + up rows of the same features in the
+// gate/up pass, one or two consecutive 128-row tiles of W_d in the down pass. ACCB accumulator
+// buffers: 2 lets the epilogue of one tile overlap the next tile's mainloop; wide tiles
+// (KA * NT = 512 columns) fill TMEM with a single buffer.
+template <int NT, int STAGES, int KA, int ACCB>
 struct Smem {
-  static constexpr int kA = GATEUP ? 2 : 1;  // weight tiles per stage
-  static constexpr uint32_t kStageBytes = kA * kATileBytes + (uint32_t)NT * kBK * 2;
+  static constexpr uint32_t kStageBytes = KA * kATileBytes + (uint32_t)NT * kBK * 2;
   static constexpr uint32_t kTilesBytes = STAGES * kStageBytes;
   static constexpr uint32_t kBarBytes = 8 * (2 * STAGES + 4) + 16;
   static constexpr uint32_t kTotal = kTilesBytes + kBarBytes + 1024;  // + alignment slack
-  static constexpr uint32_t kAccCols = GATEUP ? 2 * NT : NT;          // per accumulator buffer
-  static constexpr uint32_t kTmemCols = 2 * kAccCols;                 // double-buffered
+  static constexpr uint32_t kAccCols = KA * NT;                       // per accumulator buffer
+  static constexpr uint32_t kTmemCols = ACCB * kAccCols;
 };
 
-template <bool GATEUP, int NT, int STAGES>
+template <bool GATEUP, int NT, int STAGES, int KA, int ACCB>
 __global__ void __launch_bounds__(kThreads, 1)
     k_tc_ffn(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b0,
-             const __grid_constant__ CUtensorMap tm_b1, const TcParams p) {
-  using S = Smem<GATEUP, NT, STAGES>;
+             const __grid_constant__ CUtensorMap tm_b1, const __grid_constant__ CUtensorMap tm_b0w,
+             const __grid_constant__ CUtensorMap tm_b1w, const TcParams p) {
+  using S = Smem<NT, STAGES, KA, ACCB>;
   static_assert(S::kTmemCols <= 512 && (S::kTmemCols & (S::kTmemCols - 1)) == 0, "TMEM cols");
   static_assert(NT % 16 == 0 && NT >= 16 && NT <= 256, "MMA N");
+  static_assert(!GATEUP || KA == 2, "gate/up tiles pair the gate and up rows");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -75,6 +80,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_w);
     prefetch_tmap(&tm_b0);
     prefetch_tmap(&tm_b1);
+    prefetch_tmap(&tm_b0w);
+    prefetch_tmap(&tm_b1w);
   }
   if (warp == 1) {
     tmem_alloc(tmem_holder, S::kTmemCols);
@@ -95,20 +102,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
         Tile t;
         decode_tile<GATEUP, NT>(p, tile, t);
+        const bool wide = t.ntok == NT;   // full token tile: one TMA box of NT rows
         const int nbox = (t.ntok + kBoxRows - 1) / kBoxRows;
-        const uint32_t bytes = S::kA * kATileBytes + (uint32_t)nbox * kBBoxBytes;
-        const int wrow = t.e * p.rows_per_expert + t.mt * kBM;
-        const CUtensorMap* bmap = (GATEUP && t.shared) ? &tm_b1 : &tm_b0;
+        const uint32_t bytes = KA * kATileBytes + (uint32_t)nbox * kBBoxBytes;
+        // gate/up: 128 features, rows [f0, f0+128) (gate) and [f + f0, ...) (up);
+        // down: KA consecutive 128-row tiles of W_d
+        const int wrow = t.e * p.rows_per_expert + t.mt * (GATEUP ? kBM : kBM * KA);
+        const int wrow1 = GATEUP ? wrow + p.f : wrow + kBM;   // second weight tile
+        const bool sh = GATEUP && t.shared;
+        const CUtensorMap* bmap = sh ? &tm_b1 : &tm_b0;
+        const CUtensorMap* bmapw = sh ? &tm_b1w : &tm_b0w;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!wait_bar(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
           uint8_t* st = smem + stage * S::kStageBytes;
           mbar_arrive_expect_tx(&full[stage], bytes);
           tma_load_2d(st, &tm_w, &full[stage], kb * kBK, wrow, pol_w);
-          if (GATEUP) tma_load_2d(st + kATileBytes, &tm_w, &full[stage], kb * kBK, wrow + p.f, pol_w);
-          uint8_t* bt = st + S::kA * kATileBytes;
-          for (int i = 0; i < nbox; ++i)
-            tma_load_2d(bt + i * kBBoxBytes, bmap, &full[stage], kb * kBK, t.brow0 + i * kBoxRows,
-                        pol_b);
+          if (KA == 2) tma_load_2d(st + kATileBytes, &tm_w, &full[stage], kb * kBK, wrow1, pol_w);
+          uint8_t* bt = st + KA * kATileBytes;
+          if (wide) {
+            tma_load_2d(bt, bmapw, &full[stage], kb * kBK, t.brow0, pol_b);
+          } else {
+            for (int i = 0; i < nbox; ++i)
+              tma_load_2d(bt + i * kBBoxBytes, bmap, &full[stage], kb * kBK,
+                          t.brow0 + i * kBoxRows, pol_b);
+          }
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
       }
@@ -138,24 +155,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t st = smem_u32(smem + stage * S::kStageBytes);
           const uint64_t da = sw128_desc(st);
           const uint64_t du = sw128_desc(st + kATileBytes);
-          const uint64_t db = sw128_desc(st + S::kA * kATileBytes);
+          const uint64_t db = sw128_desc(st + KA * kATileBytes);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint32_t accum = (kb | kk) ? 1u : 0u;
             mma_bf16_ss(d0, da + 2 * kk, db + 2 * kk, idesc, accum);
-            if (GATEUP) mma_bf16_ss(d0 + NT, du + 2 * kk, db + 2 * kk, idesc, accum);
+            if (KA == 2) mma_bf16_ss(d0 + NT, du + 2 * kk, db + 2 * kk, idesc, accum);
           }
           mma_commit(&empty[stage]);  // frees the stage once these MMAs have read it
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
         mma_commit(&acc_full[acc]);   // accumulator ready for the epilogue
-        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        if (++acc == ACCB) { acc = 0; acc_phase ^= 1u; }
       }
     }
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
-    run_epilogue<GATEUP, NT, S::kAccCols>(p, total, tmem_base, acc_full, acc_empty, abort_flag);
+    run_epilogue<GATEUP, NT, S::kAccCols, KA, ACCB>(p, total, tmem_base, acc_full, acc_empty,
+                                                    abort_flag);
   }
 
   tc_fence_before();
@@ -166,25 +184,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <bool GATEUP, int NT, int STAGES>
+template <bool GATEUP, int NT, int STAGES, int KA, int ACCB>
 cudaError_t launch_variant(const CUtensorMap& w, const CUtensorMap& b0, const CUtensorMap& b1,
-                           const TcParams& p, cudaStream_t st) {
-  using S = Smem<GATEUP, NT, STAGES>;
+                           const CUtensorMap& b0w, const CUtensorMap& b1w, const TcParams& p,
+                           cudaStream_t st) {
+  using S = Smem<NT, STAGES, KA, ACCB>;
   static_assert(S::kTotal <= 227 * 1024, "shared memory");
-  auto kern = k_tc_ffn<GATEUP, NT, STAGES>;
+  auto kern = k_tc_ffn<GATEUP, NT, STAGES, KA, ACCB>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)S::kTotal);
   if (e != cudaSuccess) return e;
-  kern<<<num_sms(), kThreads, S::kTotal, st>>>(w, b0, b1, p);
+  kern<<<num_sms(), kThreads, S::kTotal, st>>>(w, b0, b1, b0w, b1w, p);
   count_launches(1);
   return cudaGetLastError();
 }
 
+// Weight rows per down-pass tile: two 128-row tiles share the token tile in the prefill
+// variant when d allows it.
+bool down_pairs(int d, bool decode) { return !decode && d % 256 == 0; }
+
 }  // namespace
 
 int tc_tile_tokens(bool gateup, bool decode) {
-  if (decode) return 64;
-  return gateup ? 128 : 256;
+  (void)gateup;
+  return decode ? 64 : 256;
+}
+
+int tc_tile_rows(bool gateup, bool decode, int d) {
+  return (!gateup && down_pairs(d, decode)) ? 2 * kBM : kBM;
 }
 
 cudaError_t launch_tc(const FfnArgs& a, const int32_t* prefix, bool gateup, bool decode,
@@ -193,7 +220,7 @@ cudaError_t launch_tc(const FfnArgs& a, const int32_t* prefix, bool gateup, bool
   p.T = a.T; p.k = a.k; p.E = a.E; p.n_shared = a.n_shared;
   p.f = a.f; p.d = a.d;
   p.K = gateup ? a.d : a.f;
-  p.mtiles = (gateup ? a.f : a.d) / kBM;
+  p.mtiles = (gateup ? a.f : a.d) / tc_tile_rows(gateup, decode, a.d);
   p.rows_per_expert = gateup ? 2 * a.f : a.d;
   p.offsets = a.offsets;
   p.prefix = prefix;
@@ -203,23 +230,29 @@ cudaError_t launch_tc(const FfnArgs& a, const int32_t* prefix, bool gateup, bool
   const uint64_t E1 = (uint64_t)a.E + a.n_shared;
   const uint64_t routed = (uint64_t)a.T * a.k;
   const uint64_t slots = routed + (uint64_t)a.n_shared * a.T;
-  CUtensorMap w, b0, b1;
+  const uint32_t nt = (uint32_t)tc_tile_tokens(gateup, decode);
+  CUtensorMap w, b0, b1, b0w, b1w;
   cudaError_t e;
   if (gateup) {
     e = encode_bf16_2d(&w, a.w13, E1 * 2 * a.f, a.d, kBM);
     if (e == cudaSuccess) e = encode_bf16_2d(&b0, a.x_perm, routed ? routed : 1, a.d, kBoxRows);
     if (e == cudaSuccess) e = encode_bf16_2d(&b1, a.x, a.T, a.d, kBoxRows);
+    if (e == cudaSuccess) e = encode_bf16_2d(&b0w, a.x_perm, routed ? routed : 1, a.d, nt);
+    if (e == cudaSuccess) e = encode_bf16_2d(&b1w, a.x, a.T, a.d, nt);
   } else {
     e = encode_bf16_2d(&w, a.w2, E1 * a.d, a.f, kBM);
     if (e == cudaSuccess) e = encode_bf16_2d(&b0, a.h, slots, a.f, kBoxRows);
+    if (e == cudaSuccess) e = encode_bf16_2d(&b0w, a.h, slots, a.f, nt);
     b1 = b0;
+    b1w = b0w;
   }
   if (e != cudaSuccess) return e;
   if (gateup)
-    return decode ? launch_variant<true, 64, 5>(w, b0, b1, p, st)
-                  : launch_variant<true, 128, 4>(w, b0, b1, p, st);
-  return decode ? launch_variant<false, 64, 8>(w, b0, b1, p, st)
-                : launch_variant<false, 256, 4>(w, b0, b1, p, st);
+    return decode ? launch_variant<true, 64, 5, 2, 2>(w, b0, b1, b0w, b1w, p, st)
+                  : launch_variant<true, 256, 3, 2, 1>(w, b0, b1, b0w, b1w, p, st);
+  if (decode) return launch_variant<false, 64, 8, 1, 2>(w, b0, b1, b0w, b1w, p, st);
+  return down_pairs(a.d, decode) ? launch_variant<false, 256, 3, 2, 1>(w, b0, b1, b0w, b1w, p, st)
+                                 : launch_variant<false, 256, 4, 1, 2>(w, b0, b1, b0w, b1w, p, st);
 }
 
 }  // namespace moe

@@ -93,14 +93,16 @@ __device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity, int* s
 
 // Epilogue warps (four consecutive warps, so every TMEM lane quadrant is covered): for each
 // tile, wait for its accumulator, read it 16 columns at a time, and store SiLU(gate) * up as
-// bf16 h (gate/up pass) or the fp32 expert output (down pass); then hand the accumulator back.
-template <bool GATEUP, int NT, uint32_t ACC_COLS>
+// bf16 h (gate/up pass: gate in columns [0, NT), up in [NT, 2NT)) or the fp32 expert output
+// (down pass: KA weight tiles of 128 output rows each, tile a in columns [a*NT, (a+1)*NT));
+// then hand the accumulator back. ACCB accumulator buffers (1 or 2) rotate.
+template <bool GATEUP, int NT, uint32_t ACC_COLS, int KA = 1, int ACCB = 2>
 __device__ __forceinline__ void run_epilogue(const TcParams& p, int total, uint32_t tmem_base,
                                              uint64_t* acc_full, uint64_t* acc_empty,
                                              volatile int* abort_flag) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;                 // TMEM lane quadrant this warp may access
-  const int row = q * 32 + lane;          // weight row within the tile
+  const int row = q * 32 + lane;          // weight row within a 128-row tile
   uint32_t acc = 0, acc_phase = 0;
   for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
     Tile t;
@@ -109,12 +111,11 @@ __device__ __forceinline__ void run_epilogue(const TcParams& p, int total, uint3
     if (!wait_bar(&acc_full[acc], acc_phase, abort_flag, p.status)) break;
     tc_fence_after();
     const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * ACC_COLS;
-    const int orow = t.mt * kBM + row;    // output feature
-    for (int c0 = 0; c0 < npad; c0 += 16) {
-      uint32_t g[16];
-      tmem_ld16(tbase + c0, g);
-      if (GATEUP) {
-        uint32_t u[16];
+    if (GATEUP) {
+      const int orow = t.mt * kBM + row;  // output feature
+      for (int c0 = 0; c0 < npad; c0 += 16) {
+        uint32_t g[16], u[16];
+        tmem_ld16(tbase + c0, g);
         tmem_ld16(tbase + NT + c0, u);
         tmem_ld_wait2(g, u);
 #pragma unroll
@@ -126,19 +127,27 @@ __device__ __forceinline__ void run_epilogue(const TcParams& p, int total, uint3
             p.h[(size_t)(t.slot0 + n) * p.f + orow] = f32_to_bf16_rn(silu * uv);
           }
         }
-      } else {
-        tmem_ld_wait(g);
+      }
+    } else {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int n = c0 + j;
-          if (n < t.ntok) p.y_perm[(size_t)(t.slot0 + n) * p.d + orow] = __uint_as_float(g[j]);
+      for (int a = 0; a < KA; ++a) {
+        const int orow = t.mt * (kBM * KA) + a * kBM + row;
+        for (int c0 = 0; c0 < npad; c0 += 16) {
+          uint32_t g[16];
+          tmem_ld16(tbase + a * NT + c0, g);
+          tmem_ld_wait(g);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int n = c0 + j;
+            if (n < t.ntok) p.y_perm[(size_t)(t.slot0 + n) * p.d + orow] = __uint_as_float(g[j]);
+          }
         }
       }
     }
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(&acc_empty[acc]);
-    if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    if (++acc == ACCB) { acc = 0; acc_phase ^= 1u; }
   }
 }
 
