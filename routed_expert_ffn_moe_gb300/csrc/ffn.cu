@@ -116,7 +116,7 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32
   pa.nt_up = fp8 ? tc_fp8_tile_tokens(true, decode) : tc_tile_tokens(true, decode);
   pa.nt_dn = fp8 ? tc_fp8_tile_tokens(false, decode) : tc_tile_tokens(false, decode);
   pa.mt_up = s.f / 128;
-  pa.mt_dn = s.d / (fp8 ? 128 : tc_tile_rows(false, decode, s.d));
+  pa.mt_dn = s.d / tc_tile_rows(false, decode, s.d);
   pa.stride = s.E + 2;
   const int stride = pa.stride;
 

@@ -313,8 +313,8 @@ cudaError_t launch_variant(const CUtensorMap& w, const CUtensorMap& b0, const CU
 }  // namespace
 
 int tc_fp8_tile_tokens(bool gateup, bool decode) {
-  if (decode) return 32;
-  return gateup ? 64 : 128;
+  (void)gateup;
+  return decode ? 32 : 256;
 }
 
 cudaError_t launch_tc_fp8(const FfnArgs& a, const int32_t* prefix, bool gateup, bool decode,

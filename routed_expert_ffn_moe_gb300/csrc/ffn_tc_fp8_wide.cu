@@ -1,11 +1,18 @@
 // Expert FFN, tensor-core path for FP8 E4M3 expert weights, wide-tile variant for large token
-// batches (W8A16). Same passages and warp roles as ffn_tc_fp8.cu; the difference is where the
-// block scale goes. With 64-128 tokens per tile, scaling the token rows would cost as much as
-// converting the weights, so here the weights themselves are dequantised: eight converter warps
-// turn each 128x128 E4M3 block into bf16(code * scale) and store it straight into TMEM with
-// tcgen05.st (one weight row per TMEM lane), and the MMA (kind::f16, bf16 x bf16 -> fp32) reads
-// A from TMEM and the bf16 token tile from shared memory. Each weight is rounded once to bf16
-// (relative error <= 2^-9).
+// batches (W8A16). Same passages as ffn_tc_fp8.cu. With 256 tokens per tile the MMA is the
+// bottleneck, so the tile shape follows the bf16 prefill kernel (two 128-row weight tiles per
+// 256-token tile, 512 TMEM columns of accumulator) and the dequantisation moves to a shared-
+// memory stage of its own:
+//
+//   TMA        E4M3 codes (128 rows x 64 K per weight tile, 64-byte swizzle) and bf16 token rows
+//              (256 x 64 K, 128-byte swizzle) -> smem ring
+//   convert    8 warps: bf16(code * block scale) into a second smem ring in the 128-byte-swizzle
+//              K-major layout the MMA reads (each weight rounded once to bf16, <= 2^-9 relative)
+//   MMA        tcgen05.mma.kind::f16, bf16 x bf16 -> fp32, both operands from smem
+//   epilogue   TMEM -> SiLU(gate) * up -> bf16 h, or the fp32 expert output
+//
+// The token stage is released by the MMA (it reads the token rows), the code stage also by the
+// converters; the converted ring by the MMA.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -17,26 +24,20 @@ namespace {
 using namespace ptx;
 using namespace tc;
 
-constexpr int kQK = 128;                          // K per stage = one scale block
-constexpr uint32_t kQTileBytes = kBM * kQK;       // 16 KB of E4M3 codes
-constexpr int kConvWarps = 8;                     // two per TMEM lane quadrant
-constexpr int kThreadsQ = 32 * (6 + kConvWarps);  // producer, MMA, 4 epilogue, converters
-constexpr uint32_t kACols = kQK / 2;              // TMEM columns of one 128 x 128 bf16 tile
+constexpr uint32_t kCodeTileBytes = kBM * kBK;    // 128 rows x 64 codes = 8 KB
+constexpr int kConvWarps = 8;
+constexpr int kConvThreads = 32 * kConvWarps;
+constexpr int kThreadsW = 32 * 6 + kConvThreads;
 
-template <bool GATEUP, int NT, int STAGES, int ASTAGES>
-struct SmemQ {
-  static constexpr int kA = GATEUP ? 2 : 1;
-  static constexpr uint32_t kBHalf = (uint32_t)NT * kBK * 2;   // NT rows x 64 K bf16
-  static constexpr uint32_t kStageBytes = kA * kQTileBytes + 2 * kBHalf;
-  static constexpr uint32_t kTilesBytes = STAGES * kStageBytes;
-  static constexpr uint32_t kBarBytes = 8 * (2 * STAGES + 2 * ASTAGES + 4) + 16;
+template <int NT, int STAGES, int CSTAGES, int KA, int ACCB>
+struct SmemW {
+  static constexpr uint32_t kStageBytes = KA * kCodeTileBytes + (uint32_t)NT * kBK * 2;
+  static constexpr uint32_t kCSlotBytes = KA * kATileBytes;   // bf16 weight tiles
+  static constexpr uint32_t kTilesBytes = STAGES * kStageBytes + CSTAGES * kCSlotBytes;
+  static constexpr uint32_t kBarBytes = 8 * (2 * STAGES + 2 * CSTAGES + 4) + 16;
   static constexpr uint32_t kTotal = kTilesBytes + kBarBytes + 1024;
-  static constexpr uint32_t kAccCols = GATEUP ? 2 * NT : NT;
-  static constexpr uint32_t kAStageCols = kA * kACols;
-  static constexpr uint32_t kUsedCols = 2 * kAccCols + ASTAGES * kAStageCols;
-  static constexpr uint32_t kTmemCols =
-      kUsedCols <= 32 ? 32 : kUsedCols <= 64 ? 64 : kUsedCols <= 128 ? 128
-      : kUsedCols <= 256 ? 256 : 512;
+  static constexpr uint32_t kAccCols = KA * NT;
+  static constexpr uint32_t kTmemCols = ACCB * kAccCols;
 };
 
 // Two E4M3 codes (low byte first) times the block scale, as a bf16 pair (low element first).
@@ -47,22 +48,32 @@ __device__ __forceinline__ uint32_t dequant2(uint32_t two, float s) {
   return *reinterpret_cast<const uint32_t*>(&b);
 }
 
-template <bool GATEUP, int NT, int STAGES, int ASTAGES>
-__global__ void __launch_bounds__(kThreadsQ, 1)
-    k_tc_ffn_fp8_wide(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b0,
-                 const __grid_constant__ CUtensorMap tm_b1, const TcParams p,
-                 const float* __restrict__ scales) {
-  using S = SmemQ<GATEUP, NT, STAGES, ASTAGES>;
-  static_assert(S::kUsedCols <= 512, "TMEM columns");
-  static_assert(NT % 16 == 0 && NT >= 16 && NT <= 256, "MMA N");
+__device__ __forceinline__ void sts_u4(uint32_t addr, const uint4& v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+template <bool GATEUP, int NT, int STAGES, int CSTAGES, int KA, int ACCB>
+__global__ void __launch_bounds__(kThreadsW, 1)
+    k_tc_ffn_fp8_wide(const __grid_constant__ CUtensorMap tm_w,
+                      const __grid_constant__ CUtensorMap tm_b0,
+                      const __grid_constant__ CUtensorMap tm_b1,
+                      const __grid_constant__ CUtensorMap tm_b0w,
+                      const __grid_constant__ CUtensorMap tm_b1w, const TcParams p,
+                      const float* __restrict__ scales) {
+  using S = SmemW<NT, STAGES, CSTAGES, KA, ACCB>;
+  static_assert(S::kTmemCols <= 512 && (S::kTmemCols & (S::kTmemCols - 1)) == 0, "TMEM cols");
+  static_assert(!GATEUP || KA == 2, "gate/up tiles pair the gate and up rows");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
+  uint8_t* cslots = smem + STAGES * S::kStageBytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kTilesBytes);
   uint64_t* empty = full + STAGES;
-  uint64_t* a_full = empty + STAGES;
-  uint64_t* a_empty = a_full + ASTAGES;
-  uint64_t* acc_full = a_empty + ASTAGES;
+  uint64_t* c_full = empty + STAGES;
+  uint64_t* c_empty = c_full + CSTAGES;
+  uint64_t* acc_full = c_empty + CSTAGES;
   uint64_t* acc_empty = acc_full + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
@@ -70,17 +81,16 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E1 = p.E + p.n_shared;
   const int total = __ldg(p.prefix + E1);
-  const int kblocks = p.K / kQK;
-  constexpr uint32_t kConvThreads = 32 * kConvWarps;
+  const int kblocks = p.K / kBK;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConvThreads + 1);  // every converter thread + the MMA commit
+      mbar_init(&empty[s], kConvThreads + 1);  // converters read the codes, the MMA the tokens
     }
-    for (int s = 0; s < ASTAGES; ++s) {
-      mbar_init(&a_full[s], kConvThreads);
-      mbar_init(&a_empty[s], 1);
+    for (int s = 0; s < CSTAGES; ++s) {
+      mbar_init(&c_full[s], kConvThreads);
+      mbar_init(&c_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -91,6 +101,8 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
     prefetch_tmap(&tm_w);
     prefetch_tmap(&tm_b0);
     prefetch_tmap(&tm_b1);
+    prefetch_tmap(&tm_b0w);
+    prefetch_tmap(&tm_b1w);
   }
   if (warp == 1) {
     tmem_alloc(tmem_holder, S::kTmemCols);
@@ -100,7 +112,6 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-  const uint32_t acol0 = 2 * S::kAccCols;  // first TMEM column of the A ring
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -112,21 +123,28 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
         Tile t;
         decode_tile<GATEUP, NT>(p, tile, t);
+        const bool wide = t.ntok == NT;
         const int nbox = (t.ntok + kBoxRows - 1) / kBoxRows;
-        const uint32_t bytes = S::kA * kQTileBytes + (uint32_t)nbox * 2 * kBBoxBytes;
-        const int wrow = t.e * p.rows_per_expert + t.mt * kBM;
-        const CUtensorMap* bmap = (GATEUP && t.shared) ? &tm_b1 : &tm_b0;
+        const uint32_t bytes = KA * kCodeTileBytes + (uint32_t)nbox * kBBoxBytes;
+        const int wrow = t.e * p.rows_per_expert + t.mt * (GATEUP ? kBM : kBM * KA);
+        const int wrow1 = GATEUP ? wrow + p.f : wrow + kBM;
+        const bool sh = GATEUP && t.shared;
+        const CUtensorMap* bmap = sh ? &tm_b1 : &tm_b0;
+        const CUtensorMap* bmapw = sh ? &tm_b1w : &tm_b0w;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!wait_bar(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
           uint8_t* st = smem + stage * S::kStageBytes;
           mbar_arrive_expect_tx(&full[stage], bytes);
-          tma_load_2d(st, &tm_w, &full[stage], kb * kQK, wrow, pol_w);
-          if (GATEUP) tma_load_2d(st + kQTileBytes, &tm_w, &full[stage], kb * kQK, wrow + p.f, pol_w);
-          uint8_t* bt = st + S::kA * kQTileBytes;
-          for (int i = 0; i < nbox; ++i)
-            for (int hk = 0; hk < 2; ++hk)
-              tma_load_2d(bt + hk * S::kBHalf + i * kBBoxBytes, bmap, &full[stage],
-                          kb * kQK + hk * kBK, t.brow0 + i * kBoxRows, pol_b);
+          tma_load_2d(st, &tm_w, &full[stage], kb * kBK, wrow, pol_w);
+          if (KA == 2) tma_load_2d(st + kCodeTileBytes, &tm_w, &full[stage], kb * kBK, wrow1, pol_w);
+          uint8_t* bt = st + KA * kCodeTileBytes;
+          if (wide) {
+            tma_load_2d(bt, bmapw, &full[stage], kb * kBK, t.brow0, pol_b);
+          } else {
+            for (int i = 0; i < nbox; ++i)
+              tma_load_2d(bt + i * kBBoxBytes, bmap, &full[stage], kb * kBK,
+                          t.brow0 + i * kBoxRows, pol_b);
+          }
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
       }
@@ -138,7 +156,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      uint32_t stage = 0, phase = 0, astage = 0, aphase = 0;
+      uint32_t stage = 0, phase = 0, cs = 0, cphase = 0;
       uint32_t acc = 0, acc_phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
@@ -151,79 +169,80 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
         const uint32_t d0 = tmem_base + acc * S::kAccCols;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!wait_bar(&full[stage], phase, abort_flag, p.status) ||
-              !wait_bar(&a_full[astage], aphase, abort_flag, p.status)) { ok = false; break; }
+              !wait_bar(&c_full[cs], cphase, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t a0 = tmem_base + acol0 + astage * S::kAStageCols;
-          const uint32_t bst = smem_u32(smem + stage * S::kStageBytes + S::kA * kQTileBytes);
+          const uint32_t ca = smem_u32(cslots + cs * S::kCSlotBytes);
+          const uint64_t da = sw128_desc(ca);
+          const uint64_t du = sw128_desc(ca + kATileBytes);
+          const uint64_t db = sw128_desc(smem_u32(smem + stage * S::kStageBytes + KA * kCodeTileBytes));
 #pragma unroll
-          for (int kk = 0; kk < kQK / 16; ++kk) {
-            const uint64_t bd = sw128_desc(bst + (kk >> 2) * S::kBHalf) + 2 * (kk & 3);
+          for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint32_t accum = (kb | kk) ? 1u : 0u;
-            mma_ts(d0, a0 + kk * 8, bd, idesc, accum);
-            if (GATEUP) mma_ts(d0 + NT, a0 + kACols + kk * 8, bd, idesc, accum);
+            mma_bf16_ss(d0, da + 2 * kk, db + 2 * kk, idesc, accum);
+            if (KA == 2) mma_bf16_ss(d0 + NT, du + 2 * kk, db + 2 * kk, idesc, accum);
           }
-          mma_commit(&empty[stage]);    // token rows consumed
-          mma_commit(&a_empty[astage]); // dequantised weights consumed
+          mma_commit(&empty[stage]);   // token rows consumed
+          mma_commit(&c_empty[cs]);    // dequantised weights consumed
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-          if (++astage == ASTAGES) { astage = 0; aphase ^= 1u; }
+          if (++cs == CSTAGES) { cs = 0; cphase ^= 1u; }
         }
         if (!ok) break;
         mma_commit(&acc_full[acc]);
-        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        if (++acc == ACCB) { acc = 0; acc_phase ^= 1u; }
       }
     }
   } else if (warp < 6) {
     // ---------------- epilogue (warps 2..5) ----------------
-    run_epilogue<GATEUP, NT, S::kAccCols>(p, total, tmem_base, acc_full, acc_empty, abort_flag);
+    run_epilogue<GATEUP, NT, S::kAccCols, KA, ACCB>(p, total, tmem_base, acc_full, acc_empty,
+                                                    abort_flag);
   } else {
     // ---------------- dequantisers (warps 6..13) ----------------
-    const int q = warp & 3;                   // TMEM lane quadrant
-    const int hk = (warp - 6) >> 2;           // which 64-wide half of the stage's K
-    const int row = q * 32 + lane;            // weight row within the tile = TMEM lane
-    const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
-    const int kbl = p.K / 128;                // scale blocks along K
-    uint32_t stage = 0, phase = 0, astage = 0, aphase = 0;
+    // task = (weight tile a, row r, 16-code chunk j): 16 codes -> two 16-byte bf16 chunks
+    const int ct = threadIdx.x - 192;
+    const int kbl = p.K / 128;               // scale blocks along K
+    uint32_t stage = 0, phase = 0, cs = 0, cphase = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
       Tile t;
       decode_tile<GATEUP, NT>(p, tile, t);
       const float* sc = scales + (size_t)t.e * (p.rows_per_expert / 128) * kbl;
-      const int rb_g = t.mt, rb_u = p.f / 128 + t.mt;
+      const int rb0 = GATEUP ? t.mt : t.mt * KA;   // scale row block of the first weight tile
+      const int rb1 = GATEUP ? p.f / 128 + t.mt : rb0 + 1;
       for (int kb = 0; kb < kblocks; ++kb) {
         if (!wait_bar(&full[stage], phase, abort_flag, p.status) ||
-            !wait_bar(&a_empty[astage], aphase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+            !wait_bar(&c_empty[cs], cphase ^ 1u, abort_flag, p.status)) { ok = false; break; }
         const uint32_t st = smem_u32(smem + stage * S::kStageBytes);
-        uint4 raw[S::kA][4];
+        const uint32_t dst = smem_u32(cslots + cs * S::kCSlotBytes);
+        const float s0 = __ldg(sc + rb0 * kbl + (kb >> 1));
+        const float s1 = KA == 2 ? __ldg(sc + rb1 * kbl + (kb >> 1)) : 0.f;
 #pragma unroll
-        for (int o = 0; o < S::kA; ++o)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t chunk = (uint32_t)(4 * hk + j) ^ (uint32_t)(row & 7);  // 128B swizzle
-            raw[o][j] = lds_u4(st + o * kQTileBytes + row * 128 + (chunk << 4));
-          }
-        mbar_arrive(&empty[stage]);           // this thread is done with the E4M3 bytes
-        float s_o[2];
-        s_o[0] = __ldg(sc + rb_g * kbl + kb);
-        s_o[1] = GATEUP ? __ldg(sc + rb_u * kbl + kb) : 0.f;
-#pragma unroll
-        for (int o = 0; o < S::kA; ++o) {
-          uint32_t out[32];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t w[4] = {raw[o][j].x, raw[o][j].y, raw[o][j].z, raw[o][j].w};
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-              out[j * 8 + 2 * m] = dequant2(w[m] & 0xFFFFu, s_o[o]);
-              out[j * 8 + 2 * m + 1] = dequant2(w[m] >> 16, s_o[o]);
-            }
-          }
-          tmem_st32(lane_base + acol0 + astage * S::kAStageCols + o * kACols + hk * 32, out);
+        for (int i = 0; i < KA * kBM * 4 / kConvThreads; ++i) {
+          const int task = ct + i * kConvThreads;
+          const int a = task / (kBM * 4);
+          const int r = (task >> 2) & (kBM - 1);
+          const int j = task & 3;
+          // source: 64-byte rows, 64-byte swizzle (16-byte chunk j ^ ((r >> 1) & 3))
+          const uint4 raw = lds_u4(st + a * kCodeTileBytes + r * 64 + ((j ^ ((r >> 1) & 3)) << 4));
+          const float s = a ? s1 : s0;
+          uint4 lo, hi;  // codes 0..7 -> chunk 2j, codes 8..15 -> chunk 2j+1
+          lo.x = dequant2(raw.x & 0xFFFFu, s);
+          lo.y = dequant2(raw.x >> 16, s);
+          lo.z = dequant2(raw.y & 0xFFFFu, s);
+          lo.w = dequant2(raw.y >> 16, s);
+          hi.x = dequant2(raw.z & 0xFFFFu, s);
+          hi.y = dequant2(raw.z >> 16, s);
+          hi.z = dequant2(raw.w & 0xFFFFu, s);
+          hi.w = dequant2(raw.w >> 16, s);
+          // destination: 128-byte rows, 128-byte swizzle (16-byte chunk c ^ (r & 7))
+          const uint32_t rowb = dst + a * kATileBytes + r * 128;
+          sts_u4(rowb + (((2 * j) ^ (r & 7)) << 4), lo);
+          sts_u4(rowb + (((2 * j + 1) ^ (r & 7)) << 4), hi);
         }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(&a_full[astage]);
+        mbar_arrive(&empty[stage]);    // done with the codes of this stage
+        fence_proxy_async_smem();      // bf16 weights -> visible to the MMA
+        mbar_arrive(&c_full[cs]);
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-        if (++astage == ASTAGES) { astage = 0; aphase ^= 1u; }
+        if (++cs == CSTAGES) { cs = 0; cphase ^= 1u; }
       }
     }
   }
@@ -236,16 +255,17 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
   }
 }
 
-template <bool GATEUP, int NT, int STAGES, int ASTAGES>
+template <bool GATEUP, int NT, int STAGES, int CSTAGES, int KA, int ACCB>
 cudaError_t launch_variant(const CUtensorMap& w, const CUtensorMap& b0, const CUtensorMap& b1,
-                           const TcParams& p, const float* scales, cudaStream_t st) {
-  using S = SmemQ<GATEUP, NT, STAGES, ASTAGES>;
+                           const CUtensorMap& b0w, const CUtensorMap& b1w, const TcParams& p,
+                           const float* scales, cudaStream_t st) {
+  using S = SmemW<NT, STAGES, CSTAGES, KA, ACCB>;
   static_assert(S::kTotal <= 227 * 1024, "shared memory");
-  auto kern = k_tc_ffn_fp8_wide<GATEUP, NT, STAGES, ASTAGES>;
+  auto kern = k_tc_ffn_fp8_wide<GATEUP, NT, STAGES, CSTAGES, KA, ACCB>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)S::kTotal);
   if (e != cudaSuccess) return e;
-  kern<<<num_sms(), kThreadsQ, S::kTotal, st>>>(w, b0, b1, p, scales);
+  kern<<<num_sms(), kThreadsW, S::kTotal, st>>>(w, b0, b1, b0w, b1w, p, scales);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -254,11 +274,12 @@ cudaError_t launch_variant(const CUtensorMap& w, const CUtensorMap& b0, const CU
 
 cudaError_t launch_tc_fp8_wide(const FfnArgs& a, const int32_t* prefix, bool gateup,
                                cudaStream_t st) {
+  constexpr int NT = 256;
   TcParams p{};
   p.T = a.T; p.k = a.k; p.E = a.E; p.n_shared = a.n_shared;
   p.f = a.f; p.d = a.d;
   p.K = gateup ? a.d : a.f;
-  p.mtiles = (gateup ? a.f : a.d) / kBM;
+  p.mtiles = (gateup ? a.f : a.d) / tc_tile_rows(gateup, false, a.d);
   p.rows_per_expert = gateup ? 2 * a.f : a.d;
   p.offsets = a.offsets;
   p.prefix = prefix;
@@ -268,21 +289,27 @@ cudaError_t launch_tc_fp8_wide(const FfnArgs& a, const int32_t* prefix, bool gat
   const uint64_t E1 = (uint64_t)a.E + a.n_shared;
   const uint64_t routed = (uint64_t)a.T * a.k;
   const uint64_t slots = routed + (uint64_t)a.n_shared * a.T;
-  CUtensorMap w, b0, b1;
+  CUtensorMap w, b0, b1, b0w, b1w;
   cudaError_t e;
   if (gateup) {
-    e = encode_u8_2d(&w, a.w13, E1 * 2 * a.f, a.d, kBM);
+    e = encode_u8_2d(&w, a.w13, E1 * 2 * a.f, a.d, kBM, 64);
     if (e == cudaSuccess) e = encode_bf16_2d(&b0, a.x_perm, routed ? routed : 1, a.d, kBoxRows);
     if (e == cudaSuccess) e = encode_bf16_2d(&b1, a.x, a.T, a.d, kBoxRows);
+    if (e == cudaSuccess) e = encode_bf16_2d(&b0w, a.x_perm, routed ? routed : 1, a.d, NT);
+    if (e == cudaSuccess) e = encode_bf16_2d(&b1w, a.x, a.T, a.d, NT);
   } else {
-    e = encode_u8_2d(&w, a.w2, E1 * a.d, a.f, kBM);
+    e = encode_u8_2d(&w, a.w2, E1 * a.d, a.f, kBM, 64);
     if (e == cudaSuccess) e = encode_bf16_2d(&b0, a.h, slots, a.f, kBoxRows);
+    if (e == cudaSuccess) e = encode_bf16_2d(&b0w, a.h, slots, a.f, NT);
     b1 = b0;
+    b1w = b0w;
   }
   if (e != cudaSuccess) return e;
   const float* sc = gateup ? a.s13 : a.s2;
-  if (gateup) return launch_variant<true, 64, 4, 2>(w, b0, b1, p, sc, st);
-  return launch_variant<false, 128, 4, 4>(w, b0, b1, p, sc, st);
+  if (gateup) return launch_variant<true, NT, 3, 2, 2, 1>(w, b0, b1, b0w, b1w, p, sc, st);
+  if (tc_tile_rows(false, false, a.d) == 2 * kBM)
+    return launch_variant<false, NT, 3, 2, 2, 1>(w, b0, b1, b0w, b1w, p, sc, st);
+  return launch_variant<false, NT, 3, 2, 1, 2>(w, b0, b1, b0w, b1w, p, sc, st);
 }
 
 }  // namespace moe

@@ -188,18 +188,20 @@ inline cudaError_t encode_bf16_2d(CUtensorMap* m, const void* base, uint64_t row
 }
 
 
-// Row-major [rows, cols] byte matrix (E4M3 codes), box of box_rows x 128 bytes, 128-byte swizzle.
+// Row-major [rows, cols] byte matrix (E4M3 codes), box of box_rows x box_cols bytes, swizzled
+// to match the box width (128-byte rows: 128-byte swizzle; 64-byte rows: 64-byte swizzle).
 inline cudaError_t encode_u8_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
-                                uint32_t box_rows) {
+                                uint32_t box_rows, uint32_t box_cols = 128) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {cols};
-  const cuuint32_t box[2] = {128, box_rows};
+  const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        box_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
