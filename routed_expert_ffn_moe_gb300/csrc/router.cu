@@ -72,6 +72,75 @@ __global__ void __launch_bounds__(128) k_router_logits(const uint16_t* __restric
       }
 }
 
+// Same per-logit order as k_router_logits, for batches of 64+ tokens: a warp owns TT tokens x
+// TE experts and issues the fused multiply-adds of expert pairs as one packed two-lane FMA
+// (__ffma2_rn: two independent fp32 fmas, each rounded to nearest). Every accumulator still sees
+// exactly the sequence of the defined order, so the logits are bit-identical.
+template <int TT, int TE>
+__global__ void __launch_bounds__(256) k_router_logits_x2(const uint16_t* __restrict__ x,
+                                                          const uint16_t* __restrict__ wg,
+                                                          const float* __restrict__ bias, int T,
+                                                          int d, int E,
+                                                          float* __restrict__ logits) {
+  static_assert(TE % 2 == 0, "experts are paired");
+  // A block of 8 warps covers 4 token tiles x 2 expert tiles, so both operands are reused
+  // through L1 by the warps that share them.
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int n_et = (E + TE - 1) / TE;
+  const int n_eb = (n_et + 1) / 2;
+  const int bt = blockIdx.x / n_eb, be = blockIdx.x - bt * n_eb;
+  const int et = 2 * be + (w & 1);
+  const int t0 = (4 * bt + (w >> 1)) * TT, e0 = et * TE;
+  if (t0 >= T || et >= n_et) return;
+  float2 acc[TT][TE / 2];
+#pragma unroll
+  for (int t = 0; t < TT; ++t)
+#pragma unroll
+    for (int q = 0; q < TE / 2; ++q) acc[t][q] = make_float2(0.f, 0.f);
+  const int chunks = d >> 3;
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  for (int c = lane; c < chunks; c += 32) {
+    uint4 xv[TT], wv[TE];
+#pragma unroll
+    for (int t = 0; t < TT; ++t)
+      xv[t] = (t0 + t < T) ? ldg_u4(x + (size_t)(t0 + t) * d + 8 * c) : zero;
+#pragma unroll
+    for (int e = 0; e < TE; ++e)
+      wv[e] = (e0 + e < E) ? ldg_u4(wg + (size_t)(e0 + e) * d + 8 * c) : zero;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float2 w2[TE / 2];
+#pragma unroll
+      for (int q = 0; q < TE / 2; ++q)
+        w2[q] = make_float2(bf16x8_elem(wv[2 * q], i), bf16x8_elem(wv[2 * q + 1], i));
+#pragma unroll
+      for (int t = 0; t < TT; ++t) {
+        const float xf = bf16x8_elem(xv[t], i);
+        const float2 x2 = make_float2(xf, xf);
+#pragma unroll
+        for (int q = 0; q < TE / 2; ++q) acc[t][q] = __ffma2_rn(x2, w2[q], acc[t][q]);
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1)
+#pragma unroll
+    for (int t = 0; t < TT; ++t)
+#pragma unroll
+      for (int q = 0; q < TE / 2; ++q) {
+        acc[t][q].x = __fadd_rn(acc[t][q].x, __shfl_xor_sync(0xffffffffu, acc[t][q].x, off));
+        acc[t][q].y = __fadd_rn(acc[t][q].y, __shfl_xor_sync(0xffffffffu, acc[t][q].y, off));
+      }
+#pragma unroll
+  for (int t = 0; t < TT; ++t)
+#pragma unroll
+    for (int e = 0; e < TE; ++e)
+      if (((t * TE + e) & 31) == lane && t0 + t < T && e0 + e < E) {
+        const float a = (e & 1) ? acc[t][e >> 1].y : acc[t][e >> 1].x;
+        logits[(size_t)(t0 + t) * E + e0 + e] = bias ? __fadd_rn(a, bias[e0 + e]) : a;
+      }
+}
+
 // (value desc, index asc): is (la, ea) ranked before (lb, eb)?
 __device__ __forceinline__ bool ranks_before(float la, int ea, float lb, int eb) {
   return la > lb || (la == lb && ea < eb);
@@ -134,7 +203,13 @@ cudaError_t launch_logits(const uint16_t* x, const uint16_t* wg, const float* bi
                           int E, float* logits, cudaStream_t st) {
   const long warps = (long)((T + TT - 1) / TT) * ((E + TE - 1) / TE);
   const long blocks = (warps + 3) / 4;
-  k_router_logits<TT, TE><<<(unsigned)blocks, 128, 0, st>>>(x, wg, bias, T, d, E, logits);
+  if (TT == 1) {
+    k_router_logits<TT, TE><<<(unsigned)blocks, 128, 0, st>>>(x, wg, bias, T, d, E, logits);
+  } else {
+    const long n_tt = (T + TT - 1) / TT, n_eb = ((E + TE - 1) / TE + 1) / 2;
+    k_router_logits_x2<TT, TE><<<(unsigned)(((n_tt + 3) / 4) * n_eb), 256, 0, st>>>(
+        x, wg, bias, T, d, E, logits);
+  }
   return cudaGetLastError();
 }
 
