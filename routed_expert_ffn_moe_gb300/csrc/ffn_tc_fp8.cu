@@ -13,7 +13,8 @@
 // applied to the (few) token rows instead:
 //
 //   TMA       E4M3 weight tiles (128 rows x 128 K) and bf16 token tiles -> smem ring
-//   convert   8 warps: codes -> f16 (exact; one cvt per two codes) written straight into TMEM
+//   convert   2 groups of 4 warps, alternating stages: codes -> f16 (exact; one cvt per two
+//             codes) written straight into TMEM
 //             with tcgen05.st, one weight row per TMEM lane; token rows -> f16(s * x) written
 //             into a smem tile per weight matrix (gate and up have their own scale)
 //   MMA       tcgen05.mma.kind::f16 (f16 x f16 -> fp32) with A (codes) read from TMEM and B
@@ -39,7 +40,8 @@ using namespace tc;
 
 constexpr int kQK = 128;                          // K per stage = one scale block
 constexpr uint32_t kQTileBytes = kBM * kQK;       // 16 KB of E4M3 codes
-constexpr int kConvWarps = 8;                     // two per TMEM lane quadrant
+constexpr int kConvGroups = 2;                    // groups take alternate stages
+constexpr int kConvWarps = 4 * kConvGroups;       // a group = one warp per TMEM lane quadrant
 constexpr int kConvThreads = 32 * kConvWarps;
 constexpr int kThreadsQ = 32 * 6 + kConvThreads;  // producer, MMA, 4 epilogue, converters
 constexpr uint32_t kACols = kQK / 2;              // TMEM columns of one 128 x 128 f16 tile
@@ -114,10 +116,10 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConvThreads);    // every converter thread has read the stage
+      mbar_init(&empty[s], 4);               // the stage's converter group (4 warps) has read it
     }
     for (int s = 0; s < CSTAGES; ++s) {
-      mbar_init(&c_full[s], kConvThreads);   // converted operands written
+      mbar_init(&c_full[s], 4);              // converted operands written
       mbar_init(&c_empty[s], 1);             // MMA commit: converted operands consumed
     }
     for (int b = 0; b < 2; ++b) {
@@ -214,48 +216,67 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
     run_epilogue<GATEUP, NT, S::kAccCols>(p, total, tmem_base, acc_full, acc_empty, abort_flag);
   } else {
     // ---------------- converters (warps 6..13) ----------------
-    const int ct = threadIdx.x - 192;         // 0..255
+    // Group g (4 warps, one per TMEM lane quadrant) converts every stage i with i % 2 == g, the
+    // whole 128-wide K of its 32 rows, so two stages are converted at once.
+    const int grp = (warp - 6) >> 2;
+    const int gt = threadIdx.x - 192 - grp * 128;  // 0..127 within the group
     const int q = warp & 3;                   // TMEM lane quadrant
-    const int hk = (warp - 6) >> 2;           // which 64-wide half of the stage's K
     const int row = q * 32 + lane;            // weight row within the tile = TMEM lane
     const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
     const int kbl = p.K / 128;                // scale blocks along K
-    uint32_t stage = 0, phase = 0, cs = 0, cphase = 0;
+    uint32_t it = 0;                          // global stage counter
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
       Tile t;
       decode_tile<GATEUP, NT>(p, tile, t);
       const int npad = (t.ntok + 15) & ~15;
       const float* sc = scales + (size_t)t.e * (p.rows_per_expert / 128) * kbl;
-      const int rb_g = t.mt, rb_u = p.f / 128 + t.mt;
-      for (int kb = 0; kb < kblocks; ++kb) {
+      const float* sc_g = sc + t.mt * kbl;                   // gate (or down) row block
+      const float* sc_u = sc + (p.f / 128 + t.mt) * kbl;     // up row block
+      for (int kb = 0; kb < kblocks; ++kb, ++it) {
+        if ((int)(it % kConvGroups) != grp) continue;
+        const uint32_t stage = it % STAGES, phase = (it / STAGES) & 1u;
+        const uint32_t cs = it % CSTAGES, cphase = (it / CSTAGES) & 1u;
+        const float s_g = __ldg(sc_g + kb);
+        const float s_u = GATEUP ? __ldg(sc_u + kb) : 0.f;
         if (!wait_bar(&full[stage], phase, abort_flag, p.status) ||
             !wait_bar(&c_empty[cs], cphase ^ 1u, abort_flag, p.status)) { ok = false; break; }
         const uint32_t st = smem_u32(smem + stage * S::kStageBytes);
         const uint32_t bsrc = st + S::kA * kQTileBytes;
         const uint32_t bdst = smem_u32(cslots + cs * S::kCSlotBytes);
-        float s_o[2];
-        s_o[0] = __ldg(sc + rb_g * kbl + kb);
-        s_o[1] = GATEUP ? __ldg(sc + rb_u * kbl + kb) : 0.f;
-        // weight codes of this thread's row and K half -> exact f16 in TMEM
-        uint4 raw[S::kA][4];
+        // weight codes of this thread's row -> exact f16 in TMEM (no scale needed)
 #pragma unroll
         for (int o = 0; o < S::kA; ++o)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t chunk = (uint32_t)(4 * hk + j) ^ (uint32_t)(row & 7);  // 128B swizzle
-            raw[o][j] = lds_u4(st + o * kQTileBytes + row * 128 + (chunk << 4));
+          for (int hk = 0; hk < 2; ++hk) {
+            uint4 raw[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t chunk = (uint32_t)(4 * hk + j) ^ (uint32_t)(row & 7);  // 128B swizzle
+              raw[j] = lds_u4(st + o * kQTileBytes + row * 128 + (chunk << 4));
+            }
+            uint32_t out[32];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t w[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+#pragma unroll
+              for (int m = 0; m < 4; ++m) {
+                out[j * 8 + 2 * m] = codes_to_f16x2(w[m] & 0xFFFFu);
+                out[j * 8 + 2 * m + 1] = codes_to_f16x2(w[m] >> 16);
+              }
+            }
+            tmem_st32(lane_base + acol0 + cs * S::kAStageCols + o * kACols + hk * 32, out);
           }
         // token rows -> f16(s * x), same 128-byte-swizzled K-major layout as the TMA source
         const int units = S::kA * npad * 16;  // (operand, row, 16-byte chunk)
-        for (int u = ct; u < units; u += kConvThreads) {
+        for (int u = gt; u < units; u += 128) {
           const int o = u / (npad * 16);
           const int rem = u - o * npad * 16;
           const int n = rem >> 4, c = rem & 15;
           const uint32_t off = (uint32_t)(c >> 3) * S::kBHalf + (uint32_t)n * 128 +
                                ((uint32_t)((c & 7) ^ (n & 7)) << 4);
           const uint4 xv = lds_u4(bsrc + off);
-          const float s = o ? s_o[1] : s_o[0];
+          const float s = o ? s_u : s_g;
           uint4 r;
           r.x = f32x2_to_f16x2_sat(__uint_as_float(xv.x << 16) * s, __uint_as_float(xv.x & 0xFFFF0000u) * s);
           r.y = f32x2_to_f16x2_sat(__uint_as_float(xv.y << 16) * s, __uint_as_float(xv.y & 0xFFFF0000u) * s);
@@ -263,27 +284,14 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
           r.w = f32x2_to_f16x2_sat(__uint_as_float(xv.w << 16) * s, __uint_as_float(xv.w & 0xFFFF0000u) * s);
           sts_u4(bdst + o * 2 * S::kBHalf + off, r);
         }
-        mbar_arrive(&empty[stage]);           // this thread is done reading the TMA stage
-#pragma unroll
-        for (int o = 0; o < S::kA; ++o) {
-          uint32_t out[32];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t w[4] = {raw[o][j].x, raw[o][j].y, raw[o][j].z, raw[o][j].w};
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-              out[j * 8 + 2 * m] = codes_to_f16x2(w[m] & 0xFFFFu);
-              out[j * 8 + 2 * m + 1] = codes_to_f16x2(w[m] >> 16);
-            }
-          }
-          tmem_st32(lane_base + acol0 + cs * S::kAStageCols + o * kACols + hk * 32, out);
-        }
         fence_proxy_async_smem();             // scaled token tiles -> visible to the MMA
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&c_full[cs]);
-        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-        if (++cs == CSTAGES) { cs = 0; cphase ^= 1u; }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&empty[stage]);         // this warp is done reading the TMA stage
+          mbar_arrive(&c_full[cs]);
+        }
       }
     }
   }

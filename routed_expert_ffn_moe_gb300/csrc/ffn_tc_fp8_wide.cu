@@ -86,10 +86,10 @@ __global__ void __launch_bounds__(kThreadsW, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConvThreads + 1);  // converters read the codes, the MMA the tokens
+      mbar_init(&empty[s], kConvWarps + 1);  // converter warps read the codes, the MMA the tokens
     }
     for (int s = 0; s < CSTAGES; ++s) {
-      mbar_init(&c_full[s], kConvThreads);
+      mbar_init(&c_full[s], kConvWarps);
       mbar_init(&c_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -208,13 +208,16 @@ __global__ void __launch_bounds__(kThreadsW, 1)
       const float* sc = scales + (size_t)t.e * (p.rows_per_expert / 128) * kbl;
       const int rb0 = GATEUP ? t.mt : t.mt * KA;   // scale row block of the first weight tile
       const int rb1 = GATEUP ? p.f / 128 + t.mt : rb0 + 1;
+      // scales run one stage ahead so their load latency hides behind the conversion
+      float s0 = __ldg(sc + rb0 * kbl), s1 = KA == 2 ? __ldg(sc + rb1 * kbl) : 0.f;
       for (int kb = 0; kb < kblocks; ++kb) {
         if (!wait_bar(&full[stage], phase, abort_flag, p.status) ||
             !wait_bar(&c_empty[cs], cphase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+        const bool more = kb + 1 < kblocks;
+        const float s0_next = more ? __ldg(sc + rb0 * kbl + ((kb + 1) >> 1)) : 0.f;
+        const float s1_next = (KA == 2 && more) ? __ldg(sc + rb1 * kbl + ((kb + 1) >> 1)) : 0.f;
         const uint32_t st = smem_u32(smem + stage * S::kStageBytes);
         const uint32_t dst = smem_u32(cslots + cs * S::kCSlotBytes);
-        const float s0 = __ldg(sc + rb0 * kbl + (kb >> 1));
-        const float s1 = KA == 2 ? __ldg(sc + rb1 * kbl + (kb >> 1)) : 0.f;
 #pragma unroll
         for (int i = 0; i < KA * kBM * 4 / kConvThreads; ++i) {
           const int task = ct + i * kConvThreads;
@@ -238,9 +241,14 @@ __global__ void __launch_bounds__(kThreadsW, 1)
           sts_u4(rowb + (((2 * j) ^ (r & 7)) << 4), lo);
           sts_u4(rowb + (((2 * j + 1) ^ (r & 7)) << 4), hi);
         }
-        mbar_arrive(&empty[stage]);    // done with the codes of this stage
         fence_proxy_async_smem();      // bf16 weights -> visible to the MMA
-        mbar_arrive(&c_full[cs]);
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&empty[stage]);  // this warp is done with the codes of this stage
+          mbar_arrive(&c_full[cs]);
+        }
+        s0 = s0_next;
+        s1 = s1_next;
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         if (++cs == CSTAGES) { cs = 0; cphase ^= 1u; }
       }

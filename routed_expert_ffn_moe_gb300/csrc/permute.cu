@@ -55,21 +55,28 @@ __global__ void __launch_bounds__(256) k_perm_count(const int32_t* __restrict__ 
     for (int e = lane; e < E; e += 32) hist[(size_t)e * nchunk + chunk] = __popc(sel[e]);
 }
 
-// One block: exclusive scan of hist (expert-major) into base; expert offsets from it.
+// One block: exclusive scan of hist (expert-major) into base; expert offsets from it. The array
+// is walked in coalesced 4096-entry pieces (4 per thread, int4 loads), each block-scanned and
+// offset by the running total of the pieces before it.
 __global__ void __launch_bounds__(1024) k_perm_scan(const int32_t* __restrict__ hist, int E,
                                                     int nchunk, int T, int k, int n_shared,
                                                     int32_t* __restrict__ base,
                                                     int32_t* __restrict__ offsets) {
   const long n = (long)E * nchunk;
-  const long per = (n + blockDim.x - 1) / blockDim.x;
-  const long beg = per * threadIdx.x, end = beg + per < n ? beg + per : n;
-  int s = 0;
-  for (long i = beg; i < end; ++i) s += hist[i];
-  int total;
-  int run = block_exclusive_scan(s, &total);
-  for (long i = beg; i < end; ++i) {
-    base[i] = run;
-    run += hist[i];
+  int carry = 0;
+  for (long b0 = 0; b0 < n; b0 += 4L * blockDim.x) {
+    const long i0 = b0 + 4L * threadIdx.x;
+    int v[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) v[q] = (i0 + q < n) ? hist[i0 + q] : 0;
+    int total;
+    int run = carry + block_exclusive_scan(v[0] + v[1] + v[2] + v[3], &total);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (i0 + q < n) base[i0 + q] = run;
+      run += v[q];
+    }
+    carry += total;
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x)

@@ -34,6 +34,7 @@ __global__ void __launch_bounds__(128) k_router_logits(const uint16_t* __restric
     for (int e = 0; e < TE; ++e) acc[t][e] = 0.f;
   const int chunks = d >> 3;
   const uint4 zero = make_uint4(0, 0, 0, 0);
+#pragma unroll 4
   for (int c = lane; c < chunks; c += 32) {
     uint4 xv[TT], wv[TE];
 #pragma unroll
@@ -213,6 +214,16 @@ cudaError_t launch_logits(const uint16_t* x, const uint16_t* wg, const float* bi
   return cudaGetLastError();
 }
 
+// Tile shape by batch: few tokens -> few experts per warp (more warps in flight for the
+// latency-bound case); 64+ tokens -> register-tiled packed-FMA kernel.
+cudaError_t launch_logits_for(const moe_shape& s, const uint16_t* x, const uint16_t* wg,
+                              const float* bias, float* logits, cudaStream_t st) {
+  if (s.T <= 8) return launch_logits<1, 2>(x, wg, bias, s.T, s.d, s.E, logits, st);
+  if (s.T <= 32) return launch_logits<1, 4>(x, wg, bias, s.T, s.d, s.E, logits, st);
+  if (s.T < 64) return launch_logits<1, 8>(x, wg, bias, s.T, s.d, s.E, logits, st);
+  return launch_logits<4, 8>(x, wg, bias, s.T, s.d, s.E, logits, st);
+}
+
 }  // namespace
 
 // ---- router without a caller-provided workspace ------------------------------------------
@@ -251,10 +262,7 @@ cudaError_t launch_route_noalloc(const moe_shape& s, const uint16_t* x, const ui
   float* logits = nullptr;
   cudaError_t e = noalloc_logits_ptr(&logits);
   if (e != cudaSuccess || s.T == 0) return e;
-  if (s.T < 64)
-    e = launch_logits<1, 8>(x, wg, bias, s.T, s.d, s.E, logits, st);
-  else
-    e = launch_logits<4, 8>(x, wg, bias, s.T, s.d, s.E, logits, st);
+  e = launch_logits_for(s, x, wg, bias, logits, st);
   if (e != cudaSuccess) return e;
   k_router_topk<<<(unsigned)((s.T + 7) / 8), 256, 0, st>>>(logits, s.T, s.E, s.k, topk_idx, topk_w);
   count_launches(2);
@@ -266,11 +274,7 @@ cudaError_t launch_route(const moe_shape& s, const uint16_t* x, const uint16_t* 
                          const WsLayout& L, cudaStream_t st) {
   if (s.T == 0) return cudaSuccess;
   float* logits = reinterpret_cast<float*>(ws + L.logits);
-  cudaError_t e;
-  if (s.T < 64)
-    e = launch_logits<1, 8>(x, wg, bias, s.T, s.d, s.E, logits, st);
-  else
-    e = launch_logits<4, 8>(x, wg, bias, s.T, s.d, s.E, logits, st);
+  cudaError_t e = launch_logits_for(s, x, wg, bias, logits, st);
   if (e != cudaSuccess) return e;
   k_router_topk<<<(unsigned)((s.T + 7) / 8), 256, 0, st>>>(logits, s.T, s.E, s.k, topk_idx, topk_w);
   count_launches(2);
