@@ -40,6 +40,8 @@ def parse_args():
     p.add_argument("--config", default="v3_decode")
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-graph", action="store_true",
+                   help="launch the four calls eagerly each step instead of replaying a CUDA graph")
     p.add_argument("--e2e-steps", type=int, default=None)
     p.add_argument("--T", type=int, default=None, help="override the token batch (profiling cases)")
     p.add_argument("--E", type=int, default=None, help="override the routed experts (profiling cases)")
@@ -251,7 +253,7 @@ def main():
 
     dev = synth.device_inputs(cfg)
     w = {k: dev[k] for k in ("wg", "bias", "w13", "w2", "s13", "s2")}
-    x = dev["x"]
+    x = dev["x"]                       # the layer's input buffer (also the e2e copy target)
     layer = moe.MoeLayer(cfg.T, cfg.d, cfg.E, cfg.k, cfg.f, cfg.n_shared, cfg.wdtype, w)
     stream = torch.cuda.current_stream()
 
@@ -265,20 +267,43 @@ def main():
             dist.barrier()
         torch.cuda.synchronize()
 
+    # One step = one layer pass. By default the four calls are captured once into a CUDA graph
+    # (the library enqueues no synchronisation or allocation) and the graph is replayed; the
+    # library's phase events are captured with it and re-recorded by every replay.
+    graph = None
+    if not args.no_graph:
+        moe.moe_profile_enable(True)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            layer.forward(x)
+        for _ in range(2):
+            graph.replay()
+        torch.cuda.synchronize()
+        launches_per_step = moe.moe_profile_read()["kernel_launches"]  # counted at capture
+
+    def step():
+        if graph is not None:
+            graph.replay()
+        else:
+            layer.forward(x)
+
     # ---- timed region: K steps on device-resident inputs --------------------------------
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     with ClockSampler(local_rank) as clocks:
-        moe.moe_profile_enable(True)
+        if graph is None:
+            moe.moe_profile_enable(True)
         start.record(stream)
         for _ in range(args.steps):
-            layer.forward(x)
+            step()
         end.record(stream)
         torch.cuda.synchronize()
         moe.moe_profile_enable(False)
     barrier()
     ms = start.elapsed_time(end) / args.steps
     prof = moe.moe_profile_read()
+    if graph is not None:  # phase events hold the last replay; launches counted at capture
+        prof["kernel_launches"] = launches_per_step * args.steps
     moe.moe_check_device_status(layer.ws)
 
     # ---- end to end: pinned host x -> device, the layer, y -> pinned host ----------------
@@ -286,13 +311,12 @@ def main():
     x_host = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
     x_host.copy_(x)
     y_host = torch.empty(layer.y.shape, dtype=layer.y.dtype, pin_memory=True)
-    x_in = torch.empty_like(x)
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(e2e_steps):
-        x_in.copy_(x_host, non_blocking=True)
-        layer.forward(x_in)
+        x.copy_(x_host, non_blocking=True)
+        step()
         y_host.copy_(layer.y, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -331,6 +355,7 @@ def main():
         "dtype": "bf16" if cfg.wdtype == "bf16" else "fp8_e4m3 weights, bf16 activations",
         "data": "synthetic",
         "config": {"workload": workload_desc(cfg), "T": cfg.T, "parallelism": f"replicas x{world}",
+                   "launch": "eager" if graph is None else "CUDA graph replay of the four calls",
                    "l2": "inputs larger than L2 (expert weights "
                          f"{(cfg.E + cfg.n_shared) * R.expert_bytes(cfg.d, cfg.f, cfg.wdtype) / 1e9:.1f} GB), no flush",
                    "experts_hit": n_hit,

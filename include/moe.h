@@ -160,6 +160,8 @@ MOE_API moe_status moe_check_device_status(void* ws, void* stream);
  * between them and its down kernels, and after -- and every call counts the kernels it
  * launches. Events are created by the library while a session is on (host-side objects; no
  * device memory is allocated). moe_profile_enable(0) stops recording.
+ * The events are recorded as external events, so a moe_expert_ffn call captured into a CUDA
+ * graph records them on every replay (moe_profile_read then reports the latest replay).
  * moe_profile_read waits for the recorded events and returns the summed device milliseconds of
  * the gate/up and down phases over the session, the number of moe_expert_ffn calls timed, and
  * the number of kernels launched by all four calls; any output pointer may be NULL. */

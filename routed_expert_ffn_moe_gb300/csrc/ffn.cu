@@ -71,6 +71,16 @@ __global__ void __launch_bounds__(256) k_gather_rows(const uint16_t* __restrict_
       __ldg(reinterpret_cast<const uint4*>(x + (long)t * d) + c);
 }
 
+// Phase events are recorded as external events while the stream is being captured into a CUDA
+// graph (so every replay records them) and as plain events otherwise.
+void record_phase(cudaEvent_t ev, cudaStream_t st) {
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaStreamIsCapturing(st, &cap);
+  cudaEventRecordWithFlags(ev, st,
+                           cap == cudaStreamCaptureStatusActive ? cudaEventRecordExternal
+                                                                : cudaEventRecordDefault);
+}
+
 // Token count from which an expert runs on the tensor cores (default 1: all of them).
 int tc_min_tokens() {
   const char* v = getenv("MOE_TC_MIN_TOKENS");
@@ -132,7 +142,7 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32
     count_launches(1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  if (ev.begin) cudaEventRecord(ev.begin, st);
+  if (ev.begin) record_phase(ev.begin, st);
 
   // Upper bound on the weight-streaming work: every slot in its own group plus one partial
   // group per expert (the device-side totals are usually far smaller).
@@ -150,11 +160,11 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32
   if (e == cudaSuccess)
     e = launch_gemv(a, plan + kPlanGemvUp * stride, plan + kPlanGemvDown * stride, true, max_up, st);
   if (e != cudaSuccess) return e;
-  if (ev.mid) cudaEventRecord(ev.mid, st);
+  if (ev.mid) record_phase(ev.mid, st);
   if (use_tc) e = tc(false, plan + kPlanTcDown * stride);
   if (e == cudaSuccess)
     e = launch_gemv(a, plan + kPlanGemvUp * stride, plan + kPlanGemvDown * stride, false, max_dn, st);
-  if (ev.end) cudaEventRecord(ev.end, st);
+  if (ev.end) record_phase(ev.end, st);
   return e;
 }
 

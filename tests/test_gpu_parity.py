@@ -160,6 +160,28 @@ def test_layer_is_deterministic():
     assert torch().equal(ia, b.topk_idx) and torch().equal(pa, b.perm_token)
 
 
+@pytest.mark.parametrize("over", [{}, {"wdtype": "fp8", "T": 70, "E": 12, "k": 3, "d": 512, "f": 384}])
+def test_layer_replays_from_a_cuda_graph(over):
+    # the four calls enqueue no synchronisation or allocation, so they can be captured once
+    cfg = synth.get_config("tiny", **over)
+    inp = synth.host_inputs(cfg)
+    w = device_weights(cfg, inp)
+    x = bf16_dev(inp.x)
+    eager = run_layer(cfg, x, w).y.clone()
+    layer = moe.MoeLayer(cfg.T, cfg.d, cfg.E, cfg.k, cfg.f, cfg.n_shared, cfg.wdtype, w)
+    layer.forward(x)
+    torch().cuda.synchronize()
+    g = torch().cuda.CUDAGraph()
+    with torch().cuda.graph(g):
+        layer.forward(x)
+    layer.y.zero_()
+    for _ in range(2):
+        g.replay()
+    torch().cuda.synchronize()
+    moe.moe_check_device_status(layer.ws)
+    assert torch().equal(eager.view(torch().int16), layer.y.view(torch().int16))
+
+
 # ---- full-size workloads --------------------------------------------------------------------
 
 def test_device_generator_matches_host_generator():
