@@ -154,6 +154,15 @@ MOE_API moe_status moe_combine(const moe_shape* shape, const float* y_perm, cons
  * MOE_ERR_CUDA if the read itself fails). */
 MOE_API moe_status moe_check_device_status(void* ws, void* stream);
 
+/* Failure-path self-test (no counterpart on the pages). Launches one kernel whose single thread
+ * waits on a shared-memory mbarrier that nothing ever completes, using the same bounded-wait
+ * pattern as the tensor-core pipelines but with a limit of `limit_us` microseconds
+ * (1 .. 2,000,000; MOE_ERR_INVALID_ARG otherwise). When the limit passes the kernel records
+ * MOE_ERR_DEVICE_TIMEOUT in the status word of `ws` (first error wins) and returns, so the
+ * context stays usable; moe_check_device_status() then reports and clears it. `ws` is a
+ * workspace of any shape (only its status word is touched). Asynchronous like the other calls. */
+MOE_API moe_status moe_selftest_bounded_wait(void* ws, uint32_t limit_us, void* stream);
+
 /* Phase timing for benchmarks and profilers (no counterpart on the pages).
  * moe_profile_enable(1) starts a session (and clears the previous one): from then on every
  * moe_expert_ffn call records three CUDA events on its stream -- before its gate/up kernels,

@@ -13,7 +13,8 @@ import os
 __all__ = ["MoeError", "MoeShape", "MOE_W_BF16", "MOE_W_FP8_E4M3_B128", "load", "lib_path",
            "moe_workspace_size", "moe_route", "moe_route_noalloc", "moe_permute",
            "moe_expert_ffn", "moe_combine",
-           "moe_check_device_status", "moe_profile_enable", "moe_profile_read",
+           "moe_check_device_status", "moe_selftest_bounded_wait", "moe_profile_enable",
+           "moe_profile_read",
            "moe_last_error_string", "shape_of", "MoeLayer", "EXPORTED"]
 
 MOE_W_BF16, MOE_W_FP8_E4M3_B128 = 0, 1
@@ -21,8 +22,8 @@ STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED",
           -3: "MOE_ERR_WORKSPACE", -4: "MOE_ERR_CUDA", -5: "MOE_ERR_DEVICE_TIMEOUT",
           -6: "MOE_ERR_DEVICE_BOUNDS"}
 EXPORTED = ("moe_workspace_size", "moe_route", "moe_route_noalloc", "moe_permute", "moe_expert_ffn", "moe_combine",
-            "moe_check_device_status", "moe_profile_enable", "moe_profile_read",
-            "moe_last_error_string")
+            "moe_check_device_status", "moe_selftest_bounded_wait", "moe_profile_enable",
+            "moe_profile_read", "moe_last_error_string")
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 
@@ -72,6 +73,8 @@ def load():
     L.moe_combine.argtypes = [shp, vp, vp, vp, vp, vp, sz, vp]
     L.moe_check_device_status.restype = i32
     L.moe_check_device_status.argtypes = [vp, vp]
+    L.moe_selftest_bounded_wait.restype = i32
+    L.moe_selftest_bounded_wait.argtypes = [vp, ctypes.c_uint32, vp]
     L.moe_profile_enable.restype = i32
     L.moe_profile_enable.argtypes = [i32]
     L.moe_profile_read.restype = i32
@@ -165,6 +168,13 @@ def moe_combine(shape, y_perm, inv_slot, topk_w, y, ws, stream=None, ws_bytes=No
 
 def moe_check_device_status(ws, stream=None):
     _check(load().moe_check_device_status(_ptr(ws), _stream(stream)), "moe_check_device_status")
+
+
+def moe_selftest_bounded_wait(ws, limit_us, stream=None):
+    """Launches a kernel whose wait never completes; after `limit_us` it records
+    MOE_ERR_DEVICE_TIMEOUT in ws's status word (read it with moe_check_device_status)."""
+    _check(load().moe_selftest_bounded_wait(_ptr(ws), int(limit_us), _stream(stream)),
+           "moe_selftest_bounded_wait")
 
 
 def moe_profile_enable(on: bool = True):

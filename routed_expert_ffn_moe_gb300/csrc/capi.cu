@@ -247,6 +247,15 @@ moe_status moe_check_device_status(void* ws, void* stream) {
   return MOE_OK;
 }
 
+moe_status moe_selftest_bounded_wait(void* ws, uint32_t limit_us, void* stream) {
+  REQUIRE_PTR(ws, 256);
+  if (limit_us < 1 || limit_us > 2000000)
+    return fail(MOE_ERR_INVALID_ARG, "limit_us=%u not in [1, 2000000]", limit_us);
+  cudaError_t e = launch_selftest_bounded_wait(static_cast<int*>(ws), 1000ull * limit_us,
+                                               static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_selftest_bounded_wait launch");
+}
+
 moe_status moe_profile_enable(int on) {
   std::lock_guard<std::mutex> lk(g_prof_mu);
   if (on) {

@@ -93,6 +93,12 @@ def test_bad_arguments_rejected_before_launch(lib):
     assert rc == -1 and "shape is NULL" in msg
     rc, msg = call("moe_check_device_status", F + 64, None)
     assert rc == -1
+    rc, msg = call("moe_selftest_bounded_wait", F, 0, None)
+    assert rc == -1 and "limit_us" in msg
+    rc, msg = call("moe_selftest_bounded_wait", F, 2_000_001, None)
+    assert rc == -1 and "limit_us" in msg
+    rc, msg = call("moe_selftest_bounded_wait", F + 16, 1000, None)
+    assert rc == -1 and "ws" in msg
 
 
 def test_binding_raises_moe_error(lib):

@@ -130,6 +130,25 @@ def test_permute_flags_out_of_range_expert_without_faulting():
     moe.moe_check_device_status(ws)  # the check cleared the flag
 
 
+def test_bounded_wait_gives_up_and_reports_timeout():
+    # A device wait that nothing completes must give up after its limit, record the timeout in
+    # the status word and leave the context usable (no trap, no hang).
+    import time
+    s = moe.shape_of(16, 256, 8, 2, 128, 1)
+    ws = torch().zeros(moe.moe_workspace_size(s), dtype=torch().uint8, device="cuda")
+    t0 = time.perf_counter()
+    moe.moe_selftest_bounded_wait(ws, 50_000)
+    torch().cuda.synchronize()
+    waited = time.perf_counter() - t0
+    assert 0.04 <= waited < 5.0
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_check_device_status(ws)
+    assert ei.value.status == -5
+    moe.moe_check_device_status(ws)  # the check cleared the word
+    # the context still runs the layer correctly afterwards
+    check_small(synth.get_config("tiny"))
+
+
 def test_combine_direct():
     rng = np.random.default_rng(12)
     T, k, d, S = 50, 4, 384, 1
