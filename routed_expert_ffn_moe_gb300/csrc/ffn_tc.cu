@@ -199,27 +199,6 @@ cudaError_t launch_variant(const CUtensorMap& w, const CUtensorMap& b0, const CU
   return cudaGetLastError();
 }
 
-// One thread waits on an mbarrier that nothing ever arrives on, with the same bounded-wait
-// pattern as the pipelines above but a caller-chosen limit: when the limit passes it records
-// MOE_ERR_DEVICE_TIMEOUT and returns, leaving the context usable.
-__global__ void k_selftest_bounded_wait(int* status, unsigned long long limit_ns) {
-  __shared__ __align__(8) uint64_t bar;
-  if (threadIdx.x == 0) {
-    mbar_init(&bar, 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const uint64_t t0 = globaltimer();
-    while (!mbar_try_wait(&bar, 0)) {
-      if (globaltimer() - t0 > limit_ns) {
-        record_error(status, MOE_ERR_DEVICE_TIMEOUT);
-        break;
-      }
-    }
-  }
-}
-
 // Weight rows per down-pass tile: two 128-row tiles share the token tile in the prefill
 // variant when d allows it.
 bool down_pairs(int d, bool decode) { return !decode && d % 256 == 0; }
@@ -233,12 +212,6 @@ int tc_tile_tokens(bool gateup, bool decode) {
 
 int tc_tile_rows(bool gateup, bool decode, int d) {
   return (!gateup && down_pairs(d, decode)) ? 2 * kBM : kBM;
-}
-
-cudaError_t launch_selftest_bounded_wait(int* status, uint64_t limit_ns, cudaStream_t st) {
-  k_selftest_bounded_wait<<<1, 32, 0, st>>>(status, (unsigned long long)limit_ns);
-  count_launches(1);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_tc(const FfnArgs& a, const int32_t* prefix, bool gateup, bool decode,

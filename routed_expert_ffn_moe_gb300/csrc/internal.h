@@ -70,7 +70,7 @@ cudaError_t launch_route_noalloc(const moe_shape& s, const uint16_t* x, const ui
                                  const float* bias, int32_t* topk_idx, float* topk_w,
                                  cudaStream_t st);
 
-// a wait that nothing completes, bounded by limit_ns (ffn_tc.cu); records the timeout status
+// a wait that nothing completes, bounded by limit_ns (selftest.cu); records the timeout status
 cudaError_t launch_selftest_bounded_wait(int* status, uint64_t limit_ns, cudaStream_t st);
 
 // profiling hooks (capi.cu): kernel launch counter and per-call phase events
