@@ -37,6 +37,7 @@ int tc_fp8_tile_tokens(bool gateup, bool decode);
 cudaError_t launch_tc_fp8(const FfnArgs& a, const int32_t* prefix, bool gateup, bool decode,
                           cudaStream_t st);
 // wide-tile variant (ffn_tc_fp8_wide.cu): E4M3 weights dequantised to bf16 into TMEM
+int tc_fp8_wide_tile_tokens();
 cudaError_t launch_tc_fp8_wide(const FfnArgs& a, const int32_t* prefix, bool gateup,
                                cudaStream_t st);
 

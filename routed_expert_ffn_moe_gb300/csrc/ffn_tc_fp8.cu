@@ -322,7 +322,7 @@ cudaError_t launch_variant(const CUtensorMap& w, const CUtensorMap& b0, const CU
 
 int tc_fp8_tile_tokens(bool gateup, bool decode) {
   (void)gateup;
-  return decode ? 32 : 256;
+  return decode ? 32 : tc_fp8_wide_tile_tokens();
 }
 
 cudaError_t launch_tc_fp8(const FfnArgs& a, const int32_t* prefix, bool gateup, bool decode,

@@ -4,15 +4,17 @@
 // 256-token tile, 512 TMEM columns of accumulator) and the dequantisation moves to a shared-
 // memory stage of its own:
 //
-//   TMA        E4M3 codes (128 rows x 64 K per weight tile, 64-byte swizzle) and bf16 token rows
-//              (256 x 64 K, 128-byte swizzle) -> smem ring
-//   convert    8 warps: bf16(code * block scale) into a second smem ring in the 128-byte-swizzle
-//              K-major layout the MMA reads (each weight rounded once to bf16, <= 2^-9 relative)
-//   MMA        tcgen05.mma.kind::f16, bf16 x bf16 -> fp32, both operands from smem
-//   epilogue   TMEM -> SiLU(gate) * up -> bf16 h, or the fp32 expert output
+//   TMA (codes)   E4M3 codes (128 rows x 64 K per weight tile, 64-byte swizzle) -> code ring
+//   TMA (tokens)  bf16 token rows (256 x 64 K, 128-byte swizzle) -> token ring
+//   convert       8 warps: bf16(code * block scale) into a third ring in the 128-byte-swizzle
+//                 K-major layout the MMA reads (each weight rounded once to bf16, <= 2^-9 relative)
+//   MMA           tcgen05.mma.kind::f16, bf16 x bf16 -> fp32, both operands from smem
+//   epilogue      TMEM -> SiLU(gate) * up -> bf16 h, or the fp32 expert output
 //
-// The token stage is released by the MMA (it reads the token rows), the code stage also by the
-// converters; the converted ring by the MMA.
+// The three rings are released independently: a code slot as soon as the converters have read
+// it, a token slot and a converted slot when the MMAs that read them complete. The codes are
+// the stream that comes from HBM, so they get the deepest ring and a producer thread of their
+// own, which runs as far ahead as the code ring allows whatever the token ring is doing.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -27,14 +29,19 @@ using namespace tc;
 constexpr uint32_t kCodeTileBytes = kBM * kBK;    // 128 rows x 64 codes = 8 KB
 constexpr int kConvWarps = 8;
 constexpr int kConvThreads = 32 * kConvWarps;
-constexpr int kThreadsW = 32 * 6 + kConvThreads;
+constexpr int kConvWarp0 = 6;                     // converters: warps 6..13
+constexpr int kTokWarp = kConvWarp0 + kConvWarps; // token producer: warp 14
+constexpr int kThreadsW = 32 * (kTokWarp + 1);
 
-template <int NT, int STAGES, int CSTAGES, int KA, int ACCB>
+template <int NT, int QS, int BS, int CS, int KA, int ACCB>
 struct SmemW {
-  static constexpr uint32_t kStageBytes = KA * kCodeTileBytes + (uint32_t)NT * kBK * 2;
-  static constexpr uint32_t kCSlotBytes = KA * kATileBytes;   // bf16 weight tiles
-  static constexpr uint32_t kTilesBytes = STAGES * kStageBytes + CSTAGES * kCSlotBytes;
-  static constexpr uint32_t kBarBytes = 8 * (2 * STAGES + 2 * CSTAGES + 4) + 16;
+  static constexpr uint32_t kQSlot = KA * kCodeTileBytes;        // E4M3 codes of the KA tiles
+  static constexpr uint32_t kBSlot = (uint32_t)NT * kBK * 2;     // bf16 token rows
+  static constexpr uint32_t kCSlot = KA * kATileBytes;           // converted bf16 weight tiles
+  static constexpr uint32_t kBOff = QS * kQSlot;
+  static constexpr uint32_t kCOff = kBOff + BS * kBSlot;
+  static constexpr uint32_t kTilesBytes = kCOff + CS * kCSlot;
+  static constexpr uint32_t kBarBytes = 8 * (2 * QS + 2 * BS + 2 * CS + 4) + 16;
   static constexpr uint32_t kTotal = kTilesBytes + kBarBytes + 1024;
   static constexpr uint32_t kAccCols = KA * NT;
   static constexpr uint32_t kTmemCols = ACCB * kAccCols;
@@ -54,7 +61,7 @@ __device__ __forceinline__ void sts_u4(uint32_t addr, const uint4& v) {
                : "memory");
 }
 
-template <bool GATEUP, int NT, int STAGES, int CSTAGES, int KA, int ACCB>
+template <bool GATEUP, int NT, int QS, int BS, int CS, int KA, int ACCB>
 __global__ void __launch_bounds__(kThreadsW, 1)
     k_tc_ffn_fp8_wide(const __grid_constant__ CUtensorMap tm_w,
                       const __grid_constant__ CUtensorMap tm_b0,
@@ -62,18 +69,21 @@ __global__ void __launch_bounds__(kThreadsW, 1)
                       const __grid_constant__ CUtensorMap tm_b0w,
                       const __grid_constant__ CUtensorMap tm_b1w, const TcParams p,
                       const float* __restrict__ scales) {
-  using S = SmemW<NT, STAGES, CSTAGES, KA, ACCB>;
+  using S = SmemW<NT, QS, BS, CS, KA, ACCB>;
   static_assert(S::kTmemCols <= 512 && (S::kTmemCols & (S::kTmemCols - 1)) == 0, "TMEM cols");
   static_assert(!GATEUP || KA == 2, "gate/up tiles pair the gate and up rows");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* cslots = smem + STAGES * S::kStageBytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kTilesBytes);
-  uint64_t* empty = full + STAGES;
-  uint64_t* c_full = empty + STAGES;
-  uint64_t* c_empty = c_full + CSTAGES;
-  uint64_t* acc_full = c_empty + CSTAGES;
+  uint8_t* bring = smem + S::kBOff;
+  uint8_t* cring = smem + S::kCOff;
+  uint64_t* q_full = reinterpret_cast<uint64_t*>(smem + S::kTilesBytes);
+  uint64_t* q_empty = q_full + QS;
+  uint64_t* b_full = q_empty + QS;
+  uint64_t* b_empty = b_full + BS;
+  uint64_t* c_full = b_empty + BS;
+  uint64_t* c_empty = c_full + CS;
+  uint64_t* acc_full = c_empty + CS;
   uint64_t* acc_empty = acc_full + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
@@ -84,13 +94,17 @@ __global__ void __launch_bounds__(kThreadsW, 1)
   const int kblocks = p.K / kBK;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConvWarps + 1);  // converter warps read the codes, the MMA the tokens
+    for (int s = 0; s < QS; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_empty[s], kConvWarps);   // every converter warp has read its codes
     }
-    for (int s = 0; s < CSTAGES; ++s) {
+    for (int s = 0; s < BS; ++s) {
+      mbar_init(&b_full[s], 1);
+      mbar_init(&b_empty[s], 1);            // MMA commit
+    }
+    for (int s = 0; s < CS; ++s) {
       mbar_init(&c_full[s], kConvWarps);
-      mbar_init(&c_empty[s], 1);
+      mbar_init(&c_empty[s], 1);            // MMA commit
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -114,9 +128,31 @@ __global__ void __launch_bounds__(kThreadsW, 1)
   const uint32_t tmem_base = *tmem_holder;
 
   if (warp == 0) {
-    // ---------------- TMA producer ----------------
+    // ---------------- TMA producer: E4M3 codes ----------------
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        Tile t;
+        decode_tile<GATEUP, NT>(p, tile, t);
+        const int wrow = t.e * p.rows_per_expert + t.mt * (GATEUP ? kBM : kBM * KA);
+        const int wrow1 = GATEUP ? wrow + p.f : wrow + kBM;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!wait_bar(&q_empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+          uint8_t* st = smem + stage * S::kQSlot;
+          mbar_arrive_expect_tx(&q_full[stage], S::kQSlot);
+          tma_load_2d(st, &tm_w, &q_full[stage], kb * kBK, wrow, pol_w);
+          if (KA == 2) tma_load_2d(st + kCodeTileBytes, &tm_w, &q_full[stage], kb * kBK, wrow1, pol_w);
+          if (++stage == QS) { stage = 0; phase ^= 1u; }
+        }
+      }
+      for (int s = 0; s < QS; ++s)
+        drain_bar(&q_full[s], (s < (int)stage) ? phase : (phase ^ 1u), p.status);
+    }
+  } else if (warp == kTokWarp) {
+    // ---------------- TMA producer: bf16 token rows ----------------
+    if (lane == 0) {
       const uint64_t pol_b = policy_evict_last();
       uint32_t stage = 0, phase = 0;
       bool ok = true;
@@ -125,38 +161,31 @@ __global__ void __launch_bounds__(kThreadsW, 1)
         decode_tile<GATEUP, NT>(p, tile, t);
         const bool wide = t.ntok == NT;
         const int nbox = (t.ntok + kBoxRows - 1) / kBoxRows;
-        const uint32_t bytes = KA * kCodeTileBytes + (uint32_t)nbox * kBBoxBytes;
-        const int wrow = t.e * p.rows_per_expert + t.mt * (GATEUP ? kBM : kBM * KA);
-        const int wrow1 = GATEUP ? wrow + p.f : wrow + kBM;
+        const uint32_t bytes = wide ? S::kBSlot : (uint32_t)nbox * kBBoxBytes;
         const bool sh = GATEUP && t.shared;
         const CUtensorMap* bmap = sh ? &tm_b1 : &tm_b0;
         const CUtensorMap* bmapw = sh ? &tm_b1w : &tm_b0w;
         for (int kb = 0; kb < kblocks; ++kb) {
-          if (!wait_bar(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
-          uint8_t* st = smem + stage * S::kStageBytes;
-          mbar_arrive_expect_tx(&full[stage], bytes);
-          tma_load_2d(st, &tm_w, &full[stage], kb * kBK, wrow, pol_w);
-          if (KA == 2) tma_load_2d(st + kCodeTileBytes, &tm_w, &full[stage], kb * kBK, wrow1, pol_w);
-          uint8_t* bt = st + KA * kCodeTileBytes;
+          if (!wait_bar(&b_empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+          uint8_t* bt = bring + stage * S::kBSlot;
+          mbar_arrive_expect_tx(&b_full[stage], bytes);
           if (wide) {
-            tma_load_2d(bt, bmapw, &full[stage], kb * kBK, t.brow0, pol_b);
+            tma_load_2d(bt, bmapw, &b_full[stage], kb * kBK, t.brow0, pol_b);
           } else {
             for (int i = 0; i < nbox; ++i)
-              tma_load_2d(bt + i * kBBoxBytes, bmap, &full[stage], kb * kBK,
+              tma_load_2d(bt + i * kBBoxBytes, bmap, &b_full[stage], kb * kBK,
                           t.brow0 + i * kBoxRows, pol_b);
           }
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          if (++stage == BS) { stage = 0; phase ^= 1u; }
         }
       }
-      for (int s = 0; s < STAGES; ++s) {
-        const uint32_t issued_phase = (s < (int)stage) ? phase : (phase ^ 1u);
-        drain_bar(&full[s], issued_phase, p.status);
-      }
+      for (int s = 0; s < BS; ++s)
+        drain_bar(&b_full[s], (s < (int)stage) ? phase : (phase ^ 1u), p.status);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      uint32_t stage = 0, phase = 0, cs = 0, cphase = 0;
+      uint32_t bs = 0, bphase = 0, cs = 0, cphase = 0;
       uint32_t acc = 0, acc_phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
@@ -168,39 +197,39 @@ __global__ void __launch_bounds__(kThreadsW, 1)
         tc_fence_after();
         const uint32_t d0 = tmem_base + acc * S::kAccCols;
         for (int kb = 0; kb < kblocks; ++kb) {
-          if (!wait_bar(&full[stage], phase, abort_flag, p.status) ||
+          if (!wait_bar(&b_full[bs], bphase, abort_flag, p.status) ||
               !wait_bar(&c_full[cs], cphase, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t ca = smem_u32(cslots + cs * S::kCSlotBytes);
+          const uint32_t ca = smem_u32(cring + cs * S::kCSlot);
           const uint64_t da = sw128_desc(ca);
           const uint64_t du = sw128_desc(ca + kATileBytes);
-          const uint64_t db = sw128_desc(smem_u32(smem + stage * S::kStageBytes + KA * kCodeTileBytes));
+          const uint64_t db = sw128_desc(smem_u32(bring + bs * S::kBSlot));
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint32_t accum = (kb | kk) ? 1u : 0u;
             mma_bf16_ss(d0, da + 2 * kk, db + 2 * kk, idesc, accum);
             if (KA == 2) mma_bf16_ss(d0 + NT, du + 2 * kk, db + 2 * kk, idesc, accum);
           }
-          mma_commit(&empty[stage]);   // token rows consumed
-          mma_commit(&c_empty[cs]);    // dequantised weights consumed
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-          if (++cs == CSTAGES) { cs = 0; cphase ^= 1u; }
+          mma_commit(&b_empty[bs]);   // token rows consumed
+          mma_commit(&c_empty[cs]);   // dequantised weights consumed
+          if (++bs == BS) { bs = 0; bphase ^= 1u; }
+          if (++cs == CS) { cs = 0; cphase ^= 1u; }
         }
         if (!ok) break;
         mma_commit(&acc_full[acc]);
         if (++acc == ACCB) { acc = 0; acc_phase ^= 1u; }
       }
     }
-  } else if (warp < 6) {
+  } else if (warp < kConvWarp0) {
     // ---------------- epilogue (warps 2..5) ----------------
     run_epilogue<GATEUP, NT, S::kAccCols, KA, ACCB>(p, total, tmem_base, acc_full, acc_empty,
                                                     abort_flag);
   } else {
     // ---------------- dequantisers (warps 6..13) ----------------
     // task = (weight tile a, row r, 16-code chunk j): 16 codes -> two 16-byte bf16 chunks
-    const int ct = threadIdx.x - 192;
+    const int ct = threadIdx.x - 32 * kConvWarp0;
     const int kbl = p.K / 128;               // scale blocks along K
-    uint32_t stage = 0, phase = 0, cs = 0, cphase = 0;
+    uint32_t qs = 0, qphase = 0, cs = 0, cphase = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
       Tile t;
@@ -211,13 +240,13 @@ __global__ void __launch_bounds__(kThreadsW, 1)
       // scales run one stage ahead so their load latency hides behind the conversion
       float s0 = __ldg(sc + rb0 * kbl), s1 = KA == 2 ? __ldg(sc + rb1 * kbl) : 0.f;
       for (int kb = 0; kb < kblocks; ++kb) {
-        if (!wait_bar(&full[stage], phase, abort_flag, p.status) ||
+        if (!wait_bar(&q_full[qs], qphase, abort_flag, p.status) ||
             !wait_bar(&c_empty[cs], cphase ^ 1u, abort_flag, p.status)) { ok = false; break; }
         const bool more = kb + 1 < kblocks;
         const float s0_next = more ? __ldg(sc + rb0 * kbl + ((kb + 1) >> 1)) : 0.f;
         const float s1_next = (KA == 2 && more) ? __ldg(sc + rb1 * kbl + ((kb + 1) >> 1)) : 0.f;
-        const uint32_t st = smem_u32(smem + stage * S::kStageBytes);
-        const uint32_t dst = smem_u32(cslots + cs * S::kCSlotBytes);
+        const uint32_t src = smem_u32(smem + qs * S::kQSlot);
+        const uint32_t dst = smem_u32(cring + cs * S::kCSlot);
 #pragma unroll
         for (int i = 0; i < KA * kBM * 4 / kConvThreads; ++i) {
           const int task = ct + i * kConvThreads;
@@ -225,7 +254,7 @@ __global__ void __launch_bounds__(kThreadsW, 1)
           const int r = (task >> 2) & (kBM - 1);
           const int j = task & 3;
           // source: 64-byte rows, 64-byte swizzle (16-byte chunk j ^ ((r >> 1) & 3))
-          const uint4 raw = lds_u4(st + a * kCodeTileBytes + r * 64 + ((j ^ ((r >> 1) & 3)) << 4));
+          const uint4 raw = lds_u4(src + a * kCodeTileBytes + r * 64 + ((j ^ ((r >> 1) & 3)) << 4));
           const float s = a ? s1 : s0;
           uint4 lo, hi;  // codes 0..7 -> chunk 2j, codes 8..15 -> chunk 2j+1
           lo.x = dequant2(raw.x & 0xFFFFu, s);
@@ -244,13 +273,13 @@ __global__ void __launch_bounds__(kThreadsW, 1)
         fence_proxy_async_smem();      // bf16 weights -> visible to the MMA
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&empty[stage]);  // this warp is done with the codes of this stage
+          mbar_arrive(&q_empty[qs]);   // this warp is done with the codes of this stage
           mbar_arrive(&c_full[cs]);
         }
         s0 = s0_next;
         s1 = s1_next;
-        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-        if (++cs == CSTAGES) { cs = 0; cphase ^= 1u; }
+        if (++qs == QS) { qs = 0; qphase ^= 1u; }
+        if (++cs == CS) { cs = 0; cphase ^= 1u; }
       }
     }
   }
@@ -263,13 +292,13 @@ __global__ void __launch_bounds__(kThreadsW, 1)
   }
 }
 
-template <bool GATEUP, int NT, int STAGES, int CSTAGES, int KA, int ACCB>
+template <bool GATEUP, int NT, int QS, int BS, int CS, int KA, int ACCB>
 cudaError_t launch_variant(const CUtensorMap& w, const CUtensorMap& b0, const CUtensorMap& b1,
                            const CUtensorMap& b0w, const CUtensorMap& b1w, const TcParams& p,
                            const float* scales, cudaStream_t st) {
-  using S = SmemW<NT, STAGES, CSTAGES, KA, ACCB>;
+  using S = SmemW<NT, QS, BS, CS, KA, ACCB>;
   static_assert(S::kTotal <= 227 * 1024, "shared memory");
-  auto kern = k_tc_ffn_fp8_wide<GATEUP, NT, STAGES, CSTAGES, KA, ACCB>;
+  auto kern = k_tc_ffn_fp8_wide<GATEUP, NT, QS, BS, CS, KA, ACCB>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)S::kTotal);
   if (e != cudaSuccess) return e;
@@ -279,6 +308,30 @@ cudaError_t launch_variant(const CUtensorMap& w, const CUtensorMap& b0, const CU
 }
 
 }  // namespace
+
+namespace {
+
+struct Maps {
+  CUtensorMap w, b0, b1, b0w, b1w;
+};
+
+// One pass (gate/up or down) with NT-token tiles: KA = 2 weight tiles per token tile when the
+// pass allows it (always for gate/up; for down when d is a multiple of 256), else 1.
+template <int NT, int QS, int BS, int CS, int ACCB2, int QS1, int BS1, int CS1>
+cudaError_t launch_pass(const Maps& m, const TcParams& p, const float* sc, bool gateup, bool pair,
+                        cudaStream_t st) {
+  if (gateup)
+    return launch_variant<true, NT, QS, BS, CS, 2, ACCB2>(m.w, m.b0, m.b1, m.b0w, m.b1w, p, sc, st);
+  if (pair)
+    return launch_variant<false, NT, QS, BS, CS, 2, ACCB2>(m.w, m.b0, m.b1, m.b0w, m.b1w, p, sc, st);
+  return launch_variant<false, NT, QS1, BS1, CS1, 1, 2>(m.w, m.b0, m.b1, m.b0w, m.b1w, p, sc, st);
+}
+
+}  // namespace
+
+// 256 tokens per tile: a measured sweep with 128-token tiles and deeper rings was slower at
+// every batch size tried (more tiles per expert, each converting the same weights).
+int tc_fp8_wide_tile_tokens() { return 256; }
 
 cudaError_t launch_tc_fp8_wide(const FfnArgs& a, const int32_t* prefix, bool gateup,
                                cudaStream_t st) {
@@ -297,27 +350,27 @@ cudaError_t launch_tc_fp8_wide(const FfnArgs& a, const int32_t* prefix, bool gat
   const uint64_t E1 = (uint64_t)a.E + a.n_shared;
   const uint64_t routed = (uint64_t)a.T * a.k;
   const uint64_t slots = routed + (uint64_t)a.n_shared * a.T;
-  CUtensorMap w, b0, b1, b0w, b1w;
+  Maps m;
   cudaError_t e;
   if (gateup) {
-    e = encode_u8_2d(&w, a.w13, E1 * 2 * a.f, a.d, kBM, 64);
-    if (e == cudaSuccess) e = encode_bf16_2d(&b0, a.x_perm, routed ? routed : 1, a.d, kBoxRows);
-    if (e == cudaSuccess) e = encode_bf16_2d(&b1, a.x, a.T, a.d, kBoxRows);
-    if (e == cudaSuccess) e = encode_bf16_2d(&b0w, a.x_perm, routed ? routed : 1, a.d, NT);
-    if (e == cudaSuccess) e = encode_bf16_2d(&b1w, a.x, a.T, a.d, NT);
+    e = encode_u8_2d(&m.w, a.w13, E1 * 2 * a.f, a.d, kBM, 64);
+    if (e == cudaSuccess) e = encode_bf16_2d(&m.b0, a.x_perm, routed ? routed : 1, a.d, kBoxRows);
+    if (e == cudaSuccess) e = encode_bf16_2d(&m.b1, a.x, a.T, a.d, kBoxRows);
+    if (e == cudaSuccess) e = encode_bf16_2d(&m.b0w, a.x_perm, routed ? routed : 1, a.d, NT);
+    if (e == cudaSuccess) e = encode_bf16_2d(&m.b1w, a.x, a.T, a.d, NT);
   } else {
-    e = encode_u8_2d(&w, a.w2, E1 * a.d, a.f, kBM, 64);
-    if (e == cudaSuccess) e = encode_bf16_2d(&b0, a.h, slots, a.f, kBoxRows);
-    if (e == cudaSuccess) e = encode_bf16_2d(&b0w, a.h, slots, a.f, NT);
-    b1 = b0;
-    b1w = b0w;
+    e = encode_u8_2d(&m.w, a.w2, E1 * a.d, a.f, kBM, 64);
+    if (e == cudaSuccess) e = encode_bf16_2d(&m.b0, a.h, slots, a.f, kBoxRows);
+    if (e == cudaSuccess) e = encode_bf16_2d(&m.b0w, a.h, slots, a.f, NT);
+    m.b1 = m.b0;
+    m.b1w = m.b0w;
   }
   if (e != cudaSuccess) return e;
   const float* sc = gateup ? a.s13 : a.s2;
-  if (gateup) return launch_variant<true, NT, 3, 2, 2, 1>(w, b0, b1, b0w, b1w, p, sc, st);
-  if (tc_tile_rows(false, false, a.d) == 2 * kBM)
-    return launch_variant<false, NT, 3, 2, 2, 1>(w, b0, b1, b0w, b1w, p, sc, st);
-  return launch_variant<false, NT, 3, 2, 1, 2>(w, b0, b1, b0w, b1w, p, sc, st);
+  const bool pair = tc_tile_rows(false, false, a.d) == 2 * kBM;
+  // rings (codes, tokens, converted weights): 4/3/2 slots for paired tiles (224 KB of shared
+  // memory), 8/3/3 for single tiles; fewer token slots measured slower.
+  return launch_pass<NT, 4, 3, 2, 1, 8, 3, 3>(m, p, sc, gateup, pair, st);
 }
 
 }  // namespace moe
