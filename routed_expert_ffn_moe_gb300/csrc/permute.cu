@@ -62,21 +62,55 @@ __global__ void __launch_bounds__(1024) k_perm_scan(const int32_t* __restrict__ 
                                                     int nchunk, int T, int k, int n_shared,
                                                     int32_t* __restrict__ base,
                                                     int32_t* __restrict__ offsets) {
+  // One block scans the expert-major [E, nchunk] counts in pieces of 16 entries per thread;
+  // each piece's loads are issued one piece ahead so their latency overlaps the block scan.
+  constexpr int kPer = 16;
   const long n = (long)E * nchunk;
+  const long step = (long)kPer * blockDim.x;
+  const auto load = [&](long b0, int (&v)[kPer]) {
+    const long i0 = b0 + (long)kPer * threadIdx.x;
+    if (i0 + kPer <= n) {  // hist is 256-byte aligned and i0 a multiple of 16 entries
+#pragma unroll
+      for (int q = 0; q < kPer / 4; ++q) {
+        const int4 w = __ldg(reinterpret_cast<const int4*>(hist + i0) + q);
+        v[4 * q] = w.x; v[4 * q + 1] = w.y; v[4 * q + 2] = w.z; v[4 * q + 3] = w.w;
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < kPer; ++q) v[q] = (i0 + q < n) ? __ldg(hist + i0 + q) : 0;
+    }
+  };
+  int cur[kPer], nxt[kPer];
+  load(0, cur);
   int carry = 0;
-  for (long b0 = 0; b0 < n; b0 += 4L * blockDim.x) {
-    const long i0 = b0 + 4L * threadIdx.x;
-    int v[4];
+  for (long b0 = 0; b0 < n; b0 += step) {
+    if (b0 + step < n) load(b0 + step, nxt);
+    int sum = 0;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) v[q] = (i0 + q < n) ? hist[i0 + q] : 0;
+    for (int q = 0; q < kPer; ++q) sum += cur[q];
     int total;
-    int run = carry + block_exclusive_scan(v[0] + v[1] + v[2] + v[3], &total);
+    int run = carry + block_exclusive_scan(sum, &total);
+    const long i0 = b0 + (long)kPer * threadIdx.x;
+    if (i0 + kPer <= n) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      if (i0 + q < n) base[i0 + q] = run;
-      run += v[q];
+      for (int q = 0; q < kPer / 4; ++q) {
+        int4 w;
+        w.x = run; run += cur[4 * q];
+        w.y = run; run += cur[4 * q + 1];
+        w.z = run; run += cur[4 * q + 2];
+        w.w = run; run += cur[4 * q + 3];
+        reinterpret_cast<int4*>(base + i0)[q] = w;
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < kPer; ++q) {
+        if (i0 + q < n) base[i0 + q] = run;
+        run += cur[q];
+      }
     }
     carry += total;
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) cur[q] = nxt[q];
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x)
