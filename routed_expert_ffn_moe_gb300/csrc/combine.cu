@@ -13,6 +13,7 @@ __global__ void __launch_bounds__(256) k_combine(const float* __restrict__ y_per
                                                  const float* __restrict__ topk_w, int T, int k,
                                                  int d, int n_shared, uint16_t* __restrict__ y,
                                                  int* status) {
+  pdl_wait_then_release();
   const int d4 = d >> 2;
   const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (long)T * d4) return;
@@ -46,10 +47,10 @@ cudaError_t launch_combine(const moe_shape& s, const float* y_perm, const int32_
                            const float* topk_w, uint16_t* y, int* status, cudaStream_t st) {
   const long n = (long)s.T * (s.d / 4);
   if (n == 0) return cudaSuccess;
-  k_combine<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(y_perm, inv_slot, topk_w, s.T, s.k, s.d,
-                                                         s.n_shared, y, status);
+  const cudaError_t e = launch_pdl(k_combine, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st,
+                                   y_perm, inv_slot, topk_w, s.T, s.k, s.d, s.n_shared, y, status);
   count_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace moe

@@ -23,6 +23,7 @@ struct PlanArgs {
 // plan[row][e]: exclusive prefix over experts of the work of each kernel; entry E1 = total.
 __global__ void __launch_bounds__(1024) k_ffn_plan(const int32_t* __restrict__ offsets,
                                                    PlanArgs a, int32_t* __restrict__ plan) {
+  pdl_wait_then_release();
   const int E1 = a.E + a.n_shared;
   int run[4] = {0, 0, 0, 0};
   for (int b = 0; b < E1; b += blockDim.x) {
@@ -57,6 +58,7 @@ __global__ void __launch_bounds__(256) k_gather_rows(const uint16_t* __restrict_
                                                      const int32_t* __restrict__ perm_token,
                                                      int T, long routed, int d,
                                                      uint16_t* __restrict__ x_perm, int* status) {
+  pdl_wait_then_release();
   const int d8 = d >> 3;
   const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= routed * d8) return;
@@ -131,16 +133,15 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32
   const int stride = pa.stride;
 
   const PhaseEvents ev = profile_phase_events();
-  k_ffn_plan<<<1, 1024, 0, st>>>(offsets, pa, plan);
+  cudaError_t e = launch_pdl(k_ffn_plan, dim3(1), dim3(1024), 0, st, offsets, pa, plan);
   count_launches(1);
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (use_tc && routed > 0) {
     const long n = routed * (s.d / 8);
-    k_gather_rows<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(x, perm_token, s.T, routed, s.d,
-                                                                a.x_perm, a.status);
+    e = launch_pdl(k_gather_rows, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, x,
+                   perm_token, s.T, routed, s.d, a.x_perm, a.status);
     count_launches(1);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (e != cudaSuccess) return e;
   }
   if (ev.begin) record_phase(ev.begin, st);
 

@@ -47,6 +47,7 @@ __device__ __forceinline__ void weights_to_f32(const uint4& v, float* out) {
 //         output y_perm[slot][r], y_perm[slot][r + 1] (fp32).
 template <bool FP8, bool GATEUP>
 __global__ void __launch_bounds__(256) k_gemv(FfnArgs a, const int32_t* __restrict__ prefix) {
+  pdl_wait_then_release();
   constexpr int CH = FP8 ? 16 : 8;  // weight elements per 16-byte chunk
   extern __shared__ uint4 xs_u4[];  // [kGroup][K] bf16
   const int K = GATEUP ? a.d : a.f;          // input width

@@ -63,7 +63,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E1 = p.E + p.n_shared;
-  const int total = __ldg(p.prefix + E1);
   const int kblocks = p.K / kBK;
 
   if (threadIdx.x == 0) {
@@ -91,6 +90,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  // the tile list (prefix) is written by the previous kernel
+  pdl_wait_then_release();
+  const int total = __ldg(p.prefix + E1);
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -194,9 +196,8 @@ cudaError_t launch_variant(const CUtensorMap& w, const CUtensorMap& b0, const CU
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)S::kTotal);
   if (e != cudaSuccess) return e;
-  kern<<<num_sms(), kThreads, S::kTotal, st>>>(w, b0, b1, b0w, b1w, p);
   count_launches(1);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(num_sms()), dim3(kThreads), S::kTotal, st, w, b0, b1, b0w, b1w, p);
 }
 
 // Weight rows per down-pass tile: two 128-row tiles share the token tile in the prefill

@@ -110,7 +110,6 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E1 = p.E + p.n_shared;
-  const int total = __ldg(p.prefix + E1);
   const int kblocks = p.K / kQK;
 
   if (threadIdx.x == 0) {
@@ -140,6 +139,9 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  // the tile list (prefix) is written by the previous kernel
+  pdl_wait_then_release();
+  const int total = __ldg(p.prefix + E1);
   const uint32_t acol0 = 2 * S::kAccCols;  // first TMEM column of the converted-weights ring
 
   if (warp == 0) {
@@ -313,9 +315,8 @@ cudaError_t launch_variant(const CUtensorMap& w, const CUtensorMap& b0, const CU
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)S::kTotal);
   if (e != cudaSuccess) return e;
-  kern<<<num_sms(), kThreadsQ, S::kTotal, st>>>(w, b0, b1, p, scales);
   count_launches(1);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(num_sms()), dim3(kThreadsQ), S::kTotal, st, w, b0, b1, p, scales);
 }
 
 }  // namespace

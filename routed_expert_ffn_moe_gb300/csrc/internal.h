@@ -80,6 +80,37 @@ struct PhaseEvents {
 };
 PhaseEvents profile_phase_events();  // all null unless a profiling session is on
 
+// ---- programmatic dependent launch -------------------------------------------------------
+// Every kernel of the layer is launched so that it may start while the kernel before it in the
+// stream is still finishing. Each kernel first does the set-up that touches no global memory
+// (shared-memory barriers, TMEM allocation, tensor-map prefetch), then pdl_wait(), which returns
+// once the previous kernel has completed and its writes are visible, and only then reads its
+// inputs. A kernel launched without the attribute passes pdl_wait() at once.
+#ifdef __CUDACC__
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
+// Wait for the previous kernel in the stream (all its writes visible), then let the next
+// kernel's blocks be scheduled as this grid's blocks are placed.
+__device__ __forceinline__ void pdl_wait_then_release() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+#endif
+
 // ---- device helpers ------------------------------------------------------------------------
 #ifdef __CUDACC__
 __device__ __forceinline__ void record_error(int* status, int code) {

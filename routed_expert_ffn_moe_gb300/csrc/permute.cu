@@ -46,6 +46,7 @@ __device__ __forceinline__ void build_masks(uint32_t* sel, const int32_t* topk_i
 __global__ void __launch_bounds__(256) k_perm_count(const int32_t* __restrict__ topk_idx, int T,
                                                     int E, int k, int nchunk,
                                                     int32_t* __restrict__ hist, int* status) {
+  pdl_wait_then_release();
   extern __shared__ uint32_t sel_all[];
   const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int chunk = blockIdx.x * kWarpsPerBlock + wid;
@@ -62,6 +63,7 @@ __global__ void __launch_bounds__(1024) k_perm_scan(const int32_t* __restrict__ 
                                                     int nchunk, int T, int k, int n_shared,
                                                     int32_t* __restrict__ base,
                                                     int32_t* __restrict__ offsets) {
+  pdl_wait_then_release();
   // One block scans the expert-major [E, nchunk] counts in pieces of 16 entries per thread;
   // each piece's loads are issued one piece ahead so their latency overlaps the block scan.
   constexpr int kPer = 16;
@@ -126,6 +128,7 @@ __global__ void __launch_bounds__(256) k_perm_scatter(const int32_t* __restrict_
                                                       const int32_t* __restrict__ base,
                                                       int32_t* __restrict__ perm_token,
                                                       int32_t* __restrict__ inv_slot) {
+  pdl_wait_then_release();
   extern __shared__ uint32_t sel_all[];
   const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int chunk = blockIdx.x * kWarpsPerBlock + wid;
@@ -159,18 +162,16 @@ cudaError_t launch_permute(const moe_shape& s, const int32_t* topk_idx, int32_t*
   const unsigned blocks = (unsigned)((nchunk + kWarpsPerBlock - 1) / kWarpsPerBlock);
   const size_t smem = (size_t)kWarpsPerBlock * s.E * sizeof(uint32_t);
   if (blocks) {
-    k_perm_count<<<blocks, 32 * kWarpsPerBlock, smem, st>>>(topk_idx, s.T, s.E, s.k, nchunk, hist,
-                                                            status);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(k_perm_count, dim3(blocks), dim3(32 * kWarpsPerBlock), smem, st,
+                               topk_idx, s.T, s.E, s.k, nchunk, hist, status);
     if (e != cudaSuccess) return e;
   }
-  k_perm_scan<<<1, 1024, 0, st>>>(hist, s.E, nchunk, s.T, s.k, s.n_shared, base, offsets);
   count_launches(blocks ? 3 : 1);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(k_perm_scan, dim3(1), dim3(1024), 0, st, hist, s.E, nchunk, s.T, s.k,
+                             s.n_shared, base, offsets);
   if (e != cudaSuccess || !blocks) return e;
-  k_perm_scatter<<<blocks, 32 * kWarpsPerBlock, smem, st>>>(topk_idx, s.T, s.E, s.k, nchunk, base,
-                                                            perm_token, inv_slot);
-  return cudaGetLastError();
+  return launch_pdl(k_perm_scatter, dim3(blocks), dim3(32 * kWarpsPerBlock), smem, st, topk_idx,
+                    s.T, s.E, s.k, nchunk, base, perm_token, inv_slot);
 }
 
 }  // namespace moe

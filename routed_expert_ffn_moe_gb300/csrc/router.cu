@@ -22,6 +22,7 @@ __global__ void __launch_bounds__(128) k_router_logits(const uint16_t* __restric
                                                        const uint16_t* __restrict__ wg,
                                                        const float* __restrict__ bias, int T,
                                                        int d, int E, float* __restrict__ logits) {
+  pdl_wait_then_release();
   const int lane = threadIdx.x & 31;
   const int warp = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int n_et = (E + TE - 1) / TE;
@@ -83,6 +84,7 @@ __global__ void __launch_bounds__(256) k_router_logits_x2(const uint16_t* __rest
                                                           const float* __restrict__ bias, int T,
                                                           int d, int E,
                                                           float* __restrict__ logits) {
+  pdl_wait_then_release();
   static_assert(TE % 2 == 0, "experts are paired");
   // A block of 8 warps covers 4 token tiles x 2 expert tiles, so both operands are reused
   // through L1 by the warps that share them.
@@ -152,6 +154,7 @@ __device__ __forceinline__ bool ranks_before(float la, int ea, float lb, int eb)
 __global__ void __launch_bounds__(256) k_router_topk(const float* __restrict__ logits, int T,
                                                      int E, int k, int32_t* __restrict__ topk_idx,
                                                      float* __restrict__ topk_w) {
+  pdl_wait_then_release();
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -205,11 +208,12 @@ cudaError_t launch_logits(const uint16_t* x, const uint16_t* wg, const float* bi
   const long warps = (long)((T + TT - 1) / TT) * ((E + TE - 1) / TE);
   const long blocks = (warps + 3) / 4;
   if (TT == 1) {
-    k_router_logits<TT, TE><<<(unsigned)blocks, 128, 0, st>>>(x, wg, bias, T, d, E, logits);
+    return launch_pdl(k_router_logits<TT, TE>, dim3((unsigned)blocks), dim3(128), 0, st, x, wg,
+                      bias, T, d, E, logits);
   } else {
     const long n_tt = (T + TT - 1) / TT, n_eb = ((E + TE - 1) / TE + 1) / 2;
-    k_router_logits_x2<TT, TE><<<(unsigned)(((n_tt + 3) / 4) * n_eb), 256, 0, st>>>(
-        x, wg, bias, T, d, E, logits);
+    return launch_pdl(k_router_logits_x2<TT, TE>, dim3((unsigned)(((n_tt + 3) / 4) * n_eb)),
+                      dim3(256), 0, st, x, wg, bias, T, d, E, logits);
   }
   return cudaGetLastError();
 }
@@ -264,9 +268,9 @@ cudaError_t launch_route_noalloc(const moe_shape& s, const uint16_t* x, const ui
   if (e != cudaSuccess || s.T == 0) return e;
   e = launch_logits_for(s, x, wg, bias, logits, st);
   if (e != cudaSuccess) return e;
-  k_router_topk<<<(unsigned)((s.T + 7) / 8), 256, 0, st>>>(logits, s.T, s.E, s.k, topk_idx, topk_w);
   count_launches(2);
-  return cudaGetLastError();
+  return launch_pdl(k_router_topk, dim3((unsigned)((s.T + 7) / 8)), dim3(256), 0, st, logits, s.T,
+                    s.E, s.k, topk_idx, topk_w);
 }
 
 cudaError_t launch_route(const moe_shape& s, const uint16_t* x, const uint16_t* wg,
@@ -276,9 +280,9 @@ cudaError_t launch_route(const moe_shape& s, const uint16_t* x, const uint16_t* 
   float* logits = reinterpret_cast<float*>(ws + L.logits);
   cudaError_t e = launch_logits_for(s, x, wg, bias, logits, st);
   if (e != cudaSuccess) return e;
-  k_router_topk<<<(unsigned)((s.T + 7) / 8), 256, 0, st>>>(logits, s.T, s.E, s.k, topk_idx, topk_w);
   count_launches(2);
-  return cudaGetLastError();
+  return launch_pdl(k_router_topk, dim3((unsigned)((s.T + 7) / 8)), dim3(256), 0, st, logits, s.T,
+                    s.E, s.k, topk_idx, topk_w);
 }
 
 }  // namespace moe
