@@ -231,7 +231,6 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
     for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
       Tile t;
       decode_tile<GATEUP, NT>(p, tile, t);
-      const int npad = (t.ntok + 15) & ~15;
       const float* sc = scales + (size_t)t.e * (p.rows_per_expert / 128) * kbl;
       const float* sc_g = sc + t.mt * kbl;                   // gate (or down) row block
       const float* sc_u = sc + (p.f / 128 + t.mt) * kbl;     // up row block
@@ -269,11 +268,13 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
             }
             tmem_st32(lane_base + acol0 + cs * S::kAStageCols + o * kACols + hk * 32, out);
           }
-        // token rows -> f16(s * x), same 128-byte-swizzled K-major layout as the TMA source
-        const int units = S::kA * npad * 16;  // (operand, row, 16-byte chunk)
+        // token rows -> f16(s * x), same 128-byte-swizzled K-major layout as the TMA source.
+        // Only the tile's ntok rows: MMA columns are independent, so the padding rows up to the
+        // next multiple of 16 only feed output columns the epilogue never reads.
+        const int units = S::kA * t.ntok * 16;  // (operand, row, 16-byte chunk)
         for (int u = gt; u < units; u += 128) {
-          const int o = u / (npad * 16);
-          const int rem = u - o * npad * 16;
+          const int o = u / (t.ntok * 16);
+          const int rem = u - o * t.ntok * 16;
           const int n = rem >> 4, c = rem & 15;
           const uint32_t off = (uint32_t)(c >> 3) * S::kBHalf + (uint32_t)n * 128 +
                                ((uint32_t)((c & 7) ^ (n & 7)) << 4);
