@@ -28,7 +28,6 @@
 // This variant serves decode-sized tiles (up to 32 tokens); wide tiles go to ffn_tc_fp8_wide.cu,
 // where dequantising the weights costs less than scaling 64-128 token rows.
 #include <cuda_bf16.h>
-#include <cuda_fp8.h>
 
 #include "tc_common.cuh"
 
@@ -68,10 +67,17 @@ __device__ __forceinline__ uint32_t idesc_f16(int M, int N) {
   return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// Two E4M3 codes (low byte first) as an exact f16 pair (low element first).
-__device__ __forceinline__ uint32_t codes_to_f16x2(uint32_t two) {
-  const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xFFFFu), __NV_E4M3);
-  return *reinterpret_cast<const uint32_t*>(&hr);
+// Four E4M3 codes (lowest byte first) as two exact f16 pairs: codes 0,1 -> lo, codes 2,3 -> hi.
+// The 16-bit halves of the word feed the conversions directly (no masking or shifting).
+__device__ __forceinline__ void codes4_to_f16x2(uint32_t four, uint32_t& lo, uint32_t& hi) {
+  asm("{\n"
+      "  .reg .b16 c01, c23;\n"
+      "  mov.b32 {c01, c23}, %2;\n"
+      "  cvt.rn.f16x2.e4m3x2 %0, c01;\n"
+      "  cvt.rn.f16x2.e4m3x2 %1, c23;\n"
+      "}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(four));
 }
 
 // f16 pair (lo, hi) = (round(lo), round(hi)), saturating to the largest finite f16.
@@ -262,8 +268,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
               const uint32_t w[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
 #pragma unroll
               for (int m = 0; m < 4; ++m) {
-                out[j * 8 + 2 * m] = codes_to_f16x2(w[m] & 0xFFFFu);
-                out[j * 8 + 2 * m + 1] = codes_to_f16x2(w[m] >> 16);
+                codes4_to_f16x2(w[m], out[j * 8 + 2 * m], out[j * 8 + 2 * m + 1]);
               }
             }
             tmem_st32(lane_base + acol0 + cs * S::kAStageCols + o * kACols + hk * 32, out);
