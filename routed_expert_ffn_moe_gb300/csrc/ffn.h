@@ -38,6 +38,8 @@ cudaError_t launch_tc_fp8(const FfnArgs& a, const int32_t* prefix, bool gateup, 
                           cudaStream_t st);
 // wide-tile variant (ffn_tc_fp8_wide.cu): E4M3 weights dequantised to bf16 into TMEM
 int tc_fp8_wide_tile_tokens();
+// plan units (weight tiles, or cluster pairs of them) per expert in a prefill-tile pass
+int tc_fp8_wide_plan_mtiles(bool gateup, int d, int f);
 cudaError_t launch_tc_fp8_wide(const FfnArgs& a, const int32_t* prefix, bool gateup,
                                cudaStream_t st);
 

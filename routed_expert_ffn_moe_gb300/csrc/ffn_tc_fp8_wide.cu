@@ -61,7 +61,7 @@ __device__ __forceinline__ void sts_u4(uint32_t addr, const uint4& v) {
                : "memory");
 }
 
-template <bool GATEUP, int NT, int QS, int BS, int CS, int KA, int ACCB>
+template <bool GATEUP, int NT, int QS, int BS, int CS, int KA, int ACCB, bool PAIR>
 __global__ void __launch_bounds__(kThreadsW, 1)
     k_tc_ffn_fp8_wide(const __grid_constant__ CUtensorMap tm_w,
                       const __grid_constant__ CUtensorMap tm_b0,
@@ -91,6 +91,16 @@ __global__ void __launch_bounds__(kThreadsW, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E1 = p.E + p.n_shared;
   const int kblocks = p.K / kBK;
+  // Cluster pairs: both CTAs walk the same list of (expert, m-tile pair, token tile) entries;
+  // this CTA takes m-tile 2 * mt + rank, and the token tile, which both need, is loaded half by
+  // each CTA and multicast to both.
+  const int rank = PAIR ? (int)cluster_ctarank() : 0;
+  const int tile0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int tstep = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  const auto decode = [&](int tile, Tile& t) {
+    decode_tile<GATEUP, NT>(p, tile, t);
+    if (PAIR) t.mt = 2 * t.mt + rank;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < QS; ++s) {
@@ -99,7 +109,7 @@ __global__ void __launch_bounds__(kThreadsW, 1)
     }
     for (int s = 0; s < BS; ++s) {
       mbar_init(&b_full[s], 1);
-      mbar_init(&b_empty[s], 1);            // MMA commit
+      mbar_init(&b_empty[s], PAIR ? 2 : 1); // MMA commit (of both CTAs of a pair)
     }
     for (int s = 0; s < CS; ++s) {
       mbar_init(&c_full[s], kConvWarps);
@@ -123,6 +133,7 @@ __global__ void __launch_bounds__(kThreadsW, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();  // the peer's barriers are initialised before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   // the tile list (prefix) is written by the previous kernel
@@ -135,9 +146,9 @@ __global__ void __launch_bounds__(kThreadsW, 1)
       const uint64_t pol_w = policy_evict_first();
       uint32_t stage = 0, phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+      for (int tile = tile0; ok && tile < total; tile += tstep) {
         Tile t;
-        decode_tile<GATEUP, NT>(p, tile, t);
+        decode(tile, t);
         const int wrow = t.e * p.rows_per_expert + t.mt * (GATEUP ? kBM : kBM * KA);
         const int wrow1 = GATEUP ? wrow + p.f : wrow + kBM;
         for (int kb = 0; kb < kblocks; ++kb) {
@@ -158,11 +169,12 @@ __global__ void __launch_bounds__(kThreadsW, 1)
       const uint64_t pol_b = policy_evict_last();
       uint32_t stage = 0, phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+      for (int tile = tile0; ok && tile < total; tile += tstep) {
         Tile t;
-        decode_tile<GATEUP, NT>(p, tile, t);
+        decode(tile, t);
         const bool wide = t.ntok == NT;
         const int nbox = (t.ntok + kBoxRows - 1) / kBoxRows;
+        // bytes this CTA receives: the whole token tile (with pairs, half of it from the peer)
         const uint32_t bytes = wide ? S::kBSlot : (uint32_t)nbox * kBBoxBytes;
         const bool sh = GATEUP && t.shared;
         const CUtensorMap* bmap = sh ? &tm_b1 : &tm_b0;
@@ -171,7 +183,18 @@ __global__ void __launch_bounds__(kThreadsW, 1)
           if (!wait_bar(&b_empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
           uint8_t* bt = bring + stage * S::kBSlot;
           mbar_arrive_expect_tx(&b_full[stage], bytes);
-          if (wide) {
+          if (PAIR) {
+            // full tile: this CTA's half of the rows (the wide map's box is NT/2 rows);
+            // partial tile: every other 16-row box
+            if (wide) {
+              tma_load_2d_mc(bt + rank * (S::kBSlot / 2), bmapw, &b_full[stage], kb * kBK,
+                             t.brow0 + rank * (NT / 2), 0x3, pol_b);
+            } else {
+              for (int i = rank; i < nbox; i += 2)
+                tma_load_2d_mc(bt + i * kBBoxBytes, bmap, &b_full[stage], kb * kBK,
+                               t.brow0 + i * kBoxRows, 0x3, pol_b);
+            }
+          } else if (wide) {
             tma_load_2d(bt, bmapw, &b_full[stage], kb * kBK, t.brow0, pol_b);
           } else {
             for (int i = 0; i < nbox; ++i)
@@ -183,6 +206,12 @@ __global__ void __launch_bounds__(kThreadsW, 1)
       }
       for (int s = 0; s < BS; ++s)
         drain_bar(&b_full[s], (s < (int)stage) ? phase : (phase ^ 1u), p.status);
+      if (PAIR) {
+        // the MMA commits of both CTAs for every issued stage have arrived here before the
+        // CTA may exit (the peer's commits target this CTA's barriers)
+        for (int s = 0; s < BS; ++s)
+          drain_bar(&b_empty[s], (s < (int)stage) ? phase : (phase ^ 1u), p.status);
+      }
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
@@ -190,9 +219,9 @@ __global__ void __launch_bounds__(kThreadsW, 1)
       uint32_t bs = 0, bphase = 0, cs = 0, cphase = 0;
       uint32_t acc = 0, acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+      for (int tile = tile0; ok && tile < total; tile += tstep) {
         Tile t;
-        decode_tile<GATEUP, NT>(p, tile, t);
+        decode(tile, t);
         const int npad = (t.ntok + 15) & ~15;
         const uint32_t idesc = idesc_bf16(kBM, npad);
         if (!wait_bar(&acc_empty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
@@ -212,7 +241,10 @@ __global__ void __launch_bounds__(kThreadsW, 1)
             mma_bf16_ss(d0, da + 2 * kk, db + 2 * kk, idesc, accum);
             if (KA == 2) mma_bf16_ss(d0 + NT, du + 2 * kk, db + 2 * kk, idesc, accum);
           }
-          mma_commit(&b_empty[bs]);   // token rows consumed
+          if (PAIR)
+            mma_commit_mc(&b_empty[bs], 0x3);  // token rows consumed, in both CTAs
+          else
+            mma_commit(&b_empty[bs]);          // token rows consumed
           mma_commit(&c_empty[cs]);   // dequantised weights consumed
           if (++bs == BS) { bs = 0; bphase ^= 1u; }
           if (++cs == CS) { cs = 0; cphase ^= 1u; }
@@ -225,7 +257,7 @@ __global__ void __launch_bounds__(kThreadsW, 1)
   } else if (warp < kConvWarp0) {
     // ---------------- epilogue (warps 2..5) ----------------
     run_epilogue<GATEUP, NT, S::kAccCols, KA, ACCB>(p, total, tmem_base, acc_full, acc_empty,
-                                                    abort_flag);
+                                                    abort_flag, tile0, tstep, PAIR ? rank : -1);
   } else {
     // ---------------- dequantisers (warps 6..13) ----------------
     // task = (weight tile a, row r, 16-code chunk j): 16 codes -> two 16-byte bf16 chunks
@@ -233,9 +265,9 @@ __global__ void __launch_bounds__(kThreadsW, 1)
     const int kbl = p.K / 128;               // scale blocks along K
     uint32_t qs = 0, qphase = 0, cs = 0, cphase = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+    for (int tile = tile0; ok && tile < total; tile += tstep) {
       Tile t;
-      decode_tile<GATEUP, NT>(p, tile, t);
+      decode(tile, t);
       const float* sc = scales + (size_t)t.e * (p.rows_per_expert / 128) * kbl;
       const int rb0 = GATEUP ? t.mt : t.mt * KA;   // scale row block of the first weight tile
       const int rb1 = GATEUP ? p.f / 128 + t.mt : rb0 + 1;
@@ -288,67 +320,87 @@ __global__ void __launch_bounds__(kThreadsW, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();  // no CTA leaves while its peer may still write to it
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, S::kTmemCols);
   }
 }
 
-template <bool GATEUP, int NT, int QS, int BS, int CS, int KA, int ACCB>
+template <bool GATEUP, int NT, int QS, int BS, int CS, int KA, int ACCB, bool PAIR>
 cudaError_t launch_variant(const CUtensorMap& w, const CUtensorMap& b0, const CUtensorMap& b1,
                            const CUtensorMap& b0w, const CUtensorMap& b1w, const TcParams& p,
                            const float* scales, cudaStream_t st) {
   using S = SmemW<NT, QS, BS, CS, KA, ACCB>;
   static_assert(S::kTotal <= 227 * 1024, "shared memory");
-  auto kern = k_tc_ffn_fp8_wide<GATEUP, NT, QS, BS, CS, KA, ACCB>;
+  auto kern = k_tc_ffn_fp8_wide<GATEUP, NT, QS, BS, CS, KA, ACCB, PAIR>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)S::kTotal);
   if (e != cudaSuccess) return e;
   count_launches(1);
+  if (PAIR)
+    return launch_pdl_cluster(kern, dim3((unsigned)(num_sms() & ~1)), dim3(kThreadsW), S::kTotal,
+                              st, 2u, w, b0, b1, b0w, b1w, p, scales);
   return launch_pdl(kern, dim3(num_sms()), dim3(kThreadsW), S::kTotal, st, w, b0, b1, b0w, b1w, p,
                     scales);
 }
-
-}  // namespace
-
-namespace {
 
 struct Maps {
   CUtensorMap w, b0, b1, b0w, b1w;
 };
 
-// One pass (gate/up or down) with NT-token tiles: KA = 2 weight tiles per token tile when the
-// pass allows it (always for gate/up; for down when d is a multiple of 256), else 1.
-template <int NT, int QS, int BS, int CS, int ACCB2, int QS1, int BS1, int CS1>
-cudaError_t launch_pass(const Maps& m, const TcParams& p, const float* sc, bool gateup, bool pair,
+// 256 tokens per tile: a measured sweep with 128-token tiles and deeper rings was slower at
+// every batch size tried (more tiles per expert, each converting the same weights).
+constexpr int kNT = 256;
+
+// Weight rows per tile of a pass: 2 x 128 (gate + up, or two W_d tiles when d allows), else 128.
+bool paired_tiles(bool gateup, int d) { return gateup || tc_tile_rows(false, false, d) == 2 * kBM; }
+
+// Cluster pairs take two consecutive m-tiles; they need an even number of them per expert.
+bool clustered(bool gateup, int d, int f) {
+  if (!paired_tiles(gateup, d)) return false;
+  const int mtiles = gateup ? f / kBM : d / (2 * kBM);
+  return mtiles % 2 == 0;
+}
+
+// One pass with kNT-token tiles; rings (codes, tokens, converted weights): 4/3/2 slots for
+// paired weight tiles (224 KB of shared memory), 8/3/3 for single tiles; fewer token slots
+// measured slower.
+template <bool PAIR>
+cudaError_t launch_pass(const Maps& m, const TcParams& p, const float* sc, bool gateup, bool paired,
                         cudaStream_t st) {
   if (gateup)
-    return launch_variant<true, NT, QS, BS, CS, 2, ACCB2>(m.w, m.b0, m.b1, m.b0w, m.b1w, p, sc, st);
-  if (pair)
-    return launch_variant<false, NT, QS, BS, CS, 2, ACCB2>(m.w, m.b0, m.b1, m.b0w, m.b1w, p, sc, st);
-  return launch_variant<false, NT, QS1, BS1, CS1, 1, 2>(m.w, m.b0, m.b1, m.b0w, m.b1w, p, sc, st);
+    return launch_variant<true, kNT, 4, 3, 2, 2, 1, PAIR>(m.w, m.b0, m.b1, m.b0w, m.b1w, p, sc, st);
+  if (paired)
+    return launch_variant<false, kNT, 4, 3, 2, 2, 1, PAIR>(m.w, m.b0, m.b1, m.b0w, m.b1w, p, sc, st);
+  return launch_variant<false, kNT, 8, 3, 3, 1, 2, false>(m.w, m.b0, m.b1, m.b0w, m.b1w, p, sc, st);
 }
 
 }  // namespace
 
-// 256 tokens per tile: a measured sweep with 128-token tiles and deeper rings was slower at
-// every batch size tried (more tiles per expert, each converting the same weights).
-int tc_fp8_wide_tile_tokens() { return 256; }
+int tc_fp8_wide_tile_tokens() { return kNT; }
+
+int tc_fp8_wide_plan_mtiles(bool gateup, int d, int f) {
+  const int rows = paired_tiles(gateup, d) && !gateup ? 2 * kBM : kBM;
+  const int mtiles = (gateup ? f : d) / rows;
+  return clustered(gateup, d, f) ? mtiles / 2 : mtiles;
+}
 
 cudaError_t launch_tc_fp8_wide(const FfnArgs& a, const int32_t* prefix, bool gateup,
                                cudaStream_t st) {
-  constexpr int NT = 256;
   TcParams p{};
   p.T = a.T; p.k = a.k; p.E = a.E; p.n_shared = a.n_shared;
   p.f = a.f; p.d = a.d;
   p.K = gateup ? a.d : a.f;
-  p.mtiles = (gateup ? a.f : a.d) / tc_tile_rows(gateup, false, a.d);
+  p.mtiles = tc_fp8_wide_plan_mtiles(gateup, a.d, a.f);
   p.rows_per_expert = gateup ? 2 * a.f : a.d;
   p.offsets = a.offsets;
   p.prefix = prefix;
   p.h = a.h;
   p.y_perm = a.y_perm;
   p.status = a.status;
+  const bool cl = clustered(gateup, a.d, a.f);
+  const uint32_t wide_rows = cl ? kNT / 2 : kNT;  // with pairs each CTA loads half a full tile
   const uint64_t E1 = (uint64_t)a.E + a.n_shared;
   const uint64_t routed = (uint64_t)a.T * a.k;
   const uint64_t slots = routed + (uint64_t)a.n_shared * a.T;
@@ -358,21 +410,20 @@ cudaError_t launch_tc_fp8_wide(const FfnArgs& a, const int32_t* prefix, bool gat
     e = encode_u8_2d(&m.w, a.w13, E1 * 2 * a.f, a.d, kBM, 64);
     if (e == cudaSuccess) e = encode_bf16_2d(&m.b0, a.x_perm, routed ? routed : 1, a.d, kBoxRows);
     if (e == cudaSuccess) e = encode_bf16_2d(&m.b1, a.x, a.T, a.d, kBoxRows);
-    if (e == cudaSuccess) e = encode_bf16_2d(&m.b0w, a.x_perm, routed ? routed : 1, a.d, NT);
-    if (e == cudaSuccess) e = encode_bf16_2d(&m.b1w, a.x, a.T, a.d, NT);
+    if (e == cudaSuccess) e = encode_bf16_2d(&m.b0w, a.x_perm, routed ? routed : 1, a.d, wide_rows);
+    if (e == cudaSuccess) e = encode_bf16_2d(&m.b1w, a.x, a.T, a.d, wide_rows);
   } else {
     e = encode_u8_2d(&m.w, a.w2, E1 * a.d, a.f, kBM, 64);
     if (e == cudaSuccess) e = encode_bf16_2d(&m.b0, a.h, slots, a.f, kBoxRows);
-    if (e == cudaSuccess) e = encode_bf16_2d(&m.b0w, a.h, slots, a.f, NT);
+    if (e == cudaSuccess) e = encode_bf16_2d(&m.b0w, a.h, slots, a.f, wide_rows);
     m.b1 = m.b0;
     m.b1w = m.b0w;
   }
   if (e != cudaSuccess) return e;
   const float* sc = gateup ? a.s13 : a.s2;
-  const bool pair = tc_tile_rows(false, false, a.d) == 2 * kBM;
-  // rings (codes, tokens, converted weights): 4/3/2 slots for paired tiles (224 KB of shared
-  // memory), 8/3/3 for single tiles; fewer token slots measured slower.
-  return launch_pass<NT, 4, 3, 2, 1, 8, 3, 3>(m, p, sc, gateup, pair, st);
+  const bool paired = paired_tiles(gateup, a.d);
+  return cl ? launch_pass<true>(m, p, sc, gateup, paired, st)
+            : launch_pass<false>(m, p, sc, gateup, paired, st);
 }
 
 }  // namespace moe

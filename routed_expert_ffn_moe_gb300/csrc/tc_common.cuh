@@ -97,16 +97,20 @@ __device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity, int* s
 // (down pass: KA weight tiles of 128 output rows each, tile a in columns [a*NT, (a+1)*NT));
 // then hand the accumulator back. ACCB accumulator buffers (1 or 2) rotate.
 template <bool GATEUP, int NT, uint32_t ACC_COLS, int KA = 1, int ACCB = 2>
+// Tiles tile0, tile0 + tstep, ...; pair_rank >= 0 marks cluster pairs, where a listed tile is a
+// pair of m-tiles and this CTA takes m-tile 2 * mt + pair_rank.
 __device__ __forceinline__ void run_epilogue(const TcParams& p, int total, uint32_t tmem_base,
                                              uint64_t* acc_full, uint64_t* acc_empty,
-                                             volatile int* abort_flag) {
+                                             volatile int* abort_flag, int tile0, int tstep,
+                                             int pair_rank) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;                 // TMEM lane quadrant this warp may access
   const int row = q * 32 + lane;          // weight row within a 128-row tile
   uint32_t acc = 0, acc_phase = 0;
-  for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+  for (int tile = tile0; tile < total; tile += tstep) {
     Tile t;
     decode_tile<GATEUP, NT>(p, tile, t);
+    if (pair_rank >= 0) t.mt = 2 * t.mt + pair_rank;
     const int npad = (t.ntok + 15) & ~15;
     if (!wait_bar(&acc_full[acc], acc_phase, abort_flag, p.status)) break;
     tc_fence_after();
@@ -149,6 +153,15 @@ __device__ __forceinline__ void run_epilogue(const TcParams& p, int total, uint3
     if (lane == 0) mbar_arrive(&acc_empty[acc]);
     if (++acc == ACCB) { acc = 0; acc_phase ^= 1u; }
   }
+}
+
+// One CTA per tile list entry, tiles blockIdx.x, blockIdx.x + gridDim.x, ...
+template <bool GATEUP, int NT, uint32_t ACC_COLS, int KA = 1, int ACCB = 2>
+__device__ __forceinline__ void run_epilogue(const TcParams& p, int total, uint32_t tmem_base,
+                                             uint64_t* acc_full, uint64_t* acc_empty,
+                                             volatile int* abort_flag) {
+  run_epilogue<GATEUP, NT, ACC_COLS, KA, ACCB>(p, total, tmem_base, acc_full, acc_empty,
+                                               abort_flag, (int)blockIdx.x, (int)gridDim.x, -1);
 }
 
 // ---- host side -------------------------------------------------------------------------------

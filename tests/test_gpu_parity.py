@@ -67,6 +67,8 @@ SMALL = [
     ("tiny", {"T": 300, "E": 40, "k": 5}),     # several permute chunks, uneven segments
     # FP8 prefill tiles (more than 32 routed slots per expert): paired and single down tiles
     ("tiny", {"T": 600, "E": 8, "k": 2, "wdtype": "fp8"}),
+    # FP8 prefill tiles in cluster pairs (even m-tile counts in both passes)
+    ("tiny", {"T": 600, "d": 512, "f": 256, "E": 8, "k": 2, "wdtype": "fp8"}),
     ("tiny", {"T": 333, "d": 384, "f": 256, "E": 6, "k": 3, "wdtype": "fp8"}),
     ("tiny", {"T": 333, "d": 384, "f": 256, "E": 6, "k": 3}),
 ]
