@@ -129,7 +129,10 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32
   pa.nt_dn = fp8 ? tc_fp8_tile_tokens(false, decode) : tc_tile_tokens(false, decode);
   pa.mt_up = s.f / 128;
   pa.mt_dn = s.d / tc_tile_rows(false, decode, s.d);
-  if (fp8 && !decode) {
+  if (!fp8) {
+    pa.mt_up = tc_plan_mtiles(true, decode, s.d, s.f);
+    pa.mt_dn = tc_plan_mtiles(false, decode, s.d, s.f);
+  } else if (!decode) {
     pa.mt_up = tc_fp8_wide_plan_mtiles(true, s.d, s.f);
     pa.mt_dn = tc_fp8_wide_plan_mtiles(false, s.d, s.f);
   }

@@ -29,6 +29,8 @@ cudaError_t launch_gemv(const FfnArgs& a, const int32_t* prefix_up, const int32_
 // tensor-core path (ffn_tc.cu): bf16 weights
 int tc_tile_tokens(bool gateup, bool decode);
 int tc_tile_rows(bool gateup, bool decode, int d);  // weight rows per tile
+// plan units (weight tiles, or cluster pairs of them) per expert
+int tc_plan_mtiles(bool gateup, bool decode, int d, int f);
 cudaError_t launch_tc(const FfnArgs& a, const int32_t* prefix, bool gateup, bool decode,
                       cudaStream_t st);
 

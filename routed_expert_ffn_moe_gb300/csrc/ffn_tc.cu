@@ -42,7 +42,7 @@ struct Smem {
   static constexpr uint32_t kTmemCols = ACCB * kAccCols;
 };
 
-template <bool GATEUP, int NT, int STAGES, int KA, int ACCB>
+template <bool GATEUP, int NT, int STAGES, int KA, int ACCB, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     k_tc_ffn(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b0,
              const __grid_constant__ CUtensorMap tm_b1, const __grid_constant__ CUtensorMap tm_b0w,
@@ -64,11 +64,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E1 = p.E + p.n_shared;
   const int kblocks = p.K / kBK;
+  // Cluster pairs: both CTAs walk the same list of (expert, m-tile pair, token tile) entries;
+  // this CTA takes m-tile 2 * mt + rank, and the token tile, which both need, is loaded half by
+  // each CTA and multicast to both.
+  const int rank = PAIR ? (int)cluster_ctarank() : 0;
+  const int tile0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int tstep = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  const auto decode = [&](int tile, Tile& t) {
+    decode_tile<GATEUP, NT>(p, tile, t);
+    if (PAIR) t.mt = 2 * t.mt + rank;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], PAIR ? 2 : 1);  // MMA commit (of both CTAs of a pair)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -88,6 +98,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();  // the peer's barriers are initialised before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   // the tile list (prefix) is written by the previous kernel
@@ -101,9 +112,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_b = policy_evict_last();   // token rows: reused by every weight tile
       uint32_t stage = 0, phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+      for (int tile = tile0; ok && tile < total; tile += tstep) {
         Tile t;
-        decode_tile<GATEUP, NT>(p, tile, t);
+        decode(tile, t);
         const bool wide = t.ntok == NT;   // full token tile: one TMA box of NT rows
         const int nbox = (t.ntok + kBoxRows - 1) / kBoxRows;
         const uint32_t bytes = KA * kATileBytes + (uint32_t)nbox * kBBoxBytes;
@@ -121,7 +132,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(st, &tm_w, &full[stage], kb * kBK, wrow, pol_w);
           if (KA == 2) tma_load_2d(st + kATileBytes, &tm_w, &full[stage], kb * kBK, wrow1, pol_w);
           uint8_t* bt = st + KA * kATileBytes;
-          if (wide) {
+          if (PAIR) {
+            // full tile: this CTA's half of the rows (the wide map's box is NT/2 rows);
+            // partial tile: every other 16-row box; both CTAs receive every byte
+            if (wide) {
+              tma_load_2d_mc(bt + rank * (NT / 2) * (kBK * 2), bmapw, &full[stage], kb * kBK,
+                             t.brow0 + rank * (NT / 2), 0x3, pol_b);
+            } else {
+              for (int i = rank; i < nbox; i += 2)
+                tma_load_2d_mc(bt + i * kBBoxBytes, bmap, &full[stage], kb * kBK,
+                               t.brow0 + i * kBoxRows, 0x3, pol_b);
+            }
+          } else if (wide) {
             tma_load_2d(bt, bmapw, &full[stage], kb * kBK, t.brow0, pol_b);
           } else {
             for (int i = 0; i < nbox; ++i)
@@ -135,6 +157,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < STAGES; ++s) {
         const uint32_t issued_phase = (s < (int)stage) ? phase : (phase ^ 1u);
         drain_bar(&full[s], issued_phase, p.status);
+        // with pairs, both CTAs' MMA commits for every issued stage arrive before the CTA exits
+        if (PAIR) drain_bar(&empty[s], issued_phase, p.status);
       }
     }
   } else if (warp == 1) {
@@ -143,9 +167,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0;
       uint32_t acc = 0, acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+      for (int tile = tile0; ok && tile < total; tile += tstep) {
         Tile t;
-        decode_tile<GATEUP, NT>(p, tile, t);
+        decode(tile, t);
         const int npad = (t.ntok + 15) & ~15;
         const uint32_t idesc = idesc_bf16(kBM, npad);
         if (!wait_bar(&acc_empty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
@@ -164,7 +188,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_bf16_ss(d0, da + 2 * kk, db + 2 * kk, idesc, accum);
             if (KA == 2) mma_bf16_ss(d0 + NT, du + 2 * kk, db + 2 * kk, idesc, accum);
           }
-          mma_commit(&empty[stage]);  // frees the stage once these MMAs have read it
+          if (PAIR)
+            mma_commit_mc(&empty[stage], 0x3);  // frees the stage in both CTAs of the pair
+          else
+            mma_commit(&empty[stage]);  // frees the stage once these MMAs have read it
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
@@ -175,28 +202,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
     run_epilogue<GATEUP, NT, S::kAccCols, KA, ACCB>(p, total, tmem_base, acc_full, acc_empty,
-                                                    abort_flag);
+                                                    abort_flag, tile0, tstep, PAIR ? rank : -1);
   }
 
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();  // no CTA leaves while its peer may still write to it
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, S::kTmemCols);
   }
 }
 
-template <bool GATEUP, int NT, int STAGES, int KA, int ACCB>
+template <bool GATEUP, int NT, int STAGES, int KA, int ACCB, bool PAIR = false>
 cudaError_t launch_variant(const CUtensorMap& w, const CUtensorMap& b0, const CUtensorMap& b1,
                            const CUtensorMap& b0w, const CUtensorMap& b1w, const TcParams& p,
                            cudaStream_t st) {
   using S = Smem<NT, STAGES, KA, ACCB>;
   static_assert(S::kTotal <= 227 * 1024, "shared memory");
-  auto kern = k_tc_ffn<GATEUP, NT, STAGES, KA, ACCB>;
+  auto kern = k_tc_ffn<GATEUP, NT, STAGES, KA, ACCB, PAIR>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)S::kTotal);
   if (e != cudaSuccess) return e;
   count_launches(1);
+  if (PAIR)
+    return launch_pdl_cluster(kern, dim3((unsigned)(num_sms() & ~1)), dim3(kThreads), S::kTotal,
+                              st, 2u, w, b0, b1, b0w, b1w, p);
   return launch_pdl(kern, dim3(num_sms()), dim3(kThreads), S::kTotal, st, w, b0, b1, b0w, b1w, p);
 }
 
@@ -215,6 +246,18 @@ int tc_tile_rows(bool gateup, bool decode, int d) {
   return (!gateup && down_pairs(d, decode)) ? 2 * kBM : kBM;
 }
 
+// Prefill tiles with two weight tiles per token tile run in cluster pairs (consecutive m-tiles,
+// token tile multicast) when an expert has an even number of such tiles.
+static bool tc_clustered(bool gateup, bool decode, int d, int f) {
+  if (decode || (!gateup && !down_pairs(d, decode))) return false;
+  return ((gateup ? f : d) / tc_tile_rows(gateup, decode, d)) % 2 == 0;
+}
+
+int tc_plan_mtiles(bool gateup, bool decode, int d, int f) {
+  const int mtiles = (gateup ? f : d) / tc_tile_rows(gateup, decode, d);
+  return tc_clustered(gateup, decode, d, f) ? mtiles / 2 : mtiles;
+}
+
 cudaError_t launch_tc(const FfnArgs& a, const int32_t* prefix, bool gateup, bool decode,
                       cudaStream_t st) {
   TcParams p{};
@@ -231,7 +274,9 @@ cudaError_t launch_tc(const FfnArgs& a, const int32_t* prefix, bool gateup, bool
   const uint64_t E1 = (uint64_t)a.E + a.n_shared;
   const uint64_t routed = (uint64_t)a.T * a.k;
   const uint64_t slots = routed + (uint64_t)a.n_shared * a.T;
-  const uint32_t nt = (uint32_t)tc_tile_tokens(gateup, decode);
+  const bool cl = tc_clustered(gateup, decode, a.d, a.f);
+  // full token tiles arrive in one box, or, with pairs, in one half-tile box from each CTA
+  const uint32_t nt = (uint32_t)tc_tile_tokens(gateup, decode) / (cl ? 2u : 1u);
   CUtensorMap w, b0, b1, b0w, b1w;
   cudaError_t e;
   if (gateup) {
@@ -250,8 +295,10 @@ cudaError_t launch_tc(const FfnArgs& a, const int32_t* prefix, bool gateup, bool
   if (e != cudaSuccess) return e;
   if (gateup)
     return decode ? launch_variant<true, 64, 5, 2, 2>(w, b0, b1, b0w, b1w, p, st)
-                  : launch_variant<true, 256, 3, 2, 1>(w, b0, b1, b0w, b1w, p, st);
+                  : cl ? launch_variant<true, 256, 3, 2, 1, true>(w, b0, b1, b0w, b1w, p, st)
+                       : launch_variant<true, 256, 3, 2, 1>(w, b0, b1, b0w, b1w, p, st);
   if (decode) return launch_variant<false, 64, 8, 1, 2>(w, b0, b1, b0w, b1w, p, st);
+  if (cl) return launch_variant<false, 256, 3, 2, 1, true>(w, b0, b1, b0w, b1w, p, st);
   return down_pairs(a.d, decode) ? launch_variant<false, 256, 3, 2, 1>(w, b0, b1, b0w, b1w, p, st)
                                  : launch_variant<false, 256, 4, 1, 2>(w, b0, b1, b0w, b1w, p, st);
 }

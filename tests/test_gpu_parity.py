@@ -69,6 +69,7 @@ SMALL = [
     ("tiny", {"T": 600, "E": 8, "k": 2, "wdtype": "fp8"}),
     # FP8 prefill tiles in cluster pairs (even m-tile counts in both passes)
     ("tiny", {"T": 600, "d": 512, "f": 256, "E": 8, "k": 2, "wdtype": "fp8"}),
+    ("tiny", {"T": 600, "d": 512, "f": 256, "E": 8, "k": 2}),                  # bf16 pairs
     ("tiny", {"T": 333, "d": 384, "f": 256, "E": 6, "k": 3, "wdtype": "fp8"}),
     ("tiny", {"T": 333, "d": 384, "f": 256, "E": 6, "k": 3}),
 ]
