@@ -125,8 +125,8 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32
   pa.group = gemv_group_tokens();
   pa.items_up = gemv_items_per_group(true, s.d, s.f);
   pa.items_dn = gemv_items_per_group(false, s.d, s.f);
-  pa.nt_up = fp8 ? tc_fp8_tile_tokens(true, decode) : tc_tile_tokens(true, decode);
-  pa.nt_dn = fp8 ? tc_fp8_tile_tokens(false, decode) : tc_tile_tokens(false, decode);
+  pa.nt_up = fp8 ? tc_fp8_tile_tokens(true, decode, routed, s.E) : tc_tile_tokens(true, decode);
+  pa.nt_dn = fp8 ? tc_fp8_tile_tokens(false, decode, routed, s.E) : tc_tile_tokens(false, decode);
   pa.mt_up = s.f / 128;
   pa.mt_dn = s.d / tc_tile_rows(false, decode, s.d);
   if (!fp8) {

@@ -35,7 +35,7 @@ cudaError_t launch_tc(const FfnArgs& a, const int32_t* prefix, bool gateup, bool
                       cudaStream_t st);
 
 // tensor-core path (ffn_tc_fp8.cu): E4M3 weights dequantised into TMEM
-int tc_fp8_tile_tokens(bool gateup, bool decode);
+int tc_fp8_tile_tokens(bool gateup, bool decode, long routed, int E);
 cudaError_t launch_tc_fp8(const FfnArgs& a, const int32_t* prefix, bool gateup, bool decode,
                           cudaStream_t st);
 // wide-tile variant (ffn_tc_fp8_wide.cu): E4M3 weights dequantised to bf16 into TMEM

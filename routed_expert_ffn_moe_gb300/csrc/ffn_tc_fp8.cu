@@ -327,9 +327,14 @@ cudaError_t launch_variant(const CUtensorMap& w, const CUtensorMap& b0, const CU
 
 }  // namespace
 
-int tc_fp8_tile_tokens(bool gateup, bool decode) {
+// Decode tiles: 32 tokens while experts average at most 16 routed tokens, else 64 (so an expert
+// near the average still fits one tile and its weights are converted once).
+static bool fp8_tile64(long routed, int E) { return routed > 16L * E; }
+
+int tc_fp8_tile_tokens(bool gateup, bool decode, long routed, int E) {
   (void)gateup;
-  return decode ? 32 : tc_fp8_wide_tile_tokens();
+  if (!decode) return tc_fp8_wide_tile_tokens();
+  return fp8_tile64(routed, E) ? 64 : 32;
 }
 
 cudaError_t launch_tc_fp8(const FfnArgs& a, const int32_t* prefix, bool gateup, bool decode,
@@ -362,6 +367,10 @@ cudaError_t launch_tc_fp8(const FfnArgs& a, const int32_t* prefix, bool gateup, 
   }
   if (e != cudaSuccess) return e;
   const float* sc = gateup ? a.s13 : a.s2;
+  if (fp8_tile64((long)routed, a.E)) {
+    if (gateup) return launch_variant<true, 64, 3, 2>(w, b0, b1, p, sc, st);
+    return launch_variant<false, 64, 5, 3>(w, b0, b1, p, sc, st);
+  }
   if (gateup) return launch_variant<true, 32, 4, 3>(w, b0, b1, p, sc, st);
   return launch_variant<false, 32, 6, 4>(w, b0, b1, p, sc, st);
 }
