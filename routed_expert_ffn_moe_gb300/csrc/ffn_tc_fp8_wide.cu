@@ -16,7 +16,7 @@
 // the stream that comes from HBM, so they get the deepest ring and a producer thread of their
 // own, which runs as far ahead as the code ring allows whatever the token ring is doing.
 #include <cuda_bf16.h>
-#include <cuda_fp8.h>
+#include <cuda_fp16.h>
 
 #include "tc_common.cuh"
 
@@ -47,12 +47,27 @@ struct SmemW {
   static constexpr uint32_t kTmemCols = ACCB * kAccCols;
 };
 
-// Two E4M3 codes (low byte first) times the block scale, as a bf16 pair (low element first).
-__device__ __forceinline__ uint32_t dequant2(uint32_t two, float s) {
-  const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xFFFFu), __NV_E4M3);
-  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
-  const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * s, f.y * s);
-  return *reinterpret_cast<const uint32_t*>(&b);
+// Four E4M3 codes (lowest byte first) times the block scale, as two bf16 pairs (codes 0,1 ->
+// lo, codes 2,3 -> hi): the word's 16-bit halves convert exactly to f16 pairs, widen to fp32,
+// and one packed fused multiply-add per pair (addend -0, so the result is the rounded product
+// q * s) precedes the single rounding to bf16.
+__device__ __forceinline__ void dequant4(uint32_t four, float2 s2, uint32_t& lo, uint32_t& hi) {
+  uint32_t h01, h23;
+  asm("{\n"
+      "  .reg .b16 c01, c23;\n"
+      "  mov.b32 {c01, c23}, %2;\n"
+      "  cvt.rn.f16x2.e4m3x2 %0, c01;\n"
+      "  cvt.rn.f16x2.e4m3x2 %1, c23;\n"
+      "}"
+      : "=r"(h01), "=r"(h23)
+      : "r"(four));
+  const float2 nz = make_float2(-0.f, -0.f);
+  const float2 f01 = __ffma2_rn(__half22float2(*reinterpret_cast<const __half2*>(&h01)), s2, nz);
+  const float2 f23 = __ffma2_rn(__half22float2(*reinterpret_cast<const __half2*>(&h23)), s2, nz);
+  const __nv_bfloat162 b01 = __floats2bfloat162_rn(f01.x, f01.y);
+  const __nv_bfloat162 b23 = __floats2bfloat162_rn(f23.x, f23.y);
+  lo = *reinterpret_cast<const uint32_t*>(&b01);
+  hi = *reinterpret_cast<const uint32_t*>(&b23);
 }
 
 __device__ __forceinline__ void sts_u4(uint32_t addr, const uint4& v) {
@@ -290,15 +305,12 @@ __global__ void __launch_bounds__(kThreadsW, 1)
           // source: 64-byte rows, 64-byte swizzle (16-byte chunk j ^ ((r >> 1) & 3))
           const uint4 raw = lds_u4(src + a * kCodeTileBytes + r * 64 + ((j ^ ((r >> 1) & 3)) << 4));
           const float s = a ? s1 : s0;
+          const float2 s2 = make_float2(s, s);
           uint4 lo, hi;  // codes 0..7 -> chunk 2j, codes 8..15 -> chunk 2j+1
-          lo.x = dequant2(raw.x & 0xFFFFu, s);
-          lo.y = dequant2(raw.x >> 16, s);
-          lo.z = dequant2(raw.y & 0xFFFFu, s);
-          lo.w = dequant2(raw.y >> 16, s);
-          hi.x = dequant2(raw.z & 0xFFFFu, s);
-          hi.y = dequant2(raw.z >> 16, s);
-          hi.z = dequant2(raw.w & 0xFFFFu, s);
-          hi.w = dequant2(raw.w >> 16, s);
+          dequant4(raw.x, s2, lo.x, lo.y);
+          dequant4(raw.y, s2, lo.z, lo.w);
+          dequant4(raw.z, s2, hi.x, hi.y);
+          dequant4(raw.w, s2, hi.z, hi.w);
           // destination: 128-byte rows, 128-byte swizzle (16-byte chunk c ^ (r & 7))
           const uint32_t rowb = dst + a * kATileBytes + r * 128;
           sts_u4(rowb + (((2 * j) ^ (r & 7)) << 4), lo);
