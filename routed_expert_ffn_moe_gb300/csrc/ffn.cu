@@ -7,6 +7,7 @@
 // work items for each kernel, and the persistent FFN kernels walk those lists.
 #include <climits>
 #include <cstdlib>
+#include <mutex>
 
 #include "ffn.h"
 
@@ -18,22 +19,51 @@ struct PlanArgs {
   int group, items_up, items_dn;   // weight-streaming: tokens per item, items per group
   int nt_up, nt_dn, mt_up, mt_dn;  // tensor-core: tokens per tile, weight tiles per expert
   int stride;
+  // Split prefill (split != 0): experts with at most cold_max tokens form a second tile list
+  // (nt_c-token tiles, mt_up_c / mt_dn_c weight tiles per expert) run on their own CTAs.
+  int split, cold_max, nt_c, mt_up_c, mt_dn_c, nsm;
+  // per pass (0 gate/up, 1 down), in SM-microseconds: streaming one cold expert's weights,
+  // tensor work per token of a hot expert, and the least a hot expert costs
+  float cold_cost[2], hot_cost_tok[2], hot_cost_min[2];
 };
 
+__device__ __forceinline__ float block_sum(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float t = 0.f;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w];
+  return t;
+}
+
 // plan[row][e]: exclusive prefix over experts of the work of each kernel; entry E1 = total.
+// With a split, row kPlanSplit holds the number of CTAs for the cold list and for the rest,
+// chosen so that both lists take about the same time by a simple cost model.
 __global__ void __launch_bounds__(1024) k_ffn_plan(const int32_t* __restrict__ offsets,
                                                    PlanArgs a, int32_t* __restrict__ plan) {
   pdl_wait_then_release();
+  __shared__ float red[32];
   const int E1 = a.E + a.n_shared;
-  int run[4] = {0, 0, 0, 0};
+  constexpr int R = kPlanTcDnCold + 1;
+  int run[R] = {};
+  float cold[2] = {0.f, 0.f}, hot[2] = {0.f, 0.f};
   for (int b = 0; b < E1; b += blockDim.x) {
     const int e = b + threadIdx.x;
-    int n[4] = {0, 0, 0, 0};
+    int n[R] = {};
     if (e < E1) {
       const int cnt = offsets[e + 1] - offsets[e];
-      if (cnt >= a.tc_min) {
+      if (a.split && cnt > 0 && cnt <= a.cold_max) {
+        n[kPlanTcUpCold] = (cnt + a.nt_c - 1) / a.nt_c * a.mt_up_c;
+        n[kPlanTcDnCold] = (cnt + a.nt_c - 1) / a.nt_c * a.mt_dn_c;
+        cold[0] += a.cold_cost[0];
+        cold[1] += a.cold_cost[1];
+      } else if (cnt >= a.tc_min) {
         n[kPlanTcUp] = (cnt + a.nt_up - 1) / a.nt_up * a.mt_up;
         n[kPlanTcDown] = (cnt + a.nt_dn - 1) / a.nt_dn * a.mt_dn;
+        hot[0] += fmaxf(a.hot_cost_min[0], a.hot_cost_tok[0] * (float)cnt);
+        hot[1] += fmaxf(a.hot_cost_min[1], a.hot_cost_tok[1] * (float)cnt);
       } else if (cnt > 0) {
         const int groups = (cnt + a.group - 1) / a.group;
         n[kPlanGemvUp] = groups * a.items_up;
@@ -41,15 +71,31 @@ __global__ void __launch_bounds__(1024) k_ffn_plan(const int32_t* __restrict__ o
       }
     }
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
+    for (int r = 0; r < R; ++r) {
       int tot;
       const int pre = block_exclusive_scan(n[r], &tot);
       if (e < E1) plan[r * a.stride + e] = run[r] + pre;
       run[r] += tot;
     }
   }
-  if (threadIdx.x == 0)
-    for (int r = 0; r < 4; ++r) plan[r * a.stride + E1] = run[r];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    cold[i] = block_sum(cold[i], red);
+    hot[i] = block_sum(hot[i], red);
+  }
+  if (threadIdx.x == 0) {
+    for (int r = 0; r < R; ++r) plan[r * a.stride + E1] = run[r];
+    for (int i = 0; i < 2; ++i) {
+      int xc = 0;  // CTAs for the cold list, an even number (the other list runs in pairs)
+      if (a.split && cold[i] > 0.f) {
+        xc = hot[i] > 0.f ? 2 * __float2int_rn(0.5f * a.nsm * cold[i] / (cold[i] + hot[i]))
+                          : a.nsm;
+        xc = min(max(xc, 2), hot[i] > 0.f ? a.nsm - 2 : a.nsm);
+      }
+      plan[kPlanSplit * a.stride + 2 * i] = xc;
+      plan[kPlanSplit * a.stride + 2 * i + 1] = a.nsm - xc;
+    }
+  }
 }
 
 // x_perm[s] = x[perm_token[s]] for every routed slot: the tensor-core path's token tiles are
@@ -89,6 +135,37 @@ int tc_min_tokens() {
   if (!v || !*v) return 1;
   const long n = strtol(v, nullptr, 10);
   return n < 1 ? 1 : (n > INT_MAX ? INT_MAX : (int)n);
+}
+
+// Second stream and fork/join events of the split prefill, one set per device, created on first
+// use (host objects; no device memory). The record/wait sequence of one call is made under a
+// lock so that calls from several host threads do not interleave their event records.
+struct SplitStreams {
+  cudaStream_t aux = nullptr;
+  cudaEvent_t ev[4] = {};
+};
+std::mutex g_split_mu;
+SplitStreams g_split[64];
+
+cudaError_t split_streams(SplitStreams** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  SplitStreams& s = g_split[dev];
+  if (!s.aux) {
+    if ((e = cudaStreamCreateWithFlags(&s.aux, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    for (auto& ev : s.ev)
+      if ((e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess) return e;
+  }
+  *out = &s;
+  return cudaSuccess;
+}
+
+// `st` waits for everything enqueued so far on `from`.
+cudaError_t join(cudaStream_t st, cudaStream_t from, cudaEvent_t ev) {
+  cudaError_t e = cudaEventRecord(ev, from);
+  return e == cudaSuccess ? cudaStreamWaitEvent(st, ev, 0) : e;
 }
 
 }  // namespace
@@ -138,6 +215,30 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32
   }
   pa.stride = s.E + 2;
   const int stride = pa.stride;
+  // Split prefill (bf16 weights, all experts on the tensor cores): experts with at most one
+  // decode tile of tokens stream their weights through the decode tiles on part of the SMs
+  // while the others run the prefill tiles on the rest, on a second stream, so that the
+  // HBM-bound and the tensor-bound experts overlap instead of taking turns on every SM.
+  const bool split = !fp8 && !decode && use_tc && !use_gemv && routed > 0;
+  if (split) {
+    // Measured rates on GB300 (one SM): decode tiles stream weights at ~78 GB/s in the gate/up
+    // pass and ~52 GB/s in the down pass (shorter tiles); prefill tiles run ~8 TFLOP/s.
+    const double bytes = s.d * (double)s.f * 2.0;       // one bf16 weight matrix of an expert
+    const double bw_up = 78e3, bw_dn = 52e3;            // bytes per microsecond
+    const double tc_sm = 8e6;                           // FLOP per microsecond
+    pa.split = 1;
+    pa.nt_c = tc_tile_tokens(true, true);
+    pa.cold_max = pa.nt_c;
+    pa.mt_up_c = tc_plan_mtiles(true, true, s.d, s.f);
+    pa.mt_dn_c = tc_plan_mtiles(false, true, s.d, s.f);
+    pa.nsm = num_sms() & ~1;
+    pa.cold_cost[0] = (float)(2.0 * bytes / bw_up);
+    pa.cold_cost[1] = (float)(bytes / bw_dn);
+    pa.hot_cost_min[0] = pa.cold_cost[0];
+    pa.hot_cost_min[1] = pa.cold_cost[1];
+    pa.hot_cost_tok[0] = (float)(4.0 * s.d * s.f / tc_sm);
+    pa.hot_cost_tok[1] = (float)(2.0 * s.d * s.f / tc_sm);
+  }
 
   const PhaseEvents ev = profile_phase_events();
   cudaError_t e = launch_pdl(k_ffn_plan, dim3(1), dim3(1024), 0, st, offsets, pa, plan);
@@ -163,6 +264,29 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32
     return fp8 ? launch_tc_fp8(a, prefix, gateup, decode, st)
                : launch_tc(a, prefix, gateup, decode, st);
   };
+
+  if (split) {
+    SplitStreams* ss = nullptr;
+    if ((e = split_streams(&ss)) != cudaSuccess) return e;
+    const int32_t* act = plan + kPlanSplit * stride;
+    std::lock_guard<std::mutex> lk(g_split_mu);
+    cudaStream_t aux = ss->aux;
+    if ((e = join(aux, st, ss->ev[0])) != cudaSuccess) return e;
+    if ((e = launch_tc(a, plan + kPlanTcUpCold * stride, true, true, st, act)) != cudaSuccess)
+      return e;
+    if ((e = launch_tc(a, plan + kPlanTcUp * stride, true, false, aux, act + 1)) != cudaSuccess)
+      return e;
+    if ((e = join(st, aux, ss->ev[1])) != cudaSuccess) return e;
+    if (ev.mid) record_phase(ev.mid, st);
+    if ((e = join(aux, st, ss->ev[2])) != cudaSuccess) return e;
+    if ((e = launch_tc(a, plan + kPlanTcDnCold * stride, false, true, st, act + 2)) != cudaSuccess)
+      return e;
+    if ((e = launch_tc(a, plan + kPlanTcDown * stride, false, false, aux, act + 3)) != cudaSuccess)
+      return e;
+    if ((e = join(st, aux, ss->ev[3])) != cudaSuccess) return e;
+    if (ev.end) record_phase(ev.end, st);
+    return cudaSuccess;
+  }
 
   if (use_tc) e = tc(true, plan + kPlanTcUp * stride);
   if (e == cudaSuccess)

@@ -67,9 +67,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Cluster pairs: both CTAs walk the same list of (expert, m-tile pair, token tile) entries;
   // this CTA takes m-tile 2 * mt + rank, and the token tile, which both need, is loaded half by
   // each CTA and multicast to both.
+  int nact = (int)gridDim.x;
+  if (p.active) {
+    pdl_wait_then_release();  // the count is written by the plan kernel
+    nact = __ldg(p.active);   // even with pairs, so both CTAs of a cluster leave together
+    if ((int)blockIdx.x >= nact) return;
+  }
   const int rank = PAIR ? (int)cluster_ctarank() : 0;
   const int tile0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-  const int tstep = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  const int tstep = PAIR ? nact >> 1 : nact;
   const auto decode = [&](int tile, Tile& t) {
     decode_tile<GATEUP, NT>(p, tile, t);
     if (PAIR) t.mt = 2 * t.mt + rank;
@@ -259,8 +265,9 @@ int tc_plan_mtiles(bool gateup, bool decode, int d, int f) {
 }
 
 cudaError_t launch_tc(const FfnArgs& a, const int32_t* prefix, bool gateup, bool decode,
-                      cudaStream_t st) {
+                      cudaStream_t st, const int32_t* active) {
   TcParams p{};
+  p.active = active;
   p.T = a.T; p.k = a.k; p.E = a.E; p.n_shared = a.n_shared;
   p.f = a.f; p.d = a.d;
   p.K = gateup ? a.d : a.f;

@@ -46,7 +46,11 @@ inline WsLayout ws_layout(const moe_shape& s) {
 }
 
 // plan rows (each E+2 int32 entries, see ffn kernels)
-enum PlanRow { kPlanGemvUp = 0, kPlanGemvDown = 1, kPlanTcUp = 2, kPlanTcDown = 3 };
+enum PlanRow {
+  kPlanGemvUp = 0, kPlanGemvDown = 1, kPlanTcUp = 2, kPlanTcDown = 3,
+  kPlanTcUpCold = 4, kPlanTcDnCold = 5,  // split prefill: the cold experts' tile lists
+  kPlanSplit = 6                         // split prefill: [CTAs for cold, CTAs for the rest]
+};
 
 // ---- launchers (each returns cudaGetLastError() of its launches) ---------------------------
 cudaError_t launch_route(const moe_shape& s, const uint16_t* x, const uint16_t* wg,

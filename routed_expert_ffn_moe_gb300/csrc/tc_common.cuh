@@ -29,6 +29,9 @@ struct TcParams {
   uint16_t* h;
   float* y_perm;
   int* status;
+  // number of CTAs that take tiles (device memory, written by the plan kernel), or null for
+  // all of them: the others leave at once
+  const int32_t* active;
 };
 
 struct Tile {

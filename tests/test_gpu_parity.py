@@ -71,6 +71,8 @@ SMALL = [
     # FP8 prefill tiles in cluster pairs (even m-tile counts in both passes)
     ("tiny", {"T": 600, "d": 512, "f": 256, "E": 8, "k": 2, "wdtype": "fp8"}),
     ("tiny", {"T": 600, "d": 512, "f": 256, "E": 8, "k": 2}),                  # bf16 pairs
+    # bf16 prefill split: cold experts on decode tiles beside hot ones on paired tiles
+    ("tiny", {"router": "zipf", "T": 600, "d": 512, "f": 256, "E": 16, "k": 2}),
     ("tiny", {"T": 333, "d": 384, "f": 256, "E": 6, "k": 3, "wdtype": "fp8"}),
     ("tiny", {"T": 333, "d": 384, "f": 256, "E": 6, "k": 3}),
 ]
@@ -187,7 +189,8 @@ def test_layer_is_deterministic():
     assert torch().equal(ia, b.topk_idx) and torch().equal(pa, b.perm_token)
 
 
-@pytest.mark.parametrize("over", [{}, {"wdtype": "fp8", "T": 70, "E": 12, "k": 3, "d": 512, "f": 384}])
+@pytest.mark.parametrize("over", [{}, {"wdtype": "fp8", "T": 70, "E": 12, "k": 3, "d": 512, "f": 384},
+                                  {"router": "zipf", "T": 600, "d": 512, "f": 256, "E": 16, "k": 2}])
 def test_layer_replays_from_a_cuda_graph(over):
     # the four calls enqueue no synchronisation or allocation, so they can be captured once
     cfg = synth.get_config("tiny", **over)
