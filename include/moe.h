@@ -17,7 +17,8 @@
  *   - Pointers named x, wg, bias, topk_*, expert_offsets, perm_token, inv_slot, w13, s13, w2,
  *     s2, y_perm, y and ws are DEVICE pointers, allocated and owned by the caller. The library
  *     never allocates, frees or synchronises in these calls; work is enqueued on `stream`
- *     (a cudaStream_t, NULL = legacy default stream) and the call returns immediately.
+ *     (a cudaStream_t, NULL = legacy default stream) and the call returns immediately
+ *     (moe_expert_ffn may also use one library-owned stream per device; see there).
  *   - `shape` is a host pointer read during the call only.
  *   - Arguments are validated on the host first: a negative status is returned before any
  *     launch and nothing is written (no side effects).
@@ -135,7 +136,12 @@ MOE_API moe_status moe_permute(const moe_shape* shape, const int32_t* topk_idx, 
  *                  for bf16.
  *   y_perm         [T*k + n_shared*T, d] fp32 out: row s = expert output for slot s, i.e.
  *                  W_d^T (SiLU(W_g^T x) * (W_u^T x)) for the slot's token and expert.
- * The intermediate h = SiLU(G) * U is kept in bf16; accumulation is fp32. */
+ * The intermediate h = SiLU(G) * U is kept in bf16; accumulation is fp32.
+ * Prefill-sized batches with bf16 weights (more than 32 routed tokens per expert on average)
+ * run the experts with few tokens and those with many on two streams at once: `stream` and a
+ * second stream the library creates on its first such call on each device (a host-side object;
+ * no device memory is allocated), ordered against `stream` with events inside the call, so the
+ * call still behaves as work enqueued on `stream` (also under CUDA-graph capture). */
 MOE_API moe_status moe_expert_ffn(const moe_shape* shape, const void* x, const int32_t* perm_token,
                           const int32_t* expert_offsets, const void* w13, const float* s13,
                           const void* w2, const float* s2, float* y_perm, void* ws,
