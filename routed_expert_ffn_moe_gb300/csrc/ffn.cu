@@ -212,6 +212,8 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32
   } else if (!decode) {
     pa.mt_up = tc_fp8_wide_plan_mtiles(true, s.d, s.f);
     pa.mt_dn = tc_fp8_wide_plan_mtiles(false, s.d, s.f);
+  } else {
+    pa.mt_dn = s.d / tc_fp8_decode_down_rows(s.d);
   }
   pa.stride = s.E + 2;
   const int stride = pa.stride;

@@ -36,6 +36,7 @@ cudaError_t launch_tc(const FfnArgs& a, const int32_t* prefix, bool gateup, bool
 
 // tensor-core path (ffn_tc_fp8.cu): E4M3 weights dequantised into TMEM
 int tc_fp8_tile_tokens(bool gateup, bool decode, long routed, int E);
+int tc_fp8_decode_down_rows(int d);  // weight rows per down tile of the decode tiles
 cudaError_t launch_tc_fp8(const FfnArgs& a, const int32_t* prefix, bool gateup, bool decode,
                           cudaStream_t st);
 // wide-tile variant (ffn_tc_fp8_wide.cu): E4M3 weights dequantised to bf16 into TMEM

@@ -45,16 +45,18 @@ constexpr int kConvThreads = 32 * kConvWarps;
 constexpr int kThreadsQ = 32 * 6 + kConvThreads;  // producer, MMA, 4 epilogue, converters
 constexpr uint32_t kACols = kQK / 2;              // TMEM columns of one 128 x 128 f16 tile
 
-template <bool GATEUP, int NT, int STAGES, int CSTAGES>
+// KA weight tiles of 128 rows share each token tile: gate and up rows of the same features in
+// the gate/up pass; one, or two consecutive, 128-row tiles of W_d in the down pass.
+template <bool GATEUP, int NT, int STAGES, int CSTAGES, int KA>
 struct SmemQ {
-  static constexpr int kA = GATEUP ? 2 : 1;
+  static constexpr int kA = KA;
   static constexpr uint32_t kBHalf = (uint32_t)NT * kBK * 2;   // NT rows x 64 K of 16-bit
   static constexpr uint32_t kStageBytes = kA * kQTileBytes + 2 * kBHalf;   // TMA ring
   static constexpr uint32_t kCSlotBytes = kA * 2 * kBHalf;                 // scaled token tiles
   static constexpr uint32_t kTilesBytes = STAGES * kStageBytes + CSTAGES * kCSlotBytes;
   static constexpr uint32_t kBarBytes = 8 * (2 * STAGES + 2 * CSTAGES + 4) + 16;
   static constexpr uint32_t kTotal = kTilesBytes + kBarBytes + 1024;
-  static constexpr uint32_t kAccCols = GATEUP ? 2 * NT : NT;
+  static constexpr uint32_t kAccCols = KA * NT;
   static constexpr uint32_t kAStageCols = kA * kACols;
   static constexpr uint32_t kUsedCols = 2 * kAccCols + CSTAGES * kAStageCols;
   static constexpr uint32_t kTmemCols =
@@ -93,13 +95,14 @@ __device__ __forceinline__ void sts_u4(uint32_t addr, const uint4& v) {
                : "memory");
 }
 
-template <bool GATEUP, int NT, int STAGES, int CSTAGES>
+template <bool GATEUP, int NT, int STAGES, int CSTAGES, int KA>
 __global__ void __launch_bounds__(kThreadsQ, 1)
     k_tc_ffn_fp8(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b0,
                  const __grid_constant__ CUtensorMap tm_b1, const TcParams p,
                  const float* __restrict__ scales) {
-  using S = SmemQ<GATEUP, NT, STAGES, CSTAGES>;
+  using S = SmemQ<GATEUP, NT, STAGES, CSTAGES, KA>;
   static_assert(S::kUsedCols <= 512, "TMEM columns");
+  static_assert(!GATEUP || KA == 2, "gate/up tiles pair the gate and up rows");
   static_assert(NT % 16 == 0 && NT >= 16 && NT <= 256, "MMA N");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -162,14 +165,16 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
         decode_tile<GATEUP, NT>(p, tile, t);
         const int nbox = (t.ntok + kBoxRows - 1) / kBoxRows;
         const uint32_t bytes = S::kA * kQTileBytes + (uint32_t)nbox * 2 * kBBoxBytes;
-        const int wrow = t.e * p.rows_per_expert + t.mt * kBM;
+        const int wrow = t.e * p.rows_per_expert + t.mt * kBM * (GATEUP ? 1 : KA);
         const CUtensorMap* bmap = (GATEUP && t.shared) ? &tm_b1 : &tm_b0;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!wait_bar(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
           uint8_t* st = smem + stage * S::kStageBytes;
           mbar_arrive_expect_tx(&full[stage], bytes);
           tma_load_2d(st, &tm_w, &full[stage], kb * kQK, wrow, pol_w);
-          if (GATEUP) tma_load_2d(st + kQTileBytes, &tm_w, &full[stage], kb * kQK, wrow + p.f, pol_w);
+          if (KA == 2)  // up rows of the same features, or the next 128 rows of W_d
+            tma_load_2d(st + kQTileBytes, &tm_w, &full[stage], kb * kQK,
+                        wrow + (GATEUP ? p.f : kBM), pol_w);
           uint8_t* bt = st + S::kA * kQTileBytes;
           for (int i = 0; i < nbox; ++i)
             for (int hk = 0; hk < 2; ++hk)
@@ -207,7 +212,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
             const uint32_t accum = (kb | kk) ? 1u : 0u;
             const uint32_t boff = (kk >> 2) * S::kBHalf;
             mma_ts(d0, a0 + kk * 8, sw128_desc(bp + boff) + 2 * (kk & 3), idesc, accum);
-            if (GATEUP)
+            if (KA == 2)
               mma_ts(d0 + NT, a0 + kACols + kk * 8,
                           sw128_desc(bp + 2 * S::kBHalf + boff) + 2 * (kk & 3), idesc, accum);
           }
@@ -221,7 +226,8 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
     }
   } else if (warp < 6) {
     // ---------------- epilogue (warps 2..5) ----------------
-    run_epilogue<GATEUP, NT, S::kAccCols>(p, total, tmem_base, acc_full, acc_empty, abort_flag);
+    run_epilogue<GATEUP, NT, S::kAccCols, KA>(p, total, tmem_base, acc_full, acc_empty,
+                                              abort_flag);
   } else {
     // ---------------- converters (warps 6..13) ----------------
     // Group g (4 warps, one per TMEM lane quadrant) converts every stage i with i % 2 == g, the
@@ -238,14 +244,15 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
       Tile t;
       decode_tile<GATEUP, NT>(p, tile, t);
       const float* sc = scales + (size_t)t.e * (p.rows_per_expert / 128) * kbl;
-      const float* sc_g = sc + t.mt * kbl;                   // gate (or down) row block
-      const float* sc_u = sc + (p.f / 128 + t.mt) * kbl;     // up row block
+      const int rb0 = GATEUP ? t.mt : t.mt * KA;             // scale row block of tile 0
+      const float* sc_g = sc + rb0 * kbl;                    // gate (or down) row block
+      const float* sc_u = sc + (GATEUP ? p.f / 128 + t.mt : rb0 + 1) * kbl;  // up / next rows
       for (int kb = 0; kb < kblocks; ++kb, ++it) {
         if ((int)(it % kConvGroups) != grp) continue;
         const uint32_t stage = it % STAGES, phase = (it / STAGES) & 1u;
         const uint32_t cs = it % CSTAGES, cphase = (it / CSTAGES) & 1u;
         const float s_g = __ldg(sc_g + kb);
-        const float s_u = GATEUP ? __ldg(sc_u + kb) : 0.f;
+        const float s_u = KA == 2 ? __ldg(sc_u + kb) : 0.f;
         if (!wait_bar(&full[stage], phase, abort_flag, p.status) ||
             !wait_bar(&c_empty[cs], cphase ^ 1u, abort_flag, p.status)) { ok = false; break; }
         const uint32_t st = smem_u32(smem + stage * S::kStageBytes);
@@ -312,12 +319,12 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
   }
 }
 
-template <bool GATEUP, int NT, int STAGES, int CSTAGES>
+template <bool GATEUP, int NT, int STAGES, int CSTAGES, int KA>
 cudaError_t launch_variant(const CUtensorMap& w, const CUtensorMap& b0, const CUtensorMap& b1,
                            const TcParams& p, const float* scales, cudaStream_t st) {
-  using S = SmemQ<GATEUP, NT, STAGES, CSTAGES>;
+  using S = SmemQ<GATEUP, NT, STAGES, CSTAGES, KA>;
   static_assert(S::kTotal <= 227 * 1024, "shared memory");
-  auto kern = k_tc_ffn_fp8<GATEUP, NT, STAGES, CSTAGES>;
+  auto kern = k_tc_ffn_fp8<GATEUP, NT, STAGES, CSTAGES, KA>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)S::kTotal);
   if (e != cudaSuccess) return e;
@@ -330,6 +337,10 @@ cudaError_t launch_variant(const CUtensorMap& w, const CUtensorMap& b0, const CU
 // Decode tiles: 32 tokens while experts average at most 16 routed tokens, else 64 (so an expert
 // near the average still fits one tile and its weights are converted once).
 static bool fp8_tile64(long routed, int E) { return routed > 16L * E; }
+
+// Down tiles pair two consecutive 128-row tiles of W_d (32 KB of codes per stage, as in the
+// gate/up pass) when d allows it: the per-stage hand-offs then move twice the bytes.
+int tc_fp8_decode_down_rows(int d) { return d % 256 == 0 ? 2 * kBM : kBM; }
 
 int tc_fp8_tile_tokens(bool gateup, bool decode, long routed, int E) {
   (void)gateup;
@@ -344,7 +355,8 @@ cudaError_t launch_tc_fp8(const FfnArgs& a, const int32_t* prefix, bool gateup, 
   p.T = a.T; p.k = a.k; p.E = a.E; p.n_shared = a.n_shared;
   p.f = a.f; p.d = a.d;
   p.K = gateup ? a.d : a.f;
-  p.mtiles = (gateup ? a.f : a.d) / kBM;
+  const bool pair_dn = !gateup && tc_fp8_decode_down_rows(a.d) == 2 * kBM;
+  p.mtiles = gateup ? a.f / kBM : a.d / tc_fp8_decode_down_rows(a.d);
   p.rows_per_expert = gateup ? 2 * a.f : a.d;
   p.offsets = a.offsets;
   p.prefix = prefix;
@@ -368,11 +380,13 @@ cudaError_t launch_tc_fp8(const FfnArgs& a, const int32_t* prefix, bool gateup, 
   if (e != cudaSuccess) return e;
   const float* sc = gateup ? a.s13 : a.s2;
   if (fp8_tile64((long)routed, a.E)) {
-    if (gateup) return launch_variant<true, 64, 3, 2>(w, b0, b1, p, sc, st);
-    return launch_variant<false, 64, 5, 3>(w, b0, b1, p, sc, st);
+    if (gateup) return launch_variant<true, 64, 3, 2, 2>(w, b0, b1, p, sc, st);
+    if (pair_dn) return launch_variant<false, 64, 3, 2, 2>(w, b0, b1, p, sc, st);
+    return launch_variant<false, 64, 5, 3, 1>(w, b0, b1, p, sc, st);
   }
-  if (gateup) return launch_variant<true, 32, 4, 3>(w, b0, b1, p, sc, st);
-  return launch_variant<false, 32, 6, 4>(w, b0, b1, p, sc, st);
+  if (gateup) return launch_variant<true, 32, 4, 3, 2>(w, b0, b1, p, sc, st);
+  if (pair_dn) return launch_variant<false, 32, 4, 3, 2>(w, b0, b1, p, sc, st);
+  return launch_variant<false, 32, 6, 4, 1>(w, b0, b1, p, sc, st);
 }
 
 }  // namespace moe

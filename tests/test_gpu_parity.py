@@ -65,6 +65,7 @@ SMALL = [
     ("tiny", {"d": 512, "f": 384, "T": 70, "E": 12, "k": 3}),
     ("tiny", {"d": 512, "f": 384, "T": 70, "E": 12, "k": 3, "wdtype": "fp8"}),
     ("tiny", {"T": 100, "E": 8, "k": 2, "wdtype": "fp8"}),   # 64-token FP8 decode tiles
+    ("tiny", {"T": 40, "d": 384, "f": 256, "E": 8, "k": 2, "wdtype": "fp8"}),  # single down tiles
     ("tiny", {"T": 300, "E": 40, "k": 5}),     # several permute chunks, uneven segments
     # FP8 prefill tiles (more than 32 routed slots per expert): paired and single down tiles
     ("tiny", {"T": 600, "E": 8, "k": 2, "wdtype": "fp8"}),
