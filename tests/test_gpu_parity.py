@@ -255,7 +255,26 @@ FULL = ["v3_decode", "v4pro_decode", "skewed_prefill", "sweep_fp8_T1", "sweep_fp
 
 @pytest.mark.parametrize("name", FULL)
 def test_full_size_routing_exact_and_sampled_outputs(name):
-    cfg = synth.get_config(name)
+    check_full(synth.get_config(name), name)
+
+
+# The largest shapes the C ABI accepts along each axis: E = 1024 experts with k = 32 choices,
+# d = 16384 (the longest router and gate/up reductions) and f = 16384 (the longest down one).
+MAXIMUM = [
+    {"T": 33, "d": 1024, "E": 1024, "k": 32, "f": 256},
+    {"T": 5, "d": 16384, "E": 4, "k": 2, "f": 128},
+    {"T": 5, "d": 128, "E": 4, "k": 2, "f": 16384},
+    {"T": 5, "d": 16384, "E": 4, "k": 2, "f": 128, "wdtype": "fp8"},
+    {"T": 5, "d": 128, "E": 4, "k": 2, "f": 16384, "wdtype": "fp8"},
+]
+
+
+@pytest.mark.parametrize("over", MAXIMUM, ids=[str(o) for o in MAXIMUM])
+def test_maximum_shapes(over):
+    check_full(synth.get_config("tiny", **over), "maximum " + str(over))
+
+
+def check_full(cfg, name):
     dev = synth.device_inputs(cfg)
     w = {k: dev[k] for k in ("wg", "bias", "w13", "w2", "s13", "s2")}
     layer = run_layer(cfg, dev["x"], w)
