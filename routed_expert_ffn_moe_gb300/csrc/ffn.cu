@@ -41,9 +41,8 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 // plan[row][e]: exclusive prefix over experts of the work of each kernel; entry E1 = total.
 // With a split, row kPlanSplit holds the number of CTAs for the cold list and for the rest,
 // chosen so that both lists take about the same time by a simple cost model.
-__global__ void __launch_bounds__(1024) k_ffn_plan(const int32_t* __restrict__ offsets,
-                                                   PlanArgs a, int32_t* __restrict__ plan) {
-  pdl_wait_then_release();
+__device__ __forceinline__ void plan_block(const int32_t* __restrict__ offsets, const PlanArgs& a,
+                                           int32_t* __restrict__ plan) {
   __shared__ float red[32];
   const int E1 = a.E + a.n_shared;
   constexpr int R = kPlanTcDnCold + 1;
@@ -98,15 +97,11 @@ __global__ void __launch_bounds__(1024) k_ffn_plan(const int32_t* __restrict__ o
   }
 }
 
-// x_perm[s] = x[perm_token[s]] for every routed slot: the tensor-core path's token tiles are
-// contiguous rows for TMA.
-__global__ void __launch_bounds__(256) k_gather_rows(const uint16_t* __restrict__ x,
-                                                     const int32_t* __restrict__ perm_token,
-                                                     int T, long routed, int d,
-                                                     uint16_t* __restrict__ x_perm, int* status) {
-  pdl_wait_then_release();
+__device__ __forceinline__ void gather_row_chunk(long i, const uint16_t* __restrict__ x,
+                                                 const int32_t* __restrict__ perm_token, int T,
+                                                 long routed, int d,
+                                                 uint16_t* __restrict__ x_perm, int* status) {
   const int d8 = d >> 3;
-  const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= routed * d8) return;
   const long s = i / d8;
   const int c = (int)(i - s * d8);
@@ -117,6 +112,24 @@ __global__ void __launch_bounds__(256) k_gather_rows(const uint16_t* __restrict_
   }
   reinterpret_cast<uint4*>(x_perm + s * d)[c] =
       __ldg(reinterpret_cast<const uint4*>(x + (long)t * d) + c);
+}
+
+// One launch for both: block 0 builds the plan from the expert offsets while the other blocks
+// gather x_perm[s] = x[perm_token[s]] for every routed slot (the tensor-core path's token tiles
+// are contiguous rows for TMA). Neither needs the other.
+__global__ void __launch_bounds__(256) k_plan_gather(const int32_t* __restrict__ offsets,
+                                                     PlanArgs a, int32_t* __restrict__ plan,
+                                                     const uint16_t* __restrict__ x,
+                                                     const int32_t* __restrict__ perm_token, int T,
+                                                     long routed, int d,
+                                                     uint16_t* __restrict__ x_perm, int* status) {
+  pdl_wait_then_release();
+  if (blockIdx.x == 0) {
+    plan_block(offsets, a, plan);
+    return;
+  }
+  gather_row_chunk((long)(blockIdx.x - 1) * blockDim.x + threadIdx.x, x, perm_token, T, routed, d,
+                   x_perm, status);
 }
 
 // Phase events are recorded as external events while the stream is being captured into a CUDA
@@ -243,16 +256,12 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32
   }
 
   const PhaseEvents ev = profile_phase_events();
-  cudaError_t e = launch_pdl(k_ffn_plan, dim3(1), dim3(1024), 0, st, offsets, pa, plan);
+  const long gather_n = (use_tc && routed > 0) ? routed * (s.d / 8) : 0;
+  cudaError_t e = launch_pdl(k_plan_gather, dim3((unsigned)(1 + (gather_n + 255) / 256)),
+                             dim3(256), 0, st, offsets, pa, plan, x, perm_token, s.T, routed, s.d,
+                             a.x_perm, a.status);
   count_launches(1);
   if (e != cudaSuccess) return e;
-  if (use_tc && routed > 0) {
-    const long n = routed * (s.d / 8);
-    e = launch_pdl(k_gather_rows, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, x,
-                   perm_token, s.T, routed, s.d, a.x_perm, a.status);
-    count_launches(1);
-    if (e != cudaSuccess) return e;
-  }
   if (ev.begin) record_phase(ev.begin, st);
 
   // Upper bound on the weight-streaming work: every slot in its own group plus one partial

@@ -150,6 +150,60 @@ __global__ void __launch_bounds__(256) k_perm_scatter(const int32_t* __restrict_
   }
 }
 
+// Small batches (at most kWarpsPerBlock chunks): the three steps above in one block. Warp w
+// builds the masks of chunk w; the (expert, chunk) counts go to shared memory, are scanned there
+// in expert-major order, and the same masks then give every pair its slot. Same result as the
+// three kernels, one launch instead of three.
+__global__ void __launch_bounds__(256) k_perm_small(const int32_t* __restrict__ topk_idx, int T,
+                                                    int E, int k, int nchunk, int n_shared,
+                                                    int32_t* __restrict__ offsets,
+                                                    int32_t* __restrict__ perm_token,
+                                                    int32_t* __restrict__ inv_slot, int* status) {
+  pdl_wait_then_release();
+  extern __shared__ uint32_t sm[];
+  uint32_t* sel_all = sm;                                       // [kWarpsPerBlock][E]
+  int* cnt = reinterpret_cast<int*>(sm + (size_t)kWarpsPerBlock * E);  // [E][nchunk]
+  const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint32_t* sel = sel_all + (size_t)wid * E;
+  build_masks(sel, topk_idx, T, E, k, wid, nchunk, status);
+  if (wid < nchunk)
+    for (int e = lane; e < E; e += 32) cnt[e * nchunk + wid] = __popc(sel[e]);
+  __syncthreads();
+  // exclusive scan of cnt in place, each thread a run of consecutive entries
+  const int n = E * nchunk;
+  const int per = (n + blockDim.x - 1) / blockDim.x;
+  const int i0 = min(n, (int)threadIdx.x * per), i1 = min(n, i0 + per);
+  int sum = 0;
+  for (int i = i0; i < i1; ++i) sum += cnt[i];
+  int total;
+  int run = block_exclusive_scan(sum, &total);
+  for (int i = i0; i < i1; ++i) {
+    const int v = cnt[i];
+    cnt[i] = run;
+    run += v;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) offsets[e] = cnt[e * nchunk];
+  if (threadIdx.x == 0) {
+    offsets[E] = T * k;
+    offsets[E + 1] = T * k + n_shared * T;
+  }
+  const int t = wid * kChunkTokens + lane;
+  if (wid >= nchunk || t >= T) return;
+  const int32_t* row = topk_idx + (size_t)t * k;
+  const uint32_t below = (1u << lane) - 1u;
+  for (int j = 0; j < k; ++j) {
+    if (!valid_choice(row, j, E)) {
+      inv_slot[(size_t)t * k + j] = -1;
+      continue;
+    }
+    const int e = row[j];
+    const int slot = cnt[e * nchunk + wid] + __popc(sel[e] & below);
+    perm_token[slot] = t;
+    inv_slot[(size_t)t * k + j] = slot;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_permute(const moe_shape& s, const int32_t* topk_idx, int32_t* offsets,
@@ -161,6 +215,12 @@ cudaError_t launch_permute(const moe_shape& s, const int32_t* topk_idx, int32_t*
   const int nchunk = L.nchunk;
   const unsigned blocks = (unsigned)((nchunk + kWarpsPerBlock - 1) / kWarpsPerBlock);
   const size_t smem = (size_t)kWarpsPerBlock * s.E * sizeof(uint32_t);
+  const size_t smem_small = smem + (size_t)s.E * nchunk * sizeof(int);
+  if (blocks == 1 && smem_small <= 48 * 1024) {
+    count_launches(1);
+    return launch_pdl(k_perm_small, dim3(1), dim3(32 * kWarpsPerBlock), smem_small, st, topk_idx,
+                      s.T, s.E, s.k, nchunk, s.n_shared, offsets, perm_token, inv_slot, status);
+  }
   if (blocks) {
     cudaError_t e = launch_pdl(k_perm_count, dim3(blocks), dim3(32 * kWarpsPerBlock), smem, st,
                                topk_idx, s.T, s.E, s.k, nchunk, hist, status);
