@@ -236,11 +236,12 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32
   // HBM-bound and the tensor-bound experts overlap instead of taking turns on every SM.
   const bool split = !fp8 && !decode && use_tc && !use_gemv && routed > 0;
   if (split) {
-    // Measured rates on GB300 (one SM): decode tiles stream weights at ~78 GB/s in the gate/up
-    // pass and ~52 GB/s in the down pass (shorter tiles); prefill tiles run ~8 TFLOP/s.
+    // Measured rates on GB300 (one SM, fitted to split sweeps of the skewed prefill layer):
+    // decode tiles stream weights at ~78 GB/s in the gate/up pass and ~52 GB/s in the down pass
+    // (shorter tiles); prefill tiles run ~7.4 TFLOP/s (gate/up) and ~8.2 TFLOP/s (down).
     const double bytes = s.d * (double)s.f * 2.0;       // one bf16 weight matrix of an expert
     const double bw_up = 78e3, bw_dn = 52e3;            // bytes per microsecond
-    const double tc_sm = 8e6;                           // FLOP per microsecond
+    const double tc_up = 7.4e6, tc_dn = 8.2e6;          // FLOP per microsecond
     pa.split = 1;
     pa.nt_c = tc_tile_tokens(true, true);
     pa.cold_max = pa.nt_c;
@@ -251,8 +252,8 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32
     pa.cold_cost[1] = (float)(bytes / bw_dn);
     pa.hot_cost_min[0] = pa.cold_cost[0];
     pa.hot_cost_min[1] = pa.cold_cost[1];
-    pa.hot_cost_tok[0] = (float)(4.0 * s.d * s.f / tc_sm);
-    pa.hot_cost_tok[1] = (float)(2.0 * s.d * s.f / tc_sm);
+    pa.hot_cost_tok[0] = (float)(4.0 * s.d * s.f / tc_up);
+    pa.hot_cost_tok[1] = (float)(2.0 * s.d * s.f / tc_dn);
   }
 
   const PhaseEvents ev = profile_phase_events();
