@@ -32,7 +32,7 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
 
-def parse_args():
+def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=200)
@@ -45,7 +45,7 @@ def parse_args():
     p.add_argument("--e2e-steps", type=int, default=None)
     p.add_argument("--T", type=int, default=None, help="override the token batch (profiling cases)")
     p.add_argument("--E", type=int, default=None, help="override the routed experts (profiling cases)")
-    return p.parse_args()
+    return p.parse_args(argv)
 
 
 def workload_desc(cfg) -> str:
@@ -220,6 +220,23 @@ def run_reference(args, cfg, rank):
 
 
 # ---------------------------------------------------------------------------------------------
+# replicas: every rank times its own layer; the job's time is the slowest rank's
+# ---------------------------------------------------------------------------------------------
+
+def max_over_ranks(values, dist, device):
+    """Element-wise maximum of `values` (floats) over all ranks of the process group."""
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_tokens_per_s(tokens_per_rank: int, world: int, ms: float) -> float:
+    """Whole-job throughput: every rank processes its own batch in (at most) `ms`."""
+    return world * tokens_per_rank / (ms * 1e-3)
+
+
+# ---------------------------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------------------------
 
@@ -324,9 +341,7 @@ def main():
     ms_e2e = e0.elapsed_time(e1) / e2e_steps
 
     if world > 1:
-        t = torch.tensor([ms, ms_e2e], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, ms_e2e = float(t[0]), float(t[1])
+        ms, ms_e2e = max_over_ranks([ms, ms_e2e], dist, "cuda")
 
     # ---- roofline of the dominant kernel (expert gate/up) and of the layer ---------------
     off = layer.expert_offsets.cpu().tolist()
@@ -347,7 +362,7 @@ def main():
     tc_peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_BF16_TFLOPS)) * 1e12
     t_floor = R.roofline_time(layer_flops, layer_bytes, tc_peak, hbm * 1e9)
 
-    value = world * cfg.T / (ms * 1e-3)
+    value = job_tokens_per_s(cfg.T, world, ms)
     out = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
@@ -370,7 +385,7 @@ def main():
                      "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "peak_source": peak_src,
                      "traffic": traffic, "algorithmic_bytes_per_launch": up_bytes},
-        "e2e": {"value": world * cfg.T / (ms_e2e * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": job_tokens_per_s(cfg.T, world, ms_e2e), "unit": "tokens/s",
                 "h2d_bytes_per_step": x.numel() * x.element_size(),
                 "d2h_bytes_per_step": layer.y.numel() * layer.y.element_size()},
         "gpu_launches": prof["kernel_launches"],
