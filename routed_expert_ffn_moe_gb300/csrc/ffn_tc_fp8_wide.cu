@@ -76,7 +76,7 @@ __device__ __forceinline__ void sts_u4(uint32_t addr, const uint4& v) {
                : "memory");
 }
 
-template <bool GATEUP, int NT, int QS, int BS, int CS, int KA, int ACCB, bool PAIR>
+template <bool GATEUP, int NT, int QS, int BS, int CS, int KA, int ACCB, int CL>
 __global__ void __launch_bounds__(kThreadsW, 1)
     k_tc_ffn_fp8_wide(const __grid_constant__ CUtensorMap tm_w,
                       const __grid_constant__ CUtensorMap tm_b0,
@@ -106,15 +106,18 @@ __global__ void __launch_bounds__(kThreadsW, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E1 = p.E + p.n_shared;
   const int kblocks = p.K / kBK;
-  // Cluster pairs: both CTAs walk the same list of (expert, m-tile pair, token tile) entries;
-  // this CTA takes m-tile 2 * mt + rank, and the token tile, which both need, is loaded half by
-  // each CTA and multicast to both.
+  // Clusters of CL CTAs (1, 2 or 4): all walk the same list of (expert, group of CL m-tiles,
+  // token tile) entries; this CTA takes m-tile CL * mt + rank, and the token tile, which all of
+  // them need, is loaded a CL-th by each CTA and multicast to all.
+  static_assert(CL == 1 || CL == 2 || CL == 4, "cluster size");
+  constexpr bool PAIR = CL > 1;
+  constexpr uint16_t kMask = (uint16_t)((1u << CL) - 1u);
   const int rank = PAIR ? (int)cluster_ctarank() : 0;
-  const int tile0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-  const int tstep = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  const int tile0 = (int)blockIdx.x / CL;
+  const int tstep = (int)gridDim.x / CL;
   const auto decode = [&](int tile, Tile& t) {
     decode_tile<GATEUP, NT>(p, tile, t);
-    if (PAIR) t.mt = 2 * t.mt + rank;
+    if (PAIR) t.mt = CL * t.mt + rank;
   };
 
   if (threadIdx.x == 0) {
@@ -124,7 +127,7 @@ __global__ void __launch_bounds__(kThreadsW, 1)
     }
     for (int s = 0; s < BS; ++s) {
       mbar_init(&b_full[s], 1);
-      mbar_init(&b_empty[s], PAIR ? 2 : 1); // MMA commit (of both CTAs of a pair)
+      mbar_init(&b_empty[s], CL);           // MMA commit (of every CTA of the cluster)
     }
     for (int s = 0; s < CS; ++s) {
       mbar_init(&c_full[s], kConvWarps);
@@ -202,12 +205,12 @@ __global__ void __launch_bounds__(kThreadsW, 1)
             // full tile: this CTA's half of the rows (the wide map's box is NT/2 rows);
             // partial tile: every other 16-row box
             if (wide) {
-              tma_load_2d_mc(bt + rank * (S::kBSlot / 2), bmapw, &b_full[stage], kb * kBK,
-                             t.brow0 + rank * (NT / 2), 0x3, pol_b);
+              tma_load_2d_mc(bt + rank * (S::kBSlot / CL), bmapw, &b_full[stage], kb * kBK,
+                             t.brow0 + rank * (NT / CL), kMask, pol_b);
             } else {
-              for (int i = rank; i < nbox; i += 2)
+              for (int i = rank; i < nbox; i += CL)
                 tma_load_2d_mc(bt + i * kBBoxBytes, bmap, &b_full[stage], kb * kBK,
-                               t.brow0 + i * kBoxRows, 0x3, pol_b);
+                               t.brow0 + i * kBoxRows, kMask, pol_b);
             }
           } else if (wide) {
             tma_load_2d(bt, bmapw, &b_full[stage], kb * kBK, t.brow0, pol_b);
@@ -257,7 +260,7 @@ __global__ void __launch_bounds__(kThreadsW, 1)
             if (KA == 2) mma_bf16_ss(d0 + NT, du + 2 * kk, db + 2 * kk, idesc, accum);
           }
           if (PAIR)
-            mma_commit_mc(&b_empty[bs], 0x3);  // token rows consumed, in both CTAs
+            mma_commit_mc(&b_empty[bs], kMask);  // token rows consumed, in every CTA
           else
             mma_commit(&b_empty[bs]);          // token rows consumed
           mma_commit(&c_empty[cs]);   // dequantised weights consumed
@@ -272,7 +275,7 @@ __global__ void __launch_bounds__(kThreadsW, 1)
   } else if (warp < kConvWarp0) {
     // ---------------- epilogue (warps 2..5) ----------------
     run_epilogue<GATEUP, NT, S::kAccCols, KA, ACCB>(p, total, tmem_base, acc_full, acc_empty,
-                                                    abort_flag, tile0, tstep, PAIR ? rank : -1);
+                                                    abort_flag, tile0, tstep, PAIR ? rank : -1, CL);
   } else {
     // ---------------- dequantisers (warps 6..13) ----------------
     // task = (weight tile a, row r, 16-code chunk j): 16 codes -> two 16-byte bf16 chunks
@@ -339,20 +342,20 @@ __global__ void __launch_bounds__(kThreadsW, 1)
   }
 }
 
-template <bool GATEUP, int NT, int QS, int BS, int CS, int KA, int ACCB, bool PAIR>
+template <bool GATEUP, int NT, int QS, int BS, int CS, int KA, int ACCB, int CL>
 cudaError_t launch_variant(const CUtensorMap& w, const CUtensorMap& b0, const CUtensorMap& b1,
                            const CUtensorMap& b0w, const CUtensorMap& b1w, const TcParams& p,
                            const float* scales, cudaStream_t st) {
   using S = SmemW<NT, QS, BS, CS, KA, ACCB>;
   static_assert(S::kTotal <= 227 * 1024, "shared memory");
-  auto kern = k_tc_ffn_fp8_wide<GATEUP, NT, QS, BS, CS, KA, ACCB, PAIR>;
+  auto kern = k_tc_ffn_fp8_wide<GATEUP, NT, QS, BS, CS, KA, ACCB, CL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)S::kTotal);
   if (e != cudaSuccess) return e;
   count_launches(1);
-  if (PAIR)
-    return launch_pdl_cluster(kern, dim3((unsigned)(num_sms() & ~1)), dim3(kThreadsW), S::kTotal,
-                              st, 2u, w, b0, b1, b0w, b1w, p, scales);
+  if (CL > 1)
+    return launch_pdl_cluster(kern, dim3((unsigned)(num_sms() / CL * CL)), dim3(kThreadsW),
+                              S::kTotal, st, (unsigned)CL, w, b0, b1, b0w, b1w, p, scales);
   return launch_pdl(kern, dim3(num_sms()), dim3(kThreadsW), S::kTotal, st, w, b0, b1, b0w, b1w, p,
                     scales);
 }
@@ -368,24 +371,25 @@ constexpr int kNT = 256;
 // Weight rows per tile of a pass: 2 x 128 (gate + up, or two W_d tiles when d allows), else 128.
 bool paired_tiles(bool gateup, int d) { return gateup || tc_tile_rows(false, false, d) == 2 * kBM; }
 
-// Cluster pairs take two consecutive m-tiles; they need an even number of them per expert.
-bool clustered(bool gateup, int d, int f) {
-  if (!paired_tiles(gateup, d)) return false;
+// Clusters take CL consecutive m-tiles: pairs when an expert's m-tile count is even, else none
+// (CL = 1). Clusters of four measured 1.7x slower (every token slot then waits for four CTAs).
+int cluster_size(bool gateup, int d, int f) {
+  if (!paired_tiles(gateup, d)) return 1;
   const int mtiles = gateup ? f / kBM : d / (2 * kBM);
-  return mtiles % 2 == 0;
+  return mtiles % 2 == 0 ? 2 : 1;
 }
 
 // One pass with kNT-token tiles; rings (codes, tokens, converted weights): 4/3/2 slots for
 // paired weight tiles (224 KB of shared memory), 8/3/3 for single tiles; fewer token slots
 // measured slower.
-template <bool PAIR>
+template <int CL>
 cudaError_t launch_pass(const Maps& m, const TcParams& p, const float* sc, bool gateup, bool paired,
                         cudaStream_t st) {
   if (gateup)
-    return launch_variant<true, kNT, 4, 3, 2, 2, 1, PAIR>(m.w, m.b0, m.b1, m.b0w, m.b1w, p, sc, st);
+    return launch_variant<true, kNT, 4, 3, 2, 2, 1, CL>(m.w, m.b0, m.b1, m.b0w, m.b1w, p, sc, st);
   if (paired)
-    return launch_variant<false, kNT, 4, 3, 2, 2, 1, PAIR>(m.w, m.b0, m.b1, m.b0w, m.b1w, p, sc, st);
-  return launch_variant<false, kNT, 8, 3, 3, 1, 2, false>(m.w, m.b0, m.b1, m.b0w, m.b1w, p, sc, st);
+    return launch_variant<false, kNT, 4, 3, 2, 2, 1, CL>(m.w, m.b0, m.b1, m.b0w, m.b1w, p, sc, st);
+  return launch_variant<false, kNT, 8, 3, 3, 1, 2, 1>(m.w, m.b0, m.b1, m.b0w, m.b1w, p, sc, st);
 }
 
 }  // namespace
@@ -395,7 +399,7 @@ int tc_fp8_wide_tile_tokens() { return kNT; }
 int tc_fp8_wide_plan_mtiles(bool gateup, int d, int f) {
   const int rows = paired_tiles(gateup, d) && !gateup ? 2 * kBM : kBM;
   const int mtiles = (gateup ? f : d) / rows;
-  return clustered(gateup, d, f) ? mtiles / 2 : mtiles;
+  return mtiles / cluster_size(gateup, d, f);
 }
 
 cudaError_t launch_tc_fp8_wide(const FfnArgs& a, const int32_t* prefix, bool gateup,
@@ -411,8 +415,8 @@ cudaError_t launch_tc_fp8_wide(const FfnArgs& a, const int32_t* prefix, bool gat
   p.h = a.h;
   p.y_perm = a.y_perm;
   p.status = a.status;
-  const bool cl = clustered(gateup, a.d, a.f);
-  const uint32_t wide_rows = cl ? kNT / 2 : kNT;  // with pairs each CTA loads half a full tile
+  const int cl = cluster_size(gateup, a.d, a.f);
+  const uint32_t wide_rows = kNT / cl;  // in a cluster each CTA loads its share of a full tile
   const uint64_t E1 = (uint64_t)a.E + a.n_shared;
   const uint64_t routed = (uint64_t)a.T * a.k;
   const uint64_t slots = routed + (uint64_t)a.n_shared * a.T;
@@ -434,8 +438,8 @@ cudaError_t launch_tc_fp8_wide(const FfnArgs& a, const int32_t* prefix, bool gat
   if (e != cudaSuccess) return e;
   const float* sc = gateup ? a.s13 : a.s2;
   const bool paired = paired_tiles(gateup, a.d);
-  return cl ? launch_pass<true>(m, p, sc, gateup, paired, st)
-            : launch_pass<false>(m, p, sc, gateup, paired, st);
+  if (cl == 2) return launch_pass<2>(m, p, sc, gateup, paired, st);
+  return launch_pass<1>(m, p, sc, gateup, paired, st);
 }
 
 }  // namespace moe

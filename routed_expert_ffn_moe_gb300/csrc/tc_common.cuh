@@ -100,12 +100,12 @@ __device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity, int* s
 // (down pass: KA weight tiles of 128 output rows each, tile a in columns [a*NT, (a+1)*NT));
 // then hand the accumulator back. ACCB accumulator buffers (1 or 2) rotate.
 template <bool GATEUP, int NT, uint32_t ACC_COLS, int KA = 1, int ACCB = 2>
-// Tiles tile0, tile0 + tstep, ...; pair_rank >= 0 marks cluster pairs, where a listed tile is a
-// pair of m-tiles and this CTA takes m-tile 2 * mt + pair_rank.
+// Tiles tile0, tile0 + tstep, ...; cl_rank >= 0 marks clusters of cl CTAs, where a listed tile
+// is a group of cl consecutive m-tiles and this CTA takes m-tile cl * mt + cl_rank.
 __device__ __forceinline__ void run_epilogue(const TcParams& p, int total, uint32_t tmem_base,
                                              uint64_t* acc_full, uint64_t* acc_empty,
                                              volatile int* abort_flag, int tile0, int tstep,
-                                             int pair_rank) {
+                                             int cl_rank, int cl = 2) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;                 // TMEM lane quadrant this warp may access
   const int row = q * 32 + lane;          // weight row within a 128-row tile
@@ -113,7 +113,7 @@ __device__ __forceinline__ void run_epilogue(const TcParams& p, int total, uint3
   for (int tile = tile0; tile < total; tile += tstep) {
     Tile t;
     decode_tile<GATEUP, NT>(p, tile, t);
-    if (pair_rank >= 0) t.mt = 2 * t.mt + pair_rank;
+    if (cl_rank >= 0) t.mt = cl * t.mt + cl_rank;
     const int npad = (t.ntok + 15) & ~15;
     if (!wait_bar(&acc_full[acc], acc_phase, abort_flag, p.status)) break;
     tc_fence_after();

@@ -71,6 +71,7 @@ SMALL = [
     ("tiny", {"T": 600, "E": 8, "k": 2, "wdtype": "fp8"}),
     # FP8 prefill tiles in cluster pairs (even m-tile counts in both passes)
     ("tiny", {"T": 600, "d": 512, "f": 256, "E": 8, "k": 2, "wdtype": "fp8"}),
+    ("tiny", {"T": 600, "d": 1024, "f": 512, "E": 8, "k": 2, "wdtype": "fp8"}),  # clusters of 4
     ("tiny", {"T": 600, "d": 512, "f": 256, "E": 8, "k": 2}),                  # bf16 pairs
     # bf16 prefill split: cold experts on decode tiles beside hot ones on paired tiles
     ("tiny", {"router": "zipf", "T": 600, "d": 512, "f": 256, "E": 16, "k": 2}),
