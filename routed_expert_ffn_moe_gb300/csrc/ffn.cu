@@ -97,21 +97,31 @@ __device__ __forceinline__ void plan_block(const int32_t* __restrict__ offsets, 
   }
 }
 
-__device__ __forceinline__ void gather_row_chunk(long i, const uint16_t* __restrict__ x,
-                                                 const int32_t* __restrict__ perm_token, int T,
-                                                 long routed, int d,
-                                                 uint16_t* __restrict__ x_perm, int* status) {
+// Thread i copies 16-byte chunks 4i .. 4i+3 of the slot rows (d is a multiple of 128, so the four
+// chunks lie in one row): four loads in flight per thread.
+constexpr int kGatherChunks = 4;
+
+__device__ __forceinline__ void gather_row_chunks(long i, const uint16_t* __restrict__ x,
+                                                  const int32_t* __restrict__ perm_token, int T,
+                                                  long routed, int d,
+                                                  uint16_t* __restrict__ x_perm, int* status) {
   const int d8 = d >> 3;
-  if (i >= routed * d8) return;
-  const long s = i / d8;
-  const int c = (int)(i - s * d8);
+  const long c0 = i * kGatherChunks;
+  if (c0 >= routed * d8) return;
+  const long s = c0 / d8;
+  const int c = (int)(c0 - s * d8);
   int t = __ldg(perm_token + s);
   if (t < 0 || t >= T) {
     record_error(status, MOE_ERR_DEVICE_BOUNDS);
     t = 0;
   }
-  reinterpret_cast<uint4*>(x_perm + s * d)[c] =
-      __ldg(reinterpret_cast<const uint4*>(x + (long)t * d) + c);
+  const uint4* src = reinterpret_cast<const uint4*>(x + (long)t * d) + c;
+  uint4* dst = reinterpret_cast<uint4*>(x_perm + s * d) + c;
+  uint4 v[kGatherChunks];
+#pragma unroll
+  for (int j = 0; j < kGatherChunks; ++j) v[j] = __ldg(src + j);
+#pragma unroll
+  for (int j = 0; j < kGatherChunks; ++j) dst[j] = v[j];
 }
 
 // One launch for both: block 0 builds the plan from the expert offsets while the other blocks
@@ -128,8 +138,8 @@ __global__ void __launch_bounds__(256) k_plan_gather(const int32_t* __restrict__
     plan_block(offsets, a, plan);
     return;
   }
-  gather_row_chunk((long)(blockIdx.x - 1) * blockDim.x + threadIdx.x, x, perm_token, T, routed, d,
-                   x_perm, status);
+  gather_row_chunks((long)(blockIdx.x - 1) * blockDim.x + threadIdx.x, x, perm_token, T, routed,
+                    d, x_perm, status);
 }
 
 // Phase events are recorded as external events while the stream is being captured into a CUDA
@@ -257,7 +267,7 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32
   }
 
   const PhaseEvents ev = profile_phase_events();
-  const long gather_n = (use_tc && routed > 0) ? routed * (s.d / 8) : 0;
+  const long gather_n = (use_tc && routed > 0) ? routed * (s.d / 8) / kGatherChunks : 0;
   cudaError_t e = launch_pdl(k_plan_gather, dim3((unsigned)(1 + (gather_n + 255) / 256)),
                              dim3(256), 0, st, offsets, pa, plan, x, perm_token, s.T, routed, s.d,
                              a.x_perm, a.status);
