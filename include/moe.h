@@ -155,6 +155,24 @@ MOE_API moe_status moe_expert_ffn(const moe_shape* shape, const void* x, const i
 MOE_API moe_status moe_combine(const moe_shape* shape, const float* y_perm, const int32_t* inv_slot,
                        const float* topk_w, void* y, void* ws, size_t ws_bytes, void* stream);
 
+/* The whole layer in one call: moe_route, moe_permute, moe_expert_ffn and moe_combine with the
+ * same arguments and results (every output buffer above is filled), with one difference in
+ * scheduling: the shared expert does not depend on the routing, so its FFN runs on a second,
+ * library-owned stream (one per device, created on the first such call; no device memory is
+ * allocated) while the router, the permutation and the row gather run on `stream` ("CANN
+ * DeepSeek-V4推理优化", 多流并行优化: the shared and the routed experts on parallel streams). The
+ * call joins both before the combine, so it behaves as work enqueued on `stream`. Calls that
+ * overlap on the GPU (different streams, same device) order their shared-expert work through
+ * that one second stream. The overlap is used for prefill-sized batches (more than 32 routed
+ * tokens per expert on average) with n_shared = 1; otherwise the four steps run in order on
+ * `stream`. y_perm [T*k + n_shared*T, d] fp32 and y [T, d] bf16 as in moe_expert_ffn and
+ * moe_combine. */
+MOE_API moe_status moe_forward(const moe_shape* shape, const void* x, const void* wg,
+                               const float* bias, const void* w13, const float* s13,
+                               const void* w2, const float* s2, int32_t* topk_idx, float* topk_w,
+                               int32_t* expert_offsets, int32_t* perm_token, int32_t* inv_slot,
+                               float* y_perm, void* y, void* ws, size_t ws_bytes, void* stream);
+
 /* Reads (and clears) the first device-side error recorded in `ws` since the last check.
  * Synchronises `stream`. Returns MOE_OK, MOE_ERR_DEVICE_BOUNDS or MOE_ERR_DEVICE_TIMEOUT (or
  * MOE_ERR_CUDA if the read itself fails). */

@@ -12,7 +12,7 @@ import os
 
 __all__ = ["MoeError", "MoeShape", "MOE_W_BF16", "MOE_W_FP8_E4M3_B128", "load", "lib_path",
            "moe_workspace_size", "moe_route", "moe_route_noalloc", "moe_permute",
-           "moe_expert_ffn", "moe_combine",
+           "moe_expert_ffn", "moe_combine", "moe_forward",
            "moe_check_device_status", "moe_selftest_bounded_wait", "moe_profile_enable",
            "moe_profile_read",
            "moe_last_error_string", "shape_of", "MoeLayer", "EXPORTED"]
@@ -21,7 +21,8 @@ MOE_W_BF16, MOE_W_FP8_E4M3_B128 = 0, 1
 STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED",
           -3: "MOE_ERR_WORKSPACE", -4: "MOE_ERR_CUDA", -5: "MOE_ERR_DEVICE_TIMEOUT",
           -6: "MOE_ERR_DEVICE_BOUNDS"}
-EXPORTED = ("moe_workspace_size", "moe_route", "moe_route_noalloc", "moe_permute", "moe_expert_ffn", "moe_combine",
+EXPORTED = ("moe_workspace_size", "moe_route", "moe_route_noalloc", "moe_permute", "moe_expert_ffn",
+            "moe_combine", "moe_forward",
             "moe_check_device_status", "moe_selftest_bounded_wait", "moe_profile_enable",
             "moe_profile_read", "moe_last_error_string")
 
@@ -71,6 +72,8 @@ def load():
     L.moe_expert_ffn.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.moe_combine.restype = i32
     L.moe_combine.argtypes = [shp, vp, vp, vp, vp, vp, sz, vp]
+    L.moe_forward.restype = i32
+    L.moe_forward.argtypes = [shp] + [vp] * 15 + [sz, vp]
     L.moe_check_device_status.restype = i32
     L.moe_check_device_status.argtypes = [vp, vp]
     L.moe_selftest_bounded_wait.restype = i32
@@ -166,6 +169,17 @@ def moe_combine(shape, y_perm, inv_slot, topk_w, y, ws, stream=None, ws_bytes=No
            "moe_combine")
 
 
+def moe_forward(shape, x, wg, bias, w13, s13, w2, s2, topk_idx, topk_w, expert_offsets,
+                perm_token, inv_slot, y_perm, y, ws, stream=None, ws_bytes=None):
+    """The four calls in one, with the shared expert's FFN overlapped with the routing."""
+    wp, wb = _ws(ws)
+    _check(load().moe_forward(ctypes.byref(shape), _ptr(x), _ptr(wg), _ptr(bias), _ptr(w13),
+                              _ptr(s13), _ptr(w2), _ptr(s2), _ptr(topk_idx), _ptr(topk_w),
+                              _ptr(expert_offsets), _ptr(perm_token), _ptr(inv_slot),
+                              _ptr(y_perm), _ptr(y), wp, wb if ws_bytes is None else ws_bytes,
+                              _stream(stream)), "moe_forward")
+
+
 def moe_check_device_status(ws, stream=None):
     _check(load().moe_check_device_status(_ptr(ws), _stream(stream)), "moe_check_device_status")
 
@@ -215,6 +229,15 @@ class MoeLayer:
         self.y = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
 
     def forward(self, x, stream=None):
+        """The layer through moe_forward (one call; the shared expert overlaps the routing)."""
+        w = self.w
+        moe_forward(self.shape, x, w["wg"], w.get("bias"), w["w13"], w.get("s13"), w["w2"],
+                    w.get("s2"), self.topk_idx, self.topk_w, self.expert_offsets, self.perm_token,
+                    self.inv_slot, self.y_perm, self.y, self.ws, stream)
+        return self.y
+
+    def forward_steps(self, x, stream=None):
+        """The layer as the four separate calls."""
         w, s = self.w, self.shape
         moe_route(s, x, w["wg"], w.get("bias"), self.topk_idx, self.topk_w, self.ws, stream)
         moe_permute(s, self.topk_idx, self.expert_offsets, self.perm_token, self.inv_slot, self.ws,

@@ -230,6 +230,50 @@ moe_status moe_combine(const moe_shape* shape, const float* y_perm, const int32_
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_combine launch");
 }
 
+moe_status moe_forward(const moe_shape* shape, const void* x, const void* wg, const float* bias,
+                       const void* w13, const float* s13, const void* w2, const float* s2,
+                       int32_t* topk_idx, float* topk_w, int32_t* expert_offsets,
+                       int32_t* perm_token, int32_t* inv_slot, float* y_perm, void* y, void* ws,
+                       size_t ws_bytes, void* stream) {
+  moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (shape->T > 0) {
+    REQUIRE_PTR(x, 16);
+    REQUIRE_PTR(topk_idx, 16);
+    REQUIRE_PTR(topk_w, 16);
+    REQUIRE_PTR(perm_token, 16);
+    REQUIRE_PTR(inv_slot, 16);
+    REQUIRE_PTR(y_perm, 16);
+    REQUIRE_PTR(y, 16);
+  }
+  REQUIRE_PTR(wg, 16);
+  REQUIRE_PTR(expert_offsets, 16);
+  REQUIRE_PTR(w13, 16);
+  REQUIRE_PTR(w2, 16);
+  if (bias && !aligned(bias, 16)) return fail(MOE_ERR_INVALID_ARG, "bias not 16-byte aligned");
+  if (shape->wdtype == MOE_W_FP8_E4M3_B128) {
+    REQUIRE_PTR(s13, 16);
+    REQUIRE_PTR(s2, 16);
+  } else if (s13 || s2) {
+    return fail(MOE_ERR_INVALID_ARG, "s13/s2 must be NULL for bf16 weights");
+  }
+  WsLayout L;
+  if ((st = check_ws(shape, ws, ws_bytes, &L)) != MOE_OK) return st;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  // A layer starts here: clear the device status word.
+  cudaError_t e = cudaMemsetAsync(static_cast<char*>(ws) + L.status, 0, sizeof(int), cs);
+  if (e != cudaSuccess) return cuda_fail(e, "moe_forward status reset");
+  if (shape->T == 0) {  // no token: only the expert offsets are defined
+    e = launch_permute(*shape, topk_idx, expert_offsets, perm_token, inv_slot,
+                       static_cast<char*>(ws), L, cs);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_forward launch");
+  }
+  e = launch_forward(*shape, static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(wg),
+                     bias, w13, s13, w2, s2, topk_idx, topk_w, expert_offsets, perm_token,
+                     inv_slot, y_perm, static_cast<uint16_t*>(y), static_cast<char*>(ws), L, cs);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_forward launch");
+}
+
 moe_status moe_check_device_status(void* ws, void* stream) {
   REQUIRE_PTR(ws, 256);
   int code = 0;

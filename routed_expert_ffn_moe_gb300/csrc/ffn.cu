@@ -164,10 +164,11 @@ int tc_min_tokens() {
 // use (host objects; no device memory). The record/wait sequence of one call is made under a
 // lock so that calls from several host threads do not interleave their event records.
 struct SplitStreams {
-  cudaStream_t aux = nullptr;
-  cudaEvent_t ev[4] = {};
+  cudaStream_t aux = nullptr;   // split prefill: the other tile list
+  cudaStream_t aux2 = nullptr;  // moe_forward: the shared expert
+  cudaEvent_t ev[6] = {};
 };
-std::mutex g_split_mu;
+std::recursive_mutex g_split_mu;
 SplitStreams g_split[64];
 
 cudaError_t split_streams(SplitStreams** out) {
@@ -178,6 +179,7 @@ cudaError_t split_streams(SplitStreams** out) {
   SplitStreams& s = g_split[dev];
   if (!s.aux) {
     if ((e = cudaStreamCreateWithFlags(&s.aux, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    if ((e = cudaStreamCreateWithFlags(&s.aux2, cudaStreamNonBlocking)) != cudaSuccess) return e;
     for (auto& ev : s.ev)
       if ((e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess) return e;
   }
@@ -191,15 +193,54 @@ cudaError_t join(cudaStream_t st, cudaStream_t from, cudaEvent_t ev) {
   return e == cudaSuccess ? cudaStreamWaitEvent(st, ev, 0) : e;
 }
 
+// Tensor-core tile shape of both passes: tokens per tile and plan units (weight tiles, or
+// cluster pairs of them) per expert.
+struct TileShape {
+  int nt_up, nt_dn, mt_up, mt_dn;
+};
+
+TileShape tile_shape(const moe_shape& s, bool fp8, bool decode, long routed) {
+  TileShape t;
+  t.nt_up = fp8 ? tc_fp8_tile_tokens(true, decode, routed, s.E) : tc_tile_tokens(true, decode);
+  t.nt_dn = fp8 ? tc_fp8_tile_tokens(false, decode, routed, s.E) : tc_tile_tokens(false, decode);
+  if (!fp8) {
+    t.mt_up = tc_plan_mtiles(true, decode, s.d, s.f);
+    t.mt_dn = tc_plan_mtiles(false, decode, s.d, s.f);
+  } else if (!decode) {
+    t.mt_up = tc_fp8_wide_plan_mtiles(true, s.d, s.f);
+    t.mt_dn = tc_fp8_wide_plan_mtiles(false, s.d, s.f);
+  } else {
+    t.mt_up = s.f / 128;
+    t.mt_dn = s.d / tc_fp8_decode_down_rows(s.d);
+  }
+  return t;
+}
+
+// The shared expert's own tile lists, for moe_forward: its segment starts at slot T*k and holds
+// the T tokens in order, so the lists depend on the shape alone. rows[0] and rows[1]: prefixes
+// over the E+1 experts for the gate/up and the down pass (zero work for the routed experts);
+// rows[2]: the expert offsets the tile decoder reads (entries E and E+1).
+__global__ void k_shared_plan(int T, int k, int E, TileShape ts, int32_t* __restrict__ rows) {
+  pdl_wait_then_release();
+  const int n = E + 2;
+  for (int e = threadIdx.x; e < n; e += blockDim.x) {
+    const bool last = e == E + 1;
+    rows[e] = last ? (T + ts.nt_up - 1) / ts.nt_up * ts.mt_up : 0;
+    rows[n + e] = last ? (T + ts.nt_dn - 1) / ts.nt_dn * ts.mt_dn : 0;
+    rows[2 * n + e] = e == E ? T * k : last ? T * k + T : 0;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32_t* perm_token,
                               const int32_t* offsets, const void* w13, const float* s13,
                               const void* w2, const float* s2, float* y_perm, char* ws,
-                              const WsLayout& L, cudaStream_t st) {
+                              const WsLayout& L, cudaStream_t st, bool with_shared) {
   if (s.T == 0) return cudaSuccess;
   FfnArgs a{};
-  a.T = s.T; a.d = s.d; a.E = s.E; a.k = s.k; a.f = s.f; a.n_shared = s.n_shared;
+  // without the shared expert (moe_forward runs it on its own stream) the tile lists end at E
+  a.T = s.T; a.d = s.d; a.E = s.E; a.k = s.k; a.f = s.f; a.n_shared = with_shared ? s.n_shared : 0;
   a.wdtype = s.wdtype;
   a.x = x; a.perm_token = perm_token; a.offsets = offsets;
   a.w13 = w13; a.s13 = s13; a.w2 = w2; a.s2 = s2;
@@ -220,24 +261,16 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32
   const bool use_tc = tc_min < INT_MAX;
   const bool use_gemv = tc_min > 1;
   PlanArgs pa{};
-  pa.E = s.E; pa.n_shared = s.n_shared;
+  pa.E = s.E; pa.n_shared = a.n_shared;
   pa.tc_min = tc_min;
   pa.group = gemv_group_tokens();
   pa.items_up = gemv_items_per_group(true, s.d, s.f);
   pa.items_dn = gemv_items_per_group(false, s.d, s.f);
-  pa.nt_up = fp8 ? tc_fp8_tile_tokens(true, decode, routed, s.E) : tc_tile_tokens(true, decode);
-  pa.nt_dn = fp8 ? tc_fp8_tile_tokens(false, decode, routed, s.E) : tc_tile_tokens(false, decode);
-  pa.mt_up = s.f / 128;
-  pa.mt_dn = s.d / tc_tile_rows(false, decode, s.d);
-  if (!fp8) {
-    pa.mt_up = tc_plan_mtiles(true, decode, s.d, s.f);
-    pa.mt_dn = tc_plan_mtiles(false, decode, s.d, s.f);
-  } else if (!decode) {
-    pa.mt_up = tc_fp8_wide_plan_mtiles(true, s.d, s.f);
-    pa.mt_dn = tc_fp8_wide_plan_mtiles(false, s.d, s.f);
-  } else {
-    pa.mt_dn = s.d / tc_fp8_decode_down_rows(s.d);
-  }
+  const TileShape ts = tile_shape(s, fp8, decode, routed);
+  pa.nt_up = ts.nt_up;
+  pa.nt_dn = ts.nt_dn;
+  pa.mt_up = ts.mt_up;
+  pa.mt_dn = ts.mt_dn;
   pa.stride = s.E + 2;
   const int stride = pa.stride;
   // Split prefill (bf16 weights, all experts on the tensor cores): experts with at most one
@@ -291,7 +324,7 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32
     SplitStreams* ss = nullptr;
     if ((e = split_streams(&ss)) != cudaSuccess) return e;
     const int32_t* act = plan + kPlanSplit * stride;
-    std::lock_guard<std::mutex> lk(g_split_mu);
+    std::lock_guard<std::recursive_mutex> lk(g_split_mu);
     cudaStream_t aux = ss->aux;
     if ((e = join(aux, st, ss->ev[0])) != cudaSuccess) return e;
     if ((e = launch_tc(a, plan + kPlanTcUpCold * stride, true, true, st, act)) != cudaSuccess)
@@ -320,6 +353,75 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32
     e = launch_gemv(a, plan + kPlanGemvUp * stride, plan + kPlanGemvDown * stride, false, max_dn, st);
   if (ev.end) record_phase(ev.end, st);
   return e;
+}
+
+// moe_forward: the shared expert's FFN needs neither the routing nor the permutation, so it runs
+// on the second stream from the start of the call while `st` routes, permutes, gathers and runs
+// the routed experts; the combine waits for both. With no shared expert, or with the
+// weight-streaming GEMV in use, the four steps simply run in order.
+cudaError_t launch_forward(const moe_shape& s, const uint16_t* x, const uint16_t* wg,
+                           const float* bias, const void* w13, const float* s13, const void* w2,
+                           const float* s2, int32_t* topk_idx, float* topk_w, int32_t* offsets,
+                           int32_t* perm_token, int32_t* inv_slot, float* y_perm, uint16_t* y,
+                           char* ws, const WsLayout& L, cudaStream_t st) {
+  int* status = reinterpret_cast<int*>(ws + L.status);
+  cudaError_t e;
+  // Prefill-sized batches only: in decode the shared expert's few tiles hold SMs that the routed
+  // experts' persistent tiles then wait for (measured: FP8 T=1 128.6 -> 169.4 us with the
+  // overlap; T=16384 14.41 -> 14.06 ms, skewed prefill 5.33 -> 5.24 ms).
+  const bool prefill = (long)s.T * s.k > 32L * s.E;
+  const bool overlap = s.n_shared == 1 && s.T > 0 && prefill && tc_min_tokens() == 1;
+  if (!overlap) {
+    if ((e = launch_route(s, x, wg, bias, topk_idx, topk_w, ws, L, st)) != cudaSuccess) return e;
+    if ((e = launch_permute(s, topk_idx, offsets, perm_token, inv_slot, ws, L, st)) != cudaSuccess)
+      return e;
+    if ((e = launch_expert_ffn(s, x, perm_token, offsets, w13, s13, w2, s2, y_perm, ws, L, st)) !=
+        cudaSuccess)
+      return e;
+    return launch_combine(s, y_perm, inv_slot, topk_w, y, status, st);
+  }
+  SplitStreams* ss = nullptr;
+  if ((e = split_streams(&ss)) != cudaSuccess) return e;
+  std::lock_guard<std::recursive_mutex> lk(g_split_mu);
+  cudaStream_t aux = ss->aux2;
+  if ((e = join(aux, st, ss->ev[4])) != cudaSuccess) return e;
+
+  // shared expert on `aux`: its tile lists, then gate/up and down
+  const bool fp8 = s.wdtype == MOE_W_FP8_E4M3_B128;
+  const long routed = (long)s.T * s.k;
+  const bool decode = routed <= 32L * s.E;
+  const TileShape ts = tile_shape(s, fp8, decode, routed);
+  int32_t* rows = reinterpret_cast<int32_t*>(ws + L.shared);
+  const int n = s.E + 2;
+  if ((e = launch_pdl(k_shared_plan, dim3(1), dim3(256), 0, aux, s.T, s.k, s.E, ts, rows)) !=
+      cudaSuccess)
+    return e;
+  count_launches(1);
+  FfnArgs a{};
+  a.T = s.T; a.d = s.d; a.E = s.E; a.k = s.k; a.f = s.f; a.n_shared = 1; a.wdtype = s.wdtype;
+  a.x = x; a.perm_token = perm_token; a.offsets = rows + 2 * n;
+  a.w13 = w13; a.s13 = s13; a.w2 = w2; a.s2 = s2;
+  a.h = reinterpret_cast<uint16_t*>(ws + L.h);
+  a.x_perm = reinterpret_cast<uint16_t*>(ws + L.x_perm);
+  a.y_perm = y_perm;
+  a.status = status;
+  for (int pass = 0; pass < 2; ++pass) {
+    const bool gateup = pass == 0;
+    e = fp8 ? launch_tc_fp8(a, rows + pass * n, gateup, decode, aux)
+            : launch_tc(a, rows + pass * n, gateup, decode, aux);
+    if (e != cudaSuccess) return e;
+  }
+  if ((e = cudaEventRecord(ss->ev[5], aux)) != cudaSuccess) return e;
+
+  // routed experts on `st`
+  if ((e = launch_route(s, x, wg, bias, topk_idx, topk_w, ws, L, st)) != cudaSuccess) return e;
+  if ((e = launch_permute(s, topk_idx, offsets, perm_token, inv_slot, ws, L, st)) != cudaSuccess)
+    return e;
+  if ((e = launch_expert_ffn(s, x, perm_token, offsets, w13, s13, w2, s2, y_perm, ws, L, st,
+                             false)) != cudaSuccess)
+    return e;
+  if ((e = cudaStreamWaitEvent(st, ss->ev[5], 0)) != cudaSuccess) return e;
+  return launch_combine(s, y_perm, inv_slot, topk_w, y, status, st);
 }
 
 }  // namespace moe

@@ -18,11 +18,12 @@ namespace moe {
 //   plan     i32 [kPlanRows, E+2] per-expert work prefixes of the FFN kernels + counters
 //   x_perm   bf16 [T*k, d]        token rows gathered in slot order (tensor-core path input)
 //   h        bf16 [T*k + S*T, f]  SiLU(gate) * up for every slot
+//   shared   i32 [3, E+2]         moe_forward: the shared expert's own tile lists and offsets
 constexpr int kChunkTokens = 32;
 constexpr int kPlanRows = 8;
 
 struct WsLayout {
-  size_t status, logits, hist, base, plan, x_perm, h, total;
+  size_t status, logits, hist, base, plan, x_perm, h, shared, total;
   int nchunk;
 };
 
@@ -41,6 +42,7 @@ inline WsLayout ws_layout(const moe_shape& s) {
   L.plan = take((size_t)kPlanRows * (E + 2) * 4 + 256);
   L.x_perm = take(T * k * (size_t)s.d * 2);
   L.h = take((T * k + (size_t)s.n_shared * T) * (size_t)s.f * 2);
+  L.shared = take(3 * (E + 2) * 4);
   L.total = off;
   return L;
 }
@@ -62,7 +64,13 @@ cudaError_t launch_permute(const moe_shape& s, const int32_t* topk_idx, int32_t*
 cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32_t* perm_token,
                               const int32_t* offsets, const void* w13, const float* s13,
                               const void* w2, const float* s2, float* y_perm, char* ws,
-                              const WsLayout& L, cudaStream_t st);
+                              const WsLayout& L, cudaStream_t st, bool with_shared = true);
+// the whole layer, the shared expert's FFN on a second stream (ffn.cu)
+cudaError_t launch_forward(const moe_shape& s, const uint16_t* x, const uint16_t* wg,
+                           const float* bias, const void* w13, const float* s13, const void* w2,
+                           const float* s2, int32_t* topk_idx, float* topk_w, int32_t* offsets,
+                           int32_t* perm_token, int32_t* inv_slot, float* y_perm, uint16_t* y,
+                           char* ws, const WsLayout& L, cudaStream_t st);
 cudaError_t launch_combine(const moe_shape& s, const float* y_perm, const int32_t* inv_slot,
                            const float* topk_w, uint16_t* y, int* status, cudaStream_t st);
 

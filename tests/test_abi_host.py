@@ -93,6 +93,16 @@ def test_bad_arguments_rejected_before_launch(lib):
     assert rc == -1 and "shape is NULL" in msg
     rc, msg = call("moe_check_device_status", F + 64, None)
     assert rc == -1
+    # moe_forward: x, wg, bias, w13, s13, w2, s2, topk_idx, topk_w, offsets, perm, inv, y_perm, y
+    fwd = [F, F, None, F, None, F, None, F, F, F, F, F, F, F]
+    bad = list(fwd); bad[13] = None
+    rc, msg = call("moe_forward", sp, *bad, F, wsz, None)
+    assert rc == -1 and "y is NULL" in msg
+    bad = list(fwd); bad[4] = F
+    rc, msg = call("moe_forward", sp, *bad, F, wsz, None)
+    assert rc == -1 and "must be NULL" in msg
+    rc, msg = call("moe_forward", sp, *fwd, F, wsz - 1, None)
+    assert rc == -3 and "workspace" in msg
     rc, msg = call("moe_selftest_bounded_wait", F, 0, None)
     assert rc == -1 and "limit_us" in msg
     rc, msg = call("moe_selftest_bounded_wait", F, 2_000_001, None)

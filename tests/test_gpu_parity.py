@@ -179,6 +179,28 @@ def test_combine_direct():
     assert np.all(np.abs(got - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-5)
 
 
+@pytest.mark.parametrize("over", [{}, {"wdtype": "fp8"},
+                                  {"router": "zipf", "T": 600, "d": 512, "f": 256, "E": 16, "k": 2},
+                                  {"T": 600, "d": 512, "f": 256, "E": 8, "k": 2, "wdtype": "fp8"},
+                                  {"n_shared": 0}])
+def test_forward_equals_the_four_calls(over):
+    # moe_forward runs the shared expert on its own stream: every output must be bit-identical
+    # to the four separate calls.
+    cfg = synth.get_config("tiny", **over)
+    inp = synth.host_inputs(cfg)
+    w = device_weights(cfg, inp)
+    x = bf16_dev(inp.x)
+    one = moe.MoeLayer(cfg.T, cfg.d, cfg.E, cfg.k, cfg.f, cfg.n_shared, cfg.wdtype, w)
+    four = moe.MoeLayer(cfg.T, cfg.d, cfg.E, cfg.k, cfg.f, cfg.n_shared, cfg.wdtype, w)
+    one.forward(x)
+    four.forward_steps(x)
+    torch().cuda.synchronize()
+    moe.moe_check_device_status(one.ws)
+    for name in ("topk_idx", "topk_w", "expert_offsets", "perm_token", "inv_slot", "y_perm", "y"):
+        a, b = getattr(one, name), getattr(four, name)
+        assert torch().equal(a, b), name
+
+
 def test_layer_is_deterministic():
     cfg = synth.get_config("tiny", T=200, E=16, k=4, d=512, f=256)
     inp = synth.host_inputs(cfg)
