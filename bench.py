@@ -284,7 +284,7 @@ def main():
             dist.barrier()
         torch.cuda.synchronize()
 
-    # One step = one layer pass. By default the four calls are captured once into a CUDA graph
+    # One step = one layer pass (one moe_forward call). By default it is captured once into a CUDA graph
     # (the library enqueues no synchronisation or allocation) and the graph is replayed; the
     # library's phase events are captured with it and re-recorded by every replay.
     graph = None
