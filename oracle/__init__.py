@@ -20,7 +20,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "moe_oracle.c")
 _LIB = os.path.join(_HERE, "libmoe_oracle.so")
 
-WD = {"bf16": 0, "fp8": 1}
+WD = {"bf16": 0, "fp8": 1, "mxfp4": 2}
 
 
 def build(force: bool = False) -> str:
@@ -47,6 +47,10 @@ def lib():
         L.oracle_bf16_value.argtypes = [ctypes.c_uint16]
         L.oracle_e4m3_value.restype = ctypes.c_double
         L.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+        L.oracle_e2m1_value.restype = ctypes.c_double
+        L.oracle_e2m1_value.argtypes = [ctypes.c_uint8]
+        L.oracle_e8m0_value.restype = ctypes.c_double
+        L.oracle_e8m0_value.argtypes = [ctypes.c_uint8]
         L.oracle_router_logits.argtypes = [vp, vp, vp, i32, i32, i32, vp]
         L.oracle_route.argtypes = [vp, i32, i32, i32, vp, vp, vp]
         L.oracle_permute.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp]
@@ -80,6 +84,19 @@ def bf16_value(h: int) -> float:
 
 def e4m3_value(q: int) -> float:
     return lib().oracle_e4m3_value(int(q))
+
+
+def e2m1_value(code: int) -> float:
+    return lib().oracle_e2m1_value(int(code))
+
+
+def e8m0_value(e: int) -> float:
+    return lib().oracle_e8m0_value(int(e))
+
+
+def _scales(s, wdtype):
+    """Scales as the C side reads them: fp32 for FP8, E8M0 bytes for MXFP4."""
+    return _c(s, np.uint8 if wdtype == "mxfp4" else np.float32)
 
 
 def bf16_to_f64(a: np.ndarray) -> np.ndarray:
@@ -127,13 +144,16 @@ def permute(topk_idx, E, n_shared=1):
 # ---- a3 + a4 -------------------------------------------------------------------------------
 
 def matvec(w, x, wdtype="bf16", s=None, row0=0, nrows=None):
-    """y[r] = sum_c W[row0 + r][c] x[c] in fp64, W row-major bf16 bits or E4M3 codes."""
+    """y[r] = sum_c W[row0 + r][c] x[c] in fp64, W row-major bf16 bits, E4M3 codes, or MXFP4
+    code pairs ([rows, cols/2] bytes)."""
     w = _c(w, np.uint16 if wdtype == "bf16" else np.uint8)
     x = _c(x, np.float64)
     rows, cols = w.shape
+    if wdtype == "mxfp4":
+        cols *= 2
     nrows = rows - row0 if nrows is None else nrows
     y = np.empty(nrows, np.float64)
-    lib().oracle_matvec(WD[wdtype], _p(w), _p(_c(s, np.float32)), cols, row0, nrows, _p(x), _p(y))
+    lib().oracle_matvec(WD[wdtype], _p(w), _p(_scales(s, wdtype)), cols, row0, nrows, _p(x), _p(y))
     return y
 
 
@@ -144,11 +164,12 @@ def expert_rows(xrows, w13, w2, wdtype="bf16", s13=None, s2=None, want_h=False):
     wt = np.uint16 if wdtype == "bf16" else np.uint8
     w13, w2 = _c(w13, wt), _c(w2, wt)
     f = w13.shape[0] // 2
-    assert w13.shape == (2 * f, d) and w2.shape == (d, f)
+    per_byte = 2 if wdtype == "mxfp4" else 1
+    assert w13.shape == (2 * f, d // per_byte) and w2.shape == (d, f // per_byte)
     y = np.empty((n, d), np.float64)
     h = np.empty((n, f), np.float64) if want_h else None
-    lib().oracle_expert_rows(_p(xrows), n, d, f, WD[wdtype], _p(w13), _p(_c(s13, np.float32)),
-                             _p(w2), _p(_c(s2, np.float32)), _p(y), _p(h))
+    lib().oracle_expert_rows(_p(xrows), n, d, f, WD[wdtype], _p(w13), _p(_scales(s13, wdtype)),
+                             _p(w2), _p(_scales(s2, wdtype)), _p(y), _p(h))
     return (y, h) if want_h else y
 
 
@@ -171,9 +192,9 @@ def moe_layer(cfg, inputs):
     ex = inputs.experts
     w13 = np.ascontiguousarray(np.stack([e.w13 for e in ex]))
     w2 = np.ascontiguousarray(np.stack([e.w2 for e in ex]))
-    fp8 = cfg.wdtype == "fp8"
-    s13 = np.ascontiguousarray(np.stack([e.s13 for e in ex])) if fp8 else None
-    s2 = np.ascontiguousarray(np.stack([e.s2 for e in ex])) if fp8 else None
+    scaled = cfg.wdtype in ("fp8", "mxfp4")
+    s13 = _scales(np.stack([e.s13 for e in ex]), cfg.wdtype) if scaled else None
+    s2 = _scales(np.stack([e.s2 for e in ex]), cfg.wdtype) if scaled else None
     slots = T * k + S * T
     out = dict(logits=np.empty((T, E), np.float32), topk_idx=np.empty((T, k), np.int32),
                topk_w=np.empty((T, k), np.float32), topk_w64=np.empty((T, k), np.float64),

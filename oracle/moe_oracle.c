@@ -30,6 +30,12 @@
  *   - slots: expert-major, ascending token within an expert; the shared expert's segment
  *     follows the routed ones, in token order; shared weight 1; no routed scaling factor.
  *   - FP8 E4M3 expert weights with one fp32 scale per 128x128 block: weight = code value * s.
+ *   - FP4 expert weights ("DeepSeek-V4-Pro on NVIDIA H200", 0.1.3: V4-Pro's MoE experts are
+ *     stored in FP4; "CANN DeepSeek-V4推理优化", 量化策略: the MoE module quantised to MXFP4)
+ *     in the MXFP4 format of the OCP Microscaling Formats spec v1.0: E2M1 elements, one E8M0
+ *     scale per 32 consecutive elements of a row; weight = element value * 2^(e - 127). The
+ *     pages name the format but not its byte layout: two codes per byte, element 2j in the low
+ *     nibble; scales row-major [rows, cols/32].
  *
  * Parity of this file is pinned by tests against the pages' worked example, closed forms,
  * library-routine reductions, brute force and invariants; see tests/test_oracle_*.py.
@@ -41,6 +47,7 @@
 
 #define WD_BF16 0
 #define WD_FP8 1
+#define WD_MXFP4 2
 
 /* ---- number formats ----------------------------------------------------------------------- */
 
@@ -65,13 +72,31 @@ double oracle_e4m3_value(uint8_t q) {
   return s ? -v : v;
 }
 
-/* Weight w[r][c] of a row-major [rows, cols] matrix stored as bf16, or as E4M3 codes with fp32
- * scales s[r/128][c/128]. */
-static double weight(int wdtype, const void* w, const float* s, int64_t cols, int64_t r,
+/* OCP MX FP4 E2M1: sign (bit 3), 2 exponent bits (bias 1), 1 mantissa bit; exponent field 0 is
+ * subnormal (m * 0.5); no infinities or NaN. Magnitudes: 0, 0.5, 1, 1.5, 2, 3, 4, 6. */
+double oracle_e2m1_value(uint8_t code) {
+  int s = (code >> 3) & 1, E = (code >> 1) & 3, m = code & 1;
+  double v = E == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, E - 1);
+  return s ? -v : v;
+}
+
+/* OCP MX E8M0 shared scale: 2^(e - 127); 0xFF is NaN. */
+double oracle_e8m0_value(uint8_t e) { return e == 0xFF ? NAN : ldexp(1.0, (int)e - 127); }
+
+/* Weight w[r][c] of a row-major [rows, cols] matrix stored as bf16; as E4M3 codes with fp32
+ * scales s[r/128][c/128]; or as MXFP4 code pairs w[r][c/2] (element c in the low nibble when c
+ * is even) with E8M0 scales s[r][c/32]. */
+static double weight(int wdtype, const void* w, const void* s, int64_t cols, int64_t r,
                      int64_t c) {
   if (wdtype == WD_BF16) return oracle_bf16_value(((const uint16_t*)w)[r * cols + c]);
+  if (wdtype == WD_MXFP4) {
+    const uint8_t pair = ((const uint8_t*)w)[r * (cols / 2) + c / 2];
+    const uint8_t code = (uint8_t)((c & 1) ? pair >> 4 : pair & 15);
+    return oracle_e2m1_value(code) *
+           oracle_e8m0_value(((const uint8_t*)s)[r * (cols / 32) + c / 32]);
+  }
   return oracle_e4m3_value(((const uint8_t*)w)[r * cols + c]) *
-         (double)s[(r / 128) * (cols / 128) + (c / 128)];
+         (double)((const float*)s)[(r / 128) * (cols / 128) + (c / 128)];
 }
 
 /* ---- a1: router ---------------------------------------------------------------------------- */
@@ -175,7 +200,7 @@ void oracle_permute(const int32_t* topk_idx, int T, int E, int k, int n_shared, 
 /* y[r] = sum_c W[row0 + r][c] * x[c] for r < nrows, over a row-major weight with `cols`
  * columns, in fp64 (the matrix-vector product that each of the gate, up and down projections
  * is). */
-void oracle_matvec(int wdtype, const void* w, const float* s, int64_t cols, int64_t row0,
+void oracle_matvec(int wdtype, const void* w, const void* s, int64_t cols, int64_t row0,
                    int64_t nrows, const double* x, double* y) {
 #pragma omp parallel for schedule(static)
   for (int64_t r = 0; r < nrows; ++r) {
@@ -189,7 +214,7 @@ void oracle_matvec(int wdtype, const void* w, const float* s, int64_t cols, int6
  *   G = x W_g^T, U = x W_u^T (w13 rows 0..f-1 are gate, f..2f-1 are up), h = SiLU(G) * U with
  *   SiLU(z) = z / (1 + e^-z), y = h W_d^T (w2 is [d, f]).  y [n, d] fp64; h_out [n, f] nullable. */
 void oracle_expert_rows(const uint16_t* xrows, int n, int d, int f, int wdtype, const void* w13,
-                        const float* s13, const void* w2, const float* s2, double* y,
+                        const void* s13, const void* w2, const void* s2, double* y,
                         double* h_out) {
   for (int i = 0; i < n; ++i) {
     double* xv = (double*)malloc(sizeof(double) * (size_t)d);
@@ -235,12 +260,15 @@ void oracle_combine(const double* y_perm, const int32_t* inv_slot, const double*
  * [E+2], perm_token [T*k], inv_slot [T*k], y_perm [T*k + n_shared*T, d] and y [T, d] (fp64). */
 void oracle_moe_layer(int T, int d, int E, int k, int f, int n_shared, int wdtype,
                       const uint16_t* x, const uint16_t* wg, const float* bias, const void* w13,
-                      const float* s13, const void* w2, const float* s2, float* logits,
+                      const void* s13, const void* w2, const void* s2, float* logits,
                       int32_t* topk_idx, float* topk_w, double* topk_w64, int32_t* offsets,
                       int32_t* perm_token, int32_t* inv_slot, double* y_perm, double* y) {
-  const int64_t wb = wdtype == WD_BF16 ? 2 : 1;
   const int64_t n13 = 2LL * f * d, n2 = (int64_t)d * f;
-  const int64_t ns13 = n13 / (128 * 128), ns2 = n2 / (128 * 128);
+  /* bytes of one expert's weights and scales in the stacked arrays */
+  const int64_t b13 = wdtype == WD_BF16 ? 2 * n13 : wdtype == WD_FP8 ? n13 : n13 / 2;
+  const int64_t b2 = wdtype == WD_BF16 ? 2 * n2 : wdtype == WD_FP8 ? n2 : n2 / 2;
+  const int64_t bs13 = wdtype == WD_FP8 ? 4 * (n13 / (128 * 128)) : n13 / 32;
+  const int64_t bs2 = wdtype == WD_FP8 ? 4 * (n2 / (128 * 128)) : n2 / 32;
   const int64_t slots = (int64_t)T * k + (int64_t)n_shared * T;
   uint16_t* xrow = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)d);
   oracle_router_logits(x, wg, bias, T, d, E, logits);
@@ -257,9 +285,9 @@ void oracle_moe_layer(int T, int d, int E, int k, int f, int n_shared, int wdtyp
       t = (int)(slot - (int64_t)T * k);
     }
     memcpy(xrow, x + (int64_t)t * d, sizeof(uint16_t) * (size_t)d);
-    oracle_expert_rows(xrow, 1, d, f, wdtype, (const char*)w13 + e * n13 * wb,
-                       s13 ? s13 + e * ns13 : NULL, (const char*)w2 + e * n2 * wb,
-                       s2 ? s2 + e * ns2 : NULL, y_perm + slot * d, NULL);
+    oracle_expert_rows(xrow, 1, d, f, wdtype, (const char*)w13 + e * b13,
+                       s13 ? (const char*)s13 + e * bs13 : NULL, (const char*)w2 + e * b2,
+                       s2 ? (const char*)s2 + e * bs2 : NULL, y_perm + slot * d, NULL);
   }
   oracle_combine(y_perm, inv_slot, topk_w64, T, k, d, n_shared, y);
   free(xrow);

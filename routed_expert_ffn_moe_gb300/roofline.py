@@ -36,16 +36,21 @@ def expected_active_u(E: int, k: int, B: int) -> float:
     return E * (1.0 - (1.0 - 1.0 / E) ** (k * B))
 
 
-def weight_bytes_per_element(wdtype: str) -> int:
-    return 2 if wdtype == "bf16" else 1
+def matrix_bytes(rows: int, cols: int, wdtype: str) -> int:
+    """HBM bytes of one [rows, cols] weight matrix with its scales: bf16 (2 bytes an element);
+    E4M3 (1 byte) plus one fp32 scale per 128x128 block; MXFP4 (half a byte) plus one E8M0
+    byte per 32 elements."""
+    n = rows * cols
+    if wdtype == "bf16":
+        return 2 * n
+    if wdtype == "fp8":
+        return n + 4 * (rows // 128) * (cols // 128)
+    return n // 2 + n // 32
 
 
 def expert_bytes(d: int, f: int, wdtype: str) -> int:
-    """HBM bytes of one expert's weights, plus its fp32 128x128 block scales when FP8."""
-    b = expert_params(d, f) * weight_bytes_per_element(wdtype)
-    if wdtype == "fp8":
-        b += 4 * (2 * f // 128) * (d // 128) + 4 * (d // 128) * (f // 128)
-    return b
+    """HBM bytes of one expert's weights (gate, up, down) with their scales."""
+    return matrix_bytes(2 * f, d, wdtype) + matrix_bytes(d, f, wdtype)
 
 
 def layer_bytes(T: int, d: int, E: int, f: int, n_shared: int, wdtype: str,
@@ -70,17 +75,11 @@ def roofline_time(flops: float, bytes_: float, peak_flops: float, peak_bw: float
 def gate_up_bytes(d: int, f: int, wdtype: str, n_experts_run: int) -> int:
     """Algorithmic bytes of the gate/up phase: the gate and up weights (+ scales) of every expert
     that runs (routed experts hit + shared)."""
-    b = 2 * f * d * weight_bytes_per_element(wdtype)
-    if wdtype == "fp8":
-        b += 4 * (2 * f // 128) * (d // 128)
-    return n_experts_run * b
+    return n_experts_run * matrix_bytes(2 * f, d, wdtype)
 
 
 def down_bytes(d: int, f: int, wdtype: str, n_experts_run: int) -> int:
-    b = d * f * weight_bytes_per_element(wdtype)
-    if wdtype == "fp8":
-        b += 4 * (d // 128) * (f // 128)
-    return n_experts_run * b
+    return n_experts_run * matrix_bytes(d, f, wdtype)
 
 
 def mib(x: float) -> float:

@@ -62,6 +62,12 @@ def lib():
         L.synth_double_to_bf16_host.argtypes = [vp, vp, i64]
         L.synth_f32_to_e4m3_host.restype = None
         L.synth_f32_to_e4m3_host.argtypes = [vp, vp, i64]
+        L.synth_quant_mxfp4_host.restype = None
+        L.synth_quant_mxfp4_host.argtypes = [vp, vp, vp, i64, i64]
+        L.synth_quant_mxfp4_device.restype = ctypes.c_int
+        L.synth_quant_mxfp4_device.argtypes = [vp, vp, vp, i64, i64, vp]
+        L.synth_f32_to_e2m1_host.restype = None
+        L.synth_f32_to_e2m1_host.argtypes = [vp, vp, i64]
         _lib = L
     return _lib
 
@@ -106,6 +112,27 @@ def quantize_e4m3(w_bf16: np.ndarray):
     q = np.empty((rows, cols), dtype=np.uint8)
     s = np.empty((rows // 128, cols // 128), dtype=np.float32)
     lib().synth_quant_e4m3_host(_ptr(w), _ptr(q), _ptr(s), rows, cols)
+    return q, s
+
+
+def f32_to_e2m1(v: np.ndarray) -> np.ndarray:
+    """fp32 values -> E2M1 codes (one per uint8), round to nearest even, saturating to +-6."""
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    out = np.empty(v.shape, dtype=np.uint8)
+    lib().synth_f32_to_e2m1_host(_ptr(v), _ptr(out), v.size)
+    return out
+
+
+def quantize_mxfp4(w_bf16: np.ndarray):
+    """MXFP4-quantise a row-major [rows, cols] bf16 matrix (uint16 bits): E2M1 code pairs
+    [rows, cols/2] (element 2j in the low nibble) and E8M0 scales [rows, cols/32], one per 32
+    consecutive elements of a row."""
+    w = np.ascontiguousarray(w_bf16, dtype=np.uint16)
+    rows, cols = w.shape
+    assert cols % 32 == 0
+    q = np.empty((rows, cols // 2), dtype=np.uint8)
+    s = np.empty((rows, cols // 32), dtype=np.uint8)
+    lib().synth_quant_mxfp4_host(_ptr(w), _ptr(q), _ptr(s), rows, cols)
     return q, s
 
 
@@ -168,7 +195,8 @@ def host_w2_expert(cfg: MoeConfig, e: int) -> np.ndarray:
 
 @dataclass
 class ExpertWeights:
-    """One expert's weights as stored on the device: bf16 bits, or E4M3 codes + fp32 scales."""
+    """One expert's weights as stored on the device: bf16 bits, E4M3 codes + fp32 scales, or
+    E2M1 code pairs + E8M0 scales."""
     w13: np.ndarray
     w2: np.ndarray
     s13: np.ndarray | None = None
@@ -179,6 +207,10 @@ def host_expert(cfg: MoeConfig, e: int) -> ExpertWeights:
     w13, w2 = host_w13_expert(cfg, e), host_w2_expert(cfg, e)
     if cfg.wdtype == "bf16":
         return ExpertWeights(w13, w2)
+    if cfg.wdtype == "mxfp4":
+        q13, s13 = quantize_mxfp4(w13)
+        q2, s2 = quantize_mxfp4(w2)
+        return ExpertWeights(q13, q2, s13, s2)
     q13, s13 = quantize_e4m3(w13)
     q2, s2 = quantize_e4m3(w2)
     return ExpertWeights(q13, q2, s13, s2)
@@ -215,7 +247,9 @@ def _dev_normal(t, seed, stream, sigma, offset=0):
 def device_inputs(cfg: MoeConfig, device="cuda"):
     """Draw every input of a config directly into HBM. Returns a dict of torch tensors:
     x [T,d] bf16, wg [E,d] bf16, bias [E] f32 or None, w13 [E+S,2f,d], w2 [E+S,d,f] (bf16, or
-    uint8 E4M3 codes), s13 [E+S,2f/128,d/128], s2 [E+S,d/128,f/128] f32 or None."""
+    uint8 E4M3 codes), s13 [E+S,2f/128,d/128], s2 [E+S,d/128,f/128] f32 or None; for MXFP4,
+    w13 [E+S,2f,d/2] and w2 [E+S,d,f/2] uint8 code pairs with s13 [E+S,2f,d/32] and
+    s2 [E+S,d,f/32] uint8 E8M0 scales."""
     import torch
     n_exp = cfg.E + cfg.n_shared
     x = _dev_normal(torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16, device=device),
@@ -232,16 +266,22 @@ def device_inputs(cfg: MoeConfig, device="cuda"):
                                     cfg.seed, stream, SIGMA_W)
             out["s" + name[1:]] = None
             continue
-        q = torch.empty(*shape, dtype=torch.uint8, device=device)
-        s = torch.empty(shape[0], shape[1] // 128, shape[2] // 128, dtype=torch.float32, device=device)
+        fp4 = cfg.wdtype == "mxfp4"
+        if fp4:
+            q = torch.empty(shape[0], shape[1], shape[2] // 2, dtype=torch.uint8, device=device)
+            s = torch.empty(shape[0], shape[1], shape[2] // 32, dtype=torch.uint8, device=device)
+        else:
+            q = torch.empty(*shape, dtype=torch.uint8, device=device)
+            s = torch.empty(shape[0], shape[1] // 128, shape[2] // 128, dtype=torch.float32,
+                            device=device)
+        quant = lib().synth_quant_mxfp4_device if fp4 else lib().synth_quant_e4m3_device
         # quantise one expert at a time so the bf16 staging buffer stays small
         stage = torch.empty(shape[1], shape[2], dtype=torch.bfloat16, device=device)
         per = shape[1] * shape[2]
         cs = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
         for e in range(n_exp):
             _dev_normal(stage, cfg.seed, stream, SIGMA_W, offset=e * per)
-            rc = lib().synth_quant_e4m3_device(stage.data_ptr(), q[e].data_ptr(), s[e].data_ptr(),
-                                               shape[1], shape[2], cs)
+            rc = quant(stage.data_ptr(), q[e].data_ptr(), s[e].data_ptr(), shape[1], shape[2], cs)
             if rc:
                 raise RuntimeError(f"synth device quantiser failed: cuda error {rc}")
         del stage
@@ -251,5 +291,5 @@ def device_inputs(cfg: MoeConfig, device="cuda"):
 
 
 __all__ = ["CONFIGS", "MoeConfig", "get_config", "sweep_config", "build", "normal_bf16",
-           "quantize_e4m3", "zipf_bias", "host_inputs", "host_expert", "host_x", "host_wg",
+           "quantize_e4m3", "quantize_mxfp4", "f32_to_e2m1", "zipf_bias", "host_inputs", "host_expert", "host_x", "host_wg",
            "host_bias", "device_inputs", "ExpertWeights", "HostInputs"]

@@ -19,7 +19,8 @@ class MoeConfig:
     k: int          # routed experts chosen per token
     f: int          # expert intermediate size
     n_shared: int   # always-on shared experts (0 or 1)
-    wdtype: str     # "bf16" or "fp8" (E4M3 with fp32 scales per 128x128 block)
+    wdtype: str     # "bf16", "fp8" (E4M3 with fp32 scales per 128x128 block) or "mxfp4"
+                    # (E2M1 with E8M0 scales per 32 consecutive elements of a row)
     router: str     # "uniform" (plain logits) or "zipf" (logits + Zipf popularity bias)
     seed: int = 0
 
@@ -40,6 +41,10 @@ CONFIGS = {
                            wdtype="bf16", router="uniform"),
     "v4pro_decode": MoeConfig("v4pro_decode", T=32, d=7168, E=384, k=6, f=3072, n_shared=1,
                               wdtype="fp8", router="uniform"),
+    # V4-Pro's routed experts in FP4, the format its public description gives them
+    # ("DeepSeek-V4-Pro on NVIDIA H200", 0.1.3; "CANN DeepSeek-V4推理优化", 量化策略: MXFP4)
+    "v4pro_decode_fp4": MoeConfig("v4pro_decode_fp4", T=32, d=7168, E=384, k=6, f=3072,
+                                  n_shared=1, wdtype="mxfp4", router="uniform"),
     "skewed_prefill": MoeConfig("skewed_prefill", T=4096, d=7168, E=256, k=8, f=2048,
                                 n_shared=1, wdtype="bf16", router="zipf"),
 }
@@ -53,9 +58,17 @@ def sweep_config(T: int) -> MoeConfig:
                      wdtype="fp8", router="uniform")
 
 
+def sweep_fp4_config(T: int) -> MoeConfig:
+    """V3 shape with MXFP4 expert weights and a plain router, at token batch T."""
+    return MoeConfig(f"sweep_fp4_T{T}", T=T, d=7168, E=256, k=8, f=2048, n_shared=1,
+                     wdtype="mxfp4", router="uniform")
+
+
 def get_config(name: str, **overrides) -> MoeConfig:
     if name.startswith("sweep_fp8_T"):
         cfg = sweep_config(int(name[len("sweep_fp8_T"):]))
+    elif name.startswith("sweep_fp4_T"):
+        cfg = sweep_fp4_config(int(name[len("sweep_fp4_T"):]))
     else:
         cfg = CONFIGS[name]
     return replace(cfg, **overrides) if overrides else cfg

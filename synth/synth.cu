@@ -17,6 +17,10 @@
 //   * FP8 E4M3 (OCP 8-bit floating point spec, bias 7, max 448, no infinities): per 128x128
 //     block of a row-major [rows, cols] matrix, s = amax/448 (s = 1 if amax = 0),
 //     q = round-to-nearest-even(w / s) saturated to +-448.
+//   * MXFP4 (OCP Microscaling Formats v1.0: E2M1 elements, one E8M0 scale per block of 32):
+//     per 32 consecutive elements of a row, X = 2^(floor(log2 amax) - 2) (2 = the largest
+//     E2M1 exponent; X = 1 if amax = 0), q = E2M1 round-to-nearest-even(w / X) saturated to
+//     +-6; two codes per byte, element 2j in the low nibble; the scale byte is log2(X) + 127.
 #include <cstdint>
 #include <cstring>
 #include <cuda_runtime.h>
@@ -107,6 +111,52 @@ SYN_HD uint8_t f32_to_e4m3(float v) {
   return (uint8_t)(sign | keep);  // keep == 8 becomes the smallest normal
 }
 
+// fp32 -> E2M1 (sign bit 3, exponent bits 2..1 with bias 1, mantissa bit 0; magnitudes 0, 0.5,
+// 1, 1.5, 2, 3, 4, 6), round to nearest with ties to the even code, saturating to +-6.
+SYN_HD uint8_t f32_to_e2m1(float v) {
+  const uint8_t sign = (uint8_t)((fbits(v) >> 28) & 0x8u);
+  const float a = v < 0.f ? -v : v;
+  uint8_t m;
+  if (a <= 0.25f) m = 0;
+  else if (a < 0.75f) m = 1;
+  else if (a <= 1.25f) m = 2;
+  else if (a < 1.75f) m = 3;
+  else if (a <= 2.5f) m = 4;
+  else if (a < 3.5f) m = 5;
+  else if (a <= 5.0f) m = 6;
+  else m = 7;  // above 5, and NaN (which the generator never draws)
+  return (uint8_t)(sign | m);
+}
+
+// One block of 32 bf16 weights -> 16 bytes of E2M1 codes and its E8M0 scale byte.
+SYN_HD void mxfp4_block(const uint16_t* w, uint8_t* q, uint8_t* s) {
+  float amax = 0.f;
+  for (int i = 0; i < 32; ++i) {
+    const float a = bf16_to_f32((uint16_t)(w[i] & 0x7FFFu));
+    amax = a > amax ? a : amax;
+  }
+  int e = 127;
+  if (amax > 0.f) {
+    e = (int)((fbits(amax) >> 23) & 0xFFu) - 2;  // floor(log2 amax) - 2, biased by 127
+    if (e < 0) e = 0;
+  }
+  uint32_t xb = e >= 1 ? (uint32_t)e << 23 : 0x00400000u;  // X = 2^(e - 127) as fp32
+  float X;
+  memcpy(&X, &xb, 4);
+  for (int i = 0; i < 16; ++i) {
+    const uint8_t lo = f32_to_e2m1(bf16_to_f32(w[2 * i]) / X);
+    const uint8_t hi = f32_to_e2m1(bf16_to_f32(w[2 * i + 1]) / X);
+    q[i] = (uint8_t)(lo | (hi << 4));
+  }
+  *s = (uint8_t)e;
+}
+
+__global__ void quant_mxfp4_kernel(const uint16_t* w, uint8_t* q, uint8_t* s, int64_t nblk) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < nblk; b += stride)
+    mxfp4_block(w + b * 32, q + b * 16, s + b);
+}
+
 __global__ void normal_bf16_kernel(uint16_t* out, uint64_t n, uint64_t key, double sigma,
                                    uint64_t offset) {
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
@@ -192,6 +242,30 @@ int synth_quant_e4m3_device(const uint16_t* w, uint8_t* q, float* s, int64_t row
   if (nblk > 0x7FFFFFFF) return 1;
   quant_e4m3_kernel<<<(unsigned)nblk, 256, 0, (cudaStream_t)stream>>>(w, q, s, rows, cols);
   return (int)cudaGetLastError();
+}
+
+// Row-major [rows, cols] bf16 -> q [rows, cols/2] E2M1 code pairs and s [rows, cols/32] E8M0.
+// The blocks of a row are consecutive, so block b covers elements 32b .. 32b+31 of the matrix.
+void synth_quant_mxfp4_host(const uint16_t* w, uint8_t* q, uint8_t* s, int64_t rows,
+                            int64_t cols) {
+  const int64_t nblk = rows * (cols / 32);
+#pragma omp parallel for schedule(static)
+  for (int64_t b = 0; b < nblk; ++b) mxfp4_block(w + b * 32, q + b * 16, s + b);
+}
+
+int synth_quant_mxfp4_device(const uint16_t* w, uint8_t* q, uint8_t* s, int64_t rows,
+                             int64_t cols, void* stream) {
+  if (cols % 32) return 1;
+  const int64_t nblk = rows * (cols / 32);
+  if (nblk == 0) return 0;
+  int64_t blocks = (nblk + 255) / 256;
+  if (blocks > 65536) blocks = 65536;
+  quant_mxfp4_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(w, q, s, nblk);
+  return (int)cudaGetLastError();
+}
+
+void synth_f32_to_e2m1_host(const float* v, uint8_t* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = f32_to_e2m1(v[i]);
 }
 
 void synth_double_to_bf16_host(const double* v, uint16_t* out, int64_t n) {

@@ -76,6 +76,68 @@ def test_e4m3_decode_roundtrips_through_the_independent_encoder():
     assert np.all(np.diff(vals[(codes < 0x80)]) > 0)  # positive codes are strictly increasing
 
 
+def test_mxfp4_element_and_scale_decode_golden_codes():
+    for row in golden_rows("mxfp4_codes.txt"):
+        kind, code, val = row.split()
+        v = (oracle.e2m1_value if kind == "e2m1" else oracle.e8m0_value)(int(code, 16))
+        if val == "nan":
+            assert math.isnan(v)
+        else:
+            assert v == float(val) and math.copysign(1.0, v) == math.copysign(1.0, float(val))
+
+
+def mxfp4_reference_quantise(w: np.ndarray):
+    """The OCP MX quantisation of fp64 weights [rows, cols], restated in numpy: per 32
+    consecutive elements of a row, X = 2^(floor(log2 amax) - 2), element = the nearest of the
+    E2M1 magnitudes to |w|/X (ties to the one with mantissa bit 0), saturating at 6. Returns
+    the dequantised fp64 weights."""
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    rows, cols = w.shape
+    b = w.reshape(rows, cols // 32, 32)
+    amax = np.abs(b).max(axis=2, keepdims=True)
+    with np.errstate(divide="ignore"):
+        X = np.where(amax > 0, 2.0 ** (np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - 2), 1.0)
+    a = np.abs(b) / X
+    dist = np.abs(a[..., None] - grid)
+    best = dist.min(axis=-1, keepdims=True)
+    cand = np.isclose(dist, best, rtol=0, atol=0)
+    # among equally near magnitudes take the even code (index 0, 2, 4, 6)
+    even = cand & (np.arange(8) % 2 == 0)
+    pick = np.where(even.any(-1), even.argmax(-1), cand.argmax(-1))
+    return (np.sign(b) * grid[pick] * X).reshape(rows, cols)
+
+
+def test_mxfp4_quantise_then_decode_matches_numpy_restatement():
+    rng = np.random.default_rng(5)
+    w = rand_bf16(rng, (64, 256), sigma=0.02)
+    # a zero block, a block with a tie at every grid midpoint, and a saturating block
+    w[0, :32] = 0
+    w[1, :32] = bf16_bits(np.resize([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 4.0], 32))
+    w[2, :32] = bf16_bits(np.resize([7.5, -7.5, 4.0, 1.0], 32))
+    q, s = synth.quantize_mxfp4(w)
+    deq = np.array([[oracle.matvec(q, np.eye(256)[c], "mxfp4", s, row0=r, nrows=1)[0]
+                     for c in range(256)] for r in range(4)])
+    ref = mxfp4_reference_quantise(oracle.bf16_to_f64(w))
+    np.testing.assert_array_equal(deq, ref[:4])
+    # the rest through the layer's own matvec: W x with x = all ones is each row's sum
+    np.testing.assert_allclose(oracle.matvec(q, np.ones(256), "mxfp4", s), ref.sum(1),
+                               rtol=1e-14, atol=1e-14)
+
+
+def test_mxfp4_scales_index_by_row_and_32_column_block_and_low_nibble_first():
+    # every element code 0x2 (1.0) except element 1 of each row (code 0x4, 2.0): byte 0 is 0x42
+    rows, cols = 4, 96
+    q = np.full((rows, cols // 2), 0x22, np.uint8)
+    q[:, 0] = 0x42
+    s = (127 + np.arange(rows * 3).reshape(rows, 3)).astype(np.uint8)  # 2^(3r + j)
+    for c in (0, 1, 40, 95):
+        x = np.zeros(cols)
+        x[c] = 1.0
+        elem = 2.0 if c == 1 else 1.0
+        expect = [elem * 2.0 ** (3 * r + c // 32) for r in range(rows)]
+        np.testing.assert_array_equal(oracle.matvec(q, x, "mxfp4", s), expect)
+
+
 def test_bf16_decode():
     assert oracle.bf16_value(0x3F80) == 1.0
     assert oracle.bf16_value(0xC000) == -2.0
@@ -258,6 +320,7 @@ def test_single_expert_layer_is_a_dense_swiglu_ffn():
 
 
 @pytest.mark.parametrize("name,over", [("tiny", {}), ("tiny", {"wdtype": "fp8"}),
+                                       ("tiny", {"wdtype": "mxfp4"}),
                                        ("tiny", {"n_shared": 0, "k": 3}),
                                        ("tiny", {"router": "zipf", "T": 21})])
 def test_layer_equals_dense_masked_evaluation(name, over):
@@ -272,6 +335,13 @@ def test_layer_equals_dense_masked_evaluation(name, over):
             return oracle.bf16_to_f64(getattr(ew, which))
         q = getattr(ew, which)
         s = getattr(ew, "s" + which[1:])
+        if cfg.wdtype == "mxfp4":
+            # the E2M1 magnitudes by the format's formula, both nibbles, times 2^(e-127)
+            codes = np.stack([q & 15, q >> 4], axis=-1).reshape(q.shape[0], -1)
+            mag = np.where((codes >> 1) & 3 == 0, 0.5 * (codes & 1),
+                           2.0 ** (((codes >> 1) & 3).astype(int) - 1) * (1 + 0.5 * (codes & 1)))
+            X_ = np.repeat(2.0 ** (s.astype(int) - 127), 32, axis=1)
+            return np.where(codes & 8, -1.0, 1.0) * mag * X_
         vals = np.array([oracle.e4m3_value(c) for c in range(256)])[q]
         return vals * np.kron(s.astype(np.float64), np.ones((128, 128)))
 

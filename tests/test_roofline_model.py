@@ -77,3 +77,16 @@ def test_layer_flops_formula():
     assert R.layer_flops(T, d, E, k, ff, 1) == 2 * T * 9 * 3 * d * ff + 2 * T * d * E
     assert R.layer_flops(T, d, E, k, ff, 1) / 1e12 == pytest.approx(0.204, abs=0.001)
     assert not math.isnan(R.layer_bytes(T, d, E, ff, 1, "bf16", 255.9))
+
+
+def test_fp4_expert_is_the_pages_33_mb_plus_its_scales():
+    # "DeepSeek-V4-Pro on NVIDIA H200", 0.1.2 and 3.2: a routed expert of 3 x 7168 x 3072 =
+    # 66.06M parameters takes about 33 MB in FP4; MXFP4 adds one scale byte per 32 elements
+    d, ff = 7168, 3072
+    params = R.expert_params(d, ff)
+    assert params / 1e6 == pytest.approx(66.06, abs=0.01)
+    elem = params // 2
+    assert elem / 1e6 == pytest.approx(33.03, abs=0.01)
+    assert R.expert_bytes(d, ff, "mxfp4") == elem + params // 32
+    assert (R.gate_up_bytes(d, ff, "mxfp4", 2) + R.down_bytes(d, ff, "mxfp4", 2)
+            == 2 * R.expert_bytes(d, ff, "mxfp4"))

@@ -88,3 +88,31 @@ def test_configs():
     assert (c.T, c.E, c.k, c.f, c.wdtype) == (32, 384, 6, 3072, "fp8")
     with pytest.raises(KeyError):
         synth.get_config("nope")
+
+
+def test_f32_to_e2m1_rounding_ties_and_saturation():
+    v = np.array([0.0, 0.24, 0.25, 0.26, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 5.01, 6.0, 100.0,
+                  -0.75, -5.01], np.float32)
+    # magnitude codes 0..7 are 0, 0.5, 1, 1.5, 2, 3, 4, 6; ties go to the even code
+    expect = [0, 0, 0, 1, 2, 2, 4, 4, 6, 6, 7, 7, 7, 0x8 | 2, 0x8 | 7]
+    np.testing.assert_array_equal(synth.f32_to_e2m1(v), expect)
+
+
+def test_mxfp4_quantiser_scale_rule_and_layout():
+    rng = np.random.default_rng(3)
+    w = synth.double_to_bf16(rng.normal(0.0, 0.02, size=(8, 128)))
+    q, s = synth.quantize_mxfp4(w)
+    assert q.shape == (8, 64) and s.shape == (8, 4)
+    f = (w.astype(np.uint32) << 16).view(np.float32).astype(np.float64).reshape(8, 4, 32)
+    amax = np.abs(f).max(2)
+    np.testing.assert_array_equal(s, np.floor(np.log2(amax)).astype(int) - 2 + 127)
+    # element 2j in the low nibble: decode both nibbles by the E2M1 formula and rebuild
+    mag = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    codes = np.stack([q & 15, q >> 4], axis=-1).reshape(8, 128)
+    vals = np.where(codes & 8, -1.0, 1.0) * mag[codes & 7]
+    X = np.repeat(2.0 ** (s.astype(int) - 127), 32, axis=1)
+    err = np.abs(vals * X - f.reshape(8, 128))
+    # within half a step of E2M1 at the element's magnitude (steps 0.5, 1, 2 by binade), or a
+    # saturation at 6 of a value below 8
+    half_step = np.where(np.abs(f.reshape(8, 128)) / X < 2, 0.25, np.where(np.abs(f.reshape(8, 128)) / X < 4, 0.5, 1.0)) * X
+    assert np.all((err <= half_step) | (np.abs(vals) == 6.0))
