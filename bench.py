@@ -49,7 +49,8 @@ def parse_args(argv=None):
 
 
 def workload_desc(cfg) -> str:
-    w = "bf16 weights" if cfg.wdtype == "bf16" else "FP8 E4M3 weights with fp32 128x128 block scales"
+    w = {"bf16": "bf16 weights", "fp8": "FP8 E4M3 weights with fp32 128x128 block scales",
+         "mxfp4": "MXFP4 weights (E2M1 codes, one E8M0 scale per 32 elements)"}[cfg.wdtype]
     r = "Zipf(s=1.1) popularity bias" if cfg.router == "zipf" else "plain router"
     return (f"{cfg.name}: T={cfg.T} tokens, d={cfg.d}, {cfg.E} routed + {cfg.n_shared} shared "
             f"experts, top-{cfg.k}, expert intermediate f={cfg.f}, SwiGLU, {w}, bf16 activations, "
@@ -384,10 +385,11 @@ def main():
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if cfg.wdtype == "bf16" else "fp8_e4m3 weights, bf16 activations",
+        "dtype": {"bf16": "bf16", "fp8": "fp8_e4m3 weights, bf16 activations",
+                  "mxfp4": "mxfp4 (e2m1 + e8m0) weights, bf16 activations as two e4m3 terms"}[cfg.wdtype],
         "data": "synthetic",
         "config": {"workload": workload_desc(cfg), "T": cfg.T, "parallelism": f"replicas x{world}",
-                   "launch": "eager" if graph is None else "CUDA graph replay of the four calls",
+                   "launch": "eager" if graph is None else "CUDA graph replay of one moe_forward call",
                    "l2": "inputs larger than L2 (expert weights "
                          f"{(cfg.E + cfg.n_shared) * R.expert_bytes(cfg.d, cfg.f, cfg.wdtype) / 1e9:.1f} GB), no flush",
                    "experts_hit": n_hit,

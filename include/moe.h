@@ -25,8 +25,10 @@
  *   - Device-side checks (an index out of range, a duplicated expert in a token's top-k row, a
  *     bounded wait that gave up) never fault: the kernel skips the bad access and records the
  *     first error code in the workspace; moe_check_device_status() reports it.
- *   - Tensors are dense row-major; "bf16" is IEEE-style bfloat16, "E4M3" is OCP FP8 E4M3.
- *   - Every pointer must be 16-byte aligned (256-byte for ws).
+ *   - Tensors are dense row-major; "bf16" is IEEE-style bfloat16, "E4M3" is OCP FP8 E4M3;
+ *     "MXFP4" is the OCP Microscaling (MX) v1.0 FP4 format: E2M1 elements with one E8M0 scale
+ *     per 32 consecutive elements of a row.
+ *   - Every pointer must be 16-byte aligned (256-byte for ws; 32-byte for MXFP4 w13 and w2).
  *   - Shapes: 1 <= E <= 1024, 1 <= k <= min(E, 32), n_shared in {0, 1}, d and f multiples of
  *     128 with 128 <= d <= 16384 and 128 <= f <= 16384, 0 <= T and T*(k+1) <= 2^30.
  *   - Not thread-safe per workspace: calls that share a workspace must be ordered on one stream.
@@ -59,7 +61,8 @@ typedef enum {
 
 typedef enum {
   MOE_W_BF16 = 0,            /* expert weights bf16                                          */
-  MOE_W_FP8_E4M3_B128 = 1    /* expert weights E4M3 with one fp32 scale per 128x128 block    */
+  MOE_W_FP8_E4M3_B128 = 1,   /* expert weights E4M3 with one fp32 scale per 128x128 block    */
+  MOE_W_MXFP4_E8M0_B32 = 2   /* expert weights MXFP4: E2M1 codes, one E8M0 scale per 32      */
 } moe_wdtype;
 
 typedef struct {
@@ -130,21 +133,31 @@ MOE_API moe_status moe_permute(const moe_shape* shape, const int32_t* topk_idx, 
  *   w13            [E+n_shared, 2f, d]: rows 0..f-1 of expert e are its gate projection, rows
  *                  f..2f-1 its up projection (one row per output feature, d contiguous).
  *   w2             [E+n_shared, d, f]: the down projection (one row per output feature).
- *                  bf16, or E4M3 codes (one byte each) for MOE_W_FP8_E4M3_B128.
- *   s13, s2        fp32 block scales [E+n_shared, 2f/128, d/128] and [E+n_shared, d/128, f/128]
- *                  for E4M3 weights (weight = code value * scale of its 128x128 block); NULL
- *                  for bf16.
+ *                  bf16; E4M3 codes (one byte each) for MOE_W_FP8_E4M3_B128; or, for
+ *                  MOE_W_MXFP4_E8M0_B32, E2M1 codes two per byte ([E+n_shared, 2f, d/2] and
+ *                  [E+n_shared, d, f/2] bytes; element 2j of a row in the low nibble of byte j,
+ *                  element 2j+1 in the high nibble), 32-byte aligned.
+ *   s13, s2        E4M3 weights: fp32 block scales [E+n_shared, 2f/128, d/128] and
+ *                  [E+n_shared, d/128, f/128] (weight = code value * scale of its 128x128
+ *                  block). MXFP4 weights: E8M0 bytes [E+n_shared, 2f, d/32] and
+ *                  [E+n_shared, d, f/32], one per 32 consecutive elements of a row (weight =
+ *                  element value * 2^(scale - 127); "DeepSeek-V4-Pro on NVIDIA H200", 0.1.3:
+ *                  FP4 expert weights; "CANN DeepSeek-V4推理优化", 量化策略: MXFP4). NULL for
+ *                  bf16.
  *   y_perm         [T*k + n_shared*T, d] fp32 out: row s = expert output for slot s, i.e.
  *                  W_d^T (SiLU(W_g^T x) * (W_u^T x)) for the slot's token and expert.
- * The intermediate h = SiLU(G) * U is kept in bf16; accumulation is fp32.
+ * The intermediate h = SiLU(G) * U is kept in bf16; accumulation is fp32. With MXFP4 weights
+ * the tensor cores multiply the E2M1 codes as stored, so the activations (x, then h) enter the
+ * products as two E4M3 terms with their own E8M0 scales per 32 elements, within 2^-8 of each
+ * 32-element block's largest magnitude (about one bf16 rounding of that element).
  * Prefill-sized batches with bf16 weights (more than 32 routed tokens per expert on average)
  * run the experts with few tokens and those with many on two streams at once: `stream` and a
  * second stream the library creates on its first such call on each device (a host-side object;
  * no device memory is allocated), ordered against `stream` with events inside the call, so the
  * call still behaves as work enqueued on `stream` (also under CUDA-graph capture). */
 MOE_API moe_status moe_expert_ffn(const moe_shape* shape, const void* x, const int32_t* perm_token,
-                          const int32_t* expert_offsets, const void* w13, const float* s13,
-                          const void* w2, const float* s2, float* y_perm, void* ws,
+                          const int32_t* expert_offsets, const void* w13, const void* s13,
+                          const void* w2, const void* s2, float* y_perm, void* ws,
                           size_t ws_bytes, void* stream);
 
 /* Combine ("第 6 章 超節點", 6.2.6 and 6.4.1: send back, restore token order, sum with the
@@ -168,8 +181,8 @@ MOE_API moe_status moe_combine(const moe_shape* shape, const float* y_perm, cons
  * `stream`. y_perm [T*k + n_shared*T, d] fp32 and y [T, d] bf16 as in moe_expert_ffn and
  * moe_combine. */
 MOE_API moe_status moe_forward(const moe_shape* shape, const void* x, const void* wg,
-                               const float* bias, const void* w13, const float* s13,
-                               const void* w2, const float* s2, int32_t* topk_idx, float* topk_w,
+                               const float* bias, const void* w13, const void* s13,
+                               const void* w2, const void* s2, int32_t* topk_idx, float* topk_w,
                                int32_t* expert_offsets, int32_t* perm_token, int32_t* inv_slot,
                                float* y_perm, void* y, void* ws, size_t ws_bytes, void* stream);
 

@@ -10,14 +10,16 @@ from __future__ import annotations
 import ctypes
 import os
 
-__all__ = ["MoeError", "MoeShape", "MOE_W_BF16", "MOE_W_FP8_E4M3_B128", "load", "lib_path",
+__all__ = ["MoeError", "MoeShape", "MOE_W_BF16", "MOE_W_FP8_E4M3_B128", "MOE_W_MXFP4_E8M0_B32",
+           "load", "lib_path",
            "moe_workspace_size", "moe_route", "moe_route_noalloc", "moe_permute",
            "moe_expert_ffn", "moe_combine", "moe_forward",
            "moe_check_device_status", "moe_selftest_bounded_wait", "moe_profile_enable",
            "moe_profile_read",
            "moe_last_error_string", "shape_of", "MoeLayer", "EXPORTED"]
 
-MOE_W_BF16, MOE_W_FP8_E4M3_B128 = 0, 1
+MOE_W_BF16, MOE_W_FP8_E4M3_B128, MOE_W_MXFP4_E8M0_B32 = 0, 1, 2
+WDTYPES = {"bf16": MOE_W_BF16, "fp8": MOE_W_FP8_E4M3_B128, "mxfp4": MOE_W_MXFP4_E8M0_B32}
 STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED",
           -3: "MOE_ERR_WORKSPACE", -4: "MOE_ERR_CUDA", -5: "MOE_ERR_DEVICE_TIMEOUT",
           -6: "MOE_ERR_DEVICE_BOUNDS"}
@@ -114,7 +116,7 @@ def _check(rc: int, where: str):
 
 def shape_of(T, d, E, k, f, n_shared=1, wdtype=MOE_W_BF16) -> MoeShape:
     if isinstance(wdtype, str):
-        wdtype = MOE_W_BF16 if wdtype == "bf16" else MOE_W_FP8_E4M3_B128
+        wdtype = WDTYPES[wdtype]
     return MoeShape(T, d, E, k, f, n_shared, wdtype)
 
 
@@ -207,8 +209,8 @@ def moe_profile_read() -> dict:
 class MoeLayer:
     """The four calls chained on one stream with buffers allocated once (torch, on `device`).
 
-    weights: dict with wg [E,d] bf16, bias [E] f32 or None, w13, w2 (bf16 or uint8 E4M3 codes),
-    s13, s2 (fp32 block scales or None). `forward(x)` returns y [T,d] bf16; intermediate tensors
+    weights: dict with wg [E,d] bf16, bias [E] f32 or None, w13, w2 (bf16, uint8 E4M3 codes or
+    uint8 MXFP4 code pairs), s13, s2 (fp32 block scales, uint8 E8M0 scales, or None). `forward(x)` returns y [T,d] bf16; intermediate tensors
     stay available as attributes (topk_idx, topk_w, expert_offsets, perm_token, inv_slot, y_perm).
     """
 

@@ -41,7 +41,8 @@ moe_status check_shape(const moe_shape* s) {
     return fail(MOE_ERR_INVALID_ARG, "f=%d not a multiple of 128 in [128, 16384]", s->f);
   if (s->T < 0 || (long long)s->T * (s->k + 1) > (1LL << 30))
     return fail(MOE_ERR_INVALID_ARG, "T=%d out of range (need 0 <= T, T*(k+1) <= 2^30)", s->T);
-  if (s->wdtype != MOE_W_BF16 && s->wdtype != MOE_W_FP8_E4M3_B128)
+  if (s->wdtype != MOE_W_BF16 && s->wdtype != MOE_W_FP8_E4M3_B128 &&
+      s->wdtype != MOE_W_MXFP4_E8M0_B32)
     return fail(MOE_ERR_INVALID_ARG, "wdtype=%d unknown", s->wdtype);
   return MOE_OK;
 }
@@ -52,6 +53,22 @@ moe_status check_shape(const moe_shape* s) {
     if (!aligned((p), (align)))                                                         \
       return fail(MOE_ERR_INVALID_ARG, "%s not %d-byte aligned", #p, (int)(align));     \
   } while (0)
+
+// Expert weights and their scales: bf16 has none; E4M3 and MXFP4 need both. MXFP4 code arrays
+// are read through tensor maps that want 32-byte aligned bases.
+moe_status check_weights(const moe_shape* s, const void* w13, const void* s13, const void* w2,
+                         const void* s2) {
+  const size_t wa = s->wdtype == MOE_W_MXFP4_E8M0_B32 ? 32 : 16;
+  REQUIRE_PTR(w13, wa);
+  REQUIRE_PTR(w2, wa);
+  if (s->wdtype == MOE_W_BF16) {
+    if (s13 || s2) return fail(MOE_ERR_INVALID_ARG, "s13/s2 must be NULL for bf16 weights");
+    return MOE_OK;
+  }
+  REQUIRE_PTR(s13, 16);
+  REQUIRE_PTR(s2, 16);
+  return MOE_OK;
+}
 
 moe_status check_ws(const moe_shape* s, const void* ws, size_t ws_bytes, WsLayout* L) {
   REQUIRE_PTR(ws, 256);
@@ -185,8 +202,8 @@ moe_status moe_permute(const moe_shape* shape, const int32_t* topk_idx, int32_t*
 }
 
 moe_status moe_expert_ffn(const moe_shape* shape, const void* x, const int32_t* perm_token,
-                          const int32_t* expert_offsets, const void* w13, const float* s13,
-                          const void* w2, const float* s2, float* y_perm, void* ws,
+                          const int32_t* expert_offsets, const void* w13, const void* s13,
+                          const void* w2, const void* s2, float* y_perm, void* ws,
                           size_t ws_bytes, void* stream) {
   moe_status st = check_shape(shape);
   if (st != MOE_OK) return st;
@@ -196,14 +213,7 @@ moe_status moe_expert_ffn(const moe_shape* shape, const void* x, const int32_t* 
     REQUIRE_PTR(y_perm, 16);
   }
   REQUIRE_PTR(expert_offsets, 16);
-  REQUIRE_PTR(w13, 16);
-  REQUIRE_PTR(w2, 16);
-  if (shape->wdtype == MOE_W_FP8_E4M3_B128) {
-    REQUIRE_PTR(s13, 16);
-    REQUIRE_PTR(s2, 16);
-  } else if (s13 || s2) {
-    return fail(MOE_ERR_INVALID_ARG, "s13/s2 must be NULL for bf16 weights");
-  }
+  if ((st = check_weights(shape, w13, s13, w2, s2)) != MOE_OK) return st;
   WsLayout L;
   if ((st = check_ws(shape, ws, ws_bytes, &L)) != MOE_OK) return st;
   cudaError_t e = launch_expert_ffn(*shape, static_cast<const uint16_t*>(x), perm_token,
@@ -231,7 +241,7 @@ moe_status moe_combine(const moe_shape* shape, const float* y_perm, const int32_
 }
 
 moe_status moe_forward(const moe_shape* shape, const void* x, const void* wg, const float* bias,
-                       const void* w13, const float* s13, const void* w2, const float* s2,
+                       const void* w13, const void* s13, const void* w2, const void* s2,
                        int32_t* topk_idx, float* topk_w, int32_t* expert_offsets,
                        int32_t* perm_token, int32_t* inv_slot, float* y_perm, void* y, void* ws,
                        size_t ws_bytes, void* stream) {
@@ -248,15 +258,8 @@ moe_status moe_forward(const moe_shape* shape, const void* x, const void* wg, co
   }
   REQUIRE_PTR(wg, 16);
   REQUIRE_PTR(expert_offsets, 16);
-  REQUIRE_PTR(w13, 16);
-  REQUIRE_PTR(w2, 16);
   if (bias && !aligned(bias, 16)) return fail(MOE_ERR_INVALID_ARG, "bias not 16-byte aligned");
-  if (shape->wdtype == MOE_W_FP8_E4M3_B128) {
-    REQUIRE_PTR(s13, 16);
-    REQUIRE_PTR(s2, 16);
-  } else if (s13 || s2) {
-    return fail(MOE_ERR_INVALID_ARG, "s13/s2 must be NULL for bf16 weights");
-  }
+  if ((st = check_weights(shape, w13, s13, w2, s2)) != MOE_OK) return st;
   WsLayout L;
   if ((st = check_ws(shape, ws, ws_bytes, &L)) != MOE_OK) return st;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);

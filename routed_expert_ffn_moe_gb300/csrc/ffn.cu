@@ -124,22 +124,69 @@ __device__ __forceinline__ void gather_row_chunks(long i, const uint16_t* __rest
   for (int j = 0; j < kGatherChunks; ++j) dst[j] = v[j];
 }
 
+// MXFP4 weights: thread i encodes 32-element block i of the slot rows as two E4M3 terms
+// (mx_common.cuh). Slot s < routed holds token perm_token[s]; slot routed + t (the shared
+// expert's segment) holds token t. Rows at or beyond nq are not this launch's.
+__device__ __forceinline__ void gather_encode_block(long i, const uint16_t* __restrict__ x,
+                                                    const int32_t* __restrict__ perm_token, int T,
+                                                    long routed, long nq, int d,
+                                                    const mx::Planes& xq, int* status) {
+  const int nb = d >> 5;
+  const long s = i / nb;
+  if (s >= nq) return;
+  const int b = (int)(i - s * nb);
+  int t = s < routed ? __ldg(perm_token + s) : (int)(s - routed);
+  if (t < 0 || t >= T) {
+    record_error(status, MOE_ERR_DEVICE_BOUNDS);
+    t = 0;
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(x + (long)t * d) + 4 * b;
+  uint4 w[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) w[j] = __ldg(src + j);
+  float v[32];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t u[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      v[8 * j + 2 * m] = __uint_as_float(u[m] << 16);
+      v[8 * j + 2 * m + 1] = __uint_as_float(u[m] & 0xFFFF0000u);
+    }
+  }
+  uint32_t hi[8], lo[8], sa, sb;
+  mx::encode32(v, hi, lo, sa, sb);
+  uint4* dh = reinterpret_cast<uint4*>(xq.hi + s * d + 32 * b);
+  uint4* dl = reinterpret_cast<uint4*>(xq.lo + s * d + 32 * b);
+  dh[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+  dh[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+  dl[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+  dl[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+  xq.s_hi[s * nb + b] = (uint8_t)sa;
+  xq.s_lo[s * nb + b] = (uint8_t)sb;
+}
+
 // One launch for both: block 0 builds the plan from the expert offsets while the other blocks
 // gather x_perm[s] = x[perm_token[s]] for every routed slot (the tensor-core path's token tiles
-// are contiguous rows for TMA). Neither needs the other.
+// are contiguous rows for TMA), or, with MXFP4 weights (xq.hi set), encode the first nq slot
+// rows as E4M3 terms. Neither needs the other.
 __global__ void __launch_bounds__(256) k_plan_gather(const int32_t* __restrict__ offsets,
                                                      PlanArgs a, int32_t* __restrict__ plan,
                                                      const uint16_t* __restrict__ x,
                                                      const int32_t* __restrict__ perm_token, int T,
                                                      long routed, int d,
-                                                     uint16_t* __restrict__ x_perm, int* status) {
+                                                     uint16_t* __restrict__ x_perm, int* status,
+                                                     mx::Planes xq, long nq) {
   pdl_wait_then_release();
   if (blockIdx.x == 0) {
     plan_block(offsets, a, plan);
     return;
   }
-  gather_row_chunks((long)(blockIdx.x - 1) * blockDim.x + threadIdx.x, x, perm_token, T, routed,
-                    d, x_perm, status);
+  const long i = (long)(blockIdx.x - 1) * blockDim.x + threadIdx.x;
+  if (xq.hi)
+    gather_encode_block(i, x, perm_token, T, routed, nq, d, xq, status);
+  else
+    gather_row_chunks(i, x, perm_token, T, routed, d, x_perm, status);
 }
 
 // Phase events are recorded as external events while the stream is being captured into a CUDA
@@ -201,6 +248,12 @@ struct TileShape {
 
 TileShape tile_shape(const moe_shape& s, bool fp8, bool decode, long routed) {
   TileShape t;
+  if (s.wdtype == MOE_W_MXFP4_E8M0_B32) {
+    t.nt_up = t.nt_dn = tc_mx_tile_tokens(decode, routed, s.E);
+    t.mt_up = s.f / 128;
+    t.mt_dn = s.d / tc_mx_down_rows(decode, s.d);
+    return t;
+  }
   t.nt_up = fp8 ? tc_fp8_tile_tokens(true, decode, routed, s.E) : tc_tile_tokens(true, decode);
   t.nt_dn = fp8 ? tc_fp8_tile_tokens(false, decode, routed, s.E) : tc_tile_tokens(false, decode);
   if (!fp8) {
@@ -219,9 +272,18 @@ TileShape tile_shape(const moe_shape& s, bool fp8, bool decode, long routed) {
 // The shared expert's own tile lists, for moe_forward: its segment starts at slot T*k and holds
 // the T tokens in order, so the lists depend on the shape alone. rows[0] and rows[1]: prefixes
 // over the E+1 experts for the gate/up and the down pass (zero work for the routed experts);
-// rows[2]: the expert offsets the tile decoder reads (entries E and E+1).
-__global__ void k_shared_plan(int T, int k, int E, TileShape ts, int32_t* __restrict__ rows) {
+// rows[2]: the expert offsets the tile decoder reads (entries E and E+1). With MXFP4 weights
+// (xq.hi set) the other blocks encode the shared segment's rows (token t at slot T*k + t).
+__global__ void k_shared_plan(int T, int k, int E, TileShape ts, int32_t* __restrict__ rows,
+                              const uint16_t* __restrict__ x, int d, mx::Planes xq,
+                              int* status) {
   pdl_wait_then_release();
+  if (blockIdx.x > 0) {
+    const long routed = (long)T * k;
+    const long i = (long)(blockIdx.x - 1) * blockDim.x + threadIdx.x + routed * (d >> 5);
+    gather_encode_block(i, x, nullptr, T, routed, routed + T, d, xq, status);
+    return;
+  }
   const int n = E + 2;
   for (int e = threadIdx.x; e < n; e += blockDim.x) {
     const bool last = e == E + 1;
@@ -234,8 +296,8 @@ __global__ void k_shared_plan(int T, int k, int E, TileShape ts, int32_t* __rest
 }  // namespace
 
 cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32_t* perm_token,
-                              const int32_t* offsets, const void* w13, const float* s13,
-                              const void* w2, const float* s2, float* y_perm, char* ws,
+                              const int32_t* offsets, const void* w13, const void* s13,
+                              const void* w2, const void* s2, float* y_perm, char* ws,
                               const WsLayout& L, cudaStream_t st, bool with_shared) {
   if (s.T == 0) return cudaSuccess;
   FfnArgs a{};
@@ -248,13 +310,20 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32
   a.x_perm = reinterpret_cast<uint16_t*>(ws + L.x_perm);
   a.y_perm = y_perm;
   a.status = reinterpret_cast<int*>(ws + L.status);
+  const bool mxq = s.wdtype == MOE_W_MXFP4_E8M0_B32;
+  const long all_slots = (long)s.T * s.k + (long)s.n_shared * s.T;
+  if (mxq) {
+    a.xq = mx::planes_at(ws + L.xq, all_slots, s.d);
+    a.hq = mx::planes_at(ws + L.hq, all_slots, s.f);
+  }
   int32_t* plan = reinterpret_cast<int32_t*>(ws + L.plan);
 
   // Experts with at least tc_min tokens go to the tensor-core GEMM, the rest to the
   // weight-streaming GEMV. Both stream each weight byte once; the tensor-core kernel does so at
   // full HBM rate from one token up, so by default it takes every expert. MOE_TC_MIN_TOKENS
   // moves the split (a tuning and testing knob; results agree within rounding either way).
-  const int tc_min = tc_min_tokens();
+  // MXFP4 weights run on the tensor cores only (the block-scaled MMA is their format's path).
+  const int tc_min = mxq ? 1 : tc_min_tokens();
   const bool fp8 = s.wdtype == MOE_W_FP8_E4M3_B128;
   const long routed = (long)s.T * s.k;
   const bool decode = routed <= 32L * s.E;  // at most ~32 tokens per routed expert on average
@@ -277,7 +346,7 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32
   // decode tile of tokens stream their weights through the decode tiles on part of the SMs
   // while the others run the prefill tiles on the rest, on a second stream, so that the
   // HBM-bound and the tensor-bound experts overlap instead of taking turns on every SM.
-  const bool split = !fp8 && !decode && use_tc && !use_gemv && routed > 0;
+  const bool split = s.wdtype == MOE_W_BF16 && !decode && use_tc && !use_gemv && routed > 0;
   if (split) {
     // Measured rates on GB300 (one SM, fitted to split sweeps of the skewed prefill layer):
     // decode tiles stream weights at ~78 GB/s in the gate/up pass and ~52 GB/s in the down pass
@@ -300,10 +369,12 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32
   }
 
   const PhaseEvents ev = profile_phase_events();
-  const long gather_n = (use_tc && routed > 0) ? routed * (s.d / 8) / kGatherChunks : 0;
+  // rows the gather writes: the routed slots, plus (MXFP4) the shared segment's encoded rows
+  const long nq = routed + (mxq ? (long)a.n_shared * s.T : 0);
+  const long gather_n = (use_tc && nq > 0) ? nq * (s.d / 8) / kGatherChunks : 0;
   cudaError_t e = launch_pdl(k_plan_gather, dim3((unsigned)(1 + (gather_n + 255) / 256)),
                              dim3(256), 0, st, offsets, pa, plan, x, perm_token, s.T, routed, s.d,
-                             a.x_perm, a.status);
+                             a.x_perm, a.status, a.xq, nq);
   count_launches(1);
   if (e != cudaSuccess) return e;
   if (ev.begin) record_phase(ev.begin, st);
@@ -316,8 +387,9 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32
   const int max_up = use_gemv ? cap(max_groups * pa.items_up) : 0;
   const int max_dn = use_gemv ? cap(max_groups * pa.items_dn) : 0;
   const auto tc = [&](bool gateup, const int32_t* prefix) {
-    return fp8 ? launch_tc_fp8(a, prefix, gateup, decode, st)
-               : launch_tc(a, prefix, gateup, decode, st);
+    return mxq ? launch_tc_mx(a, prefix, gateup, decode, st)
+           : fp8 ? launch_tc_fp8(a, prefix, gateup, decode, st)
+                 : launch_tc(a, prefix, gateup, decode, st);
   };
 
   if (split) {
@@ -360,8 +432,8 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32
 // the routed experts; the combine waits for both. With no shared expert, or with the
 // weight-streaming GEMV in use, the four steps simply run in order.
 cudaError_t launch_forward(const moe_shape& s, const uint16_t* x, const uint16_t* wg,
-                           const float* bias, const void* w13, const float* s13, const void* w2,
-                           const float* s2, int32_t* topk_idx, float* topk_w, int32_t* offsets,
+                           const float* bias, const void* w13, const void* s13, const void* w2,
+                           const void* s2, int32_t* topk_idx, float* topk_w, int32_t* offsets,
                            int32_t* perm_token, int32_t* inv_slot, float* y_perm, uint16_t* y,
                            char* ws, const WsLayout& L, cudaStream_t st) {
   int* status = reinterpret_cast<int*>(ws + L.status);
@@ -393,10 +465,6 @@ cudaError_t launch_forward(const moe_shape& s, const uint16_t* x, const uint16_t
   const TileShape ts = tile_shape(s, fp8, decode, routed);
   int32_t* rows = reinterpret_cast<int32_t*>(ws + L.shared);
   const int n = s.E + 2;
-  if ((e = launch_pdl(k_shared_plan, dim3(1), dim3(256), 0, aux, s.T, s.k, s.E, ts, rows)) !=
-      cudaSuccess)
-    return e;
-  count_launches(1);
   FfnArgs a{};
   a.T = s.T; a.d = s.d; a.E = s.E; a.k = s.k; a.f = s.f; a.n_shared = 1; a.wdtype = s.wdtype;
   a.x = x; a.perm_token = perm_token; a.offsets = rows + 2 * n;
@@ -405,10 +473,23 @@ cudaError_t launch_forward(const moe_shape& s, const uint16_t* x, const uint16_t
   a.x_perm = reinterpret_cast<uint16_t*>(ws + L.x_perm);
   a.y_perm = y_perm;
   a.status = status;
+  const bool mxq = s.wdtype == MOE_W_MXFP4_E8M0_B32;
+  if (mxq) {
+    const long all_slots = routed + s.T;
+    a.xq = mx::planes_at(ws + L.xq, all_slots, s.d);
+    a.hq = mx::planes_at(ws + L.hq, all_slots, s.f);
+  }
+  // MXFP4: the shared segment's rows are encoded here, the routed ones by the routed path's gather
+  const long enc = mxq ? (long)s.T * (s.d / 32) : 0;
+  if ((e = launch_pdl(k_shared_plan, dim3((unsigned)(1 + (enc + 255) / 256)), dim3(256), 0, aux,
+                      s.T, s.k, s.E, ts, rows, x, s.d, a.xq, status)) != cudaSuccess)
+    return e;
+  count_launches(1);
   for (int pass = 0; pass < 2; ++pass) {
     const bool gateup = pass == 0;
-    e = fp8 ? launch_tc_fp8(a, rows + pass * n, gateup, decode, aux)
-            : launch_tc(a, rows + pass * n, gateup, decode, aux);
+    e = mxq ? launch_tc_mx(a, rows + pass * n, gateup, decode, aux)
+        : fp8 ? launch_tc_fp8(a, rows + pass * n, gateup, decode, aux)
+              : launch_tc(a, rows + pass * n, gateup, decode, aux);
     if (e != cudaSuccess) return e;
   }
   if ((e = cudaEventRecord(ss->ev[5], aux)) != cudaSuccess) return e;

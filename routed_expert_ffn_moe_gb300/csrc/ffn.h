@@ -2,6 +2,7 @@
 #pragma once
 
 #include "internal.h"
+#include "mx_common.cuh"
 
 namespace moe {
 
@@ -11,13 +12,14 @@ struct FfnArgs {
   const int32_t* perm_token;   // [T*k]
   const int32_t* offsets;      // [E+2]
   const void* w13;             // [E+S, 2f, d]
-  const float* s13;            // FP8 scales or null
+  const void* s13;             // FP8 (fp32) or MXFP4 (E8M0) scales, or null
   const void* w2;              // [E+S, d, f]
-  const float* s2;
+  const void* s2;
   uint16_t* h;                 // [slots, f] bf16 (workspace)
   uint16_t* x_perm;            // [T*k, d] bf16 (workspace)
   float* y_perm;               // [slots, d] fp32
   int* status;                 // device error word
+  mx::Planes xq, hq;           // MXFP4 weights: x and h as E4M3 terms (workspace), [slots, d|f]
 };
 
 // weight-streaming path (ffn_gemv.cu)
@@ -39,6 +41,11 @@ int tc_fp8_tile_tokens(bool gateup, bool decode, long routed, int E);
 int tc_fp8_decode_down_rows(int d);  // weight rows per down tile of the decode tiles
 cudaError_t launch_tc_fp8(const FfnArgs& a, const int32_t* prefix, bool gateup, bool decode,
                           cudaStream_t st);
+// tensor-core path (ffn_tc_mxfp4.cu): MXFP4 weights fed to block-scaled MMAs as stored
+int tc_mx_tile_tokens(bool decode, long routed, int E);
+int tc_mx_down_rows(bool decode, int d);  // weight rows per down tile
+cudaError_t launch_tc_mx(const FfnArgs& a, const int32_t* prefix, bool gateup, bool decode,
+                         cudaStream_t st);
 // wide-tile variant (ffn_tc_fp8_wide.cu): E4M3 weights dequantised to bf16 into TMEM
 int tc_fp8_wide_tile_tokens();
 // plan units (weight tiles, or cluster pairs of them) per expert in a prefill-tile pass

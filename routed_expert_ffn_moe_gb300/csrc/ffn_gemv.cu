@@ -63,7 +63,7 @@ __global__ void __launch_bounds__(256) k_gemv(FfnArgs a, const int32_t* __restri
   const size_t wexp_rows = GATEUP ? 2 * (size_t)a.f : (size_t)a.d;
   const int sblk_cols = K / 128;
   const char* Wb = reinterpret_cast<const char*>(GATEUP ? a.w13 : a.w2);
-  const float* Sb = GATEUP ? a.s13 : a.s2;
+  const float* Sb = static_cast<const float*>(GATEUP ? a.s13 : a.s2);
 
   for (int item = blockIdx.x; item < total; item += gridDim.x) {
     int lo = 0, hi = E1;  // largest e with prefix[e] <= item

@@ -378,7 +378,7 @@ cudaError_t launch_tc_fp8(const FfnArgs& a, const int32_t* prefix, bool gateup, 
     b1 = b0;
   }
   if (e != cudaSuccess) return e;
-  const float* sc = gateup ? a.s13 : a.s2;
+  const float* sc = static_cast<const float*>(gateup ? a.s13 : a.s2);
   if (fp8_tile64((long)routed, a.E)) {
     if (gateup) return launch_variant<true, 64, 3, 2, 2>(w, b0, b1, p, sc, st);
     if (pair_dn) return launch_variant<false, 64, 3, 2, 2>(w, b0, b1, p, sc, st);

@@ -436,7 +436,7 @@ cudaError_t launch_tc_fp8_wide(const FfnArgs& a, const int32_t* prefix, bool gat
     m.b1w = m.b0w;
   }
   if (e != cudaSuccess) return e;
-  const float* sc = gateup ? a.s13 : a.s2;
+  const float* sc = static_cast<const float*>(gateup ? a.s13 : a.s2);
   const bool paired = paired_tiles(gateup, a.d);
   if (cl == 2) return launch_pass<2>(m, p, sc, gateup, paired, st);
   return launch_pass<1>(m, p, sc, gateup, paired, st);

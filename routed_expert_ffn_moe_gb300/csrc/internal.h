@@ -23,7 +23,7 @@ constexpr int kChunkTokens = 32;
 constexpr int kPlanRows = 8;
 
 struct WsLayout {
-  size_t status, logits, hist, base, plan, x_perm, h, shared, total;
+  size_t status, logits, hist, base, plan, x_perm, h, shared, xq, hq, total;
   int nchunk;
 };
 
@@ -40,9 +40,15 @@ inline WsLayout ws_layout(const moe_shape& s) {
   L.hist = take(E * (size_t)L.nchunk * 4);
   L.base = take(E * (size_t)L.nchunk * 4);
   L.plan = take((size_t)kPlanRows * (E + 2) * 4 + 256);
-  L.x_perm = take(T * k * (size_t)s.d * 2);
-  L.h = take((T * k + (size_t)s.n_shared * T) * (size_t)s.f * 2);
+  const size_t slots = T * k + (size_t)s.n_shared * T;
+  const bool mxfp4 = s.wdtype == MOE_W_MXFP4_E8M0_B32;
+  // bf16 / E4M3 weights: gathered bf16 token rows and bf16 h. MXFP4 weights: both as two E4M3
+  // terms with their scales (x before the gate/up pass, h before the down pass).
+  L.x_perm = take(mxfp4 ? 0 : T * k * (size_t)s.d * 2);
+  L.h = take(mxfp4 ? 0 : slots * (size_t)s.f * 2);
   L.shared = take(3 * (E + 2) * 4);
+  L.xq = take(mxfp4 ? slots * (2 * (size_t)s.d + 2 * (size_t)(s.d / 32)) : 0);
+  L.hq = take(mxfp4 ? slots * (2 * (size_t)s.f + 2 * (size_t)(s.f / 32)) : 0);
   L.total = off;
   return L;
 }
@@ -62,13 +68,13 @@ cudaError_t launch_permute(const moe_shape& s, const int32_t* topk_idx, int32_t*
                            int32_t* perm_token, int32_t* inv_slot, char* ws, const WsLayout& L,
                            cudaStream_t st);
 cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32_t* perm_token,
-                              const int32_t* offsets, const void* w13, const float* s13,
-                              const void* w2, const float* s2, float* y_perm, char* ws,
+                              const int32_t* offsets, const void* w13, const void* s13,
+                              const void* w2, const void* s2, float* y_perm, char* ws,
                               const WsLayout& L, cudaStream_t st, bool with_shared = true);
 // the whole layer, the shared expert's FFN on a second stream (ffn.cu)
 cudaError_t launch_forward(const moe_shape& s, const uint16_t* x, const uint16_t* wg,
-                           const float* bias, const void* w13, const float* s13, const void* w2,
-                           const float* s2, int32_t* topk_idx, float* topk_w, int32_t* offsets,
+                           const float* bias, const void* w13, const void* s13, const void* w2,
+                           const void* s2, int32_t* topk_idx, float* topk_w, int32_t* offsets,
                            int32_t* perm_token, int32_t* inv_slot, float* y_perm, uint16_t* y,
                            char* ws, const WsLayout& L, cudaStream_t st);
 cudaError_t launch_combine(const moe_shape& s, const float* y_perm, const int32_t* inv_slot,

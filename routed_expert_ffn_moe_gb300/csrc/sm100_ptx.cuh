@@ -163,6 +163,30 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t adesc, uin
       : "memory");
 }
 
+// Instruction descriptor of kind::mxf8f6f4 with block scaling: A E2M1, B E4M3, E8M0 scales (one
+// per 32-wide K block of every row of A and of B), fp32 accumulator, both operands K-major.
+// sf_a / sf_b pick the byte of each 32-bit TMEM scale word that this instruction's K block uses.
+__device__ __forceinline__ uint32_t idesc_mx_e2m1_e4m3(int M, int N, uint32_t sf_a, uint32_t sf_b) {
+  return (sf_b << 4) | (5u << 7) | (0u << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
+         ((uint32_t)(M >> 4) << 24) | (sf_a << 29);
+}
+
+// D[tmem] (+)= (A * 2^scale_A)[smem] * (B * 2^scale_B)[smem]^T over one 32-wide K block, the
+// scales read from TMEM at sfa / sfb (kind::mxf8f6f4, one E8M0 scale per row per K block).
+__device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      "  .reg .pred p;\n"
+      "  setp.ne.b32 p, %6, 0;\n"
+      "  tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+      " [%0], %1, %2, %3, [%4], [%5], p;\n"
+      "}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+
 // D[tmem] (+)= A[tmem] * B[smem]^T: A is 128 lanes (one row of M per lane) x K/2 columns, two
 // 16-bit elements per 32-bit column in increasing K order.
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
@@ -189,6 +213,13 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
       "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
+}
+
+// 32 lanes x 4 columns of 32 bits.
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t (&r)[4]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
+               : "memory");
 }
 
 // 32 lanes x 16 columns of 32 bits.

@@ -11,6 +11,8 @@ import synth
 TOL_MAX_ABS_BF16 = 2e-2
 TOL_REL_L2_BF16 = 1e-2
 TOL_REL_L2_FP8 = 3e-2
+# MXFP4 weights enter the products exactly and the activations carry about one bf16 rounding
+# (two E4M3 terms per element), so the bf16 bars apply to them too.
 # gate weights: fp32 softmax over the k chosen logits vs the fp64 renormalised softmax
 TOL_TOPK_W = 2e-6
 
@@ -70,7 +72,7 @@ def assert_y_close(y_gpu_bits, y_ref, wdtype, what="y"):
     ma = float(err.max())
     excess = float((err - bf16_half_ulp(y_ref)).max())
     rl = rel_l2(y, y_ref)
-    if wdtype == "bf16":
+    if wdtype in ("bf16", "mxfp4"):
         assert excess <= TOL_MAX_ABS_BF16 and rl <= TOL_REL_L2_BF16, (what, ma, excess, rl)
     else:
         assert rl <= TOL_REL_L2_FP8, (what, ma, rl)

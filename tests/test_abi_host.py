@@ -111,6 +111,28 @@ def test_bad_arguments_rejected_before_launch(lib):
     assert rc == -1 and "ws" in msg
 
 
+def test_mxfp4_arguments_rejected_before_launch(lib):
+    s4 = moe.shape_of(16, 256, 8, 2, 128, 1, "mxfp4")
+    sp = ctypes.byref(s4)
+    wsz = moe.moe_workspace_size(s4)
+    # the workspace holds x and h as two E4M3 terms plus a scale byte per 32 elements each
+    slots = 16 * 3
+    assert wsz >= slots * (2 * 256 + 2 * 8) + slots * (2 * 128 + 2 * 4)
+    F = FAKE
+    # shape, x, perm_token, offsets, w13, s13, w2, s2, y_perm, ws, ws_bytes, stream
+    rc, msg = call("moe_expert_ffn", sp, F, F, F, F + 16, F, F, F, F, F, wsz, None)
+    assert rc == -1 and "w13 not 32-byte aligned" in msg
+    rc, msg = call("moe_expert_ffn", sp, F, F, F, F, None, F, F, F, F, wsz, None)
+    assert rc == -1 and "s13 is NULL" in msg
+    rc, msg = call("moe_expert_ffn", sp, F, F, F, F, F, F, F + 8, F, F, wsz, None)
+    assert rc == -1 and "s2 not 16-byte aligned" in msg
+    # moe_forward: x, wg, bias, w13, s13, w2, s2, topk_idx, topk_w, offsets, perm, inv, y_perm, y
+    fwd = [F, F, None, F, F, F + 16, F, F, F, F, F, F, F, F]
+    rc, msg = call("moe_forward", sp, *fwd, F, wsz, None)
+    assert rc == -1 and "w2 not 32-byte aligned" in msg
+    assert moe.moe_workspace_size(moe.MoeShape(16, 256, 8, 2, 128, 1, 3)) == 0
+
+
 def test_binding_raises_moe_error(lib):
     s = moe.shape_of(16, 256, 8, 2, 128)
     with pytest.raises(moe.MoeError) as ei:

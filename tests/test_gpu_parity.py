@@ -1,8 +1,8 @@
 """GPU parity: each C-ABI call and the whole layer against the CPU oracle, on seeded inputs.
 
 Routing indices and the permutation must match bit for bit; gate weights within 2e-6; the
-layer output within max-abs 2e-2 and relative-L2 1e-2 (bf16 weights) or relative-L2 3e-2 (FP8
-weights) of the fp64 oracle."""
+layer output within max-abs 2e-2 and relative-L2 1e-2 (bf16 and MXFP4 weights) or relative-L2
+3e-2 (FP8 weights) of the fp64 oracle."""
 import numpy as np
 import pytest
 
@@ -77,6 +77,17 @@ SMALL = [
     ("tiny", {"router": "zipf", "T": 600, "d": 512, "f": 256, "E": 16, "k": 2}),
     ("tiny", {"T": 333, "d": 384, "f": 256, "E": 6, "k": 3, "wdtype": "fp8"}),
     ("tiny", {"T": 333, "d": 384, "f": 256, "E": 6, "k": 3}),
+    # MXFP4 weights on block-scaled MMAs: 32-token decode tiles (paired and single down tiles),
+    # 64-token decode tiles, 128-token prefill tiles, ragged and degenerate batches
+    ("tiny", {"wdtype": "mxfp4"}),
+    ("tiny", {"T": 40, "d": 384, "f": 256, "E": 8, "k": 2, "wdtype": "mxfp4"}),
+    ("tiny", {"d": 512, "f": 384, "T": 70, "E": 12, "k": 3, "wdtype": "mxfp4"}),
+    ("tiny", {"T": 600, "E": 8, "k": 2, "wdtype": "mxfp4"}),
+    ("tiny", {"T": 333, "d": 384, "f": 256, "E": 6, "k": 3, "wdtype": "mxfp4"}),
+    ("tiny", {"router": "zipf", "T": 45, "wdtype": "mxfp4"}),
+    ("tiny", {"T": 1, "wdtype": "mxfp4"}),
+    ("tiny", {"T": 0, "wdtype": "mxfp4"}),
+    ("tiny", {"n_shared": 0, "T": 37, "wdtype": "mxfp4"}),
 ]
 
 
@@ -182,7 +193,8 @@ def test_combine_direct():
 @pytest.mark.parametrize("over", [{}, {"wdtype": "fp8"},
                                   {"router": "zipf", "T": 600, "d": 512, "f": 256, "E": 16, "k": 2},
                                   {"T": 600, "d": 512, "f": 256, "E": 8, "k": 2, "wdtype": "fp8"},
-                                  {"n_shared": 0}])
+                                  {"n_shared": 0}, {"wdtype": "mxfp4"},
+                                  {"T": 600, "d": 512, "f": 256, "E": 8, "k": 2, "wdtype": "mxfp4"}])
 def test_forward_equals_the_four_calls(over):
     # moe_forward runs the shared expert on its own stream: every output must be bit-identical
     # to the four separate calls.
@@ -214,7 +226,8 @@ def test_layer_is_deterministic():
 
 
 @pytest.mark.parametrize("over", [{}, {"wdtype": "fp8", "T": 70, "E": 12, "k": 3, "d": 512, "f": 384},
-                                  {"router": "zipf", "T": 600, "d": 512, "f": 256, "E": 16, "k": 2}])
+                                  {"router": "zipf", "T": 600, "d": 512, "f": 256, "E": 16, "k": 2},
+                                  {"wdtype": "mxfp4", "T": 600, "E": 8, "k": 2}])
 def test_layer_replays_from_a_cuda_graph(over):
     # the four calls enqueue no synchronisation or allocation, so they can be captured once
     cfg = synth.get_config("tiny", **over)
@@ -256,6 +269,14 @@ def test_device_generator_matches_host_generator():
     assert rc == 0
     np.testing.assert_array_equal(q.cpu().numpy(), q_h)
     np.testing.assert_array_equal(s.cpu().numpy(), s_h)
+    q4_h, s4_h = synth.quantize_mxfp4(w)
+    q4 = t.empty(256, 192, dtype=t.uint8, device="cuda")
+    s4 = t.empty(256, 12, dtype=t.uint8, device="cuda")
+    rc = synth.lib().synth_quant_mxfp4_device(bf16_dev(w).data_ptr(), q4.data_ptr(), s4.data_ptr(),
+                                              256, 384, ctypes.c_void_p(t.cuda.current_stream().cuda_stream))
+    assert rc == 0
+    np.testing.assert_array_equal(q4.cpu().numpy(), q4_h)
+    np.testing.assert_array_equal(s4.cpu().numpy(), s4_h)
 
 
 def sample_tokens(cfg, idx, n_even=6):
@@ -273,7 +294,8 @@ def sample_tokens(cfg, idx, n_even=6):
 
 FULL = ["v3_decode", "v4pro_decode", "skewed_prefill", "sweep_fp8_T1", "sweep_fp8_T8",
         "sweep_fp8_T64", "sweep_fp8_T256", "sweep_fp8_T1024", "sweep_fp8_T4096",
-        "sweep_fp8_T16384"]
+        "sweep_fp8_T16384", "v4pro_decode_fp4", "sweep_fp4_T1", "sweep_fp4_T256",
+        "sweep_fp4_T4096"]
 
 
 @pytest.mark.parametrize("name", FULL)
@@ -289,6 +311,8 @@ MAXIMUM = [
     {"T": 5, "d": 128, "E": 4, "k": 2, "f": 16384},
     {"T": 5, "d": 16384, "E": 4, "k": 2, "f": 128, "wdtype": "fp8"},
     {"T": 5, "d": 128, "E": 4, "k": 2, "f": 16384, "wdtype": "fp8"},
+    {"T": 5, "d": 16384, "E": 4, "k": 2, "f": 128, "wdtype": "mxfp4"},
+    {"T": 5, "d": 128, "E": 4, "k": 2, "f": 16384, "wdtype": "mxfp4"},
 ]
 
 
