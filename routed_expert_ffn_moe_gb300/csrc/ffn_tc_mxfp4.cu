@@ -37,7 +37,7 @@ constexpr uint32_t kWSmem = kBM * kMxK;          // one weight tile in shared me
 constexpr uint32_t kWTx = kBM * kMxK / 2;        // the bytes TMA reads for it (8 KB)
 constexpr uint32_t kTBox = kBoxRows * kMxK;      // one 16-row box of E4M3 token codes
 constexpr int kThreadsMx = 32 * 10;              // producer, MMA, 4 epilogue, 4 scale writers
-constexpr int kSfAhead = 4;                      // stages the scale words are loaded ahead
+constexpr int kSfAhead = 4;                      // K slices the scale words are loaded ahead
 
 struct MxParams {
   const uint8_t* w_scales;    // [rows of the weight map, K/32] E8M0
@@ -46,19 +46,23 @@ struct MxParams {
   mx::Planes h;               // gate/up output: h as the down pass's terms, [slots, f]
 };
 
-template <bool GATEUP, int NT, int STAGES, int KA, int ACCB, bool FOLD>
+// A ring stage holds SUB consecutive 128-wide K slices (each: KA weight tiles and the token
+// tile): the per-stage hand-offs (barrier waits, commit) are paid once per SUB slices.
+template <bool GATEUP, int NT, int STAGES, int KA, int ACCB, bool FOLD, int SUB>
 struct SmemMx {
   static constexpr uint32_t kBTile = (uint32_t)NT * kMxK;  // one term's token tile
-  static constexpr uint32_t kStageBytes = KA * kWSmem + 2 * kBTile;
+  static constexpr uint32_t kSliceBytes = KA * kWSmem + 2 * kBTile;
+  static constexpr uint32_t kStageBytes = SUB * kSliceBytes;
   static constexpr uint32_t kTilesBytes = STAGES * kStageBytes;
-  static constexpr uint32_t kBarBytes = 8 * (3 * STAGES + 2 * ACCB) + 16;
+  static constexpr uint32_t kBarBytes = 8 * (2 * STAGES + 2 * ACCB) + 16;
   static constexpr uint32_t kTotal = kTilesBytes + kBarBytes + 1024;
   static constexpr uint32_t kAccN = FOLD ? 2 * NT : NT;  // accumulator columns per weight tile
   static constexpr uint32_t kAccCols = KA * kAccN;
   // scale words of the token rows: one 4-column group per 128 B rows (folded: hi then lo rows),
   // or one group per term
   static constexpr uint32_t kBSfCols = FOLD ? (2 * NT <= 128 ? 4 : 8) : 8;
-  static constexpr uint32_t kSfCols = 4 * KA + kBSfCols;  // per stage: KA weight tiles, tokens
+  // per stage: a 4-column group per (slice, weight tile), then the token groups of each slice
+  static constexpr uint32_t kSfCols = SUB * (4 * KA + kBSfCols);
   static constexpr uint32_t kUsedCols = ACCB * kAccCols + STAGES * kSfCols;
   static constexpr uint32_t kTmemCols =
       kUsedCols <= 32 ? 32 : kUsedCols <= 64 ? 64 : kUsedCols <= 128 ? 128
@@ -186,11 +190,11 @@ __device__ __forceinline__ void down_epilogue_folded(const TcParams& p, int tota
   }
 }
 
-template <bool GATEUP, int NT, int STAGES, int KA, int ACCB, bool FOLD>
+template <bool GATEUP, int NT, int STAGES, int KA, int ACCB, bool FOLD, int SUB>
 __global__ void __launch_bounds__(kThreadsMx, 1)
     k_tc_ffn_mx(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_hi,
                 const __grid_constant__ CUtensorMap tm_lo, const TcParams p, const MxParams q) {
-  using S = SmemMx<GATEUP, NT, STAGES, KA, ACCB, FOLD>;
+  using S = SmemMx<GATEUP, NT, STAGES, KA, ACCB, FOLD, SUB>;
   static_assert(S::kUsedCols <= 512, "TMEM columns");
   static_assert(!FOLD || 2 * NT <= 256, "MMA N");
   static_assert(!GATEUP || KA == 2, "gate/up tiles pair the gate and up rows");
@@ -200,22 +204,20 @@ __global__ void __launch_bounds__(kThreadsMx, 1)
                                              ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kTilesBytes);
   uint64_t* empty = full + STAGES;
-  uint64_t* sf_full = empty + STAGES;
-  uint64_t* acc_full = sf_full + STAGES;
+  uint64_t* acc_full = empty + STAGES;
   uint64_t* acc_empty = acc_full + ACCB;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + ACCB);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E1 = p.E + p.n_shared;
-  const int kblocks = p.K / kMxK;
-  const int ksb = p.K / 32;  // scale bytes per row
+  const int kblocks = p.K / (kMxK * SUB);  // stages per tile
+  const int ksb = p.K / 32;                // scale bytes per row
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);    // MMA commit: the stage's tiles and scale words are consumed
-      mbar_init(&sf_full[s], 4);  // the four scale writers
+      mbar_init(&full[s], 5);   // the producer's expect-tx arrival and the four scale writers
+      mbar_init(&empty[s], 1);  // MMA commit: the stage's tiles and scale words are consumed
     }
     for (int b = 0; b < ACCB; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -250,23 +252,28 @@ __global__ void __launch_bounds__(kThreadsMx, 1)
         Tile t;
         decode_tile<GATEUP, NT>(p, tile, t);
         const int nbox = (t.ntok + kBoxRows - 1) / kBoxRows;
-        const uint32_t bytes = KA * kWTx + (uint32_t)nbox * 2 * kTBox;
+        const uint32_t bytes = SUB * (KA * kWTx + (uint32_t)nbox * 2 * kTBox);
         const int wrow = t.e * p.rows_per_expert + t.mt * kBM * (GATEUP ? 1 : KA);
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!wait_bar(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
           uint8_t* st = smem + stage * S::kStageBytes;
           mbar_arrive_expect_tx(&full[stage], bytes);
-          tma_load_2d(st, &tm_w, &full[stage], kb * kMxK, wrow, pol_w);
-          if (KA == 2)  // up rows of the same features, or the next 128 rows of W_d
-            tma_load_2d(st + kWSmem, &tm_w, &full[stage], kb * kMxK,
-                        wrow + (GATEUP ? p.f : kBM), pol_w);
-          uint8_t* bt = st + KA * kWSmem;
-          for (int i = 0; i < nbox; ++i) {
-            tma_load_2d(bt + i * kTBox, &tm_hi, &full[stage], kb * kMxK,
-                        t.slot0 + i * kBoxRows, pol_b);
-            // folded: the lo rows right after the tile's nbox boxes of hi rows
-            tma_load_2d(bt + (FOLD ? (nbox + i) * kTBox : S::kBTile + i * kTBox), &tm_lo,
-                        &full[stage], kb * kMxK, t.slot0 + i * kBoxRows, pol_b);
+#pragma unroll
+          for (int sb = 0; sb < SUB; ++sb) {
+            uint8_t* sl = st + sb * S::kSliceBytes;
+            const int xk = (kb * SUB + sb) * kMxK;
+            tma_load_2d(sl, &tm_w, &full[stage], xk, wrow, pol_w);
+            if (KA == 2)  // up rows of the same features, or the next 128 rows of W_d
+              tma_load_2d(sl + kWSmem, &tm_w, &full[stage], xk, wrow + (GATEUP ? p.f : kBM),
+                          pol_w);
+            uint8_t* bt = sl + KA * kWSmem;
+            for (int i = 0; i < nbox; ++i) {
+              tma_load_2d(bt + i * kTBox, &tm_hi, &full[stage], xk, t.slot0 + i * kBoxRows,
+                          pol_b);
+              // folded: the lo rows right after the tile's nbox boxes of hi rows
+              tma_load_2d(bt + (FOLD ? (nbox + i) * kTBox : S::kBTile + i * kTBox), &tm_lo,
+                          &full[stage], xk, t.slot0 + i * kBoxRows, pol_b);
+            }
           }
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -289,24 +296,31 @@ __global__ void __launch_bounds__(kThreadsMx, 1)
         if (!wait_bar(&acc_empty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t d0 = tmem_base + acc * S::kAccCols;
+        uint32_t idesc[kMxK / 32];
+#pragma unroll
+        for (int kk = 0; kk < kMxK / 32; ++kk)
+          idesc[kk] = idesc_mx_e2m1_e4m3(kBM, FOLD ? 2 * npad : npad, kk, kk);
         for (int kb = 0; kb < kblocks; ++kb) {
-          if (!wait_bar(&full[stage], phase, abort_flag, p.status) ||
-              !wait_bar(&sf_full[stage], phase, abort_flag, p.status)) { ok = false; break; }
+          if (!wait_bar(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(smem + stage * S::kStageBytes);
-          const uint32_t bh = a0 + KA * kWSmem, bl = bh + S::kBTile;
           const uint32_t sfc = tmem_base + sf0 + stage * S::kSfCols;
 #pragma unroll
-          for (int kk = 0; kk < kMxK / 32; ++kk) {
-            const uint32_t idesc = idesc_mx_e2m1_e4m3(kBM, FOLD ? 2 * npad : npad, kk, kk);
+          for (int sb = 0; sb < SUB; ++sb) {
+            const uint32_t a0 = smem_u32(smem + stage * S::kStageBytes + sb * S::kSliceBytes);
+            const uint64_t bh = sw128_desc(a0 + KA * kWSmem);
+            const uint64_t bl = sw128_desc(a0 + KA * kWSmem + S::kBTile);
+            const uint32_t sfb = sfc + 4 * KA * SUB + sb * S::kBSfCols;
 #pragma unroll
-            for (int o = 0; o < KA; ++o) {
-              const uint64_t ad = sw128_desc(a0 + o * kWSmem) + 2 * kk;
-              mma_mx(d0 + o * S::kAccN, ad, sw128_desc(bh) + 2 * kk, idesc, sfc + 4 * o,
-                     sfc + 4 * KA, (kb | kk) ? 1u : 0u);
-              if (!FOLD)
-                mma_mx(d0 + o * S::kAccN, ad, sw128_desc(bl) + 2 * kk, idesc, sfc + 4 * o,
-                       sfc + 4 * KA + 4, 1u);
+            for (int kk = 0; kk < kMxK / 32; ++kk) {
+#pragma unroll
+              for (int o = 0; o < KA; ++o) {
+                const uint64_t ad = sw128_desc(a0 + o * kWSmem) + 2 * kk;
+                const uint32_t sfa = sfc + 4 * (sb * KA + o);
+                mma_mx(d0 + o * S::kAccN, ad, bh + 2 * kk, idesc[kk], sfa, sfb,
+                       (kb | sb | kk) ? 1u : 0u);
+                if (!FOLD)
+                  mma_mx(d0 + o * S::kAccN, ad, bl + 2 * kk, idesc[kk], sfa, sfb + 4, 1u);
+              }
             }
           }
           mma_commit(&empty[stage]);
@@ -330,14 +344,16 @@ __global__ void __launch_bounds__(kThreadsMx, 1)
                                                      abort_flag);
   } else {
     // ---------------- scale writers (warps 6..9) ----------------
-    // Warp of lane quadrant qd writes, per stage: weight row 32*qd + lane's word (its four
-    // K-block scales of this stage) at column 4*o + qd of the stage's group, and the B rows'
-    // words in every lane quadrant, B row 32*c + lane in column c of the token groups, which is
-    // where the MMA reads them. B row r is token r's hi term (r < npad) and token r - npad's lo
-    // term after it when folded; else the hi and the lo rows have a group each. The words are
-    // loaded kSfAhead stages ahead of their store (a register ring).
+    // Warp of lane quadrant qd writes, per K slice of a stage: weight row 32*qd + lane's word
+    // (its four K-block scales of the slice) at column qd of the slice's group for that weight
+    // tile, and the B rows' words in every lane quadrant, B row 32*c + lane in column c of the
+    // slice's token groups, which is where the MMA reads them. B row r is token r's hi term
+    // (r < npad) and token r - npad's lo term after it when folded; else the hi and the lo rows
+    // have a group each. Then it arrives on the stage's full barrier. The words are loaded
+    // kSfAhead slices ahead of their store (a register ring).
     const int qd = warp & 3;
     const uint32_t lane_base = tmem_base + ((uint32_t)(qd * 32) << 16);
+    const int nslices = kblocks * SUB;
     uint32_t it = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
@@ -348,10 +364,10 @@ __global__ void __launch_bounds__(kThreadsMx, 1)
       const size_t wstep = (size_t)(GATEUP ? p.f : kBM) * ksb;  // to the second weight tile
       const int npad = (t.ntok + 15) & ~15;
       uint32_t ra[kSfAhead][2], rb[kSfAhead][8];
-      const auto load = [&](uint32_t (&a)[2], uint32_t (&b)[8], int kb) {
-        if (kb >= kblocks) return;
-        a[0] = ldg_u32(wa + 4 * kb);
-        a[1] = KA == 2 ? ldg_u32(wa + wstep + 4 * kb) : 0u;
+      const auto load = [&](uint32_t (&a)[2], uint32_t (&b)[8], int ks) {
+        if (ks >= nslices) return;
+        a[0] = ldg_u32(wa + 4 * ks);
+        a[1] = KA == 2 ? ldg_u32(wa + wstep + 4 * ks) : 0u;
 #pragma unroll
         for (int c = 0; c < (int)S::kBSfCols; ++c) {
           int n = 32 * (FOLD ? c : (c & 3)) + lane;  // token of B row 32c + lane
@@ -360,31 +376,38 @@ __global__ void __launch_bounds__(kThreadsMx, 1)
           b[c] = 0x7F7F7F7Fu;
           if (n < t.ntok)
             b[c] = ldg_u32((lo ? q.t_scale_lo : q.t_scale_hi) + (size_t)(t.slot0 + n) * ksb +
-                           4 * kb);
+                           4 * ks);
         }
       };
 #pragma unroll
       for (int j = 0; j < kSfAhead; ++j) load(ra[j], rb[j], j);
-      for (int kb0 = 0; ok && kb0 < kblocks; kb0 += kSfAhead) {
+      // ks walks the tile's K slices; slice ks is part sb = ks % SUB of stage `it`
+      for (int ks0 = 0; ok && ks0 < nslices; ks0 += kSfAhead) {
 #pragma unroll
         for (int j = 0; j < kSfAhead; ++j) {
-          const int kb = kb0 + j;
-          if (kb >= kblocks) break;
+          const int ks = ks0 + j;
+          if (ks >= nslices) break;
+          const int sb = ks % SUB;
           const uint32_t stage = it % STAGES, phase = (it / STAGES) & 1u;
-          if (!wait_bar(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
-          tc_fence_after();
+          if (sb == 0) {
+            if (!wait_bar(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+            tc_fence_after();
+          }
           const uint32_t col = lane_base + sf0 + stage * S::kSfCols;
-          tmem_st1(col + qd, ra[j][0]);
-          if (KA == 2) tmem_st1(col + 4 + qd, ra[j][1]);
-          tmem_st4(col + 4 * KA, *reinterpret_cast<const uint32_t(*)[4]>(&rb[j][0]));
+          tmem_st1(col + 4 * (sb * KA) + qd, ra[j][0]);
+          if (KA == 2) tmem_st1(col + 4 * (sb * KA + 1) + qd, ra[j][1]);
+          const uint32_t bcol = col + 4 * KA * SUB + sb * S::kBSfCols;
+          tmem_st4(bcol, *reinterpret_cast<const uint32_t(*)[4]>(&rb[j][0]));
           if (S::kBSfCols == 8)
-            tmem_st4(col + 4 * KA + 4, *reinterpret_cast<const uint32_t(*)[4]>(&rb[j][4]));
-          tmem_st_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sf_full[stage]);
-          ++it;
-          load(ra[j], rb[j], kb + kSfAhead);
+            tmem_st4(bcol + 4, *reinterpret_cast<const uint32_t(*)[4]>(&rb[j][4]));
+          if (sb == SUB - 1) {
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&full[stage]);
+            ++it;
+          }
+          load(ra[j], rb[j], ks + kSfAhead);
         }
       }
     }
@@ -398,12 +421,12 @@ __global__ void __launch_bounds__(kThreadsMx, 1)
   }
 }
 
-template <bool GATEUP, int NT, int STAGES, int KA, int ACCB, bool FOLD>
+template <bool GATEUP, int NT, int STAGES, int KA, int ACCB, bool FOLD, int SUB = 1>
 cudaError_t launch_variant(const CUtensorMap& w, const CUtensorMap& hi, const CUtensorMap& lo,
                            const TcParams& p, const MxParams& q, cudaStream_t st) {
-  using S = SmemMx<GATEUP, NT, STAGES, KA, ACCB, FOLD>;
+  using S = SmemMx<GATEUP, NT, STAGES, KA, ACCB, FOLD, SUB>;
   static_assert(S::kTotal <= 227 * 1024, "shared memory");
-  auto kern = k_tc_ffn_mx<GATEUP, NT, STAGES, KA, ACCB, FOLD>;
+  auto kern = k_tc_ffn_mx<GATEUP, NT, STAGES, KA, ACCB, FOLD, SUB>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)S::kTotal);
   if (e != cudaSuccess) return e;
@@ -429,11 +452,11 @@ cudaError_t encode_e2m1_2d(CUtensorMap* m, const void* base, uint64_t rows, uint
 
 }  // namespace
 
-// Token tile by batch: 32 tokens while experts average at most 16 routed tokens, 64 up to the
-// decode bound, 128 for prefill batches.
+// Token tile by batch: 16 tokens while experts average at most 4 routed tokens, 32 up to 16, 64
+// up to the decode bound, 128 for prefill batches.
 int tc_mx_tile_tokens(bool decode, long routed, int E) {
   if (!decode) return 128;
-  return routed > 16L * E ? 64 : 32;
+  return routed > 16L * E ? 64 : routed > 4L * E ? 32 : 16;
 }
 
 // Down tiles pair two 128-row tiles of W_d (decode tiles, when d allows it); prefill down tiles
@@ -479,6 +502,25 @@ cudaError_t launch_tc_mx(const FfnArgs& a, const int32_t* prefix, bool gateup, b
     if (gateup) return launch_variant<true, 64, 4, 2, 1, true>(w, hi, lo, p, q, st);
     if (dn_rows == 2 * kBM) return launch_variant<false, 64, 4, 2, 1, true>(w, hi, lo, p, q, st);
     return launch_variant<false, 64, 6, 1, 2, true>(w, hi, lo, p, q, st);
+  }
+  // Two 128-wide K slices per stage where K allows (measured: V4-Pro decode 1148 -> 1053 us; the
+  // MMA-issuing thread's per-stage waits and commit are paid half as often)
+  const bool sub2 = K % 256 == 0;
+  if (nt == 16) {
+    if (sub2) {
+      if (gateup) return launch_variant<true, 16, 3, 2, 2, true, 2>(w, hi, lo, p, q, st);
+      if (dn_rows == 2 * kBM)
+        return launch_variant<false, 16, 3, 2, 2, true, 2>(w, hi, lo, p, q, st);
+      return launch_variant<false, 16, 5, 1, 2, true, 2>(w, hi, lo, p, q, st);
+    }
+    if (gateup) return launch_variant<true, 16, 6, 2, 2, true>(w, hi, lo, p, q, st);
+    if (dn_rows == 2 * kBM) return launch_variant<false, 16, 6, 2, 2, true>(w, hi, lo, p, q, st);
+    return launch_variant<false, 16, 10, 1, 2, true>(w, hi, lo, p, q, st);
+  }
+  if (sub2) {
+    if (gateup) return launch_variant<true, 32, 2, 2, 2, true, 2>(w, hi, lo, p, q, st);
+    if (dn_rows == 2 * kBM) return launch_variant<false, 32, 2, 2, 2, true, 2>(w, hi, lo, p, q, st);
+    return launch_variant<false, 32, 4, 1, 2, true, 2>(w, hi, lo, p, q, st);
   }
   if (gateup) return launch_variant<true, 32, 5, 2, 2, true>(w, hi, lo, p, q, st);
   if (dn_rows == 2 * kBM) return launch_variant<false, 32, 5, 2, 2, true>(w, hi, lo, p, q, st);
