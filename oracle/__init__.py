@@ -54,11 +54,13 @@ def lib():
         L.oracle_router_logits.argtypes = [vp, vp, vp, i32, i32, i32, vp]
         L.oracle_route.argtypes = [vp, i32, i32, i32, vp, vp, vp]
         L.oracle_permute.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp]
+        L.oracle_route_hash.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp]
         L.oracle_matvec.argtypes = [i32, vp, vp, i64, i64, i64, vp, vp]
         L.oracle_expert_rows.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
         L.oracle_combine.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp]
         L.oracle_moe_layer.argtypes = [i32] * 7 + [vp] * 16
-        for fn in ("oracle_router_logits", "oracle_route", "oracle_permute", "oracle_matvec",
+        for fn in ("oracle_router_logits", "oracle_route", "oracle_route_hash", "oracle_permute",
+                   "oracle_matvec",
                    "oracle_expert_rows", "oracle_combine", "oracle_moe_layer"):
             getattr(L, fn).restype = None
         _lib = L
@@ -125,6 +127,22 @@ def route(logits, k):
     w = np.empty((T, k), np.float32)
     w64 = np.empty((T, k), np.float64)
     lib().oracle_route(_p(logits), T, E, k, _p(idx), _p(w), _p(w64))
+    return idx, w, w64
+
+
+def route_hash(logits, token_ids, tid2eid):
+    """Hash routing: the k experts of each token from tid2eid[token_id] (table order) and the
+    soft router's renormalised gate at them. -> topk_idx, topk_w (fp32), topk_w64."""
+    logits = _c(logits, np.float32)
+    tid = _c(token_ids, np.int32)
+    table = _c(tid2eid, np.int32)
+    T, E = logits.shape
+    k = table.shape[1]
+    assert tid.shape == (T,) and np.all((tid >= 0) & (tid < table.shape[0]))
+    idx = np.empty((T, k), np.int32)
+    w = np.empty((T, k), np.float32)
+    w64 = np.empty((T, k), np.float64)
+    lib().oracle_route_hash(_p(logits), _p(tid), _p(table), T, E, k, _p(idx), _p(w), _p(w64))
     return idx, w, w64
 
 

@@ -27,6 +27,11 @@
  *     multiply-add starting from +0; then the 32 lane sums are combined by an xor butterfly
  *     (partner offsets 16, 8, 4, 2, 1, plain fp32 add); then + bias[e] if a bias is given.
  *   - topk_idx lists the chosen experts by descending logit, ties by ascending index.
+ *   - hash routing ("CANN DeepSeek-V4推理优化", MoE 专家模型规格: V4's first layers choose
+ *     experts by hash routing, the others by learned soft routing; the page defines no hash):
+ *     a token's k experts are a fixed function of its token id, given as a table
+ *     tid2eid[vocab][k] of distinct experts and listed in the table's order; the gate weights
+ *     are the soft router's gate at those experts (softmax over all E, keep the k, renormalise).
  *   - slots: expert-major, ascending token within an expert; the shared expert's segment
  *     follows the routed ones, in token order; shared weight 1; no routed scaling factor.
  *   - FP8 E4M3 expert weights with one fp32 scale per 128x128 block: weight = code value * s.
@@ -163,6 +168,28 @@ void oracle_route(const float* logits, int T, int E, int k, int32_t* topk_idx, f
     }
     free(order);
     free(p);
+  }
+}
+
+/* Hash routing: topk_idx[t] = tid2eid[token_ids[t]] (k entries, in the table's order);
+ * topk_w[t, j] = p[e_j] / sum_j' p[e_j'] with p = softmax over all E of the token's logits
+ * (fp64), i.e. the soft router's renormalised gate at the hashed experts. */
+void oracle_route_hash(const float* logits, const int32_t* token_ids, const int32_t* tid2eid,
+                       int T, int E, int k, int32_t* topk_idx, float* topk_w, double* topk_w64) {
+  for (int t = 0; t < T; ++t) {
+    const float* l = logits + (int64_t)t * E;
+    const int32_t* row = tid2eid + (int64_t)token_ids[t] * k;
+    double lmax = -INFINITY, z = 0.0, zsel = 0.0;
+    for (int e = 0; e < E; ++e)
+      if ((double)l[e] > lmax) lmax = (double)l[e];
+    for (int e = 0; e < E; ++e) z += exp((double)l[e] - lmax);
+    for (int j = 0; j < k; ++j) zsel += exp((double)l[row[j]] - lmax) / z;
+    for (int j = 0; j < k; ++j) {
+      const double g = exp((double)l[row[j]] - lmax) / z / zsel;
+      topk_idx[(int64_t)t * k + j] = row[j];
+      topk_w[(int64_t)t * k + j] = (float)g;
+      if (topk_w64) topk_w64[(int64_t)t * k + j] = g;
+    }
   }
 }
 

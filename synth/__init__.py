@@ -24,6 +24,7 @@ _SRC = os.path.join(_HERE, "synth.cu")
 _LIB = os.path.join(_HERE, "libsynth.so")
 
 STREAM_X, STREAM_WG, STREAM_W13, STREAM_W2, STREAM_ZIPF = 1, 2, 3, 4, 6
+STREAM_HASH, STREAM_TOKEN_IDS = 7, 8
 SIGMA_X, SIGMA_W = 1.0, 0.02
 
 
@@ -151,6 +152,26 @@ def zipf_bias(E: int, seed: int, s: float = 1.1, alpha: float = 1.5) -> np.ndarr
     z = rank ** (-s)
     z /= z.sum()
     return (alpha * np.log(z)).astype(np.float32)
+
+
+def hash_table(vocab: int, E: int, k: int, seed: int = 0) -> np.ndarray:
+    """A hash-routing table tid2eid [vocab, k] int32: row v holds k distinct experts, the first
+    k of a Fisher-Yates shuffle of range(E) driven by SplitMix64 stream 7 (draws E*v onwards)."""
+    kh = key(seed, STREAM_HASH)
+    out = np.empty((vocab, k), dtype=np.int32)
+    for v in range(vocab):
+        perm = list(range(E))
+        for i in range(k):
+            j = i + _splitmix_draw(kh, E * v + i) % (E - i)
+            perm[i], perm[j] = perm[j], perm[i]
+        out[v] = perm[:k]
+    return out
+
+
+def token_ids(T: int, vocab: int, seed: int = 0) -> np.ndarray:
+    """Token ids [T] int32 uniform in [0, vocab) (SplitMix64 stream 8)."""
+    kt = key(seed, STREAM_TOKEN_IDS)
+    return np.array([_splitmix_draw(kt, t) % vocab for t in range(T)], dtype=np.int32)
 
 
 def _splitmix_draw(k: int, n: int) -> int:
@@ -291,5 +312,6 @@ def device_inputs(cfg: MoeConfig, device="cuda"):
 
 
 __all__ = ["CONFIGS", "MoeConfig", "get_config", "sweep_config", "build", "normal_bf16",
-           "quantize_e4m3", "quantize_mxfp4", "f32_to_e2m1", "zipf_bias", "host_inputs", "host_expert", "host_x", "host_wg",
+           "quantize_e4m3", "quantize_mxfp4", "f32_to_e2m1", "zipf_bias", "hash_table",
+           "token_ids", "host_inputs", "host_expert", "host_x", "host_wg",
            "host_bias", "device_inputs", "ExpertWeights", "HostInputs"]

@@ -226,6 +226,33 @@ def test_topk_weights_sum_to_one_and_equal_softmax_over_chosen():
         np.testing.assert_allclose(w64[t], softmax(l[t, idx[t]].astype(np.float64)), rtol=1e-13)
 
 
+def test_hash_route_with_the_soft_choices_as_table_is_the_soft_route():
+    # a table that holds, for each token id, exactly the soft router's choice: both routes agree
+    rng = np.random.default_rng(11)
+    T, E, k = 40, 24, 5
+    logits = rng.normal(size=(T, E)).astype(np.float32)
+    idx, w, w64 = oracle.route(logits, k)
+    h_idx, h_w, h_w64 = oracle.route_hash(logits, np.arange(T, dtype=np.int32), idx)
+    np.testing.assert_array_equal(h_idx, idx)
+    np.testing.assert_array_equal(h_w, w)
+    np.testing.assert_allclose(h_w64, w64, rtol=1e-15, atol=0)
+
+
+def test_hash_route_weights_are_the_softmax_of_the_hashed_logits():
+    rng = np.random.default_rng(12)
+    T, E, k, vocab = 33, 16, 4, 50
+    logits = rng.normal(size=(T, E)).astype(np.float32) * 3
+    table = np.stack([rng.permutation(E)[:k] for _ in range(vocab)]).astype(np.int32)
+    tid = rng.integers(0, vocab, T).astype(np.int32)
+    idx, _, w64 = oracle.route_hash(logits, tid, table)
+    np.testing.assert_array_equal(idx, table[tid])  # the table's experts, in its order
+    chosen = np.take_along_axis(logits.astype(np.float64), table[tid], axis=1)
+    np.testing.assert_allclose(w64, softmax(chosen, axis=1), rtol=1e-12, atol=0)
+    # k = 1: the one hashed expert gets weight 1
+    _, _, w1 = oracle.route_hash(logits, tid, table[:, :1])
+    np.testing.assert_array_equal(w1, 1.0)
+
+
 def test_topk_ties_go_to_lower_index():
     x = rand_bf16(np.random.default_rng(3), (4, 256))
     row = rand_bf16(np.random.default_rng(4), (1, 256), 0.02)

@@ -116,3 +116,17 @@ def test_mxfp4_quantiser_scale_rule_and_layout():
     # saturation at 6 of a value below 8
     half_step = np.where(np.abs(f.reshape(8, 128)) / X < 2, 0.25, np.where(np.abs(f.reshape(8, 128)) / X < 4, 0.5, 1.0)) * X
     assert np.all((err <= half_step) | (np.abs(vals) == 6.0))
+
+
+def test_hash_table_rows_are_distinct_experts_and_seeded():
+    t = synth.hash_table(300, 16, 6, seed=3)
+    assert t.shape == (300, 6) and t.dtype == np.int32
+    assert np.all((t >= 0) & (t < 16))
+    assert all(len(set(r)) == 6 for r in t.tolist())
+    np.testing.assert_array_equal(t, synth.hash_table(300, 16, 6, seed=3))
+    assert not np.array_equal(t, synth.hash_table(300, 16, 6, seed=4))
+    # every expert shows up in about the same share of rows
+    counts = np.bincount(t.ravel(), minlength=16)
+    assert counts.min() > 0.7 * counts.mean() and counts.max() < 1.3 * counts.mean()
+    ids = synth.token_ids(1000, 300, seed=3)
+    assert ids.dtype == np.int32 and ids.min() >= 0 and ids.max() < 300
