@@ -114,6 +114,24 @@ MOE_API moe_status moe_route_noalloc(const moe_shape* shape, const void* x, cons
                                      const float* bias, int32_t* topk_idx, float* topk_w,
                                      void* stream);
 
+/* Hash routing ("CANN DeepSeek-V4推理优化", MoE 专家模型规格: V4's first layers pick experts by
+ * hash routing, the others by learned soft routing). The page gives no hash function; here the
+ * choice is a table supplied with the model, and the gate weights are the soft router's:
+ *   token_ids      [T] int32 token ids in [0, vocab).
+ *   tid2eid        [vocab, k] int32: row v holds the k distinct experts (in [0, E)) of token
+ *                  id v.
+ *   topk_idx       [T, k] int32 out: tid2eid[token_ids[t]], in the table's order.
+ *   topk_w         [T, k] fp32 out: softmax over the token's E router logits (computed as in
+ *                  moe_route), kept at those k experts and renormalised -- equal to
+ *                  exp(l_j - max) / sum over the k, in fp32.
+ * x, wg, bias, ws as in moe_route (the logits use ws; the status word is cleared: a layer
+ * starts here). A token id or table entry out of range is recorded as MOE_ERR_DEVICE_BOUNDS
+ * (the entry is replaced by 0). Returns MOE_ERR_INVALID_ARG for vocab < 1. */
+MOE_API moe_status moe_route_hash(const moe_shape* shape, const void* x, const void* wg,
+                                  const float* bias, const int32_t* token_ids,
+                                  const int32_t* tid2eid, int32_t vocab, int32_t* topk_idx,
+                                  float* topk_w, void* ws, size_t ws_bytes, void* stream);
+
 /* Token -> expert permutation ("第 6 章 超節點", 6.2.6).
  *   topk_idx       [T, k] int32, each row k distinct experts in [0, E).
  *   expert_offsets [E+2] int32 out: expert e (< E) owns slots [offsets[e], offsets[e+1]);

@@ -12,7 +12,7 @@ import os
 
 __all__ = ["MoeError", "MoeShape", "MOE_W_BF16", "MOE_W_FP8_E4M3_B128", "MOE_W_MXFP4_E8M0_B32",
            "load", "lib_path",
-           "moe_workspace_size", "moe_route", "moe_route_noalloc", "moe_permute",
+           "moe_workspace_size", "moe_route", "moe_route_hash", "moe_route_noalloc", "moe_permute",
            "moe_expert_ffn", "moe_combine", "moe_forward",
            "moe_check_device_status", "moe_selftest_bounded_wait", "moe_profile_enable",
            "moe_profile_read",
@@ -23,7 +23,8 @@ WDTYPES = {"bf16": MOE_W_BF16, "fp8": MOE_W_FP8_E4M3_B128, "mxfp4": MOE_W_MXFP4_
 STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED",
           -3: "MOE_ERR_WORKSPACE", -4: "MOE_ERR_CUDA", -5: "MOE_ERR_DEVICE_TIMEOUT",
           -6: "MOE_ERR_DEVICE_BOUNDS"}
-EXPORTED = ("moe_workspace_size", "moe_route", "moe_route_noalloc", "moe_permute", "moe_expert_ffn",
+EXPORTED = ("moe_workspace_size", "moe_route", "moe_route_hash", "moe_route_noalloc", "moe_permute",
+            "moe_expert_ffn",
             "moe_combine", "moe_forward",
             "moe_check_device_status", "moe_selftest_bounded_wait", "moe_profile_enable",
             "moe_profile_read", "moe_last_error_string")
@@ -66,6 +67,8 @@ def load():
     L.moe_workspace_size.argtypes = [shp]
     L.moe_route.restype = i32
     L.moe_route.argtypes = [shp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.moe_route_hash.restype = i32
+    L.moe_route_hash.argtypes = [shp, vp, vp, vp, vp, vp, ctypes.c_int32, vp, vp, vp, sz, vp]
     L.moe_route_noalloc.restype = i32
     L.moe_route_noalloc.argtypes = [shp, vp, vp, vp, vp, vp, vp]
     L.moe_permute.restype = i32
@@ -137,6 +140,17 @@ def moe_route(shape, x, wg, bias, topk_idx, topk_w, ws, stream=None, ws_bytes=No
     _check(load().moe_route(ctypes.byref(shape), _ptr(x), _ptr(wg), _ptr(bias), _ptr(topk_idx),
                             _ptr(topk_w), wp, wb if ws_bytes is None else ws_bytes,
                             _stream(stream)), "moe_route")
+
+
+def moe_route_hash(shape, x, wg, bias, token_ids, tid2eid, topk_idx, topk_w, ws, stream=None,
+                   ws_bytes=None):
+    """Hash routing: experts from tid2eid [vocab, k] by token id, the soft router's gate."""
+    wp, wb = _ws(ws)
+    _check(load().moe_route_hash(ctypes.byref(shape), _ptr(x), _ptr(wg), _ptr(bias),
+                                 _ptr(token_ids), _ptr(tid2eid), int(tid2eid.shape[0]),
+                                 _ptr(topk_idx), _ptr(topk_w), wp,
+                                 wb if ws_bytes is None else ws_bytes, _stream(stream)),
+           "moe_route_hash")
 
 
 def moe_route_noalloc(shape, x, wg, bias, topk_idx, topk_w, stream=None):
@@ -236,6 +250,18 @@ class MoeLayer:
         moe_forward(self.shape, x, w["wg"], w.get("bias"), w["w13"], w.get("s13"), w["w2"],
                     w.get("s2"), self.topk_idx, self.topk_w, self.expert_offsets, self.perm_token,
                     self.inv_slot, self.y_perm, self.y, self.ws, stream)
+        return self.y
+
+    def forward_hash(self, x, token_ids, tid2eid, stream=None):
+        """The layer with hash routing (moe_route_hash, then permute, expert FFN, combine)."""
+        w, s = self.w, self.shape
+        moe_route_hash(s, x, w["wg"], w.get("bias"), token_ids, tid2eid, self.topk_idx,
+                       self.topk_w, self.ws, stream)
+        moe_permute(s, self.topk_idx, self.expert_offsets, self.perm_token, self.inv_slot, self.ws,
+                    stream)
+        moe_expert_ffn(s, x, self.perm_token, self.expert_offsets, w["w13"], w.get("s13"),
+                       w["w2"], w.get("s2"), self.y_perm, self.ws, stream)
+        moe_combine(s, self.y_perm, self.inv_slot, self.topk_w, self.y, self.ws, stream)
         return self.y
 
     def forward_steps(self, x, stream=None):

@@ -160,6 +160,33 @@ moe_status moe_route(const moe_shape* shape, const void* x, const void* wg, cons
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_route launch");
 }
 
+moe_status moe_route_hash(const moe_shape* shape, const void* x, const void* wg, const float* bias,
+                          const int32_t* token_ids, const int32_t* tid2eid, int32_t vocab,
+                          int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes,
+                          void* stream) {
+  moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (vocab < 1) return fail(MOE_ERR_INVALID_ARG, "vocab=%d not positive", vocab);
+  if (shape->T > 0) {
+    REQUIRE_PTR(x, 16);
+    REQUIRE_PTR(token_ids, 16);
+    REQUIRE_PTR(topk_idx, 16);
+    REQUIRE_PTR(topk_w, 16);
+  }
+  REQUIRE_PTR(wg, 16);
+  REQUIRE_PTR(tid2eid, 16);
+  if (bias && !aligned(bias, 16)) return fail(MOE_ERR_INVALID_ARG, "bias not 16-byte aligned");
+  WsLayout L;
+  if ((st = check_ws(shape, ws, ws_bytes, &L)) != MOE_OK) return st;
+  cudaError_t e = cudaMemsetAsync(static_cast<char*>(ws) + L.status, 0, sizeof(int),
+                                  static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "moe_route_hash status reset");
+  e = launch_route_hash(*shape, static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(wg),
+                        bias, token_ids, tid2eid, vocab, topk_idx, topk_w, static_cast<char*>(ws),
+                        L, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_route_hash launch");
+}
+
 moe_status moe_route_noalloc(const moe_shape* shape, const void* x, const void* wg,
                              const float* bias, int32_t* topk_idx, float* topk_w, void* stream) {
   moe_status st = check_shape(shape);

@@ -64,6 +64,11 @@ enum PlanRow {
 cudaError_t launch_route(const moe_shape& s, const uint16_t* x, const uint16_t* wg,
                          const float* bias, int32_t* topk_idx, float* topk_w, char* ws,
                          const WsLayout& L, cudaStream_t st);
+// hash routing: logits as in launch_route, experts from a token-id table (router.cu)
+cudaError_t launch_route_hash(const moe_shape& s, const uint16_t* x, const uint16_t* wg,
+                              const float* bias, const int32_t* token_ids,
+                              const int32_t* tid2eid, int vocab, int32_t* topk_idx,
+                              float* topk_w, char* ws, const WsLayout& L, cudaStream_t st);
 cudaError_t launch_permute(const moe_shape& s, const int32_t* topk_idx, int32_t* offsets,
                            int32_t* perm_token, int32_t* inv_slot, char* ws, const WsLayout& L,
                            cudaStream_t st);

@@ -133,6 +133,22 @@ def test_mxfp4_arguments_rejected_before_launch(lib):
     assert moe.moe_workspace_size(moe.MoeShape(16, 256, 8, 2, 128, 1, 3)) == 0
 
 
+def test_hash_route_arguments_rejected_before_launch(lib):
+    s = moe.shape_of(16, 256, 8, 2, 128)
+    sp = ctypes.byref(s)
+    wsz = moe.moe_workspace_size(s)
+    F = FAKE
+    # shape, x, wg, bias, token_ids, tid2eid, vocab, topk_idx, topk_w, ws, ws_bytes, stream
+    rc, msg = call("moe_route_hash", sp, F, F, None, F, F, 0, F, F, F, wsz, None)
+    assert rc == -1 and "vocab=0" in msg
+    rc, msg = call("moe_route_hash", sp, F, F, None, None, F, 100, F, F, F, wsz, None)
+    assert rc == -1 and "token_ids is NULL" in msg
+    rc, msg = call("moe_route_hash", sp, F, F, None, F, F + 4, 100, F, F, F, wsz, None)
+    assert rc == -1 and "tid2eid not 16-byte aligned" in msg
+    rc, msg = call("moe_route_hash", sp, F, F, None, F, F, 100, F, F, F, wsz - 1, None)
+    assert rc == -3
+
+
 def test_binding_raises_moe_error(lib):
     s = moe.shape_of(16, 256, 8, 2, 128)
     with pytest.raises(moe.MoeError) as ei:

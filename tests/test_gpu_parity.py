@@ -343,3 +343,94 @@ def check_full(cfg, name):
     y_ref = oracle.token_outputs(x_h[toks], r_idx[toks], r_w64[toks], experts, shared, cfg.wdtype)
     y_gpu = bf16_host(layer.y)[toks]
     assert_y_close(y_gpu, y_ref, cfg.wdtype, what=name)
+
+
+# ---- hash routing ----------------------------------------------------------------------------
+
+def _hash_inputs(cfg, vocab=97):
+    table = synth.hash_table(vocab, cfg.E, cfg.k, seed=cfg.seed)
+    tid = synth.token_ids(cfg.T, vocab, seed=cfg.seed)
+    return table, tid
+
+
+@pytest.mark.parametrize("over", [{}, {"T": 300, "E": 40, "k": 5},
+                                  {"T": 256, "d": 7168, "E": 256, "k": 8, "f": 128}])
+def test_hash_route_matches_oracle(over):
+    cfg = synth.get_config("tiny", **over)
+    table, tid = _hash_inputs(cfg)
+    x, wg, bias = synth.host_x(cfg), synth.host_wg(cfg), synth.host_bias(cfg)
+    r_idx, _, r_w64 = oracle.route_hash(oracle.router_logits(x, wg, bias), tid, table)
+    s = moe.shape_of(cfg.T, cfg.d, cfg.E, cfg.k, cfg.f, cfg.n_shared, cfg.wdtype)
+    t = torch()
+    ws = t.empty(moe.moe_workspace_size(s), dtype=t.uint8, device="cuda")
+    idx = t.empty(cfg.T, cfg.k, dtype=t.int32, device="cuda")
+    w = t.empty(cfg.T, cfg.k, dtype=t.float32, device="cuda")
+    moe.moe_route_hash(s, bf16_dev(x), bf16_dev(wg), to_dev(bias), to_dev(tid), to_dev(table),
+                       idx, w, ws)
+    moe.moe_check_device_status(ws)
+    np.testing.assert_array_equal(idx.cpu().numpy(), r_idx)
+    np.testing.assert_allclose(w.cpu().numpy(), r_w64, rtol=0, atol=TOL_TOPK_W)
+
+
+def test_hash_route_with_the_soft_choices_as_table_is_bit_identical_to_moe_route():
+    cfg = synth.get_config("tiny", T=200, E=40, k=6)
+    inp = synth.host_inputs(cfg)
+    s = moe.shape_of(cfg.T, cfg.d, cfg.E, cfg.k, cfg.f, cfg.n_shared, cfg.wdtype)
+    t = torch()
+    ws = t.empty(moe.moe_workspace_size(s), dtype=t.uint8, device="cuda")
+    idx = t.empty(cfg.T, cfg.k, dtype=t.int32, device="cuda")
+    w = t.empty(cfg.T, cfg.k, dtype=t.float32, device="cuda")
+    x, wg = bf16_dev(inp.x), bf16_dev(inp.wg)
+    moe.moe_route(s, x, wg, None, idx, w, ws)
+    hidx, hw = t.empty_like(idx), t.empty_like(w)
+    moe.moe_route_hash(s, x, wg, None, t.arange(cfg.T, dtype=t.int32, device="cuda"), idx.clone(),
+                       hidx, hw, ws)
+    moe.moe_check_device_status(ws)
+    assert t.equal(hidx, idx) and t.equal(hw.view(t.int32), w.view(t.int32))
+
+
+@pytest.mark.parametrize("over", [{}, {"wdtype": "fp8"}, {"wdtype": "mxfp4"},
+                                  {"T": 300, "E": 40, "k": 5, "d": 512, "f": 256}])
+def test_hash_routed_layer_matches_oracle(over):
+    cfg = synth.get_config("tiny", **over)
+    inp = synth.host_inputs(cfg)
+    table, tid = _hash_inputs(cfg)
+    w = device_weights(cfg, inp)
+    layer = moe.MoeLayer(cfg.T, cfg.d, cfg.E, cfg.k, cfg.f, cfg.n_shared, cfg.wdtype, w)
+    layer.forward_hash(bf16_dev(inp.x), to_dev(tid), to_dev(table))
+    torch().cuda.synchronize()
+    moe.moe_check_device_status(layer.ws)
+    r_idx, _, r_w64 = oracle.route_hash(oracle.router_logits(inp.x, inp.wg, inp.bias), tid, table)
+    np.testing.assert_array_equal(layer.topk_idx.cpu().numpy(), r_idx)
+    r_off, r_perm, r_inv = oracle.permute(r_idx, cfg.E, cfg.n_shared)
+    np.testing.assert_array_equal(layer.expert_offsets.cpu().numpy(), r_off)
+    np.testing.assert_array_equal(layer.perm_token.cpu().numpy(), r_perm)
+    experts = {e: inp.experts[e] for e in range(cfg.E)}
+    shared = inp.experts[cfg.E] if cfg.n_shared else None
+    y_ref = oracle.token_outputs(inp.x, r_idx, r_w64, experts, shared, cfg.wdtype)
+    assert_y_close(bf16_host(layer.y), y_ref, cfg.wdtype, what="hash-routed layer")
+
+
+def test_hash_route_flags_bad_token_id_and_table_entry_without_faulting():
+    cfg = synth.get_config("tiny")
+    table, tid = _hash_inputs(cfg)
+    s = moe.shape_of(cfg.T, cfg.d, cfg.E, cfg.k, cfg.f, cfg.n_shared, cfg.wdtype)
+    t = torch()
+    ws = t.empty(moe.moe_workspace_size(s), dtype=t.uint8, device="cuda")
+    idx = t.empty(cfg.T, cfg.k, dtype=t.int32, device="cuda")
+    w = t.empty(cfg.T, cfg.k, dtype=t.float32, device="cuda")
+    x, wg = bf16_dev(synth.host_x(cfg)), bf16_dev(synth.host_wg(cfg))
+    for bad_tid, bad_table in ((True, False), (False, True)):
+        tid_b, table_b = tid.copy(), table.copy()
+        if bad_tid:
+            tid_b[3] = table.shape[0]          # one past the last row
+        else:
+            table_b[tid[5], 1] = cfg.E          # an expert that does not exist
+        moe.moe_route_hash(s, x, wg, None, to_dev(tid_b), to_dev(table_b), idx, w, ws)
+        with pytest.raises(moe.MoeError) as err:
+            moe.moe_check_device_status(ws)
+        assert err.value.status == -6
+        assert np.all((idx.cpu().numpy() >= 0) & (idx.cpu().numpy() < cfg.E))
+    # the context is still usable: a clean call passes its check
+    moe.moe_route_hash(s, x, wg, None, to_dev(tid), to_dev(table), idx, w, ws)
+    moe.moe_check_device_status(ws)
