@@ -166,25 +166,66 @@ __device__ __forceinline__ void gather_encode_block(long i, const uint16_t* __re
   xq.s_lo[s * nb + b] = (uint8_t)sb;
 }
 
+// MXFP4 weights, prefill tiles: thread i writes 32-element block i of the slot rows (the same
+// rows as above) as f16, round to nearest, saturating at +-65504 (exact for bf16 values in f16's
+// normal range).
+__device__ __forceinline__ void gather_f16_block(long i, const uint16_t* __restrict__ x,
+                                                 const int32_t* __restrict__ perm_token, int T,
+                                                 long routed, long nq, int d,
+                                                 uint16_t* __restrict__ out, int* status) {
+  const int nb = d >> 5;
+  const long s = i / nb;
+  if (s >= nq) return;
+  const int b = (int)(i - s * nb);
+  int t = s < routed ? __ldg(perm_token + s) : (int)(s - routed);
+  if (t < 0 || t >= T) {
+    record_error(status, MOE_ERR_DEVICE_BOUNDS);
+    t = 0;
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(x + (long)t * d) + 4 * b;
+  uint4* dst = reinterpret_cast<uint4*>(out + s * d) + 4 * b;
+  uint4 w[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) w[j] = __ldg(src + j);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint32_t u[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+      asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;"
+          : "=r"(u[m])
+          : "f"(__uint_as_float(u[m] & 0xFFFF0000u)), "f"(__uint_as_float(u[m] << 16)));
+    dst[j] = make_uint4(u[0], u[1], u[2], u[3]);
+  }
+}
+
+// What the gather writes for the tensor-core passes.
+enum GatherMode : int {
+  kGatherBf16 = 0,  // bf16 and FP8 weights: x rows of the routed slots, bf16
+  kGatherMxTerms = 1,  // MXFP4 decode tiles: the slot rows as two E4M3 terms (xq)
+  kGatherF16 = 2,  // MXFP4 prefill tiles: the slot rows as f16 (x_perm)
+};
+
 // One launch for both: block 0 builds the plan from the expert offsets while the other blocks
-// gather x_perm[s] = x[perm_token[s]] for every routed slot (the tensor-core path's token tiles
-// are contiguous rows for TMA), or, with MXFP4 weights (xq.hi set), encode the first nq slot
-// rows as E4M3 terms. Neither needs the other.
+// gather the token rows the tensor-core passes read as contiguous TMA rows (GatherMode). Neither
+// needs the other.
 __global__ void __launch_bounds__(256) k_plan_gather(const int32_t* __restrict__ offsets,
                                                      PlanArgs a, int32_t* __restrict__ plan,
                                                      const uint16_t* __restrict__ x,
                                                      const int32_t* __restrict__ perm_token, int T,
                                                      long routed, int d,
                                                      uint16_t* __restrict__ x_perm, int* status,
-                                                     mx::Planes xq, long nq) {
+                                                     mx::Planes xq, long nq, int mode) {
   pdl_wait_then_release();
   if (blockIdx.x == 0) {
     plan_block(offsets, a, plan);
     return;
   }
   const long i = (long)(blockIdx.x - 1) * blockDim.x + threadIdx.x;
-  if (xq.hi)
+  if (mode == kGatherMxTerms)
     gather_encode_block(i, x, perm_token, T, routed, nq, d, xq, status);
+  else if (mode == kGatherF16)
+    gather_f16_block(i, x, perm_token, T, routed, nq, d, x_perm, status);
   else
     gather_row_chunks(i, x, perm_token, T, routed, d, x_perm, status);
 }
@@ -248,12 +289,13 @@ struct TileShape {
 
 TileShape tile_shape(const moe_shape& s, bool fp8, bool decode, long routed) {
   TileShape t;
-  if (s.wdtype == MOE_W_MXFP4_E8M0_B32) {
+  if (s.wdtype == MOE_W_MXFP4_E8M0_B32 && decode) {
     t.nt_up = t.nt_dn = tc_mx_tile_tokens(decode, routed, s.E);
     t.mt_up = s.f / 128;
     t.mt_dn = s.d / tc_mx_down_rows(decode, s.d);
     return t;
   }
+  if (s.wdtype == MOE_W_MXFP4_E8M0_B32) fp8 = true;  // the FP8 prefill tiles, f16 operands
   t.nt_up = fp8 ? tc_fp8_tile_tokens(true, decode, routed, s.E) : tc_tile_tokens(true, decode);
   t.nt_dn = fp8 ? tc_fp8_tile_tokens(false, decode, routed, s.E) : tc_tile_tokens(false, decode);
   if (!fp8) {
@@ -273,15 +315,19 @@ TileShape tile_shape(const moe_shape& s, bool fp8, bool decode, long routed) {
 // the T tokens in order, so the lists depend on the shape alone. rows[0] and rows[1]: prefixes
 // over the E+1 experts for the gate/up and the down pass (zero work for the routed experts);
 // rows[2]: the expert offsets the tile decoder reads (entries E and E+1). With MXFP4 weights
-// (xq.hi set) the other blocks encode the shared segment's rows (token t at slot T*k + t).
+// the other blocks write the shared segment's rows (token t at slot T*k + t) in the form the
+// passes read (GatherMode: E4M3 terms or f16).
 __global__ void k_shared_plan(int T, int k, int E, TileShape ts, int32_t* __restrict__ rows,
                               const uint16_t* __restrict__ x, int d, mx::Planes xq,
-                              int* status) {
+                              uint16_t* __restrict__ x16, int mode, int* status) {
   pdl_wait_then_release();
   if (blockIdx.x > 0) {
     const long routed = (long)T * k;
     const long i = (long)(blockIdx.x - 1) * blockDim.x + threadIdx.x + routed * (d >> 5);
-    gather_encode_block(i, x, nullptr, T, routed, routed + T, d, xq, status);
+    if (mode == kGatherMxTerms)
+      gather_encode_block(i, x, nullptr, T, routed, routed + T, d, xq, status);
+    else
+      gather_f16_block(i, x, nullptr, T, routed, routed + T, d, x16, status);
     return;
   }
   const int n = E + 2;
@@ -369,12 +415,13 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32
   }
 
   const PhaseEvents ev = profile_phase_events();
-  // rows the gather writes: the routed slots, plus (MXFP4) the shared segment's encoded rows
+  // rows the gather writes: the routed slots, plus (MXFP4) the shared segment's rows
   const long nq = routed + (mxq ? (long)a.n_shared * s.T : 0);
   const long gather_n = (use_tc && nq > 0) ? nq * (s.d / 8) / kGatherChunks : 0;
+  const int mode = !mxq ? kGatherBf16 : decode ? kGatherMxTerms : kGatherF16;
   cudaError_t e = launch_pdl(k_plan_gather, dim3((unsigned)(1 + (gather_n + 255) / 256)),
                              dim3(256), 0, st, offsets, pa, plan, x, perm_token, s.T, routed, s.d,
-                             a.x_perm, a.status, a.xq, nq);
+                             a.x_perm, a.status, a.xq, nq, mode);
   count_launches(1);
   if (e != cudaSuccess) return e;
   if (ev.begin) record_phase(ev.begin, st);
@@ -481,8 +528,10 @@ cudaError_t launch_forward(const moe_shape& s, const uint16_t* x, const uint16_t
   }
   // MXFP4: the shared segment's rows are encoded here, the routed ones by the routed path's gather
   const long enc = mxq ? (long)s.T * (s.d / 32) : 0;
+  const int mode = decode ? kGatherMxTerms : kGatherF16;
   if ((e = launch_pdl(k_shared_plan, dim3((unsigned)(1 + (enc + 255) / 256)), dim3(256), 0, aux,
-                      s.T, s.k, s.E, ts, rows, x, s.d, a.xq, status)) != cudaSuccess)
+                      s.T, s.k, s.E, ts, rows, x, s.d, a.xq, a.x_perm, mode, status)) !=
+      cudaSuccess)
     return e;
   count_launches(1);
   for (int pass = 0; pass < 2; ++pass) {

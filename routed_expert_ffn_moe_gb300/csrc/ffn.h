@@ -52,5 +52,8 @@ int tc_fp8_wide_tile_tokens();
 int tc_fp8_wide_plan_mtiles(bool gateup, int d, int f);
 cudaError_t launch_tc_fp8_wide(const FfnArgs& a, const int32_t* prefix, bool gateup,
                                cudaStream_t st);
+// the same prefill tiles for MXFP4 weights (dequantised to f16; x and h as f16 rows)
+cudaError_t launch_tc_mx_wide(const FfnArgs& a, const int32_t* prefix, bool gateup,
+                              cudaStream_t st);
 
 }  // namespace moe

@@ -11,6 +11,13 @@
 //   MMA           tcgen05.mma.kind::f16, bf16 x bf16 -> fp32, both operands from smem
 //   epilogue      TMEM -> SiLU(gate) * up -> bf16 h, or the fp32 expert output
 //
+// MXFP4 weights (MX): the same kernel with E2M1 code pairs (128 rows x 64 codes = 32 bytes a row,
+// 32-byte swizzle) and one E8M0 scale per 32 codes of a row. The dequantised weight
+// q * 2^(e-127) is exact in f16 (one cvt per two codes, one f16x2 multiply by the power of two)
+// for blocks whose scale lies in f16's range (2^-24 .. 2^15; a block's largest weight between
+// 2^-19 and 2^16), so the MMA runs on f16 operands: the token rows and h are f16 as well
+// (exact for bf16 x in f16's normal range; h rounded once to f16).
+//
 // The three rings are released independently: a code slot as soon as the converters have read
 // it, a token slot and a converted slot when the MMAs that read them complete. The codes are
 // the stream that comes from HBM, so they get the deepest ring and a producer thread of their
@@ -27,15 +34,17 @@ using namespace ptx;
 using namespace tc;
 
 constexpr uint32_t kCodeTileBytes = kBM * kBK;    // 128 rows x 64 codes = 8 KB
+template <bool MX>
+constexpr uint32_t code_tile_bytes() { return MX ? kCodeTileBytes / 2 : kCodeTileBytes; }
 constexpr int kConvWarps = 8;
 constexpr int kConvThreads = 32 * kConvWarps;
 constexpr int kConvWarp0 = 6;                     // converters: warps 6..13
 constexpr int kTokWarp = kConvWarp0 + kConvWarps; // token producer: warp 14
 constexpr int kThreadsW = 32 * (kTokWarp + 1);
 
-template <int NT, int QS, int BS, int CS, int KA, int ACCB>
+template <int NT, int QS, int BS, int CS, int KA, int ACCB, bool MX>
 struct SmemW {
-  static constexpr uint32_t kQSlot = KA * kCodeTileBytes;        // E4M3 codes of the KA tiles
+  static constexpr uint32_t kQSlot = KA * code_tile_bytes<MX>();  // codes of the KA tiles
   static constexpr uint32_t kBSlot = (uint32_t)NT * kBK * 2;     // bf16 token rows
   static constexpr uint32_t kCSlot = KA * kATileBytes;           // converted bf16 weight tiles
   static constexpr uint32_t kBOff = QS * kQSlot;
@@ -70,21 +79,45 @@ __device__ __forceinline__ void dequant4(uint32_t four, float2 s2, uint32_t& lo,
   hi = *reinterpret_cast<const uint32_t*>(&b23);
 }
 
+// 2^(e-127) as an f16 pair, the exponent clamped to f16's range (subnormals down to 2^-24).
+__device__ __forceinline__ uint32_t f16x2_pow2(uint32_t e) {
+  const int k = min((int)e - 127, 15);
+  const uint32_t h = k >= -14 ? (uint32_t)(k + 15) << 10 : (k >= -24 ? 1u << (k + 24) : 0u);
+  return h | (h << 16);
+}
+
+// Eight E2M1 codes (a word, lowest nibble first) times 2^k as four f16 pairs: each byte converts
+// exactly to an f16 pair, and one f16x2 multiply by the power of two scales it (exact in range).
+__device__ __forceinline__ void dequant_e2m1x8(uint32_t w, uint32_t s2, uint32_t (&o)[4]) {
+  asm("{\n"
+      "  .reg .b8 b0, b1, b2, b3;\n"
+      "  mov.b32 {b0, b1, b2, b3}, %4;\n"
+      "  cvt.rn.f16x2.e2m1x2 %0, b0;\n"
+      "  cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      "  cvt.rn.f16x2.e2m1x2 %2, b2;\n"
+      "  cvt.rn.f16x2.e2m1x2 %3, b3;\n"
+      "}"
+      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+      : "r"(w));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(o[i]) : "r"(s2));
+}
+
 __device__ __forceinline__ void sts_u4(uint32_t addr, const uint4& v) {
   asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
                "r"(v.w)
                : "memory");
 }
 
-template <bool GATEUP, int NT, int QS, int BS, int CS, int KA, int ACCB, int CL>
+template <bool GATEUP, int NT, int QS, int BS, int CS, int KA, int ACCB, int CL, bool MX>
 __global__ void __launch_bounds__(kThreadsW, 1)
     k_tc_ffn_fp8_wide(const __grid_constant__ CUtensorMap tm_w,
                       const __grid_constant__ CUtensorMap tm_b0,
                       const __grid_constant__ CUtensorMap tm_b1,
                       const __grid_constant__ CUtensorMap tm_b0w,
                       const __grid_constant__ CUtensorMap tm_b1w, const TcParams p,
-                      const float* __restrict__ scales) {
-  using S = SmemW<NT, QS, BS, CS, KA, ACCB>;
+                      const void* __restrict__ scales) {
+  using S = SmemW<NT, QS, BS, CS, KA, ACCB, MX>;
   static_assert(S::kTmemCols <= 512 && (S::kTmemCols & (S::kTmemCols - 1)) == 0, "TMEM cols");
   static_assert(!GATEUP || KA == 2, "gate/up tiles pair the gate and up rows");
   extern __shared__ uint8_t smem_raw[];
@@ -173,8 +206,10 @@ __global__ void __launch_bounds__(kThreadsW, 1)
           if (!wait_bar(&q_empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
           uint8_t* st = smem + stage * S::kQSlot;
           mbar_arrive_expect_tx(&q_full[stage], S::kQSlot);
-          tma_load_2d(st, &tm_w, &q_full[stage], kb * kBK, wrow, pol_w);
-          if (KA == 2) tma_load_2d(st + kCodeTileBytes, &tm_w, &q_full[stage], kb * kBK, wrow1, pol_w);
+          const int xq = MX ? kb * (kBK / 2) : kb * kBK;  // in bytes of the code map
+          tma_load_2d(st, &tm_w, &q_full[stage], xq, wrow, pol_w);
+          if (KA == 2)
+            tma_load_2d(st + code_tile_bytes<MX>(), &tm_w, &q_full[stage], xq, wrow1, pol_w);
           if (++stage == QS) { stage = 0; phase ^= 1u; }
         }
       }
@@ -241,7 +276,10 @@ __global__ void __launch_bounds__(kThreadsW, 1)
         Tile t;
         decode(tile, t);
         const int npad = (t.ntok + 15) & ~15;
-        const uint32_t idesc = idesc_bf16(kBM, npad);
+        // bf16 x bf16, or (MX) f16 x f16 (A and B formats 0), fp32 accumulate
+        const uint32_t idesc =
+            MX ? (1u << 4) | ((uint32_t)(npad >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24)
+               : idesc_bf16(kBM, npad);
         if (!wait_bar(&acc_empty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t d0 = tmem_base + acc * S::kAccCols;
@@ -274,8 +312,64 @@ __global__ void __launch_bounds__(kThreadsW, 1)
     }
   } else if (warp < kConvWarp0) {
     // ---------------- epilogue (warps 2..5) ----------------
-    run_epilogue<GATEUP, NT, S::kAccCols, KA, ACCB>(p, total, tmem_base, acc_full, acc_empty,
-                                                    abort_flag, tile0, tstep, PAIR ? rank : -1, CL);
+    run_epilogue<GATEUP, NT, S::kAccCols, KA, ACCB, MX>(p, total, tmem_base, acc_full, acc_empty,
+                                                        abort_flag, tile0, tstep,
+                                                        PAIR ? rank : -1, CL);
+  } else if (MX) {
+    // ---------------- dequantisers, MXFP4 (warps 6..13) ----------------
+    // thread = (row r, 32-code chunk j) of every weight tile a: 16 bytes of code pairs and their
+    // scale byte -> four 16-byte f16 chunks (4j .. 4j+3 of the row's eight)
+    const int ct = threadIdx.x - 32 * kConvWarp0;
+    const int r = ct >> 1, j = ct & 1;
+    const uint8_t* wsc = static_cast<const uint8_t*>(scales);
+    const int ksb = p.K / 32;
+    uint32_t qs = 0, qphase = 0, cs = 0, cphase = 0;
+    bool ok = true;
+    for (int tile = tile0; ok && tile < total; tile += tstep) {
+      Tile t;
+      decode(tile, t);
+      const int wrow = t.e * p.rows_per_expert + t.mt * (GATEUP ? kBM : kBM * KA);
+      const int wrow1 = GATEUP ? wrow + p.f : wrow + kBM;
+      const uint8_t* s0p = wsc + (size_t)(wrow + r) * ksb + j;   // byte for stage kb: + 2 kb
+      const uint8_t* s1p = wsc + (size_t)(wrow1 + r) * ksb + j;
+      // scale bytes run one stage ahead so their load latency hides behind the conversion
+      uint32_t e0 = __ldg(s0p), e1 = KA == 2 ? __ldg(s1p) : 127u;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!wait_bar(&q_full[qs], qphase, abort_flag, p.status) ||
+            !wait_bar(&c_empty[cs], cphase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+        const bool more = kb + 1 < kblocks;
+        const uint32_t e0n = more ? __ldg(s0p + 2 * (kb + 1)) : 127u;
+        const uint32_t e1n = (KA == 2 && more) ? __ldg(s1p + 2 * (kb + 1)) : 127u;
+        const uint32_t src = smem_u32(smem + qs * S::kQSlot);
+        const uint32_t dst = smem_u32(cring + cs * S::kCSlot);
+#pragma unroll
+        for (int a = 0; a < KA; ++a) {
+          // source: 32-byte rows, 32-byte swizzle (16-byte chunk j ^ ((r >> 2) & 1))
+          const uint4 raw =
+              lds_u4(src + a * code_tile_bytes<MX>() + r * 32 + ((j ^ ((r >> 2) & 1)) << 4));
+          const uint32_t s2 = f16x2_pow2(a ? e1 : e0);
+          const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+          const uint32_t rowb = dst + a * kATileBytes + r * 128;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t o[4];
+            dequant_e2m1x8(w[q], s2, o);
+            // destination: 128-byte rows, 128-byte swizzle (16-byte chunk c ^ (r & 7))
+            sts_u4(rowb + (((4 * j + q) ^ (r & 7)) << 4), make_uint4(o[0], o[1], o[2], o[3]));
+          }
+        }
+        fence_proxy_async_smem();      // f16 weights -> visible to the MMA
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&q_empty[qs]);   // this warp is done with the codes of this stage
+          mbar_arrive(&c_full[cs]);
+        }
+        e0 = e0n;
+        e1 = e1n;
+        if (++qs == QS) { qs = 0; qphase ^= 1u; }
+        if (++cs == CS) { cs = 0; cphase ^= 1u; }
+      }
+    }
   } else {
     // ---------------- dequantisers (warps 6..13) ----------------
     // task = (weight tile a, row r, 16-code chunk j): 16 codes -> two 16-byte bf16 chunks
@@ -286,7 +380,7 @@ __global__ void __launch_bounds__(kThreadsW, 1)
     for (int tile = tile0; ok && tile < total; tile += tstep) {
       Tile t;
       decode(tile, t);
-      const float* sc = scales + (size_t)t.e * (p.rows_per_expert / 128) * kbl;
+      const float* sc = static_cast<const float*>(scales) + (size_t)t.e * (p.rows_per_expert / 128) * kbl;
       const int rb0 = GATEUP ? t.mt : t.mt * KA;   // scale row block of the first weight tile
       const int rb1 = GATEUP ? p.f / 128 + t.mt : rb0 + 1;
       // scales run one stage ahead so their load latency hides behind the conversion
@@ -342,13 +436,13 @@ __global__ void __launch_bounds__(kThreadsW, 1)
   }
 }
 
-template <bool GATEUP, int NT, int QS, int BS, int CS, int KA, int ACCB, int CL>
+template <bool GATEUP, int NT, int QS, int BS, int CS, int KA, int ACCB, int CL, bool MX>
 cudaError_t launch_variant(const CUtensorMap& w, const CUtensorMap& b0, const CUtensorMap& b1,
                            const CUtensorMap& b0w, const CUtensorMap& b1w, const TcParams& p,
-                           const float* scales, cudaStream_t st) {
-  using S = SmemW<NT, QS, BS, CS, KA, ACCB>;
+                           const void* scales, cudaStream_t st) {
+  using S = SmemW<NT, QS, BS, CS, KA, ACCB, MX>;
   static_assert(S::kTotal <= 227 * 1024, "shared memory");
-  auto kern = k_tc_ffn_fp8_wide<GATEUP, NT, QS, BS, CS, KA, ACCB, CL>;
+  auto kern = k_tc_ffn_fp8_wide<GATEUP, NT, QS, BS, CS, KA, ACCB, CL, MX>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)S::kTotal);
   if (e != cudaSuccess) return e;
@@ -382,14 +476,17 @@ int cluster_size(bool gateup, int d, int f) {
 // One pass with kNT-token tiles; rings (codes, tokens, converted weights): 4/3/2 slots for
 // paired weight tiles (224 KB of shared memory), 8/3/3 for single tiles; fewer token slots
 // measured slower.
-template <int CL>
-cudaError_t launch_pass(const Maps& m, const TcParams& p, const float* sc, bool gateup, bool paired,
-                        cudaStream_t st) {
+template <int CL, bool MX>
+cudaError_t launch_pass(const Maps& m, const TcParams& p, const void* sc, bool gateup,
+                        bool paired, cudaStream_t st) {
   if (gateup)
-    return launch_variant<true, kNT, 4, 3, 2, 2, 1, CL>(m.w, m.b0, m.b1, m.b0w, m.b1w, p, sc, st);
+    return launch_variant<true, kNT, 4, 3, 2, 2, 1, CL, MX>(m.w, m.b0, m.b1, m.b0w, m.b1w, p, sc,
+                                                            st);
   if (paired)
-    return launch_variant<false, kNT, 4, 3, 2, 2, 1, CL>(m.w, m.b0, m.b1, m.b0w, m.b1w, p, sc, st);
-  return launch_variant<false, kNT, 8, 3, 3, 1, 2, 1>(m.w, m.b0, m.b1, m.b0w, m.b1w, p, sc, st);
+    return launch_variant<false, kNT, 4, 3, 2, 2, 1, CL, MX>(m.w, m.b0, m.b1, m.b0w, m.b1w, p, sc,
+                                                             st);
+  return launch_variant<false, kNT, 8, 3, 3, 1, 2, 1, MX>(m.w, m.b0, m.b1, m.b0w, m.b1w, p, sc,
+                                                          st);
 }
 
 }  // namespace
@@ -436,10 +533,54 @@ cudaError_t launch_tc_fp8_wide(const FfnArgs& a, const int32_t* prefix, bool gat
     m.b1w = m.b0w;
   }
   if (e != cudaSuccess) return e;
-  const float* sc = static_cast<const float*>(gateup ? a.s13 : a.s2);
+  const void* sc = gateup ? a.s13 : a.s2;
   const bool paired = paired_tiles(gateup, a.d);
-  if (cl == 2) return launch_pass<2>(m, p, sc, gateup, paired, st);
-  return launch_pass<1>(m, p, sc, gateup, paired, st);
+  if (cl == 2) return launch_pass<2, false>(m, p, sc, gateup, paired, st);
+  return launch_pass<1, false>(m, p, sc, gateup, paired, st);
+}
+
+// MXFP4 weights on the same prefill tiles: x (all slot rows, the shared segment included) and h
+// are f16 rows in the workspace (x_perm and h), so the shared expert's token map is the slot
+// rows from T*k on.
+cudaError_t launch_tc_mx_wide(const FfnArgs& a, const int32_t* prefix, bool gateup,
+                              cudaStream_t st) {
+  TcParams p{};
+  p.T = a.T; p.k = a.k; p.E = a.E; p.n_shared = a.n_shared;
+  p.f = a.f; p.d = a.d;
+  p.K = gateup ? a.d : a.f;
+  p.mtiles = tc_fp8_wide_plan_mtiles(gateup, a.d, a.f);
+  p.rows_per_expert = gateup ? 2 * a.f : a.d;
+  p.offsets = a.offsets;
+  p.prefix = prefix;
+  p.h = a.h;
+  p.y_perm = a.y_perm;
+  p.status = a.status;
+  const int cl = cluster_size(gateup, a.d, a.f);
+  const uint32_t wide_rows = kNT / cl;
+  const uint64_t E1 = (uint64_t)a.E + a.n_shared;
+  const uint64_t routed = (uint64_t)a.T * a.k;
+  const uint64_t slots = routed + (uint64_t)a.T;  // rows of the workspace's f16 x and h
+  Maps m;
+  cudaError_t e;
+  if (gateup) {
+    const uint16_t* xs = a.x_perm + routed * (uint64_t)a.d;  // the shared segment's rows
+    e = encode_u8_2d(&m.w, a.w13, E1 * 2 * a.f, a.d / 2, kBM, 32);
+    if (e == cudaSuccess) e = encode_bf16_2d(&m.b0, a.x_perm, slots, a.d, kBoxRows);
+    if (e == cudaSuccess) e = encode_bf16_2d(&m.b1, xs, a.T, a.d, kBoxRows);
+    if (e == cudaSuccess) e = encode_bf16_2d(&m.b0w, a.x_perm, slots, a.d, wide_rows);
+    if (e == cudaSuccess) e = encode_bf16_2d(&m.b1w, xs, a.T, a.d, wide_rows);
+  } else {
+    e = encode_u8_2d(&m.w, a.w2, E1 * a.d, a.f / 2, kBM, 32);
+    if (e == cudaSuccess) e = encode_bf16_2d(&m.b0, a.h, slots, a.f, kBoxRows);
+    if (e == cudaSuccess) e = encode_bf16_2d(&m.b0w, a.h, slots, a.f, wide_rows);
+    m.b1 = m.b0;
+    m.b1w = m.b0w;
+  }
+  if (e != cudaSuccess) return e;
+  const void* sc = gateup ? a.s13 : a.s2;
+  const bool paired = paired_tiles(gateup, a.d);
+  if (cl == 2) return launch_pass<2, true>(m, p, sc, gateup, paired, st);
+  return launch_pass<1, true>(m, p, sc, gateup, paired, st);
 }
 
 }  // namespace moe

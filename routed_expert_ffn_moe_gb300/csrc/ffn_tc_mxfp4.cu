@@ -452,10 +452,11 @@ cudaError_t encode_e2m1_2d(CUtensorMap* m, const void* base, uint64_t rows, uint
 
 }  // namespace
 
-// Token tile by batch: 16 tokens while experts average at most 4 routed tokens, 32 up to 16, 64
-// up to the decode bound, 128 for prefill batches.
+// Token tile of the decode batches: 16 tokens while experts average at most 4 routed tokens, 32
+// up to 16, 64 up to the decode bound. (Prefill batches run the f16 prefill tiles of
+// ffn_tc_fp8_wide.cu.)
 int tc_mx_tile_tokens(bool decode, long routed, int E) {
-  if (!decode) return 128;
+  (void)decode;
   return routed > 16L * E ? 64 : routed > 4L * E ? 32 : 16;
 }
 
@@ -465,6 +466,7 @@ int tc_mx_down_rows(bool decode, int d) { return decode && d % 256 == 0 ? 2 * kB
 
 cudaError_t launch_tc_mx(const FfnArgs& a, const int32_t* prefix, bool gateup, bool decode,
                          cudaStream_t st) {
+  if (!decode) return launch_tc_mx_wide(a, prefix, gateup, st);
   TcParams p{};
   p.T = a.T; p.k = a.k; p.E = a.E; p.n_shared = a.n_shared;
   p.f = a.f; p.d = a.d;
@@ -494,10 +496,6 @@ cudaError_t launch_tc_mx(const FfnArgs& a, const int32_t* prefix, bool gateup, b
   if (e == cudaSuccess) e = encode_u8_2d(&lo, tok.lo, slots ? slots : 1, K, kBoxRows);
   if (e != cudaSuccess) return e;
   const int nt = tc_mx_tile_tokens(decode, (long)routed, a.E);
-  if (nt == 128) {
-    if (gateup) return launch_variant<true, 128, 3, 2, 1, false>(w, hi, lo, p, q, st);
-    return launch_variant<false, 128, 4, 1, 2, false>(w, hi, lo, p, q, st);
-  }
   if (nt == 64) {
     if (gateup) return launch_variant<true, 64, 4, 2, 1, true>(w, hi, lo, p, q, st);
     if (dn_rows == 2 * kBM) return launch_variant<false, 64, 4, 2, 1, true>(w, hi, lo, p, q, st);

@@ -42,10 +42,11 @@ inline WsLayout ws_layout(const moe_shape& s) {
   L.plan = take((size_t)kPlanRows * (E + 2) * 4 + 256);
   const size_t slots = T * k + (size_t)s.n_shared * T;
   const bool mxfp4 = s.wdtype == MOE_W_MXFP4_E8M0_B32;
-  // bf16 / E4M3 weights: gathered bf16 token rows and bf16 h. MXFP4 weights: both as two E4M3
-  // terms with their scales (x before the gate/up pass, h before the down pass).
-  L.x_perm = take(mxfp4 ? 0 : T * k * (size_t)s.d * 2);
-  L.h = take(mxfp4 ? 0 : slots * (size_t)s.f * 2);
+  // bf16 / E4M3 weights: gathered bf16 token rows and bf16 h. MXFP4 weights: f16 x (every
+  // slot, the shared segment included) and f16 h for the prefill tiles, and both as two E4M3
+  // terms with their scales for the decode tiles (xq, hq).
+  L.x_perm = take((mxfp4 ? slots : T * k) * (size_t)s.d * 2);
+  L.h = take(slots * (size_t)s.f * 2);
   L.shared = take(3 * (E + 2) * 4);
   L.xq = take(mxfp4 ? slots * (2 * (size_t)s.d + 2 * (size_t)(s.d / 32)) : 0);
   L.hq = take(mxfp4 ? slots * (2 * (size_t)s.f + 2 * (size_t)(s.f / 32)) : 0);
@@ -185,6 +186,13 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) {
   uint16_t r;
   asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(v));
   return r;
+}
+
+// fp32 -> f16, round to nearest even, magnitudes beyond the largest finite f16 saturate to it.
+__device__ __forceinline__ uint16_t f32_to_f16_satfinite(float v) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(0.f), "f"(v));
+  return (uint16_t)(r & 0xFFFFu);
 }
 
 // Exclusive scan of one int per thread over a block of up to 1024 threads; returns the

@@ -98,8 +98,9 @@ __device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity, int* s
 // tile, wait for its accumulator, read it 16 columns at a time, and store SiLU(gate) * up as
 // bf16 h (gate/up pass: gate in columns [0, NT), up in [NT, 2NT)) or the fp32 expert output
 // (down pass: KA weight tiles of 128 output rows each, tile a in columns [a*NT, (a+1)*NT));
-// then hand the accumulator back. ACCB accumulator buffers (1 or 2) rotate.
-template <bool GATEUP, int NT, uint32_t ACC_COLS, int KA = 1, int ACCB = 2>
+// then hand the accumulator back. ACCB accumulator buffers (1 or 2) rotate. H_F16 writes h as
+// f16 (round to nearest, saturating at +-65504) instead of bf16.
+template <bool GATEUP, int NT, uint32_t ACC_COLS, int KA = 1, int ACCB = 2, bool H_F16 = false>
 // Tiles tile0, tile0 + tstep, ...; cl_rank >= 0 marks clusters of cl CTAs, where a listed tile
 // is a group of cl consecutive m-tiles and this CTA takes m-tile cl * mt + cl_rank.
 __device__ __forceinline__ void run_epilogue(const TcParams& p, int total, uint32_t tmem_base,
@@ -131,7 +132,8 @@ __device__ __forceinline__ void run_epilogue(const TcParams& p, int total, uint3
           if (n < t.ntok) {
             const float gv = __uint_as_float(g[j]), uv = __uint_as_float(u[j]);
             const float silu = gv / (1.0f + __expf(-gv));
-            p.h[(size_t)(t.slot0 + n) * p.f + orow] = f32_to_bf16_rn(silu * uv);
+            p.h[(size_t)(t.slot0 + n) * p.f + orow] =
+                H_F16 ? f32_to_f16_satfinite(silu * uv) : f32_to_bf16_rn(silu * uv);
           }
         }
       }
@@ -204,8 +206,8 @@ inline cudaError_t encode_bf16_2d(CUtensorMap* m, const void* base, uint64_t row
 }
 
 
-// Row-major [rows, cols] byte matrix (E4M3 codes), box of box_rows x box_cols bytes, swizzled
-// to match the box width (128-byte rows: 128-byte swizzle; 64-byte rows: 64-byte swizzle).
+// Row-major [rows, cols] byte matrix (E4M3 codes, or MXFP4 code pairs), box of box_rows x
+// box_cols bytes, swizzled to match the box width (128, 64 or 32 bytes).
 inline cudaError_t encode_u8_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
                                 uint32_t box_rows, uint32_t box_cols = 128) {
   EncodeTiledFn fn = encode_fn();
@@ -216,7 +218,9 @@ inline cudaError_t encode_u8_2d(CUtensorMap* m, const void* base, uint64_t rows,
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        box_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                        box_cols == 64   ? CU_TENSOR_MAP_SWIZZLE_64B
+                        : box_cols == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                         : CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
