@@ -13,11 +13,9 @@
 //             token rows' two E4M3 terms (mx_common.cuh) -> shared-memory ring
 //   scales    4 warps: the weight rows' and the token rows' scale words -> TMEM; the MMA reads
 //             row m's word from TMEM lane m, column (m / 32) of the word group
-//   MMA       per 32-wide K block and weight tile: decode tiles (FOLD) put the hi and the lo
-//             term rows of the tokens one after the other in one B tile, so one MMA of N = 2 x
-//             tokens covers both and the epilogue adds the two halves; prefill tiles (128 tokens,
-//             where N = 256 would leave TMEM no room for the scale words) run one MMA per term
-//             into the same accumulator
+//   MMA       per 32-wide K block and weight tile: the hi and the lo term rows of the tokens sit
+//             one after the other in one B tile, so one MMA of N = 2 x tokens covers both and the
+//             epilogue adds the two halves
 //   epilogue  gate/up: SiLU(gate) * up, written straight as the down pass's two E4M3 terms;
 //             down: the fp32 expert output
 //
@@ -51,7 +49,7 @@ struct MxParams {
 
 // A ring stage holds SUB consecutive 128-wide K slices (each: KA weight tiles and the token
 // tile): the per-stage hand-offs (barrier waits, commit) are paid once per SUB slices.
-template <bool GATEUP, int NT, int STAGES, int KA, int ACCB, bool FOLD, int SUB>
+template <bool GATEUP, int NT, int STAGES, int KA, int ACCB, int SUB>
 struct SmemMx {
   static constexpr uint32_t kBTile = (uint32_t)NT * kMxK;  // one term's token tile
   static constexpr uint32_t kSliceBytes = KA * kWSmem + 2 * kBTile;
@@ -59,11 +57,10 @@ struct SmemMx {
   static constexpr uint32_t kTilesBytes = STAGES * kStageBytes;
   static constexpr uint32_t kBarBytes = 8 * (2 * STAGES + 2 * ACCB) + 16;
   static constexpr uint32_t kTotal = kTilesBytes + kBarBytes + 1024;
-  static constexpr uint32_t kAccN = FOLD ? 2 * NT : NT;  // accumulator columns per weight tile
+  static constexpr uint32_t kAccN = 2 * NT;  // accumulator columns per weight tile: hi, then lo
   static constexpr uint32_t kAccCols = KA * kAccN;
-  // scale words of the token rows: one 4-column group per 128 B rows (folded: hi then lo rows),
-  // or one group per term
-  static constexpr uint32_t kBSfCols = FOLD ? (2 * NT <= 128 ? 4 : 8) : 8;
+  // scale words of the token B rows (hi rows, then lo rows): one 4-column group per 128 rows
+  static constexpr uint32_t kBSfCols = 2 * NT <= 128 ? 4 : 8;
   // per stage: a 4-column group per (slice, weight tile), then the token groups of each slice
   static constexpr uint32_t kSfCols = SUB * (4 * KA + kBSfCols);
   static constexpr uint32_t kUsedCols = ACCB * kAccCols + STAGES * kSfCols;
@@ -84,7 +81,7 @@ __device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
 // Gate/up epilogue (warps 2..5): h = SiLU(gate) * up for the tile's tokens, encoded as two E4M3
 // terms per element with one scale byte per term and 32 consecutive features -- exactly the 32
 // lanes of one warp, so the block maximum is a warp reduction.
-template <int NT, int ACCB, uint32_t ACC_COLS, uint32_t ACC_N, bool FOLD>
+template <int NT, int ACCB, uint32_t ACC_COLS, uint32_t ACC_N>
 __device__ __forceinline__ void gateup_epilogue(const TcParams& p, const MxParams& q, int total,
                                                 uint32_t tmem_base, uint64_t* acc_full,
                                                 uint64_t* acc_empty, volatile int* abort_flag) {
@@ -105,12 +102,10 @@ __device__ __forceinline__ void gateup_epilogue(const TcParams& p, const MxParam
       uint32_t g[16], u[16], g2[16], u2[16];
       tmem_ld16(tbase + c0, g);
       tmem_ld16(tbase + ACC_N + c0, u);
-      if (FOLD) {  // the lo term's products, npad columns further on
-        tmem_ld16(tbase + npad + c0, g2);
-        tmem_ld16(tbase + ACC_N + npad + c0, u2);
-      }
+      tmem_ld16(tbase + npad + c0, g2);  // the lo term's products, npad columns further on
+      tmem_ld16(tbase + ACC_N + npad + c0, u2);
       tmem_ld_wait2(g, u);
-      if (FOLD) tmem_ld_wait2(g2, u2);
+      tmem_ld_wait2(g2, u2);
 #pragma unroll
       for (int j = 0; j < 16; j += 2) {
         const int n = c0 + j;
@@ -118,11 +113,8 @@ __device__ __forceinline__ void gateup_epilogue(const TcParams& p, const MxParam
         float v[2];
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
-          float gv = __uint_as_float(g[j + i]), uv = __uint_as_float(u[j + i]);
-          if (FOLD) {
-            gv += __uint_as_float(g2[j + i]);
-            uv += __uint_as_float(u2[j + i]);
-          }
+          const float gv = __uint_as_float(g[j + i]) + __uint_as_float(g2[j + i]);
+          const float uv = __uint_as_float(u[j + i]) + __uint_as_float(u2[j + i]);
           v[i] = n + i < t.ntok ? gv / (1.0f + __expf(-gv)) * uv : 0.f;
         }
         uint32_t hi0, lo0, hi1, lo1, a0, b0, a1, b1;
@@ -151,10 +143,10 @@ __device__ __forceinline__ void gateup_epilogue(const TcParams& p, const MxParam
   }
 }
 
-// Down epilogue of the folded tiles (warps 2..5): the expert output of token n and weight row r
-// is the sum of the hi-term column n and the lo-term column npad + n of the accumulator.
+// Down epilogue (warps 2..5): the expert output of token n and weight row r is the sum of the
+// hi-term column n and the lo-term column npad + n of the accumulator.
 template <int NT, int KA, int ACCB, uint32_t ACC_COLS, uint32_t ACC_N>
-__device__ __forceinline__ void down_epilogue_folded(const TcParams& p, int total,
+__device__ __forceinline__ void down_epilogue(const TcParams& p, int total,
                                                      uint32_t tmem_base, uint64_t* acc_full,
                                                      uint64_t* acc_empty,
                                                      volatile int* abort_flag) {
@@ -193,13 +185,13 @@ __device__ __forceinline__ void down_epilogue_folded(const TcParams& p, int tota
   }
 }
 
-template <bool GATEUP, int NT, int STAGES, int KA, int ACCB, bool FOLD, int SUB>
+template <bool GATEUP, int NT, int STAGES, int KA, int ACCB, int SUB>
 __global__ void __launch_bounds__(kThreadsMx, 1)
     k_tc_ffn_mx(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_hi,
                 const __grid_constant__ CUtensorMap tm_lo, const TcParams p, const MxParams q) {
-  using S = SmemMx<GATEUP, NT, STAGES, KA, ACCB, FOLD, SUB>;
+  using S = SmemMx<GATEUP, NT, STAGES, KA, ACCB, SUB>;
   static_assert(S::kUsedCols <= 512, "TMEM columns");
-  static_assert(!FOLD || 2 * NT <= 256, "MMA N");
+  static_assert(2 * NT <= 256, "MMA N");
   static_assert(!GATEUP || KA == 2, "gate/up tiles pair the gate and up rows");
   static_assert(NT % 16 == 0 && NT >= 16 && NT <= 128, "token tile");
   extern __shared__ uint8_t smem_raw[];
@@ -273,8 +265,8 @@ __global__ void __launch_bounds__(kThreadsMx, 1)
             for (int i = 0; i < nbox; ++i) {
               tma_load_2d(bt + i * kTBox, &tm_hi, &full[stage], xk, t.slot0 + i * kBoxRows,
                           pol_b);
-              // folded: the lo rows right after the tile's nbox boxes of hi rows
-              tma_load_2d(bt + (FOLD ? (nbox + i) * kTBox : S::kBTile + i * kTBox), &tm_lo,
+              // the lo rows right after the tile's nbox boxes of hi rows
+              tma_load_2d(bt + (nbox + i) * kTBox, &tm_lo,
                           &full[stage], xk, t.slot0 + i * kBoxRows, pol_b);
             }
           }
@@ -303,7 +295,7 @@ __global__ void __launch_bounds__(kThreadsMx, 1)
         uint32_t idesc[kMxK / 32];
 #pragma unroll
         for (int kk = 0; kk < kMxK / 32; ++kk)
-          idesc[kk] = idesc_mx_e2m1_e4m3(kBM, FOLD ? 2 * npad : npad, kk, kk);
+          idesc[kk] = idesc_mx_e2m1_e4m3(kBM, 2 * npad, kk, kk);
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!wait_bar(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
@@ -313,13 +305,11 @@ __global__ void __launch_bounds__(kThreadsMx, 1)
             const uint32_t a0 = smem_u32(smem + stage * S::kStageBytes + sb * S::kSliceBytes);
             const uint64_t ad = sw128_desc(a0 + o * kWSmem);
             const uint64_t bh = sw128_desc(a0 + KA * kWSmem);
-            const uint64_t bl = sw128_desc(a0 + KA * kWSmem + S::kBTile);
             const uint32_t sfa = sfc + 4 * (sb * KA + o);
             const uint32_t sfb = sfc + 4 * KA * SUB + sb * S::kBSfCols;
 #pragma unroll
             for (int kk = 0; kk < kMxK / 32; ++kk) {
               mma_mx(dp, ad + 2 * kk, bh + 2 * kk, idesc[kk], sfa, sfb, (kb | sb | kk) ? 1u : 0u);
-              if (!FOLD) mma_mx(dp, ad + 2 * kk, bl + 2 * kk, idesc[kk], sfa, sfb + 4, 1u);
             }
           }
           mma_commit(&empty[stage]);
@@ -333,23 +323,19 @@ __global__ void __launch_bounds__(kThreadsMx, 1)
   } else if (warp < 6) {
     // ---------------- epilogue (warps 2..5) ----------------
     if (GATEUP)
-      gateup_epilogue<NT, ACCB, S::kAccCols, S::kAccN, FOLD>(p, q, total, tmem_base, acc_full,
-                                                             acc_empty, abort_flag);
-    else if (FOLD)
-      down_epilogue_folded<NT, KA, ACCB, S::kAccCols, S::kAccN>(p, total, tmem_base, acc_full,
-                                                                acc_empty, abort_flag);
+      gateup_epilogue<NT, ACCB, S::kAccCols, S::kAccN>(p, q, total, tmem_base, acc_full,
+                                                       acc_empty, abort_flag);
     else
-      run_epilogue<false, NT, S::kAccCols, KA, ACCB>(p, total, tmem_base, acc_full, acc_empty,
-                                                     abort_flag);
+      down_epilogue<NT, KA, ACCB, S::kAccCols, S::kAccN>(p, total, tmem_base, acc_full,
+                                                         acc_empty, abort_flag);
   } else if (warp < 10) {
     // ---------------- scale writers (warps 6..9) ----------------
     // Warp of lane quadrant qd writes, per K slice of a stage: weight row 32*qd + lane's word
     // (its four K-block scales of the slice) at column qd of the slice's group for that weight
     // tile, and the B rows' words in every lane quadrant, B row 32*c + lane in column c of the
     // slice's token groups, which is where the MMA reads them. B row r is token r's hi term
-    // (r < npad) and token r - npad's lo term after it when folded; else the hi and the lo rows
-    // have a group each. Then it arrives on the stage's full barrier. The words are loaded
-    // kSfAhead slices ahead of their store (a register ring).
+    // (r < npad) and token r - npad's lo term after it. Then it arrives on the stage's full
+    // barrier. The words are loaded kSfAhead slices ahead of their store (a register ring).
     const int qd = warp & 3;
     const uint32_t lane_base = tmem_base + ((uint32_t)(qd * 32) << 16);
     const int nslices = kblocks * SUB;
@@ -369,9 +355,9 @@ __global__ void __launch_bounds__(kThreadsMx, 1)
         a[1] = KA == 2 ? ldg_u32(wa + wstep + 4 * ks) : 0u;
 #pragma unroll
         for (int c = 0; c < (int)S::kBSfCols; ++c) {
-          int n = 32 * (FOLD ? c : (c & 3)) + lane;  // token of B row 32c + lane
-          bool lo = FOLD ? n >= npad : c >= 4;
-          if (FOLD && lo) n -= npad;
+          int n = 32 * c + lane;  // token of B row 32c + lane
+          const bool lo = n >= npad;
+          if (lo) n -= npad;
           b[c] = 0x7F7F7F7Fu;
           if (n < t.ntok)
             b[c] = ldg_u32((lo ? q.t_scale_lo : q.t_scale_hi) + (size_t)(t.slot0 + n) * ksb +
@@ -420,12 +406,12 @@ __global__ void __launch_bounds__(kThreadsMx, 1)
   }
 }
 
-template <bool GATEUP, int NT, int STAGES, int KA, int ACCB, bool FOLD, int SUB = 1>
+template <bool GATEUP, int NT, int STAGES, int KA, int ACCB, int SUB = 1>
 cudaError_t launch_variant(const CUtensorMap& w, const CUtensorMap& hi, const CUtensorMap& lo,
                            const TcParams& p, const MxParams& q, cudaStream_t st) {
-  using S = SmemMx<GATEUP, NT, STAGES, KA, ACCB, FOLD, SUB>;
+  using S = SmemMx<GATEUP, NT, STAGES, KA, ACCB, SUB>;
   static_assert(S::kTotal <= 227 * 1024, "shared memory");
-  auto kern = k_tc_ffn_mx<GATEUP, NT, STAGES, KA, ACCB, FOLD, SUB>;
+  auto kern = k_tc_ffn_mx<GATEUP, NT, STAGES, KA, ACCB, SUB>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)S::kTotal);
   if (e != cudaSuccess) return e;
@@ -459,9 +445,11 @@ int tc_mx_tile_tokens(bool decode, long routed, int E) {
   return routed > 16L * E ? 64 : routed > 4L * E ? 32 : 16;
 }
 
-// Down tiles pair two 128-row tiles of W_d (decode tiles, when d allows it); prefill down tiles
-// take one, so that two accumulators of 128 tokens still fit TMEM beside the scale words.
-int tc_mx_down_rows(bool decode, int d) { return decode && d % 256 == 0 ? 2 * kBM : kBM; }
+// Down tiles pair two 128-row tiles of W_d when d allows it (two MMA issuers, one a tile).
+int tc_mx_down_rows(bool decode, int d) {
+  (void)decode;
+  return d % 256 == 0 ? 2 * kBM : kBM;
+}
 
 cudaError_t launch_tc_mx(const FfnArgs& a, const int32_t* prefix, bool gateup, bool decode,
                          cudaStream_t st) {
@@ -496,32 +484,32 @@ cudaError_t launch_tc_mx(const FfnArgs& a, const int32_t* prefix, bool gateup, b
   if (e != cudaSuccess) return e;
   const int nt = tc_mx_tile_tokens(decode, (long)routed, a.E);
   if (nt == 64) {
-    if (gateup) return launch_variant<true, 64, 4, 2, 1, true>(w, hi, lo, p, q, st);
-    if (dn_rows == 2 * kBM) return launch_variant<false, 64, 4, 2, 1, true>(w, hi, lo, p, q, st);
-    return launch_variant<false, 64, 6, 1, 2, true>(w, hi, lo, p, q, st);
+    if (gateup) return launch_variant<true, 64, 4, 2, 1>(w, hi, lo, p, q, st);
+    if (dn_rows == 2 * kBM) return launch_variant<false, 64, 4, 2, 1>(w, hi, lo, p, q, st);
+    return launch_variant<false, 64, 6, 1, 2>(w, hi, lo, p, q, st);
   }
   // Two 128-wide K slices per stage where K allows (measured: V4-Pro decode 1148 -> 1053 us; the
   // MMA-issuing thread's per-stage waits and commit are paid half as often)
   const bool sub2 = K % 256 == 0;
   if (nt == 16) {
     if (sub2) {
-      if (gateup) return launch_variant<true, 16, 3, 2, 2, true, 2>(w, hi, lo, p, q, st);
+      if (gateup) return launch_variant<true, 16, 3, 2, 2, 2>(w, hi, lo, p, q, st);
       if (dn_rows == 2 * kBM)
-        return launch_variant<false, 16, 3, 2, 2, true, 2>(w, hi, lo, p, q, st);
-      return launch_variant<false, 16, 5, 1, 2, true, 2>(w, hi, lo, p, q, st);
+        return launch_variant<false, 16, 3, 2, 2, 2>(w, hi, lo, p, q, st);
+      return launch_variant<false, 16, 5, 1, 2, 2>(w, hi, lo, p, q, st);
     }
-    if (gateup) return launch_variant<true, 16, 6, 2, 2, true>(w, hi, lo, p, q, st);
-    if (dn_rows == 2 * kBM) return launch_variant<false, 16, 6, 2, 2, true>(w, hi, lo, p, q, st);
-    return launch_variant<false, 16, 10, 1, 2, true>(w, hi, lo, p, q, st);
+    if (gateup) return launch_variant<true, 16, 6, 2, 2>(w, hi, lo, p, q, st);
+    if (dn_rows == 2 * kBM) return launch_variant<false, 16, 6, 2, 2>(w, hi, lo, p, q, st);
+    return launch_variant<false, 16, 10, 1, 2>(w, hi, lo, p, q, st);
   }
   if (sub2) {
-    if (gateup) return launch_variant<true, 32, 2, 2, 2, true, 2>(w, hi, lo, p, q, st);
-    if (dn_rows == 2 * kBM) return launch_variant<false, 32, 2, 2, 2, true, 2>(w, hi, lo, p, q, st);
-    return launch_variant<false, 32, 4, 1, 2, true, 2>(w, hi, lo, p, q, st);
+    if (gateup) return launch_variant<true, 32, 2, 2, 2, 2>(w, hi, lo, p, q, st);
+    if (dn_rows == 2 * kBM) return launch_variant<false, 32, 2, 2, 2, 2>(w, hi, lo, p, q, st);
+    return launch_variant<false, 32, 4, 1, 2, 2>(w, hi, lo, p, q, st);
   }
-  if (gateup) return launch_variant<true, 32, 5, 2, 2, true>(w, hi, lo, p, q, st);
-  if (dn_rows == 2 * kBM) return launch_variant<false, 32, 5, 2, 2, true>(w, hi, lo, p, q, st);
-  return launch_variant<false, 32, 8, 1, 2, true>(w, hi, lo, p, q, st);
+  if (gateup) return launch_variant<true, 32, 5, 2, 2>(w, hi, lo, p, q, st);
+  if (dn_rows == 2 * kBM) return launch_variant<false, 32, 5, 2, 2>(w, hi, lo, p, q, st);
+  return launch_variant<false, 32, 8, 1, 2>(w, hi, lo, p, q, st);
 }
 
 }  // namespace moe
