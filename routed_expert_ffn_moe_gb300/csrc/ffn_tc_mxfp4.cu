@@ -438,11 +438,12 @@ cudaError_t encode_e2m1_2d(CUtensorMap* m, const void* base, uint64_t rows, uint
 }  // namespace
 
 // Token tile of the decode batches: 16 tokens while experts average at most 4 routed tokens, 32
-// up to 16, 64 up to the decode bound. (Prefill batches run the f16 prefill tiles of
-// ffn_tc_fp8_wide.cu.)
+// up to 16, 48 up to the decode bound of 32 (few experts then exceed one tile, and 48-token
+// tiles leave TMEM room for two accumulators: measured T=1024 1757 -> 1713 us against 64-token
+// tiles with one). Prefill batches run the f16 prefill tiles of ffn_tc_fp8_wide.cu.
 int tc_mx_tile_tokens(bool decode, long routed, int E) {
   (void)decode;
-  return routed > 16L * E ? 64 : routed > 4L * E ? 32 : 16;
+  return routed > 16L * E ? 48 : routed > 4L * E ? 32 : 16;
 }
 
 // Down tiles pair two 128-row tiles of W_d when d allows it (two MMA issuers, one a tile).
@@ -483,10 +484,10 @@ cudaError_t launch_tc_mx(const FfnArgs& a, const int32_t* prefix, bool gateup, b
   if (e == cudaSuccess) e = encode_u8_2d(&lo, tok.lo, slots ? slots : 1, K, kBoxRows);
   if (e != cudaSuccess) return e;
   const int nt = tc_mx_tile_tokens(decode, (long)routed, a.E);
-  if (nt == 64) {
-    if (gateup) return launch_variant<true, 64, 4, 2, 1>(w, hi, lo, p, q, st);
-    if (dn_rows == 2 * kBM) return launch_variant<false, 64, 4, 2, 1>(w, hi, lo, p, q, st);
-    return launch_variant<false, 64, 6, 1, 2>(w, hi, lo, p, q, st);
+  if (nt == 48) {
+    if (gateup) return launch_variant<true, 48, 5, 2, 2>(w, hi, lo, p, q, st);
+    if (dn_rows == 2 * kBM) return launch_variant<false, 48, 5, 2, 2>(w, hi, lo, p, q, st);
+    return launch_variant<false, 48, 6, 1, 2>(w, hi, lo, p, q, st);
   }
   // Two 128-wide K slices per stage where K allows (measured: V4-Pro decode 1148 -> 1053 us; the
   // MMA-issuing thread's per-stage waits and commit are paid half as often)

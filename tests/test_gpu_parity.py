@@ -77,9 +77,11 @@ SMALL = [
     ("tiny", {"router": "zipf", "T": 600, "d": 512, "f": 256, "E": 16, "k": 2}),
     ("tiny", {"T": 333, "d": 384, "f": 256, "E": 6, "k": 3, "wdtype": "fp8"}),
     ("tiny", {"T": 333, "d": 384, "f": 256, "E": 6, "k": 3}),
-    # MXFP4 weights on block-scaled MMAs: 32-token decode tiles (paired and single down tiles),
-    # 64-token decode tiles, 128-token prefill tiles, ragged and degenerate batches
+    # MXFP4 weights: block-scaled MMAs on 16-, 32- and 48-token decode tiles (paired and single
+    # down tiles, one or two K slices per stage), f16 prefill tiles, ragged and degenerate batches
     ("tiny", {"wdtype": "mxfp4"}),
+    ("tiny", {"T": 10, "d": 384, "f": 256, "E": 8, "k": 2, "wdtype": "mxfp4"}),
+    ("tiny", {"T": 100, "d": 384, "f": 256, "E": 8, "k": 2, "wdtype": "mxfp4"}),
     ("tiny", {"T": 40, "d": 384, "f": 256, "E": 8, "k": 2, "wdtype": "mxfp4"}),
     ("tiny", {"d": 512, "f": 384, "T": 70, "E": 12, "k": 3, "wdtype": "mxfp4"}),
     ("tiny", {"T": 600, "E": 8, "k": 2, "wdtype": "mxfp4"}),
