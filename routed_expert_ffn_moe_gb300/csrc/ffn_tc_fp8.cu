@@ -42,7 +42,10 @@ constexpr uint32_t kQTileBytes = kBM * kQK;       // 16 KB of E4M3 codes
 constexpr int kConvGroups = 2;                    // groups take alternate stages
 constexpr int kConvWarps = 4 * kConvGroups;       // a group = one warp per TMEM lane quadrant
 constexpr int kConvThreads = 32 * kConvWarps;
-constexpr int kThreadsQ = 32 * 6 + kConvThreads;  // producer, MMA, 4 epilogue, converters
+// warps: 0 producer, 1 MMA issuer of weight tile 0, 2..5 epilogue, 6..13 converters, 14 MMA
+// issuer of weight tile 1 (two issuing threads issue MMAs faster than one)
+constexpr int kIssuer2 = 6 + kConvWarps;
+constexpr int kThreadsQ = 32 * (kIssuer2 + 1);
 constexpr uint32_t kACols = kQK / 2;              // TMEM columns of one 128 x 128 f16 tile
 
 // KA weight tiles of 128 rows share each token tile: gate and up rows of the same features in
@@ -128,10 +131,10 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
     }
     for (int s = 0; s < CSTAGES; ++s) {
       mbar_init(&c_full[s], 4);              // converted operands written
-      mbar_init(&c_empty[s], 1);             // MMA commit: converted operands consumed
+      mbar_init(&c_empty[s], KA);            // MMA commits (one per issuer): operands consumed
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_full[b], KA);           // one commit per issuer
       mbar_init(&acc_empty[b], 4);
     }
     *abort_flag = 0;
@@ -188,9 +191,10 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
         drain_bar(&full[s], issued_phase, p.status);
       }
     }
-  } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
+  } else if (warp == 1 || warp == kIssuer2) {
+    // ---------------- MMA issuers: warp 1 weight tile 0, warp 14 weight tile 1 ----------------
+    const int o = warp == 1 ? 0 : 1;
+    if (lane == 0 && o < KA) {
       uint32_t cs = 0, cphase = 0;
       uint32_t acc = 0, acc_phase = 0;
       bool ok = true;
@@ -201,20 +205,17 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
         const uint32_t idesc = idesc_f16(kBM, npad);
         if (!wait_bar(&acc_empty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
-        const uint32_t d0 = tmem_base + acc * S::kAccCols;
+        const uint32_t d0 = tmem_base + acc * S::kAccCols + o * NT;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!wait_bar(&c_full[cs], cphase, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t a0 = tmem_base + acol0 + cs * S::kAStageCols;
-          const uint32_t bp = smem_u32(cslots + cs * S::kCSlotBytes);
+          const uint32_t a0 = tmem_base + acol0 + cs * S::kAStageCols + o * kACols;
+          const uint32_t bp = smem_u32(cslots + cs * S::kCSlotBytes) + o * 2 * S::kBHalf;
 #pragma unroll
           for (int kk = 0; kk < kQK / 16; ++kk) {
             const uint32_t accum = (kb | kk) ? 1u : 0u;
             const uint32_t boff = (kk >> 2) * S::kBHalf;
             mma_ts(d0, a0 + kk * 8, sw128_desc(bp + boff) + 2 * (kk & 3), idesc, accum);
-            if (KA == 2)
-              mma_ts(d0 + NT, a0 + kACols + kk * 8,
-                          sw128_desc(bp + 2 * S::kBHalf + boff) + 2 * (kk & 3), idesc, accum);
           }
           mma_commit(&c_empty[cs]);
           if (++cs == CSTAGES) { cs = 0; cphase ^= 1u; }
@@ -228,7 +229,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
     // ---------------- epilogue (warps 2..5) ----------------
     run_epilogue<GATEUP, NT, S::kAccCols, KA>(p, total, tmem_base, acc_full, acc_empty,
                                               abort_flag);
-  } else {
+  } else if (warp < kIssuer2) {
     // ---------------- converters (warps 6..13) ----------------
     // Group g (4 warps, one per TMEM lane quadrant) converts every stage i with i % 2 == g, the
     // whole 128-wide K of its 32 rows, so two stages are converted at once.
