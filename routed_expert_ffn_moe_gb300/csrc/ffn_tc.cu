@@ -42,8 +42,12 @@ struct Smem {
   static constexpr uint32_t kTmemCols = ACCB * kAccCols;
 };
 
+// warps: 0 producer, 1 MMA issuer of weight tile 0, 2..5 epilogue, 6 MMA issuer of weight tile 1
+// (two issuing threads issue MMAs faster than one)
+constexpr int kThreadsB = 32 * 7;
+
 template <bool GATEUP, int NT, int STAGES, int KA, int ACCB, bool PAIR>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsB, 1)
     k_tc_ffn(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b0,
              const __grid_constant__ CUtensorMap tm_b1, const __grid_constant__ CUtensorMap tm_b0w,
              const __grid_constant__ CUtensorMap tm_b1w, const TcParams p) {
@@ -84,10 +88,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], PAIR ? 2 : 1);  // MMA commit (of both CTAs of a pair)
+      mbar_init(&empty[s], (PAIR ? 2 : 1) * KA);  // MMA commits: each issuer, both CTAs of a pair
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_full[b], KA);  // one commit per issuer
       mbar_init(&acc_empty[b], 4);  // one arrival per epilogue warp
     }
     *abort_flag = 0;
@@ -167,9 +171,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (PAIR) drain_bar(&empty[s], issued_phase, p.status);
       }
     }
-  } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
+  } else if (warp == 1 || warp == 6) {
+    // ---------------- MMA issuers: warp 1 weight tile 0, warp 6 weight tile 1 ----------------
+    const int o = warp == 1 ? 0 : 1;
+    if (lane == 0 && o < KA) {
       uint32_t stage = 0, phase = 0;
       uint32_t acc = 0, acc_phase = 0;
       bool ok = true;
@@ -180,20 +185,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t idesc = idesc_bf16(kBM, npad);
         if (!wait_bar(&acc_empty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
-        const uint32_t d0 = tmem_base + acc * S::kAccCols;
+        const uint32_t d0 = tmem_base + acc * S::kAccCols + o * NT;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!wait_bar(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
           const uint32_t st = smem_u32(smem + stage * S::kStageBytes);
-          const uint64_t da = sw128_desc(st);
-          const uint64_t du = sw128_desc(st + kATileBytes);
+          const uint64_t da = sw128_desc(st + o * kATileBytes);
           const uint64_t db = sw128_desc(st + KA * kATileBytes);
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint32_t accum = (kb | kk) ? 1u : 0u;
-            mma_bf16_ss(d0, da + 2 * kk, db + 2 * kk, idesc, accum);
-            if (KA == 2) mma_bf16_ss(d0 + NT, du + 2 * kk, db + 2 * kk, idesc, accum);
-          }
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            mma_bf16_ss(d0, da + 2 * kk, db + 2 * kk, idesc, (kb | kk) ? 1u : 0u);
           if (PAIR)
             mma_commit_mc(&empty[stage], 0x3);  // frees the stage in both CTAs of the pair
           else
@@ -205,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (++acc == ACCB) { acc = 0; acc_phase ^= 1u; }
       }
     }
-  } else {
+  } else if (warp < 6) {
     // ---------------- epilogue (warps 2..5) ----------------
     run_epilogue<GATEUP, NT, S::kAccCols, KA, ACCB>(p, total, tmem_base, acc_full, acc_empty,
                                                     abort_flag, tile0, tstep, PAIR ? rank : -1);
@@ -232,9 +233,9 @@ cudaError_t launch_variant(const CUtensorMap& w, const CUtensorMap& b0, const CU
   if (e != cudaSuccess) return e;
   count_launches(1);
   if (PAIR)
-    return launch_pdl_cluster(kern, dim3((unsigned)(num_sms() & ~1)), dim3(kThreads), S::kTotal,
+    return launch_pdl_cluster(kern, dim3((unsigned)(num_sms() & ~1)), dim3(kThreadsB), S::kTotal,
                               st, 2u, w, b0, b1, b0w, b1w, p);
-  return launch_pdl(kern, dim3(num_sms()), dim3(kThreads), S::kTotal, st, w, b0, b1, b0w, b1w, p);
+  return launch_pdl(kern, dim3(num_sms()), dim3(kThreadsB), S::kTotal, st, w, b0, b1, b0w, b1w, p);
 }
 
 // Weight rows per down-pass tile: two 128-row tiles share the token tile in the prefill
