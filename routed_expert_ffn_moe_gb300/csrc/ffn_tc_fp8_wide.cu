@@ -40,7 +40,8 @@ constexpr int kConvWarps = 8;
 constexpr int kConvThreads = 32 * kConvWarps;
 constexpr int kConvWarp0 = 6;                     // converters: warps 6..13
 constexpr int kTokWarp = kConvWarp0 + kConvWarps; // token producer: warp 14
-constexpr int kThreadsW = 32 * (kTokWarp + 1);
+constexpr int kIssuer2 = kTokWarp + 1;            // MMA issuer of weight tile 1: warp 15
+constexpr int kThreadsW = 32 * (kIssuer2 + 1);
 
 template <int NT, int QS, int BS, int CS, int KA, int ACCB, bool MX>
 struct SmemW {
@@ -160,14 +161,14 @@ __global__ void __launch_bounds__(kThreadsW, 1)
     }
     for (int s = 0; s < BS; ++s) {
       mbar_init(&b_full[s], 1);
-      mbar_init(&b_empty[s], CL);           // MMA commit (of every CTA of the cluster)
+      mbar_init(&b_empty[s], CL * KA);      // MMA commits (each issuer, every CTA of the cluster)
     }
     for (int s = 0; s < CS; ++s) {
       mbar_init(&c_full[s], kConvWarps);
-      mbar_init(&c_empty[s], 1);            // MMA commit
+      mbar_init(&c_empty[s], KA);           // MMA commits (one per issuer)
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_full[b], KA);          // one commit per issuer
       mbar_init(&acc_empty[b], 4);
     }
     *abort_flag = 0;
@@ -266,9 +267,10 @@ __global__ void __launch_bounds__(kThreadsW, 1)
           drain_bar(&b_empty[s], (s < (int)stage) ? phase : (phase ^ 1u), p.status);
       }
     }
-  } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
+  } else if (warp == 1 || warp == kIssuer2) {
+    // ---------------- MMA issuers: warp 1 weight tile 0, warp 15 weight tile 1 ----------------
+    const int o = warp == 1 ? 0 : 1;
+    if (lane == 0 && o < KA) {
       uint32_t bs = 0, bphase = 0, cs = 0, cphase = 0;
       uint32_t acc = 0, acc_phase = 0;
       bool ok = true;
@@ -282,21 +284,16 @@ __global__ void __launch_bounds__(kThreadsW, 1)
                : idesc_bf16(kBM, npad);
         if (!wait_bar(&acc_empty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
-        const uint32_t d0 = tmem_base + acc * S::kAccCols;
+        const uint32_t d0 = tmem_base + acc * S::kAccCols + o * NT;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!wait_bar(&b_full[bs], bphase, abort_flag, p.status) ||
               !wait_bar(&c_full[cs], cphase, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t ca = smem_u32(cring + cs * S::kCSlot);
-          const uint64_t da = sw128_desc(ca);
-          const uint64_t du = sw128_desc(ca + kATileBytes);
+          const uint64_t da = sw128_desc(smem_u32(cring + cs * S::kCSlot) + o * kATileBytes);
           const uint64_t db = sw128_desc(smem_u32(bring + bs * S::kBSlot));
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint32_t accum = (kb | kk) ? 1u : 0u;
-            mma_bf16_ss(d0, da + 2 * kk, db + 2 * kk, idesc, accum);
-            if (KA == 2) mma_bf16_ss(d0 + NT, du + 2 * kk, db + 2 * kk, idesc, accum);
-          }
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            mma_bf16_ss(d0, da + 2 * kk, db + 2 * kk, idesc, (kb | kk) ? 1u : 0u);
           if (PAIR)
             mma_commit_mc(&b_empty[bs], kMask);  // token rows consumed, in every CTA
           else
