@@ -13,10 +13,11 @@
 // each weight byte exactly once per call, at full tile width. Gate/up tiles issue two MMAs per
 // K step (gate rows and up rows of the same output features) into two accumulators.
 //
-// Warp roles (6 warps, one CTA per SM, persistent over a device-built tile list):
+// Warp roles (7 warps, one CTA per SM, persistent over a device-built tile list):
 //   warp 0     TMA producer (one thread): weight tile + token tile per stage
-//   warp 1     TMEM owner and MMA issuer (one thread)
+//   warp 1     TMEM owner and MMA issuer of weight tile 0 (one thread)
 //   warps 2-5  epilogue: TMEM -> registers -> SiLU(gate)*up -> bf16 h, or fp32 expert output
+//   warp 6     MMA issuer of weight tile 1 (one thread), when the tile pairs two weight tiles
 // Accumulators are double-buffered in TMEM so the epilogue of tile i overlaps the mainloop of
 // tile i+1. Every wait is bounded: a wait that gives up records MOE_ERR_DEVICE_TIMEOUT and the
 // CTA winds down, frees its TMEM and exits.

@@ -17,7 +17,8 @@
 //             codes) written straight into TMEM
 //             with tcgen05.st, one weight row per TMEM lane; token rows -> f16(s * x) written
 //             into a smem tile per weight matrix (gate and up have their own scale)
-//   MMA       tcgen05.mma.kind::f16 (f16 x f16 -> fp32) with A (codes) read from TMEM and B
+//   MMA       one issuing thread per weight tile (warps 1 and 14):
+//             tcgen05.mma.kind::f16 (f16 x f16 -> fp32) with A (codes) read from TMEM and B
 //             (scaled tokens) from smem
 //   epilogue  as in the bf16 kernel: TMEM accumulators -> SiLU(gate) * up -> bf16 h, or fp32
 //

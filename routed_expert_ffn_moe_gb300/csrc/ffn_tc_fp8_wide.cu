@@ -8,7 +8,8 @@
 //   TMA (tokens)  bf16 token rows (256 x 64 K, 128-byte swizzle) -> token ring
 //   convert       8 warps: bf16(code * block scale) into a third ring in the 128-byte-swizzle
 //                 K-major layout the MMA reads (each weight rounded once to bf16, <= 2^-9 relative)
-//   MMA           tcgen05.mma.kind::f16, bf16 x bf16 -> fp32, both operands from smem
+//   MMA           tcgen05.mma.kind::f16, bf16 x bf16 -> fp32, both operands from smem, one
+//                 issuing thread per weight tile (warps 1 and 15)
 //   epilogue      TMEM -> SiLU(gate) * up -> bf16 h, or the fp32 expert output
 //
 // MXFP4 weights (MX): the same kernel with E2M1 code pairs (128 rows x 64 codes = 32 bytes a row,
