@@ -93,7 +93,13 @@ MOE_API size_t moe_workspace_size(const moe_shape* shape);
  * choice is reproducible bit for bit: d is cut into 8-element chunks, lane j of 32 accumulates
  * chunks j, j+32, ... element by element with fused multiply-add from +0, the 32 lane sums
  * are combined by an xor butterfly (offsets 16, 8, 4, 2, 1), then the bias is added.
- * Inputs must be finite. */
+ * Batches of 1024 tokens or more, with E a multiple of 128 and d a multiple of 64, first form
+ * approximate logits on the tensor cores; each is within 2^-12 |x[t]| |wg[e]| of the defined
+ * logit, so only the experts that can still reach the top k (the candidates) get their logits
+ * recomputed in the order above, and the choice and the gate weights are the same bits. Words
+ * 1 and 2 of the workspace (bytes 4..11) then hold the number of tokens whose logits were all
+ * recomputed because a recomputed logit missed its bound (0 in every test), and the largest
+ * share of the bound a candidate used (fp32 bits). Inputs must be finite. */
 MOE_API moe_status moe_route(const moe_shape* shape, const void* x, const void* wg, const float* bias,
                      int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes, void* stream);
 

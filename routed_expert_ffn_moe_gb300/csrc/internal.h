@@ -19,11 +19,16 @@ namespace moe {
 //   x_perm   bf16 [T*k, d]        token rows gathered in slot order (tensor-core path input)
 //   h        bf16 [T*k + S*T, f]  SiLU(gate) * up for every slot
 //   shared   i32 [3, E+2]         moe_forward: the shared expert's own tile lists and offsets
+//   rtc      i32 [4] + f32 [E]    tensor-core router: its one-matrix tile plan, then |wg[e]|
+// Status words after the error code: [1] tokens whose logits the tensor-core router had to
+// recompute in full (a bound check failed), [2] the largest share of its error bound that a
+// candidate logit used (fp32 bits); both written by that router only.
 constexpr int kChunkTokens = 32;
+constexpr int kStatusRouterFull = 1, kStatusRouterBoundUse = 2;
 constexpr int kPlanRows = 8;
 
 struct WsLayout {
-  size_t status, logits, hist, base, plan, x_perm, h, shared, xq, hq, total;
+  size_t status, logits, hist, base, plan, x_perm, h, shared, xq, hq, rtc, total;
   int nchunk;
 };
 
@@ -50,6 +55,7 @@ inline WsLayout ws_layout(const moe_shape& s) {
   L.shared = take(3 * (E + 2) * 4);
   L.xq = take(mxfp4 ? slots * (2 * (size_t)s.d + 2 * (size_t)(s.d / 32)) : 0);
   L.hq = take(mxfp4 ? slots * (2 * (size_t)s.f + 2 * (size_t)(s.f / 32)) : 0);
+  L.rtc = take(16 + E * 4);
   L.total = off;
   return L;
 }

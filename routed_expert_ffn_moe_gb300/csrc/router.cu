@@ -6,8 +6,10 @@
 // 专家模型规格). Ascend fuses the gate into one "GatingTopK" kernel (same page, 融合Kernel);
 // here the logits GEMM and the selection are two kernels so the selection can see all E
 // logits of a token at once.
+#include <cstdlib>
 #include <mutex>
 
+#include "ffn.h"
 #include "internal.h"
 
 namespace moe {
@@ -244,6 +246,280 @@ __global__ void __launch_bounds__(256) k_router_hash(const float* __restrict__ l
   }
 }
 
+// ---- large batches: approximate logits on the tensor cores, exact logits of the candidates --
+//
+// The logits GEMM of a large batch runs on the tensor cores (bf16 products, fp32 accumulation
+// in the MMA's own order), so each approximate logit a[t,e] may differ from the defined logit
+// l[t,e] by a rounding error. Both are within eps[t,e] = 2^-12 |x_t| |wg_e| (+ 2^-22 |a|, for
+// the bias addition) of each other: sum |x_i w_i| <= |x||w| (Cauchy-Schwarz), and each of the
+// two fp32 sums, the defined one and the MMA's, errs by at most about n 2^-24 sum |x_i w_i|
+// for its n roundings (n <= ~1100 at d = 16384: 2^-13.9), so together at most 2^-12.9 |x||w|;
+// the errors measured on the GPU are near 2^-21 |x||w|. With lo = a - eps and
+// hi = a + eps (rounded outward) and theta the k-th largest lo, at least k experts have
+// l >= theta, so every expert of the top-k has hi >= theta, and an expert with hi < theta has
+// l < theta <= the k-th largest l: it is neither chosen nor tied with a chosen one. The
+// candidates {hi >= theta} get their defined logits recomputed in the defined order, and the
+// selection and the gate weights run on those exactly as k_router_topk runs on all E, so the
+// result is identical bit for bit. Each recomputed logit is checked against its bound; if one
+// misses it, the token's logits are all recomputed (and counted in the status word), so an
+// error beyond the bound cannot change a choice unseen.
+
+constexpr float kBoundC = 0x1p-12f;
+constexpr float kNormUp = 1.0f + 0x1p-10f;  // covers the rounding of the fp32 norms
+
+// Block 0 writes the one-matrix tile plan of the logits GEMM (expert offsets {0, T}, tile prefix
+// {0, tiles}) and clears the router's status words; every warp then takes experts e and writes
+// |wg_e| (rounded up).
+__global__ void __launch_bounds__(256) k_router_prep(const uint16_t* __restrict__ wg, int T, int d,
+                                                     int E, int tiles, int32_t* __restrict__ plan,
+                                                     float* __restrict__ wnorm, int* status) {
+  pdl_wait_then_release();
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    plan[0] = 0;
+    plan[1] = T;
+    plan[2] = 0;
+    plan[3] = tiles;
+    status[kStatusRouterFull] = 0;
+    status[kStatusRouterBoundUse] = 0;
+  }
+  const int lane = threadIdx.x & 31;
+  const int chunks = d >> 3;
+  for (int e = blockIdx.x * 8 + (threadIdx.x >> 5); e < E; e += gridDim.x * 8) {
+    const uint16_t* we = wg + (size_t)e * d;
+    float ss = 0.f;
+    for (int c = lane; c < chunks; c += 32) {
+      const uint4 v = ldg_u4(we + 8 * c);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float f = bf16x8_elem(v, i);
+        ss = fmaf(f, f, ss);
+      }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    if (lane == 0) wnorm[e] = sqrtf(ss) * kNormUp;
+  }
+}
+
+// NC defined logits of token row xt at once (experts e[0..NC)), in the order of
+// k_router_logits: lane j accumulates chunks j, j+32, ... element by element from +0, then the
+// xor butterfly. The x chunk is loaded once for the NC experts. Every lane returns the sums.
+template <int NC>
+__device__ __forceinline__ void defined_logits(const uint16_t* __restrict__ xt,
+                                               const uint16_t* __restrict__ wg, const int (&e)[NC],
+                                               int d, int lane, float (&out)[NC]) {
+  float acc[NC];
+#pragma unroll
+  for (int j = 0; j < NC; ++j) acc[j] = 0.f;
+  const int chunks = d >> 3;
+#pragma unroll 4
+  for (int c = lane; c < chunks; c += 32) {
+    const uint4 xv = ldg_u4(xt + 8 * c);
+    uint4 wv[NC];
+#pragma unroll
+    for (int j = 0; j < NC; ++j) wv[j] = ldg_u4(wg + (size_t)e[j] * d + 8 * c);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float xf = bf16x8_elem(xv, i);
+#pragma unroll
+      for (int j = 0; j < NC; ++j) acc[j] = __fmaf_rn(xf, bf16x8_elem(wv[j], i), acc[j]);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1)
+#pragma unroll
+    for (int j = 0; j < NC; ++j)
+      acc[j] = __fadd_rn(acc[j], __shfl_xor_sync(0xffffffffu, acc[j], off));
+#pragma unroll
+  for (int j = 0; j < NC; ++j) out[j] = acc[j];
+}
+
+// One warp per token; lane j holds experts j + 32m, m < MAXM (E <= 32 MAXM). approx holds the
+// tensor-core logits without the bias. Up to 256 experts, two blocks share an SM.
+template <int MAXM>
+__global__ void __launch_bounds__(256, MAXM <= 8 ? 2 : 1) k_router_select(
+    const uint16_t* __restrict__ x, const uint16_t* __restrict__ wg, const float* __restrict__ bias,
+    const float* __restrict__ approx, const float* __restrict__ wnorm, int T, int d, int E, int k,
+    int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int* status) {
+  constexpr int kGroup = 4;  // candidates whose defined logits are formed together
+  __shared__ int cand[8][32 * MAXM];
+  pdl_wait_then_release();
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int t = blockIdx.x * 8 + w;
+  if (t >= T) return;
+  const uint16_t* xt = x + (size_t)t * d;
+
+  // |x_t|, rounded up
+  float ss = 0.f;
+  for (int c = lane; c < (d >> 3); c += 32) {
+    const uint4 v = ldg_u4(xt + 8 * c);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float f = bf16x8_elem(v, i);
+      ss = fmaf(f, f, ss);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  const float nx = sqrtf(ss) * kNormUp;
+
+  // approximate logits with the bias, their bounds, and the outward-rounded intervals
+  float ah[MAXM], eps[MAXM], lo[MAXM];
+#pragma unroll
+  for (int m = 0; m < MAXM; ++m) {
+    const int e = lane + 32 * m;
+    if (e < E) {
+      const float a = approx[(size_t)t * E + e];
+      ah[m] = bias ? __fadd_rn(a, bias[e]) : a;
+      eps[m] = __fadd_ru(__fmul_ru(__fmul_ru(kBoundC, nx), wnorm[e]),
+                         __fmul_ru(0x1p-22f, fabsf(ah[m]))) + 0x1p-126f;
+      lo[m] = __fsub_rd(ah[m], eps[m]);
+    } else {
+      ah[m] = eps[m] = 0.f;
+      lo[m] = -INFINITY;
+    }
+  }
+  // theta: the k-th largest lower bound (k rounds of a warp arg-max)
+  float theta = -INFINITY;
+  {
+    uint32_t taken = 0;
+    for (int j = 0; j < k; ++j) {
+      float bl = -INFINITY;
+      int bm = -1;
+#pragma unroll
+      for (int m = 0; m < MAXM; ++m)
+        if (!((taken >> m) & 1u) && lane + 32 * m < E && (bm < 0 || lo[m] > bl)) {
+          bl = lo[m];
+          bm = m;
+        }
+      int be = bm < 0 ? 0x7FFFFFFF : lane + 32 * bm;
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) {
+        const float ol = __shfl_xor_sync(0xffffffffu, bl, off);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+        if (ranks_before(ol, oe, bl, be)) {
+          bl = ol;
+          be = oe;
+        }
+      }
+      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+      theta = bl;
+    }
+  }
+
+  // candidates: hi >= theta, listed in expert order
+  uint32_t mine = 0;
+#pragma unroll
+  for (int m = 0; m < MAXM; ++m)
+    if (lane + 32 * m < E && __fadd_ru(ah[m], eps[m]) >= theta) mine |= 1u << m;
+  int n = 0;
+#pragma unroll
+  for (int m = 0; m < MAXM; ++m) {
+    const uint32_t b = __ballot_sync(0xffffffffu, (mine >> m) & 1u);
+    if ((mine >> m) & 1u) cand[w][n + __popc(b & ((1u << lane) - 1u))] = lane + 32 * m;
+    n += __popc(b);
+  }
+  __syncwarp();
+
+  // their defined logits (kept by the lane that holds the expert), each checked against its
+  // bound
+  float lx[MAXM];
+#pragma unroll
+  for (int m = 0; m < MAXM; ++m) lx[m] = -INFINITY;
+  float use = 0.f;
+  bool miss = false;
+  for (int g = 0; g < n; g += kGroup) {
+    int e[kGroup];
+#pragma unroll
+    for (int j = 0; j < kGroup; ++j) e[j] = cand[w][min(g + j, n - 1)];
+    float sdef[kGroup];
+    defined_logits<kGroup>(xt, wg, e, d, lane, sdef);
+#pragma unroll
+    for (int j = 0; j < kGroup; ++j) {
+      if (g + j >= n) break;
+      const float l = bias ? __fadd_rn(sdef[j], bias[e[j]]) : sdef[j];
+      const int src = e[j] & 31, mj = e[j] >> 5;
+      float a_j = 0.f, eps_j = 1.f;
+#pragma unroll
+      for (int m = 0; m < MAXM; ++m)
+        if (m == mj) {
+          a_j = ah[m];
+          eps_j = eps[m];
+          if (lane == src) lx[m] = l;
+        }
+      a_j = __shfl_sync(0xffffffffu, a_j, src);
+      eps_j = __shfl_sync(0xffffffffu, eps_j, src);
+      const float r = fabsf(l - a_j) / eps_j;
+      use = fmaxf(use, r);
+      miss |= !(r <= 1.f);
+    }
+  }
+  if (miss) {
+    // a recomputed logit missed its bound: form every logit of this token in the defined order
+    for (int g = 0; g < E; g += kGroup) {
+      int e[kGroup];
+#pragma unroll
+      for (int j = 0; j < kGroup; ++j) e[j] = min(g + j, E - 1);
+      float sdef[kGroup];
+      defined_logits<kGroup>(xt, wg, e, d, lane, sdef);
+#pragma unroll
+      for (int j = 0; j < kGroup; ++j) {
+        const float l = bias ? __fadd_rn(sdef[j], bias[e[j]]) : sdef[j];
+#pragma unroll
+        for (int m = 0; m < MAXM; ++m)
+          if (g + j < E && e[j] == lane + 32 * m) lx[m] = l;
+      }
+    }
+    mine = 0;
+#pragma unroll
+    for (int m = 0; m < MAXM; ++m)
+      if (lane + 32 * m < E) mine |= 1u << m;
+    if (lane == 0) atomicAdd(status + kStatusRouterFull, 1);
+  }
+  if (lane == 0) atomicMax(status + kStatusRouterBoundUse, __float_as_int(use));
+
+  // top-k over the defined logits of the candidates, then the gate weights, as k_router_topk
+  const float (&l)[MAXM] = lx;
+  uint32_t taken = 0;
+  float my_l = -INFINITY;
+  int my_e = 0;
+  for (int j = 0; j < k; ++j) {
+    float bl = -INFINITY;
+    int be = 0x7FFFFFFF;
+#pragma unroll
+    for (int m = 0; m < MAXM; ++m) {
+      const int e = lane + 32 * m;
+      if (((mine >> m) & 1u) && !((taken >> m) & 1u) && ranks_before(l[m], e, bl, be)) {
+        bl = l[m];
+        be = e;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+      const float ol = __shfl_xor_sync(0xffffffffu, bl, off);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+      if (ranks_before(ol, oe, bl, be)) {
+        bl = ol;
+        be = oe;
+      }
+    }
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    if (lane == j) {
+      my_l = bl;
+      my_e = be;
+    }
+  }
+  const float lmax = __shfl_sync(0xffffffffu, my_l, 0);
+  const float ex = lane < k ? expf(my_l - lmax) : 0.f;
+  float sum = ex;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  if (lane < k) {
+    topk_idx[(size_t)t * k + lane] = my_e;
+    topk_w[(size_t)t * k + lane] = ex / sum;
+  }
+}
+
 template <int TT, int TE, int UNROLL = 4>
 cudaError_t launch_logits(const uint16_t* x, const uint16_t* wg, const float* bias, int T, int d,
                           int E, float* logits, cudaStream_t st) {
@@ -318,10 +594,68 @@ cudaError_t launch_route_noalloc(const moe_shape& s, const uint16_t* x, const ui
                     s.E, s.k, topk_idx, topk_w);
 }
 
+// Batches from this many tokens take the tensor-core router (MOE_ROUTER_TC_MIN_TOKENS
+// overrides it); it needs E % 128 == 0 (whole 128-row tiles of wg) and d % 64 == 0.
+static long router_tc_min_tokens() {
+  const char* v = getenv("MOE_ROUTER_TC_MIN_TOKENS");
+  return v && *v ? atol(v) : 1024;
+}
+
+static bool router_uses_tc(const moe_shape& s) {
+  return s.E % 128 == 0 && s.d % 64 == 0 && s.E <= 1024 && s.T >= router_tc_min_tokens();
+}
+
+template <int MAXM>
+static cudaError_t launch_select(const moe_shape& s, const uint16_t* x, const uint16_t* wg,
+                                 const float* bias, const float* approx, const float* wnorm,
+                                 int32_t* topk_idx, float* topk_w, int* status, cudaStream_t st) {
+  return launch_pdl(k_router_select<MAXM>, dim3((unsigned)((s.T + 7) / 8)), dim3(256), 0, st, x,
+                    wg, bias, approx, wnorm, s.T, s.d, s.E, s.k, topk_idx, topk_w, status);
+}
+
+static cudaError_t launch_route_tc(const moe_shape& s, const uint16_t* x, const uint16_t* wg,
+                                   const float* bias, int32_t* topk_idx, float* topk_w, char* ws,
+                                   const WsLayout& L, cudaStream_t st) {
+  int32_t* plan = reinterpret_cast<int32_t*>(ws + L.rtc);
+  float* wnorm = reinterpret_cast<float*>(ws + L.rtc + 16);
+  float* approx = reinterpret_cast<float*>(ws + L.logits);
+  int* status = reinterpret_cast<int*>(ws + L.status);
+  // the logits GEMM as the down pass of one expert: "h" = x [T, d], "W_d" = wg [E, d], output
+  // rows of E logits, 64-token tiles of 128 experts
+  const int tiles = (s.T + tc_tile_tokens(false, true) - 1) / tc_tile_tokens(false, true) *
+                    (s.E / tc_tile_rows(false, true, s.E));
+  const int nb = (s.E + 7) / 8 < 2 * num_sms() ? (s.E + 7) / 8 : 2 * num_sms();
+  cudaError_t e = launch_pdl(k_router_prep, dim3((unsigned)nb), dim3(256), 0, st, wg, s.T, s.d,
+                             s.E, tiles, plan, wnorm, status);
+  if (e != cudaSuccess) return e;
+  count_launches(2);  // prep and select (launch_tc counts its own)
+  FfnArgs a{};
+  a.T = s.T;
+  a.k = 1;
+  a.E = 1;
+  a.n_shared = 0;
+  a.d = s.E;
+  a.f = s.d;
+  a.wdtype = MOE_W_BF16;
+  a.offsets = plan;
+  a.w2 = wg;
+  a.h = const_cast<uint16_t*>(x);  // read only: the down pass loads its rows through TMA
+  a.y_perm = approx;
+  a.status = status;
+  e = launch_tc(a, plan + 2, false, true, st);
+  if (e != cudaSuccess) return e;
+  if (s.E <= 256)
+    return launch_select<8>(s, x, wg, bias, approx, wnorm, topk_idx, topk_w, status, st);
+  if (s.E <= 512)
+    return launch_select<16>(s, x, wg, bias, approx, wnorm, topk_idx, topk_w, status, st);
+  return launch_select<32>(s, x, wg, bias, approx, wnorm, topk_idx, topk_w, status, st);
+}
+
 cudaError_t launch_route(const moe_shape& s, const uint16_t* x, const uint16_t* wg,
                          const float* bias, int32_t* topk_idx, float* topk_w, char* ws,
                          const WsLayout& L, cudaStream_t st) {
   if (s.T == 0) return cudaSuccess;
+  if (router_uses_tc(s)) return launch_route_tc(s, x, wg, bias, topk_idx, topk_w, ws, L, st);
   float* logits = reinterpret_cast<float*>(ws + L.logits);
   cudaError_t e = launch_logits_for(s, x, wg, bias, logits, st);
   if (e != cudaSuccess) return e;

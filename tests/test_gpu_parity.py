@@ -90,6 +90,10 @@ SMALL = [
     ("tiny", {"T": 1, "wdtype": "mxfp4"}),
     ("tiny", {"T": 0, "wdtype": "mxfp4"}),
     ("tiny", {"n_shared": 0, "T": 37, "wdtype": "mxfp4"}),
+    # a batch large enough for the tensor-core router (E a multiple of 128), with the shared
+    # expert's FFN overlapping it on the second stream
+    ("tiny", {"T": 1100, "d": 512, "f": 256, "E": 128, "k": 4}),
+    ("tiny", {"T": 1100, "d": 512, "f": 256, "E": 128, "k": 4, "router": "zipf", "wdtype": "fp8"}),
 ]
 
 
@@ -196,7 +200,8 @@ def test_combine_direct():
                                   {"router": "zipf", "T": 600, "d": 512, "f": 256, "E": 16, "k": 2},
                                   {"T": 600, "d": 512, "f": 256, "E": 8, "k": 2, "wdtype": "fp8"},
                                   {"n_shared": 0}, {"wdtype": "mxfp4"},
-                                  {"T": 600, "d": 512, "f": 256, "E": 8, "k": 2, "wdtype": "mxfp4"}])
+                                  {"T": 600, "d": 512, "f": 256, "E": 8, "k": 2, "wdtype": "mxfp4"},
+                                  {"T": 1100, "d": 512, "f": 256, "E": 128, "k": 4}])
 def test_forward_equals_the_four_calls(over):
     # moe_forward runs the shared expert on its own stream: every output must be bit-identical
     # to the four separate calls.
@@ -229,7 +234,8 @@ def test_layer_is_deterministic():
 
 @pytest.mark.parametrize("over", [{}, {"wdtype": "fp8", "T": 70, "E": 12, "k": 3, "d": 512, "f": 384},
                                   {"router": "zipf", "T": 600, "d": 512, "f": 256, "E": 16, "k": 2},
-                                  {"wdtype": "mxfp4", "T": 600, "E": 8, "k": 2}])
+                                  {"wdtype": "mxfp4", "T": 600, "E": 8, "k": 2},
+                                  {"T": 1100, "d": 512, "f": 256, "E": 128, "k": 4}])
 def test_layer_replays_from_a_cuda_graph(over):
     # the four calls enqueue no synchronisation or allocation, so they can be captured once
     cfg = synth.get_config("tiny", **over)
