@@ -253,8 +253,10 @@ __global__ void __launch_bounds__(256) k_router_hash(const float* __restrict__ l
 // l[t,e] by a rounding error. Both are within eps[t,e] = 2^-12 |x_t| |wg_e| (+ 2^-22 |a|, for
 // the bias addition) of each other: sum |x_i w_i| <= |x||w| (Cauchy-Schwarz), and each of the
 // two fp32 sums, the defined one and the MMA's, errs by at most about n 2^-24 sum |x_i w_i|
-// for its n roundings (n <= ~1100 at d = 16384: 2^-13.9), so together at most 2^-12.9 |x||w|;
-// the errors measured on the GPU are near 2^-21 |x||w|. With lo = a - eps and
+// for its n roundings (n <= ~1100 at d = 16384: 2^-13.9), so together at most 2^-12.9 |x||w|,
+// if the MMA's internal additions round no worse than fp32 (its accumulation order and precision
+// are not documented, hence the check below); the errors measured on the GPU are near
+// 2^-21 |x||w|. With lo = a - eps and
 // hi = a + eps (rounded outward) and theta the k-th largest lo, at least k experts have
 // l >= theta, so every expert of the top-k has hi >= theta, and an expert with hi < theta has
 // l < theta <= the k-th largest l: it is neither chosen nor tied with a chosen one. The
