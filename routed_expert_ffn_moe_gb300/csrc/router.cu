@@ -263,9 +263,11 @@ __global__ void __launch_bounds__(256) k_router_hash(const float* __restrict__ l
 // candidates {hi >= theta} get their defined logits recomputed in the defined order, and the
 // selection and the gate weights run on those exactly as k_router_topk runs on all E, so the
 // result is identical bit for bit. Each recomputed logit is checked against its bound; if one
-// misses it, the token's logits are all recomputed (and counted in the status word), so an
-// error beyond the bound cannot change a choice unseen.
+// misses it, the token's logits are all recomputed (and counted in the status word): a bound
+// that failed would show on the candidates, the logits nearest the choice.
 
+// The bound coefficient. MOE_ROUTER_TC_BOUND overrides it; a negative value makes every token
+// take the full recomputation (a test runs that path this way).
 constexpr float kBoundC = 0x1p-12f;
 constexpr float kNormUp = 1.0f + 0x1p-10f;  // covers the rounding of the fp32 norms
 
@@ -342,7 +344,7 @@ template <int MAXM>
 __global__ void __launch_bounds__(256, MAXM <= 8 ? 2 : 1) k_router_select(
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ wg, const float* __restrict__ bias,
     const float* __restrict__ approx, const float* __restrict__ wnorm, int T, int d, int E, int k,
-    int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int* status) {
+    float bound_c, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int* status) {
   constexpr int kGroup = 4;  // candidates whose defined logits are formed together
   __shared__ int cand[8][32 * MAXM];
   pdl_wait_then_release();
@@ -373,7 +375,7 @@ __global__ void __launch_bounds__(256, MAXM <= 8 ? 2 : 1) k_router_select(
     if (e < E) {
       const float a = approx[(size_t)t * E + e];
       ah[m] = bias ? __fadd_rn(a, bias[e]) : a;
-      eps[m] = __fadd_ru(__fmul_ru(__fmul_ru(kBoundC, nx), wnorm[e]),
+      eps[m] = __fadd_ru(__fmul_ru(__fmul_ru(fmaxf(bound_c, 0.f), nx), wnorm[e]),
                          __fmul_ru(0x1p-22f, fabsf(ah[m]))) + 0x1p-126f;
       lo[m] = __fsub_rd(ah[m], eps[m]);
     } else {
@@ -429,7 +431,7 @@ __global__ void __launch_bounds__(256, MAXM <= 8 ? 2 : 1) k_router_select(
 #pragma unroll
   for (int m = 0; m < MAXM; ++m) lx[m] = -INFINITY;
   float use = 0.f;
-  bool miss = false;
+  bool miss = bound_c < 0.f;
   for (int g = 0; g < n; g += kGroup) {
     int e[kGroup];
 #pragma unroll
@@ -603,6 +605,11 @@ static long router_tc_min_tokens() {
   return v && *v ? atol(v) : 1024;
 }
 
+static float router_tc_bound() {
+  const char* v = getenv("MOE_ROUTER_TC_BOUND");
+  return v && *v ? (float)atof(v) : kBoundC;
+}
+
 static bool router_uses_tc(const moe_shape& s) {
   return s.E % 128 == 0 && s.d % 64 == 0 && s.E <= 1024 && s.T >= router_tc_min_tokens();
 }
@@ -612,7 +619,8 @@ static cudaError_t launch_select(const moe_shape& s, const uint16_t* x, const ui
                                  const float* bias, const float* approx, const float* wnorm,
                                  int32_t* topk_idx, float* topk_w, int* status, cudaStream_t st) {
   return launch_pdl(k_router_select<MAXM>, dim3((unsigned)((s.T + 7) / 8)), dim3(256), 0, st, x,
-                    wg, bias, approx, wnorm, s.T, s.d, s.E, s.k, topk_idx, topk_w, status);
+                    wg, bias, approx, wnorm, s.T, s.d, s.E, s.k, router_tc_bound(), topk_idx,
+                    topk_w, status);
 }
 
 static cudaError_t launch_route_tc(const moe_shape& s, const uint16_t* x, const uint16_t* wg,

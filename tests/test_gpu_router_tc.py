@@ -91,3 +91,17 @@ def test_tc_router_exact_and_near_ties_and_zero_tokens(monkeypatch, bias):
         if wg[e, i] & 0x7FFF:
             wg[e, i] = bf16_next(wg[e, i])
     check_both(monkeypatch, cfg, x, wg, synth.host_bias(cfg))
+
+
+def test_tc_router_full_recomputation_path(monkeypatch):
+    # A negative bound coefficient sends every token down the path a missed bound takes: all E
+    # logits recomputed in the defined order. The counter says so, and the results are still
+    # the fp32 router's bits.
+    cfg = synth.get_config("tiny", T=1024, d=1024, E=256, k=8, f=128, router="zipf")
+    x, wg, bias = synth.host_x(cfg), synth.host_wg(cfg), synth.host_bias(cfg)
+    i_f, w_f, _ = route(monkeypatch, cfg, x, wg, bias, TC_NEVER)
+    monkeypatch.setenv("MOE_ROUTER_TC_BOUND", "-1")
+    i_tc, w_tc, st = route(monkeypatch, cfg, x, wg, bias, TC_ALWAYS)
+    assert int(st[1]) == cfg.T
+    np.testing.assert_array_equal(i_tc, i_f)
+    np.testing.assert_array_equal(w_tc.view(np.int32), w_f.view(np.int32))
