@@ -250,21 +250,22 @@ __global__ void __launch_bounds__(256) k_router_hash(const float* __restrict__ l
 //
 // The logits GEMM of a large batch runs on the tensor cores (bf16 products, fp32 accumulation
 // in the MMA's own order), so each approximate logit a[t,e] may differ from the defined logit
-// l[t,e] by a rounding error. Both are within eps[t,e] = 2^-12 |x_t| |wg_e| (+ 2^-22 |a|, for
-// the bias addition) of each other: sum |x_i w_i| <= |x||w| (Cauchy-Schwarz), and each of the
-// two fp32 sums, the defined one and the MMA's, errs by at most about n 2^-24 sum |x_i w_i|
-// for its n roundings (n <= ~1100 at d = 16384: 2^-13.9), so together at most 2^-12.9 |x||w|,
-// if the MMA's internal additions round no worse than fp32 (its accumulation order and precision
-// are not documented, hence the check below); the errors measured on the GPU are near
-// 2^-21 |x||w|. With lo = a - eps and
-// hi = a + eps (rounded outward) and theta the k-th largest lo, at least k experts have
-// l >= theta, so every expert of the top-k has hi >= theta, and an expert with hi < theta has
-// l < theta <= the k-th largest l: it is neither chosen nor tied with a chosen one. The
-// candidates {hi >= theta} get their defined logits recomputed in the defined order, and the
-// selection and the gate weights run on those exactly as k_router_topk runs on all E, so the
-// result is identical bit for bit. Each recomputed logit is checked against its bound; if one
-// misses it, the token's logits are all recomputed (and counted in the status word): a bound
-// that failed would show on the candidates, the logits nearest the choice.
+// l[t,e] by a rounding error. Both are taken to lie within eps[t,e] = 2^-12 |x_t| |wg_e|
+// (+ 2^-22 |a|, for the bias addition) of each other: sum |x_i w_i| <= |x||w| (Cauchy-Schwarz),
+// and each of the two fp32 sums, the defined one and the MMA's, errs by at most about
+// n 2^-24 sum |x_i w_i| for its n roundings (n <= ~1100 at d = 16384: 2^-13.9), so together at
+// most 2^-12.9 |x||w|, provided the MMA's internal additions round no worse than fp32 (its
+// accumulation order and precision are not documented, hence the check below). The errors
+// measured on the GPU are near 2^-21 |x||w|.
+//
+// With lo = a - eps and hi = a + eps (rounded outward) and theta the k-th largest lo, at least k
+// experts have l >= theta, so every expert of the top-k has hi >= theta, and an expert with
+// hi < theta has l < theta <= the k-th largest l: it is neither chosen nor tied with a chosen
+// one. The candidates {hi >= theta} get their defined logits recomputed in the defined order,
+// and the selection and the gate weights run on those exactly as k_router_topk runs on all E,
+// so the result is identical bit for bit. Each recomputed logit is checked against its bound;
+// if one misses it, the token's logits are all recomputed (and counted in the status word): a
+// bound that failed would show on the candidates, the logits nearest the choice.
 
 // The bound coefficient. MOE_ROUTER_TC_BOUND overrides it; a negative value makes every token
 // take the full recomputation (a test runs that path this way).
