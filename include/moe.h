@@ -98,7 +98,7 @@ MOE_API size_t moe_workspace_size(const moe_shape* shape);
  * logit, so only the experts that can still reach the top k (the candidates) get their logits
  * recomputed in the order above, and the choice and the gate weights are the same bits. Words
  * 1 and 2 of the workspace (bytes 4..11) then hold the number of tokens whose logits were all
- * recomputed because a recomputed logit missed its bound (0 in every test), and the largest
+ * recomputed because a recomputed logit missed its bound (0 on every test input), and the largest
  * share of the bound a candidate used (fp32 bits). Inputs must be finite. */
 MOE_API moe_status moe_route(const moe_shape* shape, const void* x, const void* wg, const float* bias,
                      int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes, void* stream);

@@ -43,8 +43,9 @@ def test_library_targets_sm_103a_only():
 def test_workspace_size_valid_and_invalid(lib):
     s = moe.shape_of(256, 7168, 256, 8, 2048, 1, "bf16")
     n = moe.moe_workspace_size(s)
-    # holds at least the logits, gathered rows and h of this shape
-    assert n >= 256 * 256 * 4 + 256 * 8 * 7168 * 2 + 256 * 9 * 2048 * 2
+    # holds at least the logits, gathered rows and h of this shape, and the tensor-core
+    # router's tile plan and row norms
+    assert n >= 256 * 256 * 4 + 256 * 8 * 7168 * 2 + 256 * 9 * 2048 * 2 + 16 + 256 * 4
     assert n % 256 == 0
     assert moe.moe_workspace_size(moe.shape_of(0, 256, 8, 2, 128)) > 0
     for bad in (moe.shape_of(16, 250, 8, 2, 128), moe.shape_of(16, 256, 8, 9, 128),
