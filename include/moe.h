@@ -94,9 +94,10 @@ MOE_API size_t moe_workspace_size(const moe_shape* shape);
  * chunks j, j+32, ... element by element with fused multiply-add from +0, the 32 lane sums
  * are combined by an xor butterfly (offsets 16, 8, 4, 2, 1), then the bias is added.
  * Batches of 1024 tokens or more, with E a multiple of 128 and d a multiple of 64, first form
- * approximate logits on the tensor cores; each is within 2^-12 |x[t]| |wg[e]| of the defined
- * logit, so only the experts that can still reach the top k (the candidates) get their logits
- * recomputed in the order above, and the choice and the gate weights are the same bits. Words
+ * approximate logits on the tensor cores; each is taken to lie within 2^-12 |x[t]| |wg[e]| of
+ * the defined logit (a bound checked on every logit recomputed), so only the experts that can
+ * still reach the top k (the candidates) get their logits recomputed in the order above, and the
+ * choice and the gate weights are the same bits. Words
  * 1 and 2 of the workspace (bytes 4..11) then hold the number of tokens whose logits were all
  * recomputed because a recomputed logit missed its bound (0 on every test input), and the largest
  * share of the bound a candidate used (fp32 bits). Inputs must be finite. */
