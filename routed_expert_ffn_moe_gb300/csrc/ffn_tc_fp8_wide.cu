@@ -1,8 +1,9 @@
 // Expert FFN, tensor-core path for FP8 E4M3 expert weights, wide-tile variant for large token
-// batches (W8A16). Same passages as ffn_tc_fp8.cu. With 256 tokens per tile the MMA is the
-// bottleneck, so the tile shape follows the bf16 prefill kernel (two 128-row weight tiles per
-// 256-token tile, 512 TMEM columns of accumulator) and the dequantisation moves to a shared-
-// memory stage of its own:
+// batches (W8A16). Same passages as ffn_tc_fp8.cu. With up to 256 tokens per tile each weight
+// element serves many tokens, so the tile shape follows the bf16 prefill kernel (two 128-row
+// weight tiles per 256-token tile, 512 TMEM columns of accumulator) and the dequantisation moves
+// to a shared-memory stage of its own (measured: the dequantisers and the MMAs take turns on the
+// two converted slots; no unit is near its limit):
 //
 //   TMA (codes)   E4M3 codes (128 rows x 64 K per weight tile, 64-byte swizzle) -> code ring
 //   TMA (tokens)  bf16 token rows (256 x 64 K, 128-byte swizzle) -> token ring
