@@ -26,8 +26,8 @@
 // than bf16) and saturates at +-65504, so the product of a block scale and an activation must
 // stay below that (block scales are amax/448, far below 1 for expert weights).
 //
-// This variant serves decode-sized tiles (up to 32 tokens); wide tiles go to ffn_tc_fp8_wide.cu,
-// where dequantising the weights costs less than scaling 64-128 token rows.
+// This variant serves decode-sized tiles (32 or 64 tokens); prefill tiles go to
+// ffn_tc_fp8_wide.cu, where dequantising the weights costs less than scaling 128-256 token rows.
 #include <cuda_bf16.h>
 
 #include "tc_common.cuh"
