@@ -18,20 +18,28 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "moe_oracle.c")
-_LIB = os.path.join(_HERE, "libmoe_oracle.so")
+# MOE_ORACLE_LIB points the wrapper at another build of this interface: the mutation test loads
+# builds with a planted mistake this way, to show that the pins catch each one.
+_LIB = os.environ.get("MOE_ORACLE_LIB") or os.path.join(_HERE, "libmoe_oracle.so")
 
 WD = {"bf16": 0, "fp8": 1, "mxfp4": 2}
 
 
-def build(force: bool = False) -> str:
+def compile_source(src: str, out: str) -> str:
     """gcc -O2, no fp contraction (so results do not depend on the host's FMA units)."""
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+           src, "-o", out + ".tmp", "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(out + ".tmp", out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    if os.environ.get("MOE_ORACLE_LIB"):  # another build, made by whoever set the variable
+        return _LIB
     if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
         return _LIB
-    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
-           _SRC, "-o", _LIB + ".tmp", "-lm"]
-    subprocess.run(cmd, check=True)
-    os.replace(_LIB + ".tmp", _LIB)
-    return _LIB
+    return compile_source(_SRC, _LIB)
 
 
 _lib = None
