@@ -73,3 +73,24 @@ def test_all_equal_logits_pick_the_lowest_indices():  # e.g. zero token rows wit
     eps = np.full(E, 1e-30)
     got, cand = candidate_topk(l, l.copy(), eps, k)
     assert got == list(range(k)) and cand.all()
+
+
+def test_the_rule_without_the_upper_bound_fails():
+    # Candidates taken as {a >= theta} instead of {a + eps >= theta} lose chosen experts: the
+    # adversarial draw (the k-th expert at the bottom of its interval) finds it.
+    def broken(l, a, eps, k):
+        eps = np.nextafter(np.maximum(eps, np.abs(a - l)), np.inf)
+        theta = np.sort(np.nextafter(a - eps, -np.inf))[::-1][k - 1]
+        return topk_by_rule(l, a >= theta, k)
+
+    E, k = 32, 4
+    rng = np.random.default_rng(7)
+    misses = 0
+    for _ in range(200):
+        l = np.sort(rng.normal(size=E))[::-1].copy()
+        eps = np.full(E, rng.uniform(0.01, 1.0))
+        a = l.copy()
+        a[:k] -= eps[:k]
+        a[k:] += eps[k:]
+        misses += broken(l, a, eps, k) != topk_by_rule(l, np.ones(E, bool), k)
+    assert misses > 0
