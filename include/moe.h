@@ -128,11 +128,10 @@ MOE_API moe_status moe_route_noalloc(const moe_shape* shape, const void* x, cons
  *   tid2eid        [vocab, k] int32: row v holds the k distinct experts (in [0, E)) of token
  *                  id v.
  *   topk_idx       [T, k] int32 out: tid2eid[token_ids[t]], in the table's order.
- *   topk_w         [T, k] fp32 out: softmax over the token's E router logits (computed as in
- *                  moe_route), kept at those k experts and renormalised -- equal to
- *                  exp(l_j - max) / sum over the k, in fp32.
- * x, wg, bias, ws as in moe_route (the logits use ws; the status word is cleared: a layer
- * starts here). A token id or table entry out of range is recorded as MOE_ERR_DEVICE_BOUNDS
+ *   topk_w         [T, k] fp32 out: softmax over the token's E router logits, kept at those k
+ *                  experts and renormalised -- equal to exp(l_j - max) / sum over the k, in
+ *                  fp32, so only the k hashed logits are formed (each in moe_route's order).
+ * x, wg, bias, ws as in moe_route (the status word is cleared: a layer starts here). A token id or table entry out of range is recorded as MOE_ERR_DEVICE_BOUNDS
  * (the entry is replaced by 0). Returns MOE_ERR_INVALID_ARG for vocab < 1. */
 MOE_API moe_status moe_route_hash(const moe_shape* shape, const void* x, const void* wg,
                                   const float* bias, const int32_t* token_ids,

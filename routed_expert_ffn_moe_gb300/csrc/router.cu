@@ -204,48 +204,6 @@ __global__ void __launch_bounds__(256) k_router_topk(const float* __restrict__ l
   }
 }
 
-// Hash routing: one warp per token. Lane j < k takes expert tid2eid[token_ids[t]][j] and its
-// logit; the gate weights are exp(l_j - l_max) / sum over those k, computed as k_router_topk
-// computes them for the soft choice (so a table holding the soft choices gives the same bits).
-// A token id or table entry out of range is recorded in the status word and replaced by 0.
-__global__ void __launch_bounds__(256) k_router_hash(const float* __restrict__ logits,
-                                                     const int32_t* __restrict__ token_ids,
-                                                     const int32_t* __restrict__ tid2eid,
-                                                     int vocab, int T, int E, int k,
-                                                     int32_t* __restrict__ topk_idx,
-                                                     float* __restrict__ topk_w, int* status) {
-  pdl_wait_then_release();
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (t >= T) return;
-  int tid = __ldg(token_ids + t);
-  if (tid < 0 || tid >= vocab) {
-    if (lane == 0) record_error(status, MOE_ERR_DEVICE_BOUNDS);
-    tid = 0;
-  }
-  int e = 0;
-  float l = -INFINITY;
-  if (lane < k) {
-    e = __ldg(tid2eid + (size_t)tid * k + lane);
-    if (e < 0 || e >= E) {
-      record_error(status, MOE_ERR_DEVICE_BOUNDS);
-      e = 0;
-    }
-    l = logits[(size_t)t * E + e];
-  }
-  float lmax = l;
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, off));
-  const float ex = lane < k ? expf(l - lmax) : 0.f;
-  float sum = ex;
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-  if (lane < k) {
-    topk_idx[(size_t)t * k + lane] = e;
-    topk_w[(size_t)t * k + lane] = ex / sum;
-  }
-}
-
 // ---- large batches: approximate logits on the tensor cores, exact logits of the candidates --
 //
 // The logits GEMM of a large batch runs on the tensor cores (bf16 products, fp32 accumulation
@@ -337,6 +295,63 @@ __device__ __forceinline__ void defined_logits(const uint16_t* __restrict__ xt,
       acc[j] = __fadd_rn(acc[j], __shfl_xor_sync(0xffffffffu, acc[j], off));
 #pragma unroll
   for (int j = 0; j < NC; ++j) out[j] = acc[j];
+}
+
+// Hash routing: one warp per token. Lane j < k takes expert e_j = tid2eid[token_ids[t]][j]; the
+// warp forms those k logits itself, in the defined order (defined_logits, four experts per
+// pass over x), and no other logit. The gate weights are exp(l_j - l_max) / sum over the k,
+// computed as k_router_topk computes them for the soft choice (so a table holding the soft
+// choices gives the same bits). A token id or table entry out of range is recorded in the
+// status word and replaced by 0.
+__global__ void __launch_bounds__(256) k_router_hash(const uint16_t* __restrict__ x,
+                                                     const uint16_t* __restrict__ wg,
+                                                     const float* __restrict__ bias,
+                                                     const int32_t* __restrict__ token_ids,
+                                                     const int32_t* __restrict__ tid2eid,
+                                                     int vocab, int T, int d, int E, int k,
+                                                     int32_t* __restrict__ topk_idx,
+                                                     float* __restrict__ topk_w, int* status) {
+  constexpr int kGroup = 4;
+  pdl_wait_then_release();
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  int tid = __ldg(token_ids + t);
+  if (tid < 0 || tid >= vocab) {
+    if (lane == 0) record_error(status, MOE_ERR_DEVICE_BOUNDS);
+    tid = 0;
+  }
+  int e = 0;
+  if (lane < k) {
+    e = __ldg(tid2eid + (size_t)tid * k + lane);
+    if (e < 0 || e >= E) {
+      record_error(status, MOE_ERR_DEVICE_BOUNDS);
+      e = 0;
+    }
+  }
+  const uint16_t* xt = x + (size_t)t * d;
+  float l = -INFINITY;
+  for (int g = 0; g < k; g += kGroup) {
+    int eg[kGroup];
+#pragma unroll
+    for (int j = 0; j < kGroup; ++j) eg[j] = __shfl_sync(0xffffffffu, e, min(g + j, k - 1));
+    float sdef[kGroup];
+    defined_logits<kGroup>(xt, wg, eg, d, lane, sdef);
+#pragma unroll
+    for (int j = 0; j < kGroup; ++j)
+      if (g + j < k && lane == g + j) l = bias ? __fadd_rn(sdef[j], bias[eg[j]]) : sdef[j];
+  }
+  float lmax = l;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, off));
+  const float ex = lane < k ? expf(l - lmax) : 0.f;
+  float sum = ex;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  if (lane < k) {
+    topk_idx[(size_t)t * k + lane] = e;
+    topk_w[(size_t)t * k + lane] = ex / sum;
+  }
 }
 
 // One warp per token; lane j holds experts j + 32m, m < MAXM (E <= 32 MAXM). approx holds the
@@ -680,12 +695,9 @@ cudaError_t launch_route_hash(const moe_shape& s, const uint16_t* x, const uint1
                               const int32_t* tid2eid, int vocab, int32_t* topk_idx,
                               float* topk_w, char* ws, const WsLayout& L, cudaStream_t st) {
   if (s.T == 0) return cudaSuccess;
-  float* logits = reinterpret_cast<float*>(ws + L.logits);
-  cudaError_t e = launch_logits_for(s, x, wg, bias, logits, st);
-  if (e != cudaSuccess) return e;
-  count_launches(2);
-  return launch_pdl(k_router_hash, dim3((unsigned)((s.T + 7) / 8)), dim3(256), 0, st, logits,
-                    token_ids, tid2eid, vocab, s.T, s.E, s.k, topk_idx, topk_w,
+  count_launches(1);
+  return launch_pdl(k_router_hash, dim3((unsigned)((s.T + 7) / 8)), dim3(256), 0, st, x, wg, bias,
+                    token_ids, tid2eid, vocab, s.T, s.d, s.E, s.k, topk_idx, topk_w,
                     reinterpret_cast<int*>(ws + L.status));
 }
 
