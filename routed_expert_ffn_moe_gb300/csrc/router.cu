@@ -5,7 +5,9 @@
 // NVIDIA H200", 0.2.2 step D4); V4 uses learned soft routing ("CANN DeepSeek-V4推理优化", MoE
 // 专家模型规格). Ascend fuses the gate into one "GatingTopK" kernel (same page, 融合Kernel);
 // here the logits GEMM and the selection are two kernels so the selection can see all E
-// logits of a token at once.
+// logits of a token at once. Batches of 1024+ tokens form approximate logits on the tensor
+// cores and recompute only the candidates' logits in the fixed order (same bits; see the
+// section below); hash routing forms only the k hashed logits of each token.
 #include <cstdlib>
 #include <mutex>
 
