@@ -13,6 +13,12 @@
  *                 "DeepSeek-V4-Pro on NVIDIA H200", section 0.1.2 and step D7).
  * On one GPU the dispatch and combine exchanges become in-HBM gathers.
  *
+ * One GPU. The library has no multi-GPU path: every call works on buffers of the current
+ * device only. Its prefill tiles run as pairs of CTAs in a 2-CTA cluster that share each token
+ * tile, each CTA loading half of it into both CTAs' shared memory (a cluster-multicast TMA
+ * load); the tensor maps of those loads describe the caller's buffers on the current device.
+ * Use the library from one-GPU jobs.
+ *
  * Conventions shared by every entry point
  *   - Pointers named x, wg, bias, topk_*, expert_offsets, perm_token, inv_slot, w13, s13, w2,
  *     s2, y_perm, y and ws are DEVICE pointers, allocated and owned by the caller. The library
@@ -112,8 +118,10 @@ MOE_API moe_status moe_route(const moe_shape* shape, const void* x, const void* 
  * and calls no allocating routine. Its logits scratch is a fixed 4 MiB device array inside the
  * library (one copy per GPU that loads the library, kept until the process exits), so it serves
  * shapes with T*E <= 1,048,576 (e.g. T <= 4096 at E = 256) and rejects larger ones with
- * MOE_ERR_INVALID_ARG. The first call on each device looks up that array's device address:
- * make that first call before any stream capture. Every call shares the one array, so calls
+ * MOE_ERR_INVALID_ARG. Each call looks up that array's device address in the current context
+ * (cudaGetSymbolAddress, which allocates nothing), so the address stays right after a
+ * cudaDeviceReset; a device's first call also loads the library's device code there, so make
+ * that first call before any stream capture. Every call shares the one array, so calls
  * that overlap on the GPU (different streams, or different host threads on the same device)
  * race on it; order them on one stream. Nothing in the array needs to start at zero: each call
  * overwrites the logits it reads. It records no device status. */

@@ -9,7 +9,6 @@
 // cores and recompute only the candidates' logits in the fixed order (same bits; see the
 // section below); hash routing forms only the k hashed logits of each token.
 #include <cstdlib>
-#include <mutex>
 
 #include "ffn.h"
 #include "internal.h"
@@ -583,23 +582,16 @@ static __device__ __align__(256) float g_noalloc_logits[kNoAllocLogits];
 
 size_t route_noalloc_max_logits() { return kNoAllocLogits; }
 
-// Device address of the array for the current device, looked up once per device (the first
-// call on a device does this set-up).
+// Device address of the array in the current device's context. It is looked up on every call
+// (cudaGetSymbolAddress allocates nothing and costs a table lookup), so the address stays right
+// after a cudaDeviceReset or under another context on the same device, where the module is
+// loaded again at a new address. On a device's first call the lookup also loads the library's
+// device code, which is why that first call should come before any stream capture.
 static cudaError_t noalloc_logits_ptr(float** out) {
-  static std::mutex mu;
-  static float* ptrs[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_logits);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lk(mu);
-  if (!ptrs[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_logits);
-    if (e != cudaSuccess) return e;
-    ptrs[dev] = static_cast<float*>(p);
-  }
-  *out = ptrs[dev];
+  *out = static_cast<float*>(p);
   return cudaSuccess;
 }
 

@@ -288,13 +288,21 @@ def test_device_generator_matches_host_generator():
 
 
 def sample_tokens(cfg, idx, n_even=6):
-    """Evenly spaced tokens plus tokens of the hottest and the coldest non-empty experts."""
+    """Tokens whose outputs are checked in full. Below 1024 tokens: evenly spaced ones plus two
+    tokens of the hottest and two of the coldest non-empty expert. From 1024 tokens: every
+    s-th token (s = 8, or T/1024 so that at most 1024 tokens are checked) plus two tokens of
+    each of the four hottest and four coldest non-empty experts."""
     T = cfg.T
-    picks = set(np.linspace(0, T - 1, min(n_even, T)).astype(int).tolist())
     counts = np.bincount(idx.ravel(), minlength=cfg.E)
-    hot = int(np.argmax(counts))
-    cold = int(np.argmin(np.where(counts > 0, counts, 1 << 30)))
-    for e in (hot, cold):
+    order = np.argsort(-counts, kind="stable")
+    nonempty = [int(e) for e in order if counts[e] > 0]
+    if T >= 1024:
+        picks = set(range(0, T, max(8, T // 1024)))
+        extremes = nonempty[:4] + nonempty[-4:]
+    else:
+        picks = set(np.linspace(0, T - 1, min(n_even, T)).astype(int).tolist())
+        extremes = nonempty[:1] + nonempty[-1:]
+    for e in extremes:
         rows = np.nonzero((idx == e).any(1))[0]
         picks.update(rows[:2].tolist())
     return sorted(picks)
@@ -302,8 +310,9 @@ def sample_tokens(cfg, idx, n_even=6):
 
 FULL = ["v3_decode", "v4pro_decode", "skewed_prefill", "sweep_fp8_T1", "sweep_fp8_T8",
         "sweep_fp8_T64", "sweep_fp8_T256", "sweep_fp8_T1024", "sweep_fp8_T4096",
-        "sweep_fp8_T16384", "v4pro_decode_fp4", "sweep_fp4_T1", "sweep_fp4_T256",
-        "sweep_fp4_T4096"]
+        "sweep_fp8_T16384", "v4pro_decode_fp4", "sweep_fp4_T1", "sweep_fp4_T8",
+        "sweep_fp4_T64", "sweep_fp4_T256", "sweep_fp4_T1024", "sweep_fp4_T4096",
+        "sweep_fp4_T16384"]
 
 
 @pytest.mark.parametrize("name", FULL)
@@ -329,14 +338,102 @@ def test_maximum_shapes(over):
     check_full(synth.get_config("tiny", **over), "maximum " + str(over))
 
 
+def weights_checksum(dev):
+    """One int64 sum of every 32-bit word of the expert weights and scales (device-side): the
+    layer must leave its inputs as they were."""
+    t = torch()
+    tot = 0
+    for k in ("w13", "w2", "s13", "s2"):
+        v = dev.get(k)
+        if v is not None:
+            tot += int(v.contiguous().view(t.int32).sum(dtype=t.int64).item())
+    return tot
+
+
+def device_expert(cfg, dev, e):
+    """Expert e's weights as the seeded generator drew them on the device (the same bits as
+    synth.host_expert, checked by test_device_generator_matches_host_generator), copied to the
+    host. Drawing them on the host instead costs ~0.2 s an expert at the V3 shape."""
+    t = torch()
+
+    def h(v):
+        if v is None:
+            return None
+        if v.dtype == t.bfloat16:
+            return v[e].view(t.int16).cpu().numpy().view(np.uint16)
+        return v[e].cpu().numpy()
+    return synth.ExpertWeights(h(dev["w13"]), h(dev["w2"]), h(dev["s13"]), h(dev["s2"]))
+
+
+def y_perm_rows_to_check(cfg, r_off, T):
+    """Slots whose expert outputs are checked against the oracle: the last row of every routed
+    expert that received tokens (each expert's weights, wherever they lie in HBM), the first and
+    last rows of the shared segment, and from 1024 tokens every row of the four hottest and the
+    four coldest non-empty experts (their deepest and shallowest token tiles)."""
+    counts = np.diff(r_off[: cfg.E + 1])
+    rows = {int(r_off[e + 1]) - 1 for e in range(cfg.E) if counts[e] > 0}
+    if cfg.n_shared and T > 0:
+        rows.update({int(r_off[cfg.E]), int(r_off[cfg.E + 1]) - 1})
+    if T >= 1024:
+        order = [int(e) for e in np.argsort(-counts, kind="stable") if counts[e] > 0]
+        for e in order[:4] + order[-4:]:
+            rows.update(range(int(r_off[e]), int(r_off[e + 1])))
+    return sorted(rows)
+
+
+def check_y_perm_rows(cfg, layer, dev, x_h, r_off, r_perm, name):
+    slots = y_perm_rows_to_check(cfg, r_off, cfg.T)
+    routed = cfg.T * cfg.k
+    by_expert = {}
+    for s in slots:
+        e = int(np.searchsorted(r_off[: cfg.E + 1], s, side="right") - 1) if s < routed else cfg.E
+        by_expert.setdefault(e, []).append(s)
+    yp = layer.y_perm
+    worst = 0.0
+    for e, ss in sorted(by_expert.items()):
+        toks = [int(r_perm[s]) if s < routed else s - routed for s in ss]
+        ew = device_expert(cfg, dev, e)
+        ref = oracle.expert_rows(x_h[toks], ew.w13, ew.w2, cfg.wdtype, ew.s13, ew.s2)
+        got = yp[ss].cpu().numpy().astype(np.float64)
+        for r in range(len(ss)):
+            rl = rel_l2(got[r], ref[r])
+            worst = max(worst, rl)
+            assert rl <= 1e-2, (name, "expert", e, "slot", ss[r], rl)
+    return len(slots), worst
+
+
+def router_uses_tc(cfg):
+    return cfg.T >= 1024 and cfg.E % 128 == 0 and cfg.d % 64 == 0 and cfg.E <= 1024
+
+
+def check_router_tc_logits(cfg, layer, x_h, wg_h, logits_nobias, name):
+    """From 1024 tokens the router first forms every logit on the tensor cores (without the
+    bias) into the workspace's logits area, and recomputes only the candidates in the defined
+    order. Every one of the T*E approximate logits must lie within the bound the selection
+    assumes, |a - l| <= 2^-12 |x_t| |wg_e|, of the defined fp32 logit l."""
+    t = torch()
+    n = cfg.T * cfg.E
+    approx = layer.ws[256: 256 + 4 * n].view(t.float32).cpu().numpy().reshape(cfg.T, cfg.E)
+    xf = oracle.bf16_to_f64(x_h)
+    wf = oracle.bf16_to_f64(wg_h)
+    bound = 2.0 ** -12 * np.outer(np.linalg.norm(xf, axis=1), np.linalg.norm(wf, axis=1))
+    share = np.abs(approx.astype(np.float64) - logits_nobias.astype(np.float64)) / bound
+    worst = float(share.max())
+    assert worst <= 1.0, (name, "tensor-core logit outside its bound", worst)
+    return worst
+
+
 def check_full(cfg, name):
     dev = synth.device_inputs(cfg)
     w = {k: dev[k] for k in ("wg", "bias", "w13", "w2", "s13", "s2")}
+    before = weights_checksum(dev)
     layer = run_layer(cfg, dev["x"], w)
+    assert weights_checksum(dev) == before, "the layer changed its weights"
     idx = layer.topk_idx.cpu().numpy()
     # routing and permutation: every token, bit for bit
     x_h = synth.host_x(cfg)
-    logits = oracle.router_logits(x_h, synth.host_wg(cfg), synth.host_bias(cfg))
+    wg_h, bias_h = synth.host_wg(cfg), synth.host_bias(cfg)
+    logits = oracle.router_logits(x_h, wg_h, bias_h)
     r_idx, _, r_w64 = oracle.route(logits, cfg.k)
     np.testing.assert_array_equal(idx, r_idx)
     np.testing.assert_allclose(layer.topk_w.cpu().numpy(), r_w64, rtol=0, atol=TOL_TOPK_W)
@@ -344,13 +441,22 @@ def check_full(cfg, name):
     np.testing.assert_array_equal(layer.expert_offsets.cpu().numpy(), r_off)
     np.testing.assert_array_equal(layer.perm_token.cpu().numpy(), r_perm)
     np.testing.assert_array_equal(layer.inv_slot.cpu().numpy(), r_inv)
+    # the tensor-core router's approximate logits, all T*E of them, within their bound
+    if router_uses_tc(cfg):
+        nob = logits if bias_h is None else oracle.router_logits(x_h, wg_h, None)
+        share = check_router_tc_logits(cfg, layer, x_h, wg_h, nob, name)
+        print(f"{name}: largest share of the router bound used by any logit {share:.3g}")
+    # expert outputs (y_perm) of every expert that ran
+    nrows, worst = check_y_perm_rows(cfg, layer, dev, x_h, r_off, r_perm, name)
     # outputs of sampled tokens, each straight from the definition
     toks = sample_tokens(cfg, r_idx)
-    experts = {int(e): synth.host_expert(cfg, int(e)) for e in np.unique(r_idx[toks])}
-    shared = synth.host_expert(cfg, cfg.E) if cfg.n_shared else None
+    experts = {int(e): device_expert(cfg, dev, int(e)) for e in np.unique(r_idx[toks])}
+    shared = device_expert(cfg, dev, cfg.E) if cfg.n_shared else None
     y_ref = oracle.token_outputs(x_h[toks], r_idx[toks], r_w64[toks], experts, shared, cfg.wdtype)
     y_gpu = bf16_host(layer.y)[toks]
-    assert_y_close(y_gpu, y_ref, cfg.wdtype, what=name)
+    ma, rl = assert_y_close(y_gpu, y_ref, cfg.wdtype, what=name)
+    print(f"{name}: {len(toks)} tokens (max-abs {ma:.3g}, rel-L2 {rl:.3g}), {nrows} expert "
+          f"output rows (worst rel-L2 {worst:.3g})")
 
 
 # ---- hash routing ----------------------------------------------------------------------------

@@ -86,3 +86,44 @@ def test_planted_mistake_fails_a_pin(tmp_path, name, old, new):
     assert source.count(old) == 1, f"{name}: the planted line must occur exactly once"
     r = run_pins(tmp_path, source.replace(old, new))
     assert r.returncode == 1, f"{name} survived the pins:\n{r.stdout[-2000:]}"
+
+
+# Mistakes planted in oracle.token_outputs (the per-token output the full-size GPU checks use):
+# each mutated copy of the function replaces the original for the duration of the case, and the
+# token_outputs pins must fail.
+PY_MUTANTS = [
+    ("token_outputs_gate_column_shifted", "y[i] += topk_w64[i, j] * yr",
+     "y[i] += topk_w64[i, (j + 1) % topk_w64.shape[1]] * yr"),
+    ("token_outputs_rows_paired_in_reverse", "for (i, j), yr in zip(pairs, ye):",
+     "for (i, j), yr in zip(pairs, ye[::-1]):"),
+    ("token_outputs_shared_dropped", "if shared is not None:", "if False:"),
+    ("token_outputs_shared_twice",
+     "y += expert_rows(x_rows, shared.w13, shared.w2, wdtype, shared.s13, shared.s2)",
+     "y += 2 * expert_rows(x_rows, shared.w13, shared.w2, wdtype, shared.s13, shared.s2)"),
+    ("token_outputs_expert_of_wrong_choice", "by_expert.setdefault(int(e), []).append((i, j))",
+     "by_expert.setdefault(int(topk_idx[i][0]), []).append((i, j))"),
+]
+
+
+def _run_token_output_pins():
+    import test_oracle_pins as pins
+    for name, over in pins.TOKEN_OUTPUT_CASES:
+        pins.test_token_outputs_equal_the_whole_layer(name, over)
+    for wd in ("bf16", "fp8"):
+        pins.test_token_outputs_of_hash_routing_equal_the_dense_masked_evaluation(wd)
+
+
+def test_unmodified_token_outputs_passes_its_pins():
+    _run_token_output_pins()
+
+
+@pytest.mark.parametrize("name,old,new", PY_MUTANTS, ids=[m[0] for m in PY_MUTANTS])
+def test_planted_mistake_in_token_outputs_fails_a_pin(monkeypatch, name, old, new):
+    import inspect
+    src = inspect.getsource(oracle.token_outputs)
+    assert src.count(old) == 1, f"{name}: the planted line must occur exactly once"
+    ns = dict(vars(oracle))
+    exec(compile(src.replace(old, new), f"<{name}>", "exec"), ns)
+    monkeypatch.setattr(oracle, "token_outputs", ns["token_outputs"])
+    with pytest.raises(AssertionError):
+        _run_token_output_pins()

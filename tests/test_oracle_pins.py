@@ -346,15 +346,9 @@ def test_single_expert_layer_is_a_dense_swiglu_ffn():
     assert np.all(out["topk_idx"] == 0) and np.all(out["topk_w"] == 1.0)
 
 
-@pytest.mark.parametrize("name,over", [("tiny", {}), ("tiny", {"wdtype": "fp8"}),
-                                       ("tiny", {"wdtype": "mxfp4"}),
-                                       ("tiny", {"n_shared": 0, "k": 3}),
-                                       ("tiny", {"router": "zipf", "T": 21})])
-def test_layer_equals_dense_masked_evaluation(name, over):
-    # every expert evaluated on every token with numpy, non-chosen ones weighted 0
-    cfg = synth.get_config(name, **over)
-    inp = synth.host_inputs(cfg)
-    out = oracle.moe_layer(cfg, inp)
+def dense_expert_outputs(cfg, inp):
+    """Every expert's SwiGLU output for every token, [E + n_shared, T, d], with numpy from the
+    format definitions (E4M3 codes by the oracle's golden-pinned decoder, E2M1 by its formula)."""
     X = oracle.bf16_to_f64(inp.x)
 
     def dense_w(ew, which):
@@ -377,13 +371,69 @@ def test_layer_equals_dense_masked_evaluation(name, over):
         W13, Wd = dense_w(ew, "w13"), dense_w(ew, "w2")
         G, U = X @ W13[: cfg.f].T, X @ W13[cfg.f:].T
         Ys.append((G * expit(G) * U) @ Wd.T)
+    return np.stack(Ys)
+
+
+def dense_masked_layer(cfg, Ys, topk_idx, topk_w64):
+    """y = shared + sum over experts of (gate weight, 0 if not chosen) x expert output."""
     mask = np.zeros((cfg.T, cfg.E))
     for t in range(cfg.T):
-        mask[t, out["topk_idx"][t]] = out["topk_w64"][t]
-    y = np.einsum("te,etd->td", mask, np.stack(Ys[: cfg.E]))
+        mask[t, topk_idx[t]] = topk_w64[t]
+    y = np.einsum("te,etd->td", mask, Ys[: cfg.E])
     if cfg.n_shared:
         y += Ys[cfg.E]
+    return y
+
+
+@pytest.mark.parametrize("name,over", [("tiny", {}), ("tiny", {"wdtype": "fp8"}),
+                                       ("tiny", {"wdtype": "mxfp4"}),
+                                       ("tiny", {"n_shared": 0, "k": 3}),
+                                       ("tiny", {"router": "zipf", "T": 21})])
+def test_layer_equals_dense_masked_evaluation(name, over):
+    # every expert evaluated on every token with numpy, non-chosen ones weighted 0
+    cfg = synth.get_config(name, **over)
+    inp = synth.host_inputs(cfg)
+    out = oracle.moe_layer(cfg, inp)
+    y = dense_masked_layer(cfg, dense_expert_outputs(cfg, inp), out["topk_idx"], out["topk_w64"])
     np.testing.assert_allclose(out["y"], y, rtol=1e-10, atol=1e-14)
+
+
+# ---- token_outputs: y of a sample of tokens, as the full-size GPU checks use it ----------------
+
+TOKEN_OUTPUT_CASES = [("tiny", {}), ("tiny", {"wdtype": "fp8"}), ("tiny", {"wdtype": "mxfp4"}),
+                      ("tiny", {"n_shared": 0}), ("tiny", {"n_shared": 0, "wdtype": "fp8"}),
+                      ("tiny", {"router": "zipf", "T": 45}), ("tiny", {"k": 8}),
+                      ("tiny", {"T": 1}), ("tiny", {"T": 1, "wdtype": "mxfp4", "k": 3})]
+
+
+@pytest.mark.parametrize("name,over", TOKEN_OUTPUT_CASES, ids=[str(o) for _, o in TOKEN_OUTPUT_CASES])
+def test_token_outputs_equal_the_whole_layer(name, over):
+    # "第 6 章 超節點", 6.2.6: a token's output is the gate-weighted sum of its experts' outputs
+    # (a1 y1 + a6 y6), plus the always-on shared expert. token_outputs forms it per token from
+    # the routing; it must equal the whole layer's y (pinned to the dense masked evaluation
+    # above) for all tokens, and for a subset given in a scrambled order.
+    cfg = synth.get_config(name, **over)
+    inp = synth.host_inputs(cfg)
+    out = oracle.moe_layer(cfg, inp)
+    experts = {e: inp.experts[e] for e in range(cfg.E)}
+    shared = inp.experts[cfg.E] if cfg.n_shared else None
+    for toks in (list(range(cfg.T)), list(range(cfg.T - 1, -1, -3))):
+        y = oracle.token_outputs(inp.x[toks], out["topk_idx"][toks], out["topk_w64"][toks],
+                                 experts, shared, cfg.wdtype)
+        np.testing.assert_allclose(y, out["y"][toks], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("wdtype", ["bf16", "fp8"])
+def test_token_outputs_of_hash_routing_equal_the_dense_masked_evaluation(wdtype):
+    cfg = synth.get_config("tiny", T=30, k=3, wdtype=wdtype)
+    inp = synth.host_inputs(cfg)
+    table = synth.hash_table(41, cfg.E, cfg.k, seed=3)
+    tid = synth.token_ids(cfg.T, 41, seed=3)
+    idx, _, w64 = oracle.route_hash(oracle.router_logits(inp.x, inp.wg, inp.bias), tid, table)
+    y_ref = dense_masked_layer(cfg, dense_expert_outputs(cfg, inp), idx, w64)
+    y = oracle.token_outputs(inp.x, idx, w64, {e: inp.experts[e] for e in range(cfg.E)},
+                             inp.experts[cfg.E], cfg.wdtype)
+    np.testing.assert_allclose(y, y_ref, rtol=1e-10, atol=1e-14)
 
 
 # ---- a5: combine ----------------------------------------------------------------------------
