@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "ffn.h"
+#include "topk.cuh"
 
 namespace moe {
 namespace {
@@ -41,7 +42,7 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 // plan[row][e]: exclusive prefix over experts of the work of each kernel; entry E1 = total.
 // With a split, row kPlanSplit holds the number of CTAs for the cold list and for the rest,
 // chosen so that both lists take about the same time by a simple cost model.
-__device__ __forceinline__ void plan_block(const int32_t* __restrict__ offsets, const PlanArgs& a,
+__device__ __forceinline__ void plan_block(const int32_t* offsets, const PlanArgs& a,
                                            int32_t* __restrict__ plan) {
   __shared__ float red[32];
   const int E1 = a.E + a.n_shared;
@@ -102,7 +103,7 @@ __device__ __forceinline__ void plan_block(const int32_t* __restrict__ offsets, 
 constexpr int kGatherChunks = 4;
 
 __device__ __forceinline__ void gather_row_chunks(long i, const uint16_t* __restrict__ x,
-                                                  const int32_t* __restrict__ perm_token, int T,
+                                                  const int32_t* perm_token, int T,
                                                   long routed, int d,
                                                   uint16_t* __restrict__ x_perm, int* status) {
   const int d8 = d >> 3;
@@ -110,7 +111,7 @@ __device__ __forceinline__ void gather_row_chunks(long i, const uint16_t* __rest
   if (c0 >= routed * d8) return;
   const long s = c0 / d8;
   const int c = (int)(c0 - s * d8);
-  int t = __ldg(perm_token + s);
+  int t = perm_token[s];  // global or shared memory
   if (t < 0 || t >= T) {
     record_error(status, MOE_ERR_DEVICE_BOUNDS);
     t = 0;
@@ -128,14 +129,14 @@ __device__ __forceinline__ void gather_row_chunks(long i, const uint16_t* __rest
 // (mx_common.cuh). Slot s < routed holds token perm_token[s]; slot routed + t (the shared
 // expert's segment) holds token t. Rows at or beyond nq are not this launch's.
 __device__ __forceinline__ void gather_encode_block(long i, const uint16_t* __restrict__ x,
-                                                    const int32_t* __restrict__ perm_token, int T,
+                                                    const int32_t* perm_token, int T,
                                                     long routed, long nq, int d,
                                                     const mx::Planes& xq, int* status) {
   const int nb = d >> 5;
   const long s = i / nb;
   if (s >= nq) return;
   const int b = (int)(i - s * nb);
-  int t = s < routed ? __ldg(perm_token + s) : (int)(s - routed);
+  int t = s < routed ? perm_token[s] : (int)(s - routed);
   if (t < 0 || t >= T) {
     record_error(status, MOE_ERR_DEVICE_BOUNDS);
     t = 0;
@@ -170,14 +171,14 @@ __device__ __forceinline__ void gather_encode_block(long i, const uint16_t* __re
 // rows as above) as f16, round to nearest, saturating at +-65504 (exact for bf16 values in f16's
 // normal range).
 __device__ __forceinline__ void gather_f16_block(long i, const uint16_t* __restrict__ x,
-                                                 const int32_t* __restrict__ perm_token, int T,
+                                                 const int32_t* perm_token, int T,
                                                  long routed, long nq, int d,
                                                  uint16_t* __restrict__ out, int* status) {
   const int nb = d >> 5;
   const long s = i / nb;
   if (s >= nq) return;
   const int b = (int)(i - s * nb);
-  int t = s < routed ? __ldg(perm_token + s) : (int)(s - routed);
+  int t = s < routed ? perm_token[s] : (int)(s - routed);
   if (t < 0 || t >= T) {
     record_error(status, MOE_ERR_DEVICE_BOUNDS);
     t = 0;
@@ -228,6 +229,109 @@ __global__ void __launch_bounds__(256) k_plan_gather(const int32_t* __restrict__
     gather_f16_block(i, x, perm_token, T, routed, nq, d, x_perm, status);
   else
     gather_row_chunks(i, x, perm_token, T, routed, d, x_perm, status);
+}
+
+// Decode batches of at most 32 tokens (one permutation chunk), moe_forward only: after the
+// router logits, one launch does what k_router_topk, k_perm_small and k_plan_gather do. Every
+// block selects the top k of every token (warp_topk_token, the router's own selection) and
+// sorts the T*k (token, choice) pairs in shared memory exactly as k_perm_small sorts one chunk
+// (a lane per token, one 32-bit mask of tokens per expert, an exclusive scan of the mask
+// popcounts in expert order): at most 32 tokens x 1024 logits and 1024 pairs, a few
+// microseconds, repeated in every block so that no block waits for another. Block 0 then writes
+// the routing, the permutation and the FFN plan; the other blocks gather their share of the
+// rows (GatherMode) with the permutation held in their own shared memory.
+constexpr int kFrontMaxT = kChunkTokens;
+
+__global__ void __launch_bounds__(256) k_route_front(
+    const float* __restrict__ logits, int T, int E, int k, int n_shared,
+    int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ perm_token, int32_t* __restrict__ inv_slot, PlanArgs a,
+    int32_t* __restrict__ plan, const uint16_t* __restrict__ x, long routed, int d,
+    uint16_t* __restrict__ x_perm, int* status, mx::Planes xq, long nq, int mode) {
+  extern __shared__ uint32_t fm[];
+  uint32_t* sel = fm;                                               // [E] token masks
+  int32_t* off_s = reinterpret_cast<int32_t*>(fm + E);              // [E + 2]
+  int32_t* idx_s = off_s + (E + 2);                                 // [T * k]
+  float* w_s = reinterpret_cast<float*>(idx_s + T * k);             // [T * k]
+  int32_t* perm_s = reinterpret_cast<int32_t*>(w_s + T * k);        // [T * k]
+  int32_t* inv_s = perm_s + T * k;                                  // [T * k]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) sel[e] = 0;
+  pdl_wait_then_release();
+  for (int t = warp; t < T; t += (int)(blockDim.x >> 5))
+    warp_topk_token(logits + (size_t)t * E, E, k, idx_s + t * k, w_s + t * k);
+  __syncthreads();
+  // the token masks of the one chunk (lane = token)
+  if (warp == 0 && lane < T) {
+    const int32_t* row = idx_s + lane * k;
+    for (int j = 0; j < k; ++j) {
+      const int e = row[j];
+      bool ok = (unsigned)e < (unsigned)E;
+      for (int j2 = 0; j2 < j && ok; ++j2) ok = row[j2] != e;
+      if (ok)
+        atomicOr(&sel[e], 1u << lane);
+      else if (blockIdx.x == 0)
+        record_error(status, MOE_ERR_DEVICE_BOUNDS);
+    }
+  }
+  __syncthreads();
+  // exclusive scan of the per-expert counts, each thread a run of consecutive experts
+  {
+    const int per = (E + (int)blockDim.x - 1) / (int)blockDim.x;
+    const int e0 = min(E, (int)threadIdx.x * per), e1 = min(E, e0 + per);
+    int sum = 0;
+    for (int e = e0; e < e1; ++e) sum += __popc(sel[e]);
+    int total;
+    int run = block_exclusive_scan(sum, &total);
+    for (int e = e0; e < e1; ++e) {
+      off_s[e] = run;
+      run += __popc(sel[e]);
+    }
+    if (threadIdx.x == 0) {
+      off_s[E] = T * k;
+      off_s[E + 1] = T * k + n_shared * T;
+    }
+  }
+  __syncthreads();
+  if (warp == 0 && lane < T) {
+    const int32_t* row = idx_s + lane * k;
+    const uint32_t below = (1u << lane) - 1u;
+    for (int j = 0; j < k; ++j) {
+      const int e = row[j];
+      bool ok = (unsigned)e < (unsigned)E;
+      for (int j2 = 0; j2 < j && ok; ++j2) ok = row[j2] != e;
+      if (!ok) {
+        inv_s[lane * k + j] = -1;
+        continue;
+      }
+      const int slot = off_s[e] + __popc(sel[e] & below);
+      perm_s[slot] = lane;
+      inv_s[lane * k + j] = slot;
+    }
+  }
+  __syncthreads();
+  if (blockIdx.x == 0) {
+    for (int i = threadIdx.x; i < T * k; i += blockDim.x) {
+      topk_idx[i] = idx_s[i];
+      topk_w[i] = w_s[i];
+      perm_token[i] = perm_s[i];
+      inv_slot[i] = inv_s[i];
+    }
+    for (int e = threadIdx.x; e < E + 2; e += blockDim.x) offsets[e] = off_s[e];
+    plan_block(off_s, a, plan);
+    return;
+  }
+  const long i = (long)(blockIdx.x - 1) * blockDim.x + threadIdx.x;
+  if (mode == kGatherMxTerms)
+    gather_encode_block(i, x, perm_s, T, routed, nq, d, xq, status);
+  else if (mode == kGatherF16)
+    gather_f16_block(i, x, perm_s, T, routed, nq, d, x_perm, status);
+  else
+    gather_row_chunks(i, x, perm_s, T, routed, d, x_perm, status);
+}
+
+size_t front_smem_bytes(int T, int E, int k) {
+  return 4 * ((size_t)E + (E + 2) + 4 * (size_t)T * k);
 }
 
 // Phase events are recorded as external events while the stream is being captured into a CUDA
@@ -339,14 +443,24 @@ __global__ void k_shared_plan(int T, int k, int E, TileShape ts, int32_t* __rest
   }
 }
 
-}  // namespace
 
-cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32_t* perm_token,
-                              const int32_t* offsets, const void* w13, const void* s13,
-                              const void* w2, const void* s2, float* y_perm, char* ws,
-                              const WsLayout& L, cudaStream_t st, bool with_shared) {
-  if (s.T == 0) return cudaSuccess;
-  FfnArgs a{};
+// Everything the FFN passes of one call need: their arguments, the plan kernel's arguments and
+// what the gather writes.
+struct FfnCall {
+  FfnArgs a;
+  PlanArgs pa;
+  int32_t* plan;
+  int stride, tc_min, mode;
+  bool fp8, mxq, decode, use_tc, use_gemv, split;
+  long routed, nq, gather_n;
+};
+
+FfnCall make_ffn_call(const moe_shape& s, const uint16_t* x, const int32_t* perm_token,
+                      const int32_t* offsets, const void* w13, const void* s13, const void* w2,
+                      const void* s2, float* y_perm, char* ws, const WsLayout& L,
+                      bool with_shared) {
+  FfnCall c{};
+  FfnArgs& a = c.a;
   // without the shared expert (moe_forward runs it on its own stream) the tile lists end at E
   a.T = s.T; a.d = s.d; a.E = s.E; a.k = s.k; a.f = s.f; a.n_shared = with_shared ? s.n_shared : 0;
   a.wdtype = s.wdtype;
@@ -356,44 +470,44 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32
   a.x_perm = reinterpret_cast<uint16_t*>(ws + L.x_perm);
   a.y_perm = y_perm;
   a.status = reinterpret_cast<int*>(ws + L.status);
-  const bool mxq = s.wdtype == MOE_W_MXFP4_E8M0_B32;
+  c.mxq = s.wdtype == MOE_W_MXFP4_E8M0_B32;
   const long all_slots = (long)s.T * s.k + (long)s.n_shared * s.T;
-  if (mxq) {
+  if (c.mxq) {
     a.xq = mx::planes_at(ws + L.xq, all_slots, s.d);
     a.hq = mx::planes_at(ws + L.hq, all_slots, s.f);
   }
-  int32_t* plan = reinterpret_cast<int32_t*>(ws + L.plan);
+  c.plan = reinterpret_cast<int32_t*>(ws + L.plan);
 
   // Experts with at least tc_min tokens go to the tensor-core GEMM, the rest to the
   // weight-streaming GEMV. Both stream each weight byte once; the tensor-core kernel does so at
   // full HBM rate from one token up, so by default it takes every expert. MOE_TC_MIN_TOKENS
   // moves the split (a tuning and testing knob; results agree within rounding either way).
   // MXFP4 weights run on the tensor cores only (the block-scaled MMA is their format's path).
-  const int tc_min = mxq ? 1 : tc_min_tokens();
-  const bool fp8 = s.wdtype == MOE_W_FP8_E4M3_B128;
-  const long routed = (long)s.T * s.k;
-  const bool decode = routed <= 32L * s.E;  // at most ~32 tokens per routed expert on average
-  const bool use_tc = tc_min < INT_MAX;
-  const bool use_gemv = tc_min > 1;
-  PlanArgs pa{};
+  c.tc_min = c.mxq ? 1 : tc_min_tokens();
+  c.fp8 = s.wdtype == MOE_W_FP8_E4M3_B128;
+  c.routed = (long)s.T * s.k;
+  c.decode = c.routed <= 32L * s.E;  // at most ~32 tokens per routed expert on average
+  c.use_tc = c.tc_min < INT_MAX;
+  c.use_gemv = c.tc_min > 1;
+  PlanArgs& pa = c.pa;
   pa.E = s.E; pa.n_shared = a.n_shared;
-  pa.tc_min = tc_min;
+  pa.tc_min = c.tc_min;
   pa.group = gemv_group_tokens();
   pa.items_up = gemv_items_per_group(true, s.d, s.f);
   pa.items_dn = gemv_items_per_group(false, s.d, s.f);
-  const TileShape ts = tile_shape(s, fp8, decode, routed);
+  const TileShape ts = tile_shape(s, c.fp8, c.decode, c.routed);
   pa.nt_up = ts.nt_up;
   pa.nt_dn = ts.nt_dn;
   pa.mt_up = ts.mt_up;
   pa.mt_dn = ts.mt_dn;
   pa.stride = s.E + 2;
-  const int stride = pa.stride;
+  c.stride = pa.stride;
   // Split prefill (bf16 weights, all experts on the tensor cores): experts with at most one
   // decode tile of tokens stream their weights through the decode tiles on part of the SMs
   // while the others run the prefill tiles on the rest, on a second stream, so that the
   // HBM-bound and the tensor-bound experts overlap instead of taking turns on every SM.
-  const bool split = s.wdtype == MOE_W_BF16 && !decode && use_tc && !use_gemv && routed > 0;
-  if (split) {
+  c.split = s.wdtype == MOE_W_BF16 && !c.decode && c.use_tc && !c.use_gemv && c.routed > 0;
+  if (c.split) {
     // Measured rates on GB300 (one SM, fitted to split sweeps of the skewed prefill layer):
     // decode tiles stream weights at ~78 GB/s in the gate/up pass and ~52 GB/s in the down pass
     // (shorter tiles); prefill tiles run ~7.4 TFLOP/s (gate/up) and ~8.2 TFLOP/s (down).
@@ -413,33 +527,36 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32
     pa.hot_cost_tok[0] = (float)(4.0 * s.d * s.f / tc_up);
     pa.hot_cost_tok[1] = (float)(2.0 * s.d * s.f / tc_dn);
   }
-
-  const PhaseEvents ev = profile_phase_events();
   // rows the gather writes: the routed slots, plus (MXFP4) the shared segment's rows
-  const long nq = routed + (mxq ? (long)a.n_shared * s.T : 0);
-  const long gather_n = (use_tc && nq > 0) ? nq * (s.d / 8) / kGatherChunks : 0;
-  const int mode = !mxq ? kGatherBf16 : decode ? kGatherMxTerms : kGatherF16;
-  cudaError_t e = launch_pdl(k_plan_gather, dim3((unsigned)(1 + (gather_n + 255) / 256)),
-                             dim3(256), 0, st, offsets, pa, plan, x, perm_token, s.T, routed, s.d,
-                             a.x_perm, a.status, a.xq, nq, mode);
-  count_launches(1);
-  if (e != cudaSuccess) return e;
+  c.nq = c.routed + (c.mxq ? (long)a.n_shared * s.T : 0);
+  c.gather_n = (c.use_tc && c.nq > 0) ? c.nq * (s.d / 8) / kGatherChunks : 0;
+  c.mode = !c.mxq ? kGatherBf16 : c.decode ? kGatherMxTerms : kGatherF16;
+  return c;
+}
+
+// The gate/up and down passes of a call whose plan (and gather) are in place.
+cudaError_t launch_passes(const moe_shape& s, const FfnCall& c, cudaStream_t st) {
+  const FfnArgs& a = c.a;
+  const int32_t* plan = c.plan;
+  const int stride = c.stride;
+  const PhaseEvents ev = profile_phase_events();
   if (ev.begin) record_phase(ev.begin, st);
+  cudaError_t e = cudaSuccess;
 
   // Upper bound on the weight-streaming work: every slot in its own group plus one partial
   // group per expert (the device-side totals are usually far smaller).
-  const long slots = routed + (long)s.n_shared * s.T;
-  const long max_groups = (slots + pa.group - 1) / pa.group + s.E + s.n_shared;
+  const long slots = c.routed + (long)s.n_shared * s.T;
+  const long max_groups = (slots + c.pa.group - 1) / c.pa.group + s.E + s.n_shared;
   const auto cap = [](long v) { return (int)(v < (1L << 30) ? v : (1L << 30)); };
-  const int max_up = use_gemv ? cap(max_groups * pa.items_up) : 0;
-  const int max_dn = use_gemv ? cap(max_groups * pa.items_dn) : 0;
+  const int max_up = c.use_gemv ? cap(max_groups * c.pa.items_up) : 0;
+  const int max_dn = c.use_gemv ? cap(max_groups * c.pa.items_dn) : 0;
   const auto tc = [&](bool gateup, const int32_t* prefix) {
-    return mxq ? launch_tc_mx(a, prefix, gateup, decode, st)
-           : fp8 ? launch_tc_fp8(a, prefix, gateup, decode, st)
-                 : launch_tc(a, prefix, gateup, decode, st);
+    return c.mxq ? launch_tc_mx(a, prefix, gateup, c.decode, st)
+           : c.fp8 ? launch_tc_fp8(a, prefix, gateup, c.decode, st)
+                   : launch_tc(a, prefix, gateup, c.decode, st);
   };
 
-  if (split) {
+  if (c.split) {
     SplitStreams* ss = nullptr;
     if ((e = split_streams(&ss)) != cudaSuccess) return e;
     const int32_t* act = plan + kPlanSplit * stride;
@@ -462,16 +579,63 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32
     return cudaSuccess;
   }
 
-  if (use_tc) e = tc(true, plan + kPlanTcUp * stride);
+  if (c.use_tc) e = tc(true, plan + kPlanTcUp * stride);
   if (e == cudaSuccess)
     e = launch_gemv(a, plan + kPlanGemvUp * stride, plan + kPlanGemvDown * stride, true, max_up, st);
   if (e != cudaSuccess) return e;
   if (ev.mid) record_phase(ev.mid, st);
-  if (use_tc) e = tc(false, plan + kPlanTcDown * stride);
+  if (c.use_tc) e = tc(false, plan + kPlanTcDown * stride);
   if (e == cudaSuccess)
     e = launch_gemv(a, plan + kPlanGemvUp * stride, plan + kPlanGemvDown * stride, false, max_dn, st);
   if (ev.end) record_phase(ev.end, st);
   return e;
+}
+
+}  // namespace
+
+cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32_t* perm_token,
+                              const int32_t* offsets, const void* w13, const void* s13,
+                              const void* w2, const void* s2, float* y_perm, char* ws,
+                              const WsLayout& L, cudaStream_t st, bool with_shared) {
+  if (s.T == 0) return cudaSuccess;
+  const FfnCall c = make_ffn_call(s, x, perm_token, offsets, w13, s13, w2, s2, y_perm, ws, L,
+                                  with_shared);
+  cudaError_t e = launch_pdl(k_plan_gather, dim3((unsigned)(1 + (c.gather_n + 255) / 256)),
+                             dim3(256), 0, st, offsets, c.pa, c.plan, x, perm_token, s.T,
+                             c.routed, s.d, c.a.x_perm, c.a.status, c.a.xq, c.nq, c.mode);
+  count_launches(1);
+  if (e != cudaSuccess) return e;
+  return launch_passes(s, c, st);
+}
+
+// moe_forward on a decode batch of at most 32 tokens with the fp32 router and every expert on the
+// tensor cores: logits, then k_route_front (top-k, permutation, plan and gather in one launch),
+// then the FFN passes and the combine. The outputs are the same bits as the four calls.
+static bool front_applies(const moe_shape& s) {
+  if (s.T < 1 || s.T > kFrontMaxT || tc_min_tokens() != 1) return false;
+  if ((long)s.T * s.k > 32L * s.E) return false;  // the FFN runs its decode tiles
+  return front_smem_bytes(s.T, s.E, s.k) <= 48 * 1024;
+}
+
+static cudaError_t launch_forward_front(const moe_shape& s, const uint16_t* x, const uint16_t* wg,
+                                        const float* bias, const void* w13, const void* s13,
+                                        const void* w2, const void* s2, int32_t* topk_idx,
+                                        float* topk_w, int32_t* offsets, int32_t* perm_token,
+                                        int32_t* inv_slot, float* y_perm, uint16_t* y, char* ws,
+                                        const WsLayout& L, cudaStream_t st) {
+  int* status = reinterpret_cast<int*>(ws + L.status);
+  float* logits = reinterpret_cast<float*>(ws + L.logits);
+  cudaError_t e = launch_router_logits(s, x, wg, bias, logits, st);
+  if (e != cudaSuccess) return e;
+  const FfnCall c = make_ffn_call(s, x, perm_token, offsets, w13, s13, w2, s2, y_perm, ws, L, true);
+  e = launch_pdl(k_route_front, dim3((unsigned)(1 + (c.gather_n + 255) / 256)), dim3(256),
+                 front_smem_bytes(s.T, s.E, s.k), st, logits, s.T, s.E, s.k, s.n_shared, topk_idx,
+                 topk_w, offsets, perm_token, inv_slot, c.pa, c.plan, x, c.routed, s.d,
+                 c.a.x_perm, status, c.a.xq, c.nq, c.mode);
+  count_launches(1);
+  if (e != cudaSuccess) return e;
+  if ((e = launch_passes(s, c, st)) != cudaSuccess) return e;
+  return launch_combine(s, y_perm, inv_slot, topk_w, y, status, st);
 }
 
 // moe_forward: the shared expert's FFN needs neither the routing nor the permutation, so it runs
@@ -490,6 +654,9 @@ cudaError_t launch_forward(const moe_shape& s, const uint16_t* x, const uint16_t
   // overlap; T=16384 14.41 -> 14.06 ms, skewed prefill 5.33 -> 5.24 ms).
   const bool prefill = (long)s.T * s.k > 32L * s.E;
   const bool overlap = s.n_shared == 1 && s.T > 0 && prefill && tc_min_tokens() == 1;
+  if (!overlap && front_applies(s) && !router_uses_tc(s))
+    return launch_forward_front(s, x, wg, bias, w13, s13, w2, s2, topk_idx, topk_w, offsets,
+                                perm_token, inv_slot, y_perm, y, ws, L, st);
   if (!overlap) {
     if ((e = launch_route(s, x, wg, bias, topk_idx, topk_w, ws, L, st)) != cudaSuccess) return e;
     if ((e = launch_permute(s, topk_idx, offsets, perm_token, inv_slot, ws, L, st)) != cudaSuccess)

@@ -76,6 +76,11 @@ cudaError_t launch_route_hash(const moe_shape& s, const uint16_t* x, const uint1
                               const float* bias, const int32_t* token_ids,
                               const int32_t* tid2eid, int vocab, int32_t* topk_idx,
                               float* topk_w, char* ws, const WsLayout& L, cudaStream_t st);
+// the fp32 router's logits alone, in the defined order (router.cu); whether a batch takes the
+// tensor-core router instead
+cudaError_t launch_router_logits(const moe_shape& s, const uint16_t* x, const uint16_t* wg,
+                                 const float* bias, float* logits, cudaStream_t st);
+bool router_uses_tc(const moe_shape& s);
 cudaError_t launch_permute(const moe_shape& s, const int32_t* topk_idx, int32_t* offsets,
                            int32_t* perm_token, int32_t* inv_slot, char* ws, const WsLayout& L,
                            cudaStream_t st);

@@ -12,6 +12,7 @@
 
 #include "ffn.h"
 #include "internal.h"
+#include "topk.cuh"
 
 namespace moe {
 namespace {
@@ -147,62 +148,15 @@ __global__ void __launch_bounds__(256) k_router_logits_x2(const uint16_t* __rest
       }
 }
 
-// (value desc, index asc): is (la, ea) ranked before (lb, eb)?
-__device__ __forceinline__ bool ranks_before(float la, int ea, float lb, int eb) {
-  return la > lb || (la == lb && ea < eb);
-}
-
 // One warp per token: k rounds of warp-wide arg-max over the E logits (lane j holds experts
 // j, j+32, ...), then the gate weights softmax(l_chosen) = exp(l_j - l_max) / sum.
 __global__ void __launch_bounds__(256) k_router_topk(const float* __restrict__ logits, int T,
                                                      int E, int k, int32_t* __restrict__ topk_idx,
                                                      float* __restrict__ topk_w) {
   pdl_wait_then_release();
-  const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
-  const float* lt = logits + (size_t)t * E;
-  float l[32];
-#pragma unroll
-  for (int m = 0; m < 32; ++m) l[m] = (lane + 32 * m < E) ? lt[lane + 32 * m] : -INFINITY;
-  uint32_t taken = 0;
-  float my_l = -INFINITY;
-  int my_e = 0;
-  for (int j = 0; j < k; ++j) {
-    float bl = -INFINITY;
-    int be = 0x7FFFFFFF;
-#pragma unroll
-    for (int m = 0; m < 32; ++m) {
-      const int e = lane + 32 * m;
-      if (e < E && !((taken >> m) & 1u) && ranks_before(l[m], e, bl, be)) {
-        bl = l[m];
-        be = e;
-      }
-    }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-      const float ol = __shfl_xor_sync(0xffffffffu, bl, off);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-      if (ranks_before(ol, oe, bl, be)) {
-        bl = ol;
-        be = oe;
-      }
-    }
-    if ((be & 31) == lane) taken |= 1u << (be >> 5);
-    if (lane == j) {
-      my_l = bl;
-      my_e = be;
-    }
-  }
-  const float lmax = __shfl_sync(0xffffffffu, my_l, 0);
-  const float ex = lane < k ? expf(my_l - lmax) : 0.f;
-  float sum = ex;
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-  if (lane < k) {
-    topk_idx[(size_t)t * k + lane] = my_e;
-    topk_w[(size_t)t * k + lane] = ex / sum;
-  }
+  warp_topk_token(logits + (size_t)t * E, E, k, topk_idx + (size_t)t * k, topk_w + (size_t)t * k);
 }
 
 // ---- large batches: approximate logits on the tensor cores, exact logits of the candidates --
@@ -620,8 +574,14 @@ static float router_tc_bound() {
   return v && *v ? (float)atof(v) : kBoundC;
 }
 
-static bool router_uses_tc(const moe_shape& s) {
+bool router_uses_tc(const moe_shape& s) {
   return s.E % 128 == 0 && s.d % 64 == 0 && s.E <= 1024 && s.T >= router_tc_min_tokens();
+}
+
+cudaError_t launch_router_logits(const moe_shape& s, const uint16_t* x, const uint16_t* wg,
+                                 const float* bias, float* logits, cudaStream_t st) {
+  count_launches(1);
+  return launch_logits_for(s, x, wg, bias, logits, st);
 }
 
 template <int MAXM>

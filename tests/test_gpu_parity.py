@@ -197,6 +197,10 @@ def test_combine_direct():
 
 
 @pytest.mark.parametrize("over", [{}, {"wdtype": "fp8"},
+                                  # decode batches of at most 32 tokens: the fused front
+                                  {"T": 1, "wdtype": "fp8"}, {"T": 32, "E": 40, "k": 6},
+                                  {"T": 7, "E": 384, "k": 6, "wdtype": "mxfp4"},
+                                  {"T": 32, "E": 1024, "k": 32, "d": 256, "f": 128},
                                   {"router": "zipf", "T": 600, "d": 512, "f": 256, "E": 16, "k": 2},
                                   {"T": 600, "d": 512, "f": 256, "E": 8, "k": 2, "wdtype": "fp8"},
                                   {"n_shared": 0}, {"wdtype": "mxfp4"},
@@ -290,14 +294,14 @@ def test_device_generator_matches_host_generator():
 def sample_tokens(cfg, idx, n_even=6):
     """Tokens whose outputs are checked in full. Below 1024 tokens: evenly spaced ones plus two
     tokens of the hottest and two of the coldest non-empty expert. From 1024 tokens: every
-    s-th token (s = 8, or T/1024 so that at most 1024 tokens are checked) plus two tokens of
+    s-th token (s = 8, or T/512 so that at most 512 tokens are checked) plus two tokens of
     each of the four hottest and four coldest non-empty experts."""
     T = cfg.T
     counts = np.bincount(idx.ravel(), minlength=cfg.E)
     order = np.argsort(-counts, kind="stable")
     nonempty = [int(e) for e in order if counts[e] > 0]
     if T >= 1024:
-        picks = set(range(0, T, max(8, T // 1024)))
+        picks = set(range(0, T, max(8, T // 512)))
         extremes = nonempty[:4] + nonempty[-4:]
     else:
         picks = set(np.linspace(0, T - 1, min(n_even, T)).astype(int).tolist())
