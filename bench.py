@@ -370,22 +370,32 @@ def measure(cfg, steps, warmup, graph=True, e2e_steps=None, min_ms=None, keep_in
     moe.moe_check_device_status(layer.ws)
 
     # One step = one layer pass (one moe_forward call), captured once into a CUDA graph (the
-    # library enqueues no synchronisation or allocation) and replayed; the library's phase
-    # events are captured with it and re-recorded by every replay.
-    g = None
-    moe.moe_profile_enable(True)
+    # library enqueues no synchronisation or allocation) and replayed. The timed graph holds the
+    # layer's kernels alone (an event recorded between two kernels would cut the programmatic
+    # launch overlap between them); a second graph, captured with the library's phase events,
+    # times the gate/up and down passes.
+    g = gp = None
+    moe.moe_profile_enable(True)    # resets the launch counter
+    moe.moe_profile_enable(False)   # no phase events; launches are still counted
     if graph:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             layer.forward(x)
-        for _ in range(2):
-            g.replay()
+        launches_per_step = moe.moe_profile_read()["kernel_launches"]
+        moe.moe_profile_enable(True)
+        gp = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gp):
+            layer.forward(x)
+        moe.moe_profile_enable(False)
+        for gr in (g, gp):
+            for _ in range(2):
+                gr.replay()
         torch.cuda.synchronize()
     else:
         layer.forward(x)
         torch.cuda.synchronize()
-    launches_per_step = moe.moe_profile_read()["kernel_launches"]
-    moe.moe_profile_enable(False)
+        launches_per_step = moe.moe_profile_read()["kernel_launches"]
+        moe.moe_profile_enable(False)
 
     def step():
         if g is not None:
@@ -418,11 +428,11 @@ def measure(cfg, steps, warmup, graph=True, e2e_steps=None, min_ms=None, keep_in
 
         # Phases of the FFN (gate/up and down) averaged over `steps` more passes: each pass is
         # read back before the next so that every pass's own events are counted.
-        # (A graph replays the events captured with it; eager passes get fresh ones.)
+        # (The phase graph replays the events captured with it; eager passes get fresh ones.)
         up = dn = 0.0
         for _ in range(steps):
-            if g is not None:
-                g.replay()
+            if gp is not None:
+                gp.replay()
             else:
                 moe.moe_profile_enable(True)
                 layer.forward(x)
@@ -502,7 +512,7 @@ def measure(cfg, steps, warmup, graph=True, e2e_steps=None, min_ms=None, keep_in
     }
     if keep_inputs:
         res["dev"] = dev
-    del g, layer, w, x, x_host, y_host
+    del g, gp, layer, w, x, x_host, y_host
     if not keep_inputs:
         del dev
     torch.cuda.synchronize()

@@ -238,8 +238,9 @@ __global__ void __launch_bounds__(256) k_plan_gather(const int32_t* __restrict__
 // (a lane per token, one 32-bit mask of tokens per expert, an exclusive scan of the mask
 // popcounts in expert order): at most 32 tokens x 1024 logits and 1024 pairs, a few
 // microseconds, repeated in every block so that no block waits for another. Block 0 then writes
-// the routing, the permutation and the FFN plan; the other blocks gather their share of the
-// rows (GatherMode) with the permutation held in their own shared memory.
+// the routing, the permutation and the tensor-core passes' tile prefixes; the other blocks
+// gather their share of the rows (GatherMode) with the permutation held in their own shared
+// memory.
 constexpr int kFrontMaxT = kChunkTokens;
 
 __global__ void __launch_bounds__(256) k_route_front(
@@ -318,7 +319,31 @@ __global__ void __launch_bounds__(256) k_route_front(
       inv_slot[i] = inv_s[i];
     }
     for (int e = threadIdx.x; e < E + 2; e += blockDim.x) offsets[e] = off_s[e];
-    plan_block(off_s, a, plan);
+    // the plan rows the decode passes read (every expert on the tensor cores, no split): the
+    // tile prefixes of the gate/up and the down pass, as plan_block writes them
+    const int E1 = a.E + a.n_shared;
+    const int per = (E1 + (int)blockDim.x - 1) / (int)blockDim.x;
+    const int e0 = min(E1, (int)threadIdx.x * per), e1 = min(E1, e0 + per);
+    int su = 0, sd = 0;
+    for (int e = e0; e < e1; ++e) {
+      const int cnt = off_s[e + 1] - off_s[e];
+      su += cnt > 0 ? (cnt + a.nt_up - 1) / a.nt_up * a.mt_up : 0;
+      sd += cnt > 0 ? (cnt + a.nt_dn - 1) / a.nt_dn * a.mt_dn : 0;
+    }
+    int tot_u, tot_d;
+    int ru = block_exclusive_scan(su, &tot_u);
+    int rd = block_exclusive_scan(sd, &tot_d);
+    for (int e = e0; e < e1; ++e) {
+      const int cnt = off_s[e + 1] - off_s[e];
+      plan[kPlanTcUp * a.stride + e] = ru;
+      plan[kPlanTcDown * a.stride + e] = rd;
+      ru += cnt > 0 ? (cnt + a.nt_up - 1) / a.nt_up * a.mt_up : 0;
+      rd += cnt > 0 ? (cnt + a.nt_dn - 1) / a.nt_dn * a.mt_dn : 0;
+    }
+    if (threadIdx.x == 0) {
+      plan[kPlanTcUp * a.stride + E1] = tot_u;
+      plan[kPlanTcDown * a.stride + E1] = tot_d;
+    }
     return;
   }
   const long i = (long)(blockIdx.x - 1) * blockDim.x + threadIdx.x;

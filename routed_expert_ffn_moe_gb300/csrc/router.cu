@@ -148,6 +148,66 @@ __global__ void __launch_bounds__(256) k_router_logits_x2(const uint16_t* __rest
       }
 }
 
+// Batches of at most kSmallT tokens: the same per-logit order, one warp per expert. The block
+// first copies the T token rows into shared memory; each lane then issues the loads of up to 32
+// of its 8-element chunks of wg_e at once (one round trip to HBM instead of one per few chunks)
+// and runs its fused multiply-add chain over them in the defined order against the token rows
+// in shared memory.
+constexpr int kSmallT = 4;
+constexpr int kSmallBatch = 32;  // chunks of wg_e in flight per lane
+
+__global__ void __launch_bounds__(128) k_router_logits_small(const uint16_t* __restrict__ x,
+                                                             const uint16_t* __restrict__ wg,
+                                                             const float* __restrict__ bias,
+                                                             int T, int d, int E,
+                                                             float* __restrict__ logits) {
+  extern __shared__ uint4 xs[];  // [T][d / 8]
+  pdl_wait_then_release();
+  const int lane = threadIdx.x & 31;
+  const int chunks = d >> 3;
+  for (int i = threadIdx.x; i < T * chunks; i += blockDim.x)
+    xs[i] = ldg_u4(reinterpret_cast<const uint4*>(x) + i);
+  __syncthreads();
+  const int e = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (e >= E) return;
+  const uint4* we = reinterpret_cast<const uint4*>(wg + (size_t)e * d);
+  float acc[kSmallT];
+#pragma unroll
+  for (int t = 0; t < kSmallT; ++t) acc[t] = 0.f;
+  const int mine = (chunks - lane + 31) / 32;  // chunks lane, lane + 32, ... below `chunks`
+  for (int b0 = 0; b0 < mine; b0 += kSmallBatch) {
+    uint4 w[kSmallBatch];
+#pragma unroll
+    for (int i = 0; i < kSmallBatch; ++i)
+      if (b0 + i < mine) w[i] = __ldg(we + lane + 32 * (b0 + i));
+#pragma unroll
+    for (int i = 0; i < kSmallBatch; ++i) {
+      if (b0 + i >= mine) break;
+      const int c = lane + 32 * (b0 + i);
+#pragma unroll
+      for (int t = 0; t < kSmallT; ++t) {
+        if (t >= T) break;
+        const uint4 xv = xs[t * chunks + c];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          acc[t] = __fmaf_rn(bf16x8_elem(xv, j), bf16x8_elem(w[i], j), acc[t]);
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1)
+#pragma unroll
+    for (int t = 0; t < kSmallT; ++t)
+      acc[t] = __fadd_rn(acc[t], __shfl_xor_sync(0xffffffffu, acc[t], off));
+  if (lane < T) {
+    float a = acc[0];
+#pragma unroll
+    for (int t = 1; t < kSmallT; ++t)
+      if (lane == t) a = acc[t];
+    logits[(size_t)lane * E + e] = bias ? __fadd_rn(a, bias[e]) : a;
+  }
+}
+
 // One warp per token: k rounds of warp-wide arg-max over the E logits (lane j holds experts
 // j, j+32, ...), then the gate weights softmax(l_chosen) = exp(l_j - l_max) / sum.
 __global__ void __launch_bounds__(256) k_router_topk(const float* __restrict__ logits, int T,
@@ -518,6 +578,15 @@ cudaError_t launch_logits_for(const moe_shape& s, const uint16_t* x, const uint1
   // At these batch sizes the logits are latency-bound: one or two experts a warp (more warps in
   // flight) and eight chunk loads in flight a lane (measured: FP8 T=1 layer 127.7 -> 124.2 us,
   // MXFP4 T=8 272.9 -> 266.3 us).
+  if (s.T <= kSmallT) {
+    const size_t smem = (size_t)s.T * s.d * 2;
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(k_router_logits_small, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+      return cudaGetLastError();
+    return launch_pdl(k_router_logits_small, dim3((unsigned)((s.E + 3) / 4)), dim3(128), smem, st,
+                      x, wg, bias, s.T, s.d, s.E, logits);
+  }
   if (s.T <= 8) return launch_logits<1, 1, 8>(x, wg, bias, s.T, s.d, s.E, logits, st);
   if (s.T <= 32) return launch_logits<1, 2, 8>(x, wg, bias, s.T, s.d, s.E, logits, st);
   if (s.T < 64) return launch_logits<1, 8>(x, wg, bias, s.T, s.d, s.E, logits, st);
