@@ -14,10 +14,9 @@
  * On one GPU the dispatch and combine exchanges become in-HBM gathers.
  *
  * One GPU. The library has no multi-GPU path: every call works on buffers of the current
- * device only. Its prefill tiles run as pairs of CTAs in a 2-CTA cluster that share each token
- * tile, each CTA loading half of it into both CTAs' shared memory (a cluster-multicast TMA
- * load); the tensor maps of those loads describe the caller's buffers on the current device.
- * Use the library from one-GPU jobs.
+ * device only, and no kernel loads from another GPU's memory or multicasts a load. Its prefill
+ * tiles run on CTA pairs (tcgen05 cta_group::2): each CTA of a 2-CTA cluster loads its own
+ * weight rows and half of the token tile, and one MMA of the pair reads both CTAs' operands.
  *
  * Conventions shared by every entry point
  *   - Pointers named x, wg, bias, topk_*, expert_offsets, perm_token, inv_slot, w13, s13, w2,

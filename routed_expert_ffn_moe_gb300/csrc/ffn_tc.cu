@@ -33,9 +33,11 @@ using namespace tc;
 // gate/up pass, one or two consecutive 128-row tiles of W_d in the down pass. ACCB accumulator
 // buffers: 2 lets the epilogue of one tile overlap the next tile's mainloop; wide tiles
 // (KA * NT = 512 columns) fill TMEM with a single buffer.
-template <int NT, int STAGES, int KA, int ACCB>
+template <int NT, int STAGES, int KA, int ACCB, bool PAIR = false>
 struct Smem {
-  static constexpr uint32_t kStageBytes = KA * kATileBytes + (uint32_t)NT * kBK * 2;
+  // weight tiles and token rows of one stage (CTA pairs: half of the token tile in each CTA)
+  static constexpr uint32_t kBBytes = (uint32_t)(PAIR ? NT / 2 : NT) * kBK * 2;
+  static constexpr uint32_t kStageBytes = KA * kATileBytes + kBBytes;
   static constexpr uint32_t kTilesBytes = STAGES * kStageBytes;
   static constexpr uint32_t kBarBytes = 8 * (2 * STAGES + 4) + 16;
   static constexpr uint32_t kTotal = kTilesBytes + kBarBytes + 1024;  // + alignment slack
@@ -52,7 +54,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     k_tc_ffn(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b0,
              const __grid_constant__ CUtensorMap tm_b1, const __grid_constant__ CUtensorMap tm_b0w,
              const __grid_constant__ CUtensorMap tm_b1w, const TcParams p) {
-  using S = Smem<NT, STAGES, KA, ACCB>;
+  using S = Smem<NT, STAGES, KA, ACCB, PAIR>;
   static_assert(S::kTmemCols <= 512 && (S::kTmemCols & (S::kTmemCols - 1)) == 0, "TMEM cols");
   static_assert(NT % 16 == 0 && NT >= 16 && NT <= 256, "MMA N");
   static_assert(!GATEUP || KA == 2, "gate/up tiles pair the gate and up rows");
@@ -69,9 +71,11 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E1 = p.E + p.n_shared;
   const int kblocks = p.K / kBK;
-  // Cluster pairs: both CTAs walk the same list of (expert, m-tile pair, token tile) entries;
-  // this CTA takes m-tile 2 * mt + rank, and the token tile, which both need, is loaded half by
-  // each CTA and multicast to both.
+  // CTA pairs (cta_group::2): both CTAs walk the same list of (expert, m-tile pair, token tile)
+  // entries; this CTA takes m-tile 2 * mt + rank and loads its own weight rows and half of the
+  // tile's (padded) token rows, the even CTA issues MMAs of M = 256 that read both CTAs'
+  // operands, and each CTA's tensor memory receives its own 128 rows. Every load of either CTA
+  // completes on the even CTA's stage barrier; the MMA commits free the stage in both.
   int nact = (int)gridDim.x;
   if (p.active) {
     pdl_wait_then_release();  // the count is written by the plan kernel
@@ -79,6 +83,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     if ((int)blockIdx.x >= nact) return;
   }
   const int rank = PAIR ? (int)cluster_ctarank() : 0;
+  const bool issuer_cta = rank == 0;  // the CTA whose threads issue the MMAs
   const int tile0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
   const int tstep = PAIR ? nact >> 1 : nact;
   const auto decode = [&](int tile, Tile& t) {
@@ -88,12 +93,12 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], (PAIR ? 2 : 1) * KA);  // MMA commits: each issuer, both CTAs of a pair
+      mbar_init(&full[s], 1);       // the (even CTA's) producer, + TMA bytes
+      mbar_init(&empty[s], KA);     // MMA commits: one per issuer
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], KA);  // one commit per issuer
-      mbar_init(&acc_empty[b], 4);  // one arrival per epilogue warp
+      mbar_init(&acc_empty[b], PAIR ? 8 : 4);  // epilogue warps (of both CTAs of a pair)
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -104,12 +109,17 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     prefetch_tmap(&tm_b1w);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_holder, S::kTmemCols);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(tmem_holder, S::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_holder, S::kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
-  if (PAIR) cluster_sync();  // the peer's barriers are initialised before any multicast
+  if (PAIR) cluster_sync();  // both CTAs' barriers are initialised before either signals the other
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   // the tile list (prefix) is written by the previous kernel
@@ -121,14 +131,19 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();  // weights: streamed once per call
       const uint64_t pol_b = policy_evict_last();   // token rows: reused by every weight tile
+      const uint32_t full0 = PAIR ? mapa_shared(smem_u32(&full[0]), 0) : 0;
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       for (int tile = tile0; ok && tile < total; tile += tstep) {
         Tile t;
         decode(tile, t);
-        const bool wide = t.ntok == NT;   // full token tile: one TMA box of NT rows
-        const int nbox = (t.ntok + kBoxRows - 1) / kBoxRows;
-        const uint32_t bytes = KA * kATileBytes + (uint32_t)nbox * kBBoxBytes;
+        const bool wide = t.ntok == NT;   // full token tile: one TMA box (NT, or NT/2 rows)
+        // this CTA's token rows: all of them, or (pairs) half of the padded count
+        const int half = PAIR ? ((t.ntok + 15) & ~15) / 2 : t.ntok;
+        const int row0 = t.brow0 + rank * half;
+        const int nbox = (half + kBoxRows - 1) / kBoxRows;
+        const uint32_t bytes =
+            KA * kATileBytes + (wide ? S::kBBytes : (uint32_t)nbox * kBBoxBytes);
         // gate/up: 128 features, rows [f0, f0+128) (gate) and [f + f0, ...) (up);
         // down: KA consecutive 128-row tiles of W_d
         const int wrow = t.e * p.rows_per_expert + t.mt * (GATEUP ? kBM : kBM * KA);
@@ -139,22 +154,27 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!wait_bar(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
           uint8_t* st = smem + stage * S::kStageBytes;
+          uint8_t* bt = st + KA * kATileBytes;
+          if (PAIR) {
+            // both CTAs load the same number of bytes, so the even CTA expects twice its own
+            if (issuer_cta) mbar_arrive_expect_tx(&full[stage], 2 * bytes);
+            const uint32_t bar = full0 + 8u * stage;
+            tma_load_2d_pair(st, &tm_w, bar, kb * kBK, wrow, pol_w);
+            if (KA == 2) tma_load_2d_pair(st + kATileBytes, &tm_w, bar, kb * kBK, wrow1, pol_w);
+            if (wide) {
+              tma_load_2d_pair(bt, bmapw, bar, kb * kBK, row0, pol_b);
+            } else {
+              for (int i = 0; i < nbox; ++i)
+                tma_load_2d_pair(bt + i * kBBoxBytes, bmap, bar, kb * kBK, row0 + i * kBoxRows,
+                                 pol_b);
+            }
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            continue;
+          }
           mbar_arrive_expect_tx(&full[stage], bytes);
           tma_load_2d(st, &tm_w, &full[stage], kb * kBK, wrow, pol_w);
           if (KA == 2) tma_load_2d(st + kATileBytes, &tm_w, &full[stage], kb * kBK, wrow1, pol_w);
-          uint8_t* bt = st + KA * kATileBytes;
-          if (PAIR) {
-            // full tile: this CTA's half of the rows (the wide map's box is NT/2 rows);
-            // partial tile: every other 16-row box; both CTAs receive every byte
-            if (wide) {
-              tma_load_2d_mc(bt + rank * (NT / 2) * (kBK * 2), bmapw, &full[stage], kb * kBK,
-                             t.brow0 + rank * (NT / 2), 0x3, pol_b);
-            } else {
-              for (int i = rank; i < nbox; i += 2)
-                tma_load_2d_mc(bt + i * kBBoxBytes, bmap, &full[stage], kb * kBK,
-                               t.brow0 + i * kBoxRows, 0x3, pol_b);
-            }
-          } else if (wide) {
+          if (wide) {
             tma_load_2d(bt, bmapw, &full[stage], kb * kBK, t.brow0, pol_b);
           } else {
             for (int i = 0; i < nbox; ++i)
@@ -164,18 +184,19 @@ __global__ void __launch_bounds__(kThreadsB, 1)
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
       }
-      // Every load this thread issued has landed before the CTA may exit.
+      // Every load issued has landed before the CTA may exit (in pairs the even CTA's barrier
+      // counts both CTAs' bytes), and in pairs the MMA commits for every issued stage have
+      // arrived here.
       for (int s = 0; s < STAGES; ++s) {
         const uint32_t issued_phase = (s < (int)stage) ? phase : (phase ^ 1u);
-        drain_bar(&full[s], issued_phase, p.status);
-        // with pairs, both CTAs' MMA commits for every issued stage arrive before the CTA exits
+        if (!PAIR || issuer_cta) drain_bar(&full[s], issued_phase, p.status);
         if (PAIR) drain_bar(&empty[s], issued_phase, p.status);
       }
     }
   } else if (warp == 1 || warp == 6) {
     // ---------------- MMA issuers: warp 1 weight tile 0, warp 6 weight tile 1 ----------------
     const int o = warp == 1 ? 0 : 1;
-    if (lane == 0 && o < KA) {
+    if (lane == 0 && o < KA && issuer_cta) {
       uint32_t stage = 0, phase = 0;
       uint32_t acc = 0, acc_phase = 0;
       bool ok = true;
@@ -183,7 +204,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         Tile t;
         decode(tile, t);
         const int npad = (t.ntok + 15) & ~15;
-        const uint32_t idesc = idesc_bf16(kBM, npad);
+        const uint32_t idesc = idesc_bf16(PAIR ? 2 * kBM : kBM, npad);
         if (!wait_bar(&acc_empty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t d0 = tmem_base + acc * S::kAccCols + o * NT;
@@ -193,32 +214,43 @@ __global__ void __launch_bounds__(kThreadsB, 1)
           const uint32_t st = smem_u32(smem + stage * S::kStageBytes);
           const uint64_t da = sw128_desc(st + o * kATileBytes);
           const uint64_t db = sw128_desc(st + KA * kATileBytes);
+          if (PAIR) {
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            mma_bf16_ss(d0, da + 2 * kk, db + 2 * kk, idesc, (kb | kk) ? 1u : 0u);
-          if (PAIR)
-            mma_commit_mc(&empty[stage], 0x3);  // frees the stage in both CTAs of the pair
-          else
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              mma_ss_pair(d0, da + 2 * kk, db + 2 * kk, idesc, (kb | kk) ? 1u : 0u);
+            mma_commit_pair(&empty[stage]);  // frees the stage in both CTAs of the pair
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              mma_bf16_ss(d0, da + 2 * kk, db + 2 * kk, idesc, (kb | kk) ? 1u : 0u);
             mma_commit(&empty[stage]);  // frees the stage once these MMAs have read it
+          }
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        mma_commit(&acc_full[acc]);   // accumulator ready for the epilogue
+        if (PAIR)
+          mma_commit_pair(&acc_full[acc]);  // accumulators ready for both CTAs' epilogues
+        else
+          mma_commit(&acc_full[acc]);       // accumulator ready for the epilogue
         if (++acc == ACCB) { acc = 0; acc_phase ^= 1u; }
       }
     }
   } else if (warp < 6) {
     // ---------------- epilogue (warps 2..5) ----------------
     run_epilogue<GATEUP, NT, S::kAccCols, KA, ACCB>(p, total, tmem_base, acc_full, acc_empty,
-                                                    abort_flag, tile0, tstep, PAIR ? rank : -1);
+                                                    abort_flag, tile0, tstep, PAIR ? rank : -1, 2,
+                                                    PAIR && !issuer_cta);
   }
 
   tc_fence_before();
   __syncthreads();
-  if (PAIR) cluster_sync();  // no CTA leaves while its peer may still write to it
+  if (PAIR) cluster_sync();  // no CTA leaves while its peer may still signal it
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, S::kTmemCols);
+    if (PAIR)
+      tmem_dealloc_pair(tmem_base, S::kTmemCols);
+    else
+      tmem_dealloc(tmem_base, S::kTmemCols);
   }
 }
 
@@ -226,7 +258,7 @@ template <bool GATEUP, int NT, int STAGES, int KA, int ACCB, bool PAIR = false>
 cudaError_t launch_variant(const CUtensorMap& w, const CUtensorMap& b0, const CUtensorMap& b1,
                            const CUtensorMap& b0w, const CUtensorMap& b1w, const TcParams& p,
                            cudaStream_t st) {
-  using S = Smem<NT, STAGES, KA, ACCB>;
+  using S = Smem<NT, STAGES, KA, ACCB, PAIR>;
   static_assert(S::kTotal <= 227 * 1024, "shared memory");
   auto kern = k_tc_ffn<GATEUP, NT, STAGES, KA, ACCB, PAIR>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -254,8 +286,8 @@ int tc_tile_rows(bool gateup, bool decode, int d) {
   return (!gateup && down_pairs(d, decode)) ? 2 * kBM : kBM;
 }
 
-// Prefill tiles with two weight tiles per token tile run in cluster pairs (consecutive m-tiles,
-// token tile multicast) when an expert has an even number of such tiles.
+// Prefill tiles with two weight tiles per token tile run on CTA pairs (cta_group::2: consecutive
+// m-tiles, half of the token tile in each CTA) when an expert has an even number of such tiles.
 static bool tc_clustered(bool gateup, bool decode, int d, int f) {
   if (decode || (!gateup && !down_pairs(d, decode))) return false;
   return ((gateup ? f : d) / tc_tile_rows(gateup, decode, d)) % 2 == 0;
@@ -284,7 +316,7 @@ cudaError_t launch_tc(const FfnArgs& a, const int32_t* prefix, bool gateup, bool
   const uint64_t routed = (uint64_t)a.T * a.k;
   const uint64_t slots = routed + (uint64_t)a.n_shared * a.T;
   const bool cl = tc_clustered(gateup, decode, a.d, a.f);
-  // full token tiles arrive in one box, or, with pairs, in one half-tile box from each CTA
+  // full token tiles arrive in one box, or, with pairs, in one half-tile box in each CTA
   const uint32_t nt = (uint32_t)tc_tile_tokens(gateup, decode) / (cl ? 2u : 1u);
   CUtensorMap w, b0, b1, b0w, b1w;
   cudaError_t e;
@@ -304,10 +336,10 @@ cudaError_t launch_tc(const FfnArgs& a, const int32_t* prefix, bool gateup, bool
   if (e != cudaSuccess) return e;
   if (gateup)
     return decode ? launch_variant<true, 64, 5, 2, 2>(w, b0, b1, b0w, b1w, p, st)
-                  : cl ? launch_variant<true, 256, 3, 2, 1, true>(w, b0, b1, b0w, b1w, p, st)
+                  : cl ? launch_variant<true, 256, 4, 2, 1, true>(w, b0, b1, b0w, b1w, p, st)
                        : launch_variant<true, 256, 3, 2, 1>(w, b0, b1, b0w, b1w, p, st);
   if (decode) return launch_variant<false, 64, 8, 1, 2>(w, b0, b1, b0w, b1w, p, st);
-  if (cl) return launch_variant<false, 256, 3, 2, 1, true>(w, b0, b1, b0w, b1w, p, st);
+  if (cl) return launch_variant<false, 256, 4, 2, 1, true>(w, b0, b1, b0w, b1w, p, st);
   return down_pairs(a.d, decode) ? launch_variant<false, 256, 3, 2, 1>(w, b0, b1, b0w, b1w, p, st)
                                  : launch_variant<false, 256, 4, 1, 2>(w, b0, b1, b0w, b1w, p, st);
 }

@@ -24,6 +24,17 @@
 // it, a token slot and a converted slot when the MMAs that read them complete. The codes are
 // the stream that comes from HBM, so they get the deepest ring and a producer thread of their
 // own, which runs as far ahead as the code ring allows whatever the token ring is doing.
+//
+// CTA pairs (cta_group::2, where an expert has an even number of 128-row tiles): the two CTAs of
+// a 2-CTA cluster take the consecutive 128-row weight tiles 2j and 2j+1 of the same expert and
+// token tile, and one MMA of M = 256 covers both: each CTA converts its own weight rows and
+// loads half of the token rows into its own shared memory, the even CTA issues the MMAs (which
+// read both CTAs' operands), and each CTA's tensor memory receives its own 128 rows. So every
+// SM stages half of each token tile (16 KB a slot instead of 32), which pays for a third
+// converted slot and a fourth token slot, and issues half as many MMA instructions. The even
+// CTA's barriers gate the MMAs: its token-slot barrier counts both CTAs' TMA bytes (the odd
+// CTA's loads complete on it), its converted-slot barrier both CTAs' converters and its
+// accumulator-empty barrier both CTAs' epilogues; the MMA commits arrive in both CTAs.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -45,10 +56,11 @@ constexpr int kTokWarp = kConvWarp0 + kConvWarps; // token producer: warp 14
 constexpr int kIssuer2 = kTokWarp + 1;            // MMA issuer of weight tile 1: warp 15
 constexpr int kThreadsW = 32 * (kIssuer2 + 1);
 
-template <int NT, int QS, int BS, int CS, int KA, int ACCB, bool MX>
+template <int NT, int QS, int BS, int CS, int KA, int ACCB, bool MX, bool PAIR>
 struct SmemW {
   static constexpr uint32_t kQSlot = KA * code_tile_bytes<MX>();  // codes of the KA tiles
-  static constexpr uint32_t kBSlot = (uint32_t)NT * kBK * 2;     // bf16 token rows
+  // bf16 token rows: the whole tile, or (CTA pairs) this CTA's half of it
+  static constexpr uint32_t kBSlot = (uint32_t)(PAIR ? NT / 2 : NT) * kBK * 2;
   static constexpr uint32_t kCSlot = KA * kATileBytes;           // converted bf16 weight tiles
   static constexpr uint32_t kBOff = QS * kQSlot;
   static constexpr uint32_t kCOff = kBOff + BS * kBSlot;
@@ -112,7 +124,7 @@ __device__ __forceinline__ void sts_u4(uint32_t addr, const uint4& v) {
                : "memory");
 }
 
-template <bool GATEUP, int NT, int QS, int BS, int CS, int KA, int ACCB, int CL, bool MX>
+template <bool GATEUP, int NT, int QS, int BS, int CS, int KA, int ACCB, bool PAIR, bool MX>
 __global__ void __launch_bounds__(kThreadsW, 1)
     k_tc_ffn_fp8_wide(const __grid_constant__ CUtensorMap tm_w,
                       const __grid_constant__ CUtensorMap tm_b0,
@@ -120,7 +132,7 @@ __global__ void __launch_bounds__(kThreadsW, 1)
                       const __grid_constant__ CUtensorMap tm_b0w,
                       const __grid_constant__ CUtensorMap tm_b1w, const TcParams p,
                       const void* __restrict__ scales) {
-  using S = SmemW<NT, QS, BS, CS, KA, ACCB, MX>;
+  using S = SmemW<NT, QS, BS, CS, KA, ACCB, MX, PAIR>;
   static_assert(S::kTmemCols <= 512 && (S::kTmemCols & (S::kTmemCols - 1)) == 0, "TMEM cols");
   static_assert(!GATEUP || KA == 2, "gate/up tiles pair the gate and up rows");
   extern __shared__ uint8_t smem_raw[];
@@ -142,18 +154,17 @@ __global__ void __launch_bounds__(kThreadsW, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E1 = p.E + p.n_shared;
   const int kblocks = p.K / kBK;
-  // Clusters of CL CTAs (1, 2 or 4): all walk the same list of (expert, group of CL m-tiles,
-  // token tile) entries; this CTA takes m-tile CL * mt + rank, and the token tile, which all of
-  // them need, is loaded a CL-th by each CTA and multicast to all.
-  static_assert(CL == 1 || CL == 2 || CL == 4, "cluster size");
-  constexpr bool PAIR = CL > 1;
-  constexpr uint16_t kMask = (uint16_t)((1u << CL) - 1u);
+  // CTA pairs: both CTAs walk the same list of (expert, pair of m-tiles, token tile) entries;
+  // this CTA takes m-tile 2 * mt + rank and rows [rank * n/2, (rank + 1) * n/2) of the tile's n
+  // (padded) token rows.
+  constexpr int CL = PAIR ? 2 : 1;
   const int rank = PAIR ? (int)cluster_ctarank() : 0;
+  const bool issuer_cta = rank == 0;  // the CTA whose threads issue the MMAs
   const int tile0 = (int)blockIdx.x / CL;
   const int tstep = (int)gridDim.x / CL;
   const auto decode = [&](int tile, Tile& t) {
     decode_tile<GATEUP, NT>(p, tile, t);
-    if (PAIR) t.mt = CL * t.mt + rank;
+    if (PAIR) t.mt = 2 * t.mt + rank;
   };
 
   if (threadIdx.x == 0) {
@@ -162,16 +173,16 @@ __global__ void __launch_bounds__(kThreadsW, 1)
       mbar_init(&q_empty[s], kConvWarps);   // every converter warp has read its codes
     }
     for (int s = 0; s < BS; ++s) {
-      mbar_init(&b_full[s], 1);
-      mbar_init(&b_empty[s], CL * KA);      // MMA commits (each issuer, every CTA of the cluster)
+      mbar_init(&b_full[s], 1);             // the (even CTA's) token producer, + TMA bytes
+      mbar_init(&b_empty[s], KA);           // MMA commits (one per issuer)
     }
     for (int s = 0; s < CS; ++s) {
-      mbar_init(&c_full[s], kConvWarps);
+      mbar_init(&c_full[s], CL * kConvWarps);  // converter warps (of both CTAs of a pair)
       mbar_init(&c_empty[s], KA);           // MMA commits (one per issuer)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], KA);          // one commit per issuer
-      mbar_init(&acc_empty[b], 4);
+      mbar_init(&acc_empty[b], 4 * CL);     // epilogue warps (of both CTAs of a pair)
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -182,12 +193,17 @@ __global__ void __launch_bounds__(kThreadsW, 1)
     prefetch_tmap(&tm_b1w);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_holder, S::kTmemCols);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(tmem_holder, S::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_holder, S::kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
-  if (PAIR) cluster_sync();  // the peer's barriers are initialised before any multicast
+  if (PAIR) cluster_sync();  // both CTAs' barriers are initialised before either signals the other
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   // the tile list (prefix) is written by the previous kernel
@@ -223,14 +239,18 @@ __global__ void __launch_bounds__(kThreadsW, 1)
     // ---------------- TMA producer: bf16 token rows ----------------
     if (lane == 0) {
       const uint64_t pol_b = policy_evict_last();
+      // pairs: every load of either CTA completes on the even CTA's barrier
+      const uint32_t b_full0 = PAIR ? mapa_shared(smem_u32(&b_full[0]), 0) : 0;
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       for (int tile = tile0; ok && tile < total; tile += tstep) {
         Tile t;
         decode(tile, t);
-        const bool wide = t.ntok == NT;
-        const int nbox = (t.ntok + kBoxRows - 1) / kBoxRows;
-        // bytes this CTA receives: the whole token tile (with pairs, half of it from the peer)
+        const bool wide = t.ntok == NT;  // one box: NT rows, or NT/2 in pairs
+        // this CTA's rows of the tile: all of them, or (pairs) half of the padded count
+        const int half = PAIR ? ((t.ntok + 15) & ~15) / 2 : t.ntok;
+        const int row0 = t.brow0 + rank * half;
+        const int nbox = (half + kBoxRows - 1) / kBoxRows;
         const uint32_t bytes = wide ? S::kBSlot : (uint32_t)nbox * kBBoxBytes;
         const bool sh = GATEUP && t.shared;
         const CUtensorMap* bmap = sh ? &tm_b1 : &tm_b0;
@@ -238,33 +258,36 @@ __global__ void __launch_bounds__(kThreadsW, 1)
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!wait_bar(&b_empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
           uint8_t* bt = bring + stage * S::kBSlot;
-          mbar_arrive_expect_tx(&b_full[stage], bytes);
           if (PAIR) {
-            // full tile: this CTA's half of the rows (the wide map's box is NT/2 rows);
-            // partial tile: every other 16-row box
+            // both halves are the same size, so the even CTA expects twice its own bytes
+            if (issuer_cta) mbar_arrive_expect_tx(&b_full[stage], 2 * bytes);
+            const uint32_t bar = b_full0 + 8u * stage;
             if (wide) {
-              tma_load_2d_mc(bt + rank * (S::kBSlot / CL), bmapw, &b_full[stage], kb * kBK,
-                             t.brow0 + rank * (NT / CL), kMask, pol_b);
+              tma_load_2d_pair(bt, bmapw, bar, kb * kBK, row0, pol_b);
             } else {
-              for (int i = rank; i < nbox; i += CL)
-                tma_load_2d_mc(bt + i * kBBoxBytes, bmap, &b_full[stage], kb * kBK,
-                               t.brow0 + i * kBoxRows, kMask, pol_b);
+              for (int i = 0; i < nbox; ++i)
+                tma_load_2d_pair(bt + i * kBBoxBytes, bmap, bar, kb * kBK, row0 + i * kBoxRows,
+                                 pol_b);
             }
-          } else if (wide) {
-            tma_load_2d(bt, bmapw, &b_full[stage], kb * kBK, t.brow0, pol_b);
           } else {
-            for (int i = 0; i < nbox; ++i)
-              tma_load_2d(bt + i * kBBoxBytes, bmap, &b_full[stage], kb * kBK,
-                          t.brow0 + i * kBoxRows, pol_b);
+            mbar_arrive_expect_tx(&b_full[stage], bytes);
+            if (wide) {
+              tma_load_2d(bt, bmapw, &b_full[stage], kb * kBK, t.brow0, pol_b);
+            } else {
+              for (int i = 0; i < nbox; ++i)
+                tma_load_2d(bt + i * kBBoxBytes, bmap, &b_full[stage], kb * kBK,
+                            t.brow0 + i * kBoxRows, pol_b);
+            }
           }
           if (++stage == BS) { stage = 0; phase ^= 1u; }
         }
       }
-      for (int s = 0; s < BS; ++s)
-        drain_bar(&b_full[s], (s < (int)stage) ? phase : (phase ^ 1u), p.status);
+      // every issued load has landed (in pairs the even CTA's barrier counts both CTAs' bytes)
+      if (!PAIR || issuer_cta)
+        for (int s = 0; s < BS; ++s)
+          drain_bar(&b_full[s], (s < (int)stage) ? phase : (phase ^ 1u), p.status);
       if (PAIR) {
-        // the MMA commits of both CTAs for every issued stage have arrived here before the
-        // CTA may exit (the peer's commits target this CTA's barriers)
+        // the MMA commits for every issued stage have arrived here before the CTA may exit
         for (int s = 0; s < BS; ++s)
           drain_bar(&b_empty[s], (s < (int)stage) ? phase : (phase ^ 1u), p.status);
       }
@@ -272,18 +295,19 @@ __global__ void __launch_bounds__(kThreadsW, 1)
   } else if (warp == 1 || warp == kIssuer2) {
     // ---------------- MMA issuers: warp 1 weight tile 0, warp 15 weight tile 1 ----------------
     const int o = warp == 1 ? 0 : 1;
-    if (lane == 0 && o < KA) {
+    if (lane == 0 && o < KA && issuer_cta) {
       uint32_t bs = 0, bphase = 0, cs = 0, cphase = 0;
       uint32_t acc = 0, acc_phase = 0;
       bool ok = true;
+      constexpr int kM = PAIR ? 2 * kBM : kBM;  // a pair's MMA covers both CTAs' weight rows
       for (int tile = tile0; ok && tile < total; tile += tstep) {
         Tile t;
         decode(tile, t);
         const int npad = (t.ntok + 15) & ~15;
         // bf16 x bf16, or (MX) f16 x f16 (A and B formats 0), fp32 accumulate
         const uint32_t idesc =
-            MX ? (1u << 4) | ((uint32_t)(npad >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24)
-               : idesc_bf16(kBM, npad);
+            MX ? (1u << 4) | ((uint32_t)(npad >> 3) << 17) | ((uint32_t)(kM >> 4) << 24)
+               : idesc_bf16(kM, npad);
         if (!wait_bar(&acc_empty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t d0 = tmem_base + acc * S::kAccCols + o * NT;
@@ -293,19 +317,27 @@ __global__ void __launch_bounds__(kThreadsW, 1)
           tc_fence_after();
           const uint64_t da = sw128_desc(smem_u32(cring + cs * S::kCSlot) + o * kATileBytes);
           const uint64_t db = sw128_desc(smem_u32(bring + bs * S::kBSlot));
+          if (PAIR) {
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            mma_bf16_ss(d0, da + 2 * kk, db + 2 * kk, idesc, (kb | kk) ? 1u : 0u);
-          if (PAIR)
-            mma_commit_mc(&b_empty[bs], kMask);  // token rows consumed, in every CTA
-          else
-            mma_commit(&b_empty[bs]);          // token rows consumed
-          mma_commit(&c_empty[cs]);   // dequantised weights consumed
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              mma_ss_pair(d0, da + 2 * kk, db + 2 * kk, idesc, (kb | kk) ? 1u : 0u);
+            mma_commit_pair(&b_empty[bs]);   // token rows consumed, in both CTAs
+            mma_commit_pair(&c_empty[cs]);   // dequantised weights consumed, in both CTAs
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              mma_bf16_ss(d0, da + 2 * kk, db + 2 * kk, idesc, (kb | kk) ? 1u : 0u);
+            mma_commit(&b_empty[bs]);        // token rows consumed
+            mma_commit(&c_empty[cs]);        // dequantised weights consumed
+          }
           if (++bs == BS) { bs = 0; bphase ^= 1u; }
           if (++cs == CS) { cs = 0; cphase ^= 1u; }
         }
         if (!ok) break;
-        mma_commit(&acc_full[acc]);
+        if (PAIR)
+          mma_commit_pair(&acc_full[acc]);
+        else
+          mma_commit(&acc_full[acc]);
         if (++acc == ACCB) { acc = 0; acc_phase ^= 1u; }
       }
     }
@@ -313,7 +345,8 @@ __global__ void __launch_bounds__(kThreadsW, 1)
     // ---------------- epilogue (warps 2..5) ----------------
     run_epilogue<GATEUP, NT, S::kAccCols, KA, ACCB, MX>(p, total, tmem_base, acc_full, acc_empty,
                                                         abort_flag, tile0, tstep,
-                                                        PAIR ? rank : -1, CL);
+                                                        PAIR ? rank : -1, CL,
+                                                        PAIR && !issuer_cta);
   } else if (MX) {
     // ---------------- dequantisers, MXFP4 (warps 6..13) ----------------
     // thread = (row r, 32-code chunk j) of every weight tile a: 16 bytes of code pairs and their
@@ -361,7 +394,10 @@ __global__ void __launch_bounds__(kThreadsW, 1)
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&q_empty[qs]);   // this warp is done with the codes of this stage
-          mbar_arrive(&c_full[cs]);
+          if (PAIR && !issuer_cta)     // the even CTA's MMA reads both CTAs' weights
+            mbar_arrive_cluster(mapa_shared(smem_u32(&c_full[cs]), 0));
+          else
+            mbar_arrive(&c_full[cs]);
         }
         e0 = e0n;
         e1 = e1n;
@@ -416,7 +452,10 @@ __global__ void __launch_bounds__(kThreadsW, 1)
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&q_empty[qs]);   // this warp is done with the codes of this stage
-          mbar_arrive(&c_full[cs]);
+          if (PAIR && !issuer_cta)     // the even CTA's MMA reads both CTAs' weights
+            mbar_arrive_cluster(mapa_shared(smem_u32(&c_full[cs]), 0));
+          else
+            mbar_arrive(&c_full[cs]);
         }
         s0 = s0_next;
         s1 = s1_next;
@@ -428,27 +467,30 @@ __global__ void __launch_bounds__(kThreadsW, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (PAIR) cluster_sync();  // no CTA leaves while its peer may still write to it
+  if (PAIR) cluster_sync();  // no CTA leaves while its peer may still signal it
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, S::kTmemCols);
+    if (PAIR)
+      tmem_dealloc_pair(tmem_base, S::kTmemCols);
+    else
+      tmem_dealloc(tmem_base, S::kTmemCols);
   }
 }
 
-template <bool GATEUP, int NT, int QS, int BS, int CS, int KA, int ACCB, int CL, bool MX>
+template <bool GATEUP, int NT, int QS, int BS, int CS, int KA, int ACCB, bool PAIR, bool MX>
 cudaError_t launch_variant(const CUtensorMap& w, const CUtensorMap& b0, const CUtensorMap& b1,
                            const CUtensorMap& b0w, const CUtensorMap& b1w, const TcParams& p,
                            const void* scales, cudaStream_t st) {
-  using S = SmemW<NT, QS, BS, CS, KA, ACCB, MX>;
+  using S = SmemW<NT, QS, BS, CS, KA, ACCB, MX, PAIR>;
   static_assert(S::kTotal <= 227 * 1024, "shared memory");
-  auto kern = k_tc_ffn_fp8_wide<GATEUP, NT, QS, BS, CS, KA, ACCB, CL, MX>;
+  auto kern = k_tc_ffn_fp8_wide<GATEUP, NT, QS, BS, CS, KA, ACCB, PAIR, MX>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)S::kTotal);
   if (e != cudaSuccess) return e;
   count_launches(1);
-  if (CL > 1)
-    return launch_pdl_cluster(kern, dim3((unsigned)(num_sms() / CL * CL)), dim3(kThreadsW),
-                              S::kTotal, st, (unsigned)CL, w, b0, b1, b0w, b1w, p, scales);
+  if (PAIR)
+    return launch_pdl_cluster(kern, dim3((unsigned)(num_sms() / 2 * 2)), dim3(kThreadsW),
+                              S::kTotal, st, 2u, w, b0, b1, b0w, b1w, p, scales);
   return launch_pdl(kern, dim3(num_sms()), dim3(kThreadsW), S::kTotal, st, w, b0, b1, b0w, b1w, p,
                     scales);
 }
@@ -464,28 +506,29 @@ constexpr int kNT = 256;
 // Weight rows per tile of a pass: 2 x 128 (gate + up, or two W_d tiles when d allows), else 128.
 bool paired_tiles(bool gateup, int d) { return gateup || tc_tile_rows(false, false, d) == 2 * kBM; }
 
-// Clusters take CL consecutive m-tiles: pairs when an expert's m-tile count is even, else none
-// (CL = 1). Clusters of four measured 1.7x slower (every token slot then waits for four CTAs).
+// CTA pairs (cta_group::2) take two consecutive m-tiles: when an expert's m-tile count is even,
+// else single CTAs (1).
 int cluster_size(bool gateup, int d, int f) {
   if (!paired_tiles(gateup, d)) return 1;
   const int mtiles = gateup ? f / kBM : d / (2 * kBM);
   return mtiles % 2 == 0 ? 2 : 1;
 }
 
-// One pass with kNT-token tiles; rings (codes, tokens, converted weights): 4/3/2 slots for
-// paired weight tiles (224 KB of shared memory), 8/3/3 for single tiles; fewer token slots
-// measured slower.
-template <int CL, bool MX>
+// One pass with kNT-token tiles; rings (codes, tokens, converted weights): CTA pairs 4/4/3 slots
+// (a token slot holds half a tile: 224 KB of shared memory); single CTAs 4/3/2 for paired weight
+// tiles (224 KB), 8/3/3 for single tiles; fewer token slots measured slower.
+template <bool PAIR, bool MX>
 cudaError_t launch_pass(const Maps& m, const TcParams& p, const void* sc, bool gateup,
                         bool paired, cudaStream_t st) {
+  constexpr int BS = PAIR ? 4 : 3, CS = PAIR ? 3 : 2;
   if (gateup)
-    return launch_variant<true, kNT, 4, 3, 2, 2, 1, CL, MX>(m.w, m.b0, m.b1, m.b0w, m.b1w, p, sc,
-                                                            st);
+    return launch_variant<true, kNT, 4, BS, CS, 2, 1, PAIR, MX>(m.w, m.b0, m.b1, m.b0w, m.b1w, p,
+                                                                sc, st);
   if (paired)
-    return launch_variant<false, kNT, 4, 3, 2, 2, 1, CL, MX>(m.w, m.b0, m.b1, m.b0w, m.b1w, p, sc,
-                                                             st);
-  return launch_variant<false, kNT, 8, 3, 3, 1, 2, 1, MX>(m.w, m.b0, m.b1, m.b0w, m.b1w, p, sc,
-                                                          st);
+    return launch_variant<false, kNT, 4, BS, CS, 2, 1, PAIR, MX>(m.w, m.b0, m.b1, m.b0w, m.b1w, p,
+                                                                 sc, st);
+  return launch_variant<false, kNT, 8, 3, 3, 1, 2, false, MX>(m.w, m.b0, m.b1, m.b0w, m.b1w, p,
+                                                              sc, st);
 }
 
 }  // namespace
@@ -534,8 +577,8 @@ cudaError_t launch_tc_fp8_wide(const FfnArgs& a, const int32_t* prefix, bool gat
   if (e != cudaSuccess) return e;
   const void* sc = gateup ? a.s13 : a.s2;
   const bool paired = paired_tiles(gateup, a.d);
-  if (cl == 2) return launch_pass<2, false>(m, p, sc, gateup, paired, st);
-  return launch_pass<1, false>(m, p, sc, gateup, paired, st);
+  if (cl == 2) return launch_pass<true, false>(m, p, sc, gateup, paired, st);
+  return launch_pass<false, false>(m, p, sc, gateup, paired, st);
 }
 
 // MXFP4 weights on the same prefill tiles: x (all slot rows, the shared segment included) and h
@@ -578,8 +621,8 @@ cudaError_t launch_tc_mx_wide(const FfnArgs& a, const int32_t* prefix, bool gate
   if (e != cudaSuccess) return e;
   const void* sc = gateup ? a.s13 : a.s2;
   const bool paired = paired_tiles(gateup, a.d);
-  if (cl == 2) return launch_pass<2, true>(m, p, sc, gateup, paired, st);
-  return launch_pass<1, true>(m, p, sc, gateup, paired, st);
+  if (cl == 2) return launch_pass<true, true>(m, p, sc, gateup, paired, st);
+  return launch_pass<false, true>(m, p, sc, gateup, paired, st);
 }
 
 }  // namespace moe

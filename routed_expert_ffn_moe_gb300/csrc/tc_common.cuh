@@ -102,11 +102,13 @@ __device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity, int* s
 // f16 (round to nearest, saturating at +-65504) instead of bf16.
 template <bool GATEUP, int NT, uint32_t ACC_COLS, int KA = 1, int ACCB = 2, bool H_F16 = false>
 // Tiles tile0, tile0 + tstep, ...; cl_rank >= 0 marks clusters of cl CTAs, where a listed tile
-// is a group of cl consecutive m-tiles and this CTA takes m-tile cl * mt + cl_rank.
+// is a group of cl consecutive m-tiles and this CTA takes m-tile cl * mt + cl_rank. With
+// empty_in_cta0 (CTA pairs whose MMAs the even CTA issues), the accumulator is handed back on
+// the even CTA's acc_empty barrier, wherever this CTA is.
 __device__ __forceinline__ void run_epilogue(const TcParams& p, int total, uint32_t tmem_base,
                                              uint64_t* acc_full, uint64_t* acc_empty,
                                              volatile int* abort_flag, int tile0, int tstep,
-                                             int cl_rank, int cl = 2) {
+                                             int cl_rank, int cl = 2, bool empty_in_cta0 = false) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;                 // TMEM lane quadrant this warp may access
   const int row = q * 32 + lane;          // weight row within a 128-row tile
@@ -155,7 +157,12 @@ __device__ __forceinline__ void run_epilogue(const TcParams& p, int total, uint3
     }
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&acc_empty[acc]);
+    if (lane == 0) {
+      if (empty_in_cta0)
+        mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[acc]), 0));
+      else
+        mbar_arrive(&acc_empty[acc]);
+    }
     if (++acc == ACCB) { acc = 0; acc_phase ^= 1u; }
   }
 }

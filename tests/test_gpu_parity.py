@@ -69,9 +69,12 @@ SMALL = [
     ("tiny", {"T": 300, "E": 40, "k": 5}),     # several permute chunks, uneven segments
     # FP8 prefill tiles (more than 32 routed slots per expert): paired and single down tiles
     ("tiny", {"T": 600, "E": 8, "k": 2, "wdtype": "fp8"}),
-    # FP8 prefill tiles in cluster pairs (even m-tile counts in both passes)
+    # FP8 prefill tiles on CTA pairs (even m-tile counts in both passes), full and ragged token
+    # tiles; MXFP4 prefill on CTA pairs
     ("tiny", {"T": 600, "d": 512, "f": 256, "E": 8, "k": 2, "wdtype": "fp8"}),
-    ("tiny", {"T": 600, "d": 1024, "f": 512, "E": 8, "k": 2, "wdtype": "fp8"}),  # clusters of 4
+    ("tiny", {"T": 600, "d": 1024, "f": 512, "E": 8, "k": 2, "wdtype": "fp8"}),
+    ("tiny", {"T": 1500, "d": 512, "f": 256, "E": 8, "k": 2, "wdtype": "fp8", "router": "zipf"}),
+    ("tiny", {"T": 600, "d": 512, "f": 256, "E": 8, "k": 2, "wdtype": "mxfp4"}),
     ("tiny", {"T": 600, "d": 512, "f": 256, "E": 8, "k": 2}),                  # bf16 pairs
     # bf16 prefill split: cold experts on decode tiles beside hot ones on paired tiles
     ("tiny", {"router": "zipf", "T": 600, "d": 512, "f": 256, "E": 16, "k": 2}),
