@@ -167,7 +167,7 @@ __device__ __forceinline__ void gather_encode_block(long i, const uint16_t* __re
   xq.s_lo[s * nb + b] = (uint8_t)sb;
 }
 
-// MXFP4 weights, prefill tiles: thread i writes 32-element block i of the slot rows (the same
+// E4M3 and MXFP4 weights, prefill tiles: thread i writes 32-element block i of the slot rows (the same
 // rows as above) as f16, round to nearest, saturating at +-65504 (exact for bf16 values in f16's
 // normal range).
 __device__ __forceinline__ void gather_f16_block(long i, const uint16_t* __restrict__ x,
@@ -204,7 +204,7 @@ __device__ __forceinline__ void gather_f16_block(long i, const uint16_t* __restr
 enum GatherMode : int {
   kGatherBf16 = 0,  // bf16 and FP8 weights: x rows of the routed slots, bf16
   kGatherMxTerms = 1,  // MXFP4 decode tiles: the slot rows as two E4M3 terms (xq)
-  kGatherF16 = 2,  // MXFP4 prefill tiles: the slot rows as f16 (x_perm)
+  kGatherF16 = 2,  // E4M3 and MXFP4 prefill tiles: the slot rows as f16 (x_perm)
 };
 
 // One launch for both: block 0 builds the plan from the expert offsets while the other blocks
@@ -555,10 +555,13 @@ FfnCall make_ffn_call(const moe_shape& s, const uint16_t* x, const int32_t* perm
     pa.hot_cost_tok[0] = (float)(4.0 * s.d * s.f / tc_up);
     pa.hot_cost_tok[1] = (float)(2.0 * s.d * s.f / tc_dn);
   }
-  // rows the gather writes: the routed slots, plus (MXFP4) the shared segment's rows
-  c.nq = c.routed + (c.mxq ? (long)a.n_shared * s.T : 0);
+  // What the gather writes: bf16 rows of the routed slots (bf16 weights, E4M3 decode tiles), or
+  // every slot's row, the shared segment's included, as f16 (E4M3 and MXFP4 prefill tiles) or
+  // as two E4M3 terms (MXFP4 decode tiles).
+  const bool f16_rows = !c.decode && (c.mxq || c.fp8);
+  c.nq = c.routed + (c.mxq || f16_rows ? (long)a.n_shared * s.T : 0);
   c.gather_n = (c.use_tc && c.nq > 0) ? c.nq * (s.d / 8) / kGatherChunks : 0;
-  c.mode = !c.mxq ? kGatherBf16 : c.decode ? kGatherMxTerms : kGatherF16;
+  c.mode = f16_rows ? kGatherF16 : c.mxq ? kGatherMxTerms : kGatherBf16;
   return c;
 }
 
@@ -729,9 +732,10 @@ cudaError_t launch_forward(const moe_shape& s, const uint16_t* x, const uint16_t
     a.xq = mx::planes_at(ws + L.xq, all_slots, s.d);
     a.hq = mx::planes_at(ws + L.hq, all_slots, s.f);
   }
-  // MXFP4: the shared segment's rows are encoded here, the routed ones by the routed path's gather
-  const long enc = mxq ? (long)s.T * (s.d / 32) : 0;
-  const int mode = decode ? kGatherMxTerms : kGatherF16;
+  // MXFP4, and E4M3 on the prefill tiles: the shared segment's rows are encoded here (two E4M3
+  // terms or f16), the routed ones by the routed path's gather
+  const long enc = (mxq || (fp8 && !decode)) ? (long)s.T * (s.d / 32) : 0;
+  const int mode = (mxq && decode) ? kGatherMxTerms : kGatherF16;
   if ((e = launch_pdl(k_shared_plan, dim3((unsigned)(1 + (enc + 255) / 256)), dim3(256), 0, aux,
                       s.T, s.k, s.E, ts, rows, x, s.d, a.xq, a.x_perm, mode, status)) !=
       cudaSuccess)

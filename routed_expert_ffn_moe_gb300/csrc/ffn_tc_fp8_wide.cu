@@ -2,23 +2,28 @@
 // batches (W8A16). Same passages as ffn_tc_fp8.cu. With up to 256 tokens per tile each weight
 // element serves many tokens, so the tile shape follows the bf16 prefill kernel (two 128-row
 // weight tiles per 256-token tile, 512 TMEM columns of accumulator) and the dequantisation moves
-// to a shared-memory stage of its own (measured: the dequantisers and the MMAs take turns on the
-// two converted slots; no unit is near its limit):
+// to a shared-memory stage of its own:
 //
 //   TMA (codes)   E4M3 codes (128 rows x 64 K per weight tile, 64-byte swizzle) -> code ring
-//   TMA (tokens)  bf16 token rows (256 x 64 K, 128-byte swizzle) -> token ring
-//   convert       8 warps: bf16(code * block scale) into a third ring in the 128-byte-swizzle
-//                 K-major layout the MMA reads (each weight rounded once to bf16, <= 2^-9 relative)
-//   MMA           tcgen05.mma.kind::f16, bf16 x bf16 -> fp32, both operands from smem, one
+//   TMA (tokens)  f16 token rows (256 x 64 K, 128-byte swizzle) -> token ring
+//   convert       8 warps: f16(code * f16(block scale)) into a third ring in the 128-byte-
+//                 swizzle K-major layout the MMA reads: one exact cvt per two codes and one f16x2
+//                 multiply (each weight rounded once, 2^-11 relative for products in f16's normal
+//                 range, i.e. for block scales above 2^-14: blocks whose largest weight is above
+//                 448 * 2^-14 = 0.027; smaller products are f16 subnormals, 2^-24 absolute)
+//   MMA           tcgen05.mma.kind::f16, f16 x f16 -> fp32, both operands from smem, one
 //                 issuing thread per weight tile (warps 1 and 15)
-//   epilogue      TMEM -> SiLU(gate) * up -> bf16 h, or the fp32 expert output
+//   epilogue      TMEM -> SiLU(gate) * up -> f16 h, or the fp32 expert output
+//
+// The token rows (x gathered in slot order, the shared expert's rows included) and h are f16:
+// exact for bf16 x in f16's normal range (|x| between 2^-14 and 65504), h rounded once to f16
+// (saturating at +-65504).
 //
 // MXFP4 weights (MX): the same kernel with E2M1 code pairs (128 rows x 64 codes = 32 bytes a row,
 // 32-byte swizzle) and one E8M0 scale per 32 codes of a row. The dequantised weight
 // q * 2^(e-127) is exact in f16 (one cvt per two codes, one f16x2 multiply by the power of two)
 // for blocks whose scale lies in f16's range (2^-24 .. 2^15; a block's largest weight between
-// 2^-19 and 2^16), so the MMA runs on f16 operands: the token rows and h are f16 as well
-// (exact for bf16 x in f16's normal range; h rounded once to f16).
+// 2^-19 and 2^16).
 //
 // The three rings are released independently: a code slot as soon as the converters have read
 // it, a token slot and a converted slot when the MMAs that read them complete. The codes are
@@ -59,9 +64,9 @@ constexpr int kThreadsW = 32 * (kIssuer2 + 1);
 template <int NT, int QS, int BS, int CS, int KA, int ACCB, bool MX, bool PAIR>
 struct SmemW {
   static constexpr uint32_t kQSlot = KA * code_tile_bytes<MX>();  // codes of the KA tiles
-  // bf16 token rows: the whole tile, or (CTA pairs) this CTA's half of it
+  // f16 token rows: the whole tile, or (CTA pairs) this CTA's half of it
   static constexpr uint32_t kBSlot = (uint32_t)(PAIR ? NT / 2 : NT) * kBK * 2;
-  static constexpr uint32_t kCSlot = KA * kATileBytes;           // converted bf16 weight tiles
+  static constexpr uint32_t kCSlot = KA * kATileBytes;           // converted f16 weight tiles
   static constexpr uint32_t kBOff = QS * kQSlot;
   static constexpr uint32_t kCOff = kBOff + BS * kBSlot;
   static constexpr uint32_t kTilesBytes = kCOff + CS * kCSlot;
@@ -71,27 +76,28 @@ struct SmemW {
   static constexpr uint32_t kTmemCols = ACCB * kAccCols;
 };
 
-// Four E4M3 codes (lowest byte first) times the block scale, as two bf16 pairs (codes 0,1 ->
-// lo, codes 2,3 -> hi): the word's 16-bit halves convert exactly to f16 pairs, widen to fp32,
-// and one packed fused multiply-add per pair (addend -0, so the result is the rounded product
-// q * s) precedes the single rounding to bf16.
-__device__ __forceinline__ void dequant4(uint32_t four, float2 s2, uint32_t& lo, uint32_t& hi) {
-  uint32_t h01, h23;
+// Four E4M3 codes (lowest byte first) times the block scale as two f16 pairs (codes 0,1 -> lo,
+// codes 2,3 -> hi): each 16-bit half of the word converts exactly to an f16 pair, and one f16x2
+// multiply by the scale (an f16 pair) rounds each product once.
+__device__ __forceinline__ void dequant4_f16(uint32_t four, uint32_t s2, uint32_t& lo,
+                                             uint32_t& hi) {
   asm("{\n"
       "  .reg .b16 c01, c23;\n"
       "  mov.b32 {c01, c23}, %2;\n"
       "  cvt.rn.f16x2.e4m3x2 %0, c01;\n"
       "  cvt.rn.f16x2.e4m3x2 %1, c23;\n"
+      "  mul.rn.f16x2 %0, %0, %3;\n"
+      "  mul.rn.f16x2 %1, %1, %3;\n"
       "}"
-      : "=r"(h01), "=r"(h23)
-      : "r"(four));
-  const float2 nz = make_float2(-0.f, -0.f);
-  const float2 f01 = __ffma2_rn(__half22float2(*reinterpret_cast<const __half2*>(&h01)), s2, nz);
-  const float2 f23 = __ffma2_rn(__half22float2(*reinterpret_cast<const __half2*>(&h23)), s2, nz);
-  const __nv_bfloat162 b01 = __floats2bfloat162_rn(f01.x, f01.y);
-  const __nv_bfloat162 b23 = __floats2bfloat162_rn(f23.x, f23.y);
-  lo = *reinterpret_cast<const uint32_t*>(&b01);
-  hi = *reinterpret_cast<const uint32_t*>(&b23);
+      : "=r"(lo), "=r"(hi)
+      : "r"(four), "r"(s2));
+}
+
+// fp32 scale -> f16 pair (round to nearest, saturating at the largest finite f16).
+__device__ __forceinline__ uint32_t f16x2_of(float v) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %1;" : "=r"(r) : "f"(v));
+  return r;
 }
 
 // 2^(e-127) as an f16 pair, the exponent clamped to f16's range (subnormals down to 2^-24).
@@ -236,7 +242,7 @@ __global__ void __launch_bounds__(kThreadsW, 1)
         drain_bar(&q_full[s], (s < (int)stage) ? phase : (phase ^ 1u), p.status);
     }
   } else if (warp == kTokWarp) {
-    // ---------------- TMA producer: bf16 token rows ----------------
+    // ---------------- TMA producer: f16 token rows ----------------
     if (lane == 0) {
       const uint64_t pol_b = policy_evict_last();
       // pairs: every load of either CTA completes on the even CTA's barrier
@@ -304,10 +310,9 @@ __global__ void __launch_bounds__(kThreadsW, 1)
         Tile t;
         decode(tile, t);
         const int npad = (t.ntok + 15) & ~15;
-        // bf16 x bf16, or (MX) f16 x f16 (A and B formats 0), fp32 accumulate
+        // f16 x f16 (A and B formats 0), fp32 accumulate
         const uint32_t idesc =
-            MX ? (1u << 4) | ((uint32_t)(npad >> 3) << 17) | ((uint32_t)(kM >> 4) << 24)
-               : idesc_bf16(kM, npad);
+            (1u << 4) | ((uint32_t)(npad >> 3) << 17) | ((uint32_t)(kM >> 4) << 24);
         if (!wait_bar(&acc_empty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t d0 = tmem_base + acc * S::kAccCols + o * NT;
@@ -343,7 +348,7 @@ __global__ void __launch_bounds__(kThreadsW, 1)
     }
   } else if (warp < kConvWarp0) {
     // ---------------- epilogue (warps 2..5) ----------------
-    run_epilogue<GATEUP, NT, S::kAccCols, KA, ACCB, MX>(p, total, tmem_base, acc_full, acc_empty,
+    run_epilogue<GATEUP, NT, S::kAccCols, KA, ACCB, true>(p, total, tmem_base, acc_full, acc_empty,
                                                         abort_flag, tile0, tstep,
                                                         PAIR ? rank : -1, CL,
                                                         PAIR && !issuer_cta);
@@ -407,7 +412,7 @@ __global__ void __launch_bounds__(kThreadsW, 1)
     }
   } else {
     // ---------------- dequantisers (warps 6..13) ----------------
-    // task = (weight tile a, row r, 16-code chunk j): 16 codes -> two 16-byte bf16 chunks
+    // task = (weight tile a, row r, 16-code chunk j): 16 codes -> two 16-byte f16 chunks
     const int ct = threadIdx.x - 32 * kConvWarp0;
     const int kbl = p.K / 128;               // scale blocks along K
     uint32_t qs = 0, qphase = 0, cs = 0, cphase = 0;
@@ -428,6 +433,7 @@ __global__ void __launch_bounds__(kThreadsW, 1)
         const float s1_next = (KA == 2 && more) ? __ldg(sc + rb1 * kbl + ((kb + 1) >> 1)) : 0.f;
         const uint32_t src = smem_u32(smem + qs * S::kQSlot);
         const uint32_t dst = smem_u32(cring + cs * S::kCSlot);
+        const uint32_t s0h = f16x2_of(s0), s1h = f16x2_of(s1);
 #pragma unroll
         for (int i = 0; i < KA * kBM * 4 / kConvThreads; ++i) {
           const int task = ct + i * kConvThreads;
@@ -436,19 +442,18 @@ __global__ void __launch_bounds__(kThreadsW, 1)
           const int j = task & 3;
           // source: 64-byte rows, 64-byte swizzle (16-byte chunk j ^ ((r >> 1) & 3))
           const uint4 raw = lds_u4(src + a * kCodeTileBytes + r * 64 + ((j ^ ((r >> 1) & 3)) << 4));
-          const float s = a ? s1 : s0;
-          const float2 s2 = make_float2(s, s);
+          const uint32_t s2 = a ? s1h : s0h;
           uint4 lo, hi;  // codes 0..7 -> chunk 2j, codes 8..15 -> chunk 2j+1
-          dequant4(raw.x, s2, lo.x, lo.y);
-          dequant4(raw.y, s2, lo.z, lo.w);
-          dequant4(raw.z, s2, hi.x, hi.y);
-          dequant4(raw.w, s2, hi.z, hi.w);
+          dequant4_f16(raw.x, s2, lo.x, lo.y);
+          dequant4_f16(raw.y, s2, lo.z, lo.w);
+          dequant4_f16(raw.z, s2, hi.x, hi.y);
+          dequant4_f16(raw.w, s2, hi.z, hi.w);
           // destination: 128-byte rows, 128-byte swizzle (16-byte chunk c ^ (r & 7))
           const uint32_t rowb = dst + a * kATileBytes + r * 128;
           sts_u4(rowb + (((2 * j) ^ (r & 7)) << 4), lo);
           sts_u4(rowb + (((2 * j + 1) ^ (r & 7)) << 4), hi);
         }
-        fence_proxy_async_smem();      // bf16 weights -> visible to the MMA
+        fence_proxy_async_smem();      // f16 weights -> visible to the MMA
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&q_empty[qs]);   // this warp is done with the codes of this stage
@@ -555,18 +560,20 @@ cudaError_t launch_tc_fp8_wide(const FfnArgs& a, const int32_t* prefix, bool gat
   p.y_perm = a.y_perm;
   p.status = a.status;
   const int cl = cluster_size(gateup, a.d, a.f);
-  const uint32_t wide_rows = kNT / cl;  // in a cluster each CTA loads its share of a full tile
+  const uint32_t wide_rows = kNT / cl;  // in a CTA pair each CTA loads half of a full tile
   const uint64_t E1 = (uint64_t)a.E + a.n_shared;
   const uint64_t routed = (uint64_t)a.T * a.k;
-  const uint64_t slots = routed + (uint64_t)a.n_shared * a.T;
+  const uint64_t slots = routed + (uint64_t)a.T;  // rows of the workspace's f16 x and h
   Maps m;
   cudaError_t e;
   if (gateup) {
+    // f16 token rows of every slot (the gather writes them), the shared expert's from T*k on
+    const uint16_t* xs = a.x_perm + routed * (uint64_t)a.d;
     e = encode_u8_2d(&m.w, a.w13, E1 * 2 * a.f, a.d, kBM, 64);
-    if (e == cudaSuccess) e = encode_bf16_2d(&m.b0, a.x_perm, routed ? routed : 1, a.d, kBoxRows);
-    if (e == cudaSuccess) e = encode_bf16_2d(&m.b1, a.x, a.T, a.d, kBoxRows);
-    if (e == cudaSuccess) e = encode_bf16_2d(&m.b0w, a.x_perm, routed ? routed : 1, a.d, wide_rows);
-    if (e == cudaSuccess) e = encode_bf16_2d(&m.b1w, a.x, a.T, a.d, wide_rows);
+    if (e == cudaSuccess) e = encode_bf16_2d(&m.b0, a.x_perm, slots, a.d, kBoxRows);
+    if (e == cudaSuccess) e = encode_bf16_2d(&m.b1, xs, a.T, a.d, kBoxRows);
+    if (e == cudaSuccess) e = encode_bf16_2d(&m.b0w, a.x_perm, slots, a.d, wide_rows);
+    if (e == cudaSuccess) e = encode_bf16_2d(&m.b1w, xs, a.T, a.d, wide_rows);
   } else {
     e = encode_u8_2d(&m.w, a.w2, E1 * a.d, a.f, kBM, 64);
     if (e == cudaSuccess) e = encode_bf16_2d(&m.b0, a.h, slots, a.f, kBoxRows);
@@ -581,9 +588,7 @@ cudaError_t launch_tc_fp8_wide(const FfnArgs& a, const int32_t* prefix, bool gat
   return launch_pass<false, false>(m, p, sc, gateup, paired, st);
 }
 
-// MXFP4 weights on the same prefill tiles: x (all slot rows, the shared segment included) and h
-// are f16 rows in the workspace (x_perm and h), so the shared expert's token map is the slot
-// rows from T*k on.
+// MXFP4 weights on the same prefill tiles, with the same f16 token rows.
 cudaError_t launch_tc_mx_wide(const FfnArgs& a, const int32_t* prefix, bool gateup,
                               cudaStream_t st) {
   TcParams p{};

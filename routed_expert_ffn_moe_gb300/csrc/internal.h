@@ -16,8 +16,10 @@ namespace moe {
 //   hist     i32 [E, nchunk]      per (expert, 32-token chunk) counts
 //   base     i32 [E, nchunk]      exclusive scan of hist: first slot of each (expert, chunk)
 //   plan     i32 [kPlanRows, E+2] per-expert work prefixes of the FFN kernels + counters
-//   x_perm   bf16 [T*k, d]        token rows gathered in slot order (tensor-core path input)
-//   h        bf16 [T*k + S*T, f]  SiLU(gate) * up for every slot
+//   x_perm   bf16 [T*k, d]        token rows gathered in slot order (tensor-core path input;
+//                                 f16 and [T*k + S*T, d] for E4M3 and MXFP4 weights)
+//   h        bf16 [T*k + S*T, f]  SiLU(gate) * up for every slot (f16 on the prefill tiles of
+//                                 E4M3 and MXFP4 weights)
 //   shared   i32 [3, E+2]         moe_forward: the shared expert's own tile lists and offsets
 //   rtc      i32 [4] + f32 [E]    tensor-core router: its one-matrix tile plan, then |wg[e]|
 // Status words after the error code: [1] tokens whose logits the tensor-core router had to
@@ -47,10 +49,11 @@ inline WsLayout ws_layout(const moe_shape& s) {
   L.plan = take((size_t)kPlanRows * (E + 2) * 4 + 256);
   const size_t slots = T * k + (size_t)s.n_shared * T;
   const bool mxfp4 = s.wdtype == MOE_W_MXFP4_E8M0_B32;
-  // bf16 / E4M3 weights: gathered bf16 token rows and bf16 h. MXFP4 weights: f16 x (every
-  // slot, the shared segment included) and f16 h for the prefill tiles, and both as two E4M3
-  // terms with their scales for the decode tiles (xq, hq).
-  L.x_perm = take((mxfp4 ? slots : T * k) * (size_t)s.d * 2);
+  const bool fp8 = s.wdtype == MOE_W_FP8_E4M3_B128;
+  // bf16 weights, and E4M3 weights on the decode tiles: gathered bf16 token rows and bf16 h.
+  // E4M3 and MXFP4 weights on the prefill tiles: f16 x (every slot, the shared segment
+  // included) and f16 h. MXFP4 decode tiles: both as two E4M3 terms with their scales (xq, hq).
+  L.x_perm = take((mxfp4 || fp8 ? slots : T * k) * (size_t)s.d * 2);
   L.h = take(slots * (size_t)s.f * 2);
   L.shared = take(3 * (E + 2) * 4);
   L.xq = take(mxfp4 ? slots * (2 * (size_t)s.d + 2 * (size_t)(s.d / 32)) : 0);
