@@ -543,7 +543,7 @@ FfnCall make_ffn_call(const moe_shape& s, const uint16_t* x, const int32_t* perm
     const double bw_up = 78e3, bw_dn = 52e3;            // bytes per microsecond
     const double tc_up = 7.4e6, tc_dn = 8.2e6;          // FLOP per microsecond
     pa.split = 1;
-    pa.nt_c = tc_tile_tokens(true, true);
+    pa.nt_c = tc_cold_tile_tokens();
     pa.cold_max = pa.nt_c;
     pa.mt_up_c = tc_plan_mtiles(true, true, s.d, s.f);
     pa.mt_dn_c = tc_plan_mtiles(false, true, s.d, s.f);
@@ -603,14 +603,15 @@ cudaError_t launch_passes(const moe_shape& s, const FfnCall& c, cudaStream_t st)
     };
     if ((e = cut(ev.begin, 0)) != cudaSuccess) return e;
     if ((e = join(aux, st, ss->ev[0])) != cudaSuccess) return e;
-    if ((e = launch_tc(a, plan + kPlanTcUpCold * stride, true, true, st, act)) != cudaSuccess)
+    if ((e = launch_tc(a, plan + kPlanTcUpCold * stride, true, true, st, act, true)) != cudaSuccess)
       return e;
     if ((e = launch_tc(a, plan + kPlanTcUp * stride, true, false, aux, act + 1)) != cudaSuccess)
       return e;
     if ((e = join(st, aux, ss->ev[1])) != cudaSuccess) return e;
     if ((e = cut(ev.mid, 1)) != cudaSuccess) return e;
     if ((e = join(aux, st, ss->ev[2])) != cudaSuccess) return e;
-    if ((e = launch_tc(a, plan + kPlanTcDnCold * stride, false, true, st, act + 2)) != cudaSuccess)
+    if ((e = launch_tc(a, plan + kPlanTcDnCold * stride, false, true, st, act + 2, true)) !=
+        cudaSuccess)
       return e;
     if ((e = launch_tc(a, plan + kPlanTcDown * stride, false, false, aux, act + 3)) != cudaSuccess)
       return e;

@@ -30,11 +30,12 @@ cudaError_t launch_gemv(const FfnArgs& a, const int32_t* prefix_up, const int32_
 
 // tensor-core path (ffn_tc.cu): bf16 weights
 int tc_tile_tokens(bool gateup, bool decode);
+int tc_cold_tile_tokens();  // tokens per tile of a split prefill's cold list
 int tc_tile_rows(bool gateup, bool decode, int d);  // weight rows per tile
 // plan units (weight tiles, or cluster pairs of them) per expert
 int tc_plan_mtiles(bool gateup, bool decode, int d, int f);
 cudaError_t launch_tc(const FfnArgs& a, const int32_t* prefix, bool gateup, bool decode,
-                      cudaStream_t st, const int32_t* active = nullptr);
+                      cudaStream_t st, const int32_t* active = nullptr, bool cold = false);
 
 // tensor-core path (ffn_tc_fp8.cu): E4M3 weights dequantised into TMEM
 int tc_fp8_tile_tokens(bool gateup, bool decode, long routed, int E);

@@ -282,6 +282,10 @@ int tc_tile_tokens(bool gateup, bool decode) {
   return decode ? 64 : 256;
 }
 
+// The cold list of a split prefill (experts with few tokens, HBM-bound): 32-token tiles, whose
+// smaller token slots leave room for deeper weight rings.
+int tc_cold_tile_tokens() { return 32; }
+
 int tc_tile_rows(bool gateup, bool decode, int d) {
   return (!gateup && down_pairs(d, decode)) ? 2 * kBM : kBM;
 }
@@ -299,7 +303,7 @@ int tc_plan_mtiles(bool gateup, bool decode, int d, int f) {
 }
 
 cudaError_t launch_tc(const FfnArgs& a, const int32_t* prefix, bool gateup, bool decode,
-                      cudaStream_t st, const int32_t* active) {
+                      cudaStream_t st, const int32_t* active, bool cold) {
   TcParams p{};
   p.active = active;
   p.T = a.T; p.k = a.k; p.E = a.E; p.n_shared = a.n_shared;
@@ -316,8 +320,10 @@ cudaError_t launch_tc(const FfnArgs& a, const int32_t* prefix, bool gateup, bool
   const uint64_t routed = (uint64_t)a.T * a.k;
   const uint64_t slots = routed + (uint64_t)a.n_shared * a.T;
   const bool cl = tc_clustered(gateup, decode, a.d, a.f);
-  // full token tiles arrive in one box, or, with pairs, in one half-tile box in each CTA
-  const uint32_t nt = (uint32_t)tc_tile_tokens(gateup, decode) / (cl ? 2u : 1u);
+  // full token tiles arrive in one box of the kernel's NT rows, or, with pairs, in one half-tile
+  // box in each CTA
+  const int tile_nt = cold ? tc_cold_tile_tokens() : tc_tile_tokens(gateup, decode);
+  const uint32_t nt = (uint32_t)tile_nt / (cl ? 2u : 1u);
   CUtensorMap w, b0, b1, b0w, b1w;
   cudaError_t e;
   if (gateup) {
@@ -334,6 +340,9 @@ cudaError_t launch_tc(const FfnArgs& a, const int32_t* prefix, bool gateup, bool
     b1w = b0w;
   }
   if (e != cudaSuccess) return e;
+  if (cold)  // 32-token tiles: 6 stages of 36 KB (gate/up), 10 of 20 KB (down)
+    return gateup ? launch_variant<true, 32, 6, 2, 2>(w, b0, b1, b0w, b1w, p, st)
+                  : launch_variant<false, 32, 10, 1, 2>(w, b0, b1, b0w, b1w, p, st);
   if (gateup)
     return decode ? launch_variant<true, 64, 5, 2, 2>(w, b0, b1, b0w, b1w, p, st)
                   : cl ? launch_variant<true, 256, 4, 2, 1, true>(w, b0, b1, b0w, b1w, p, st)
