@@ -231,17 +231,19 @@ __global__ void __launch_bounds__(256) k_plan_gather(const int32_t* __restrict__
     gather_row_chunks(i, x, perm_token, T, routed, d, x_perm, status);
 }
 
-// Decode batches of at most 32 tokens (one permutation chunk), moe_forward only: after the
+// Decode batches of at most 8 tokens (one permutation chunk), moe_forward only: after the
 // router logits, one launch does what k_router_topk, k_perm_small and k_plan_gather do. Every
 // block selects the top k of every token (warp_topk_token, the router's own selection) and
 // sorts the T*k (token, choice) pairs in shared memory exactly as k_perm_small sorts one chunk
 // (a lane per token, one 32-bit mask of tokens per expert, an exclusive scan of the mask
-// popcounts in expert order): at most 32 tokens x 1024 logits and 1024 pairs, a few
-// microseconds, repeated in every block so that no block waits for another. Block 0 then writes
+// popcounts in expert order): at most 8 tokens (a warp each) x 1024 logits, a few
+// microseconds, repeated in every block so that no block waits for another. (At 32 tokens the
+// repeated selection made the front no faster than the three kernels it replaces: V4-Pro
+// decode 1576 us with it at 256 threads, 1559 us at 512, 1555 us without.) Block 0 then writes
 // the routing, the permutation and the tensor-core passes' tile prefixes; the other blocks
 // gather their share of the rows (GatherMode) with the permutation held in their own shared
 // memory.
-constexpr int kFrontMaxT = kChunkTokens;
+constexpr int kFrontMaxT = 8;
 
 __global__ void __launch_bounds__(256) k_route_front(
     const float* __restrict__ logits, int T, int E, int k, int n_shared,
@@ -648,7 +650,7 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32
   return launch_passes(s, c, st);
 }
 
-// moe_forward on a decode batch of at most 32 tokens with the fp32 router and every expert on the
+// moe_forward on a decode batch of at most 8 tokens with the fp32 router and every expert on the
 // tensor cores: logits, then k_route_front (top-k, permutation, plan and gather in one launch),
 // then the FFN passes and the combine. The outputs are the same bits as the four calls.
 static bool front_applies(const moe_shape& s) {

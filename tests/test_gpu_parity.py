@@ -200,10 +200,11 @@ def test_combine_direct():
 
 
 @pytest.mark.parametrize("over", [{}, {"wdtype": "fp8"},
-                                  # decode batches of at most 32 tokens: the fused front
-                                  {"T": 1, "wdtype": "fp8"}, {"T": 32, "E": 40, "k": 6},
+                                  # decode batches of at most 8 tokens: the fused front
+                                  {"T": 1, "wdtype": "fp8"}, {"T": 8, "E": 40, "k": 6},
                                   {"T": 7, "E": 384, "k": 6, "wdtype": "mxfp4"},
-                                  {"T": 32, "E": 1024, "k": 32, "d": 256, "f": 128},
+                                  {"T": 8, "E": 1024, "k": 32, "d": 256, "f": 128},
+                                  {"T": 32, "E": 40, "k": 6},
                                   {"router": "zipf", "T": 600, "d": 512, "f": 256, "E": 16, "k": 2},
                                   {"T": 600, "d": 512, "f": 256, "E": 8, "k": 2, "wdtype": "fp8"},
                                   {"n_shared": 0}, {"wdtype": "mxfp4"},
