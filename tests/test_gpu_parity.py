@@ -295,17 +295,24 @@ def test_device_generator_matches_host_generator():
     np.testing.assert_array_equal(s4.cpu().numpy(), s4_h)
 
 
+# The oracle decodes MXFP4 weights about 2.5x slower than E4M3 ones, so its full-size samples
+# are smaller (the GPU suite stays within its time limit; the MXFP4 prefill tiles are the FP8
+# kernel's, checked at the full FP8 sample).
+def max_sampled_tokens(cfg):
+    return 192 if cfg.wdtype == "mxfp4" else 512
+
+
 def sample_tokens(cfg, idx, n_even=6):
     """Tokens whose outputs are checked in full. Below 1024 tokens: evenly spaced ones plus two
     tokens of the hottest and two of the coldest non-empty expert. From 1024 tokens: every
-    s-th token (s = 8, or T/512 so that at most 512 tokens are checked) plus two tokens of
-    each of the four hottest and four coldest non-empty experts."""
+    s-th token (s = 8, or T/512 so that at most 512 tokens are checked; 192 for MXFP4 weights)
+    plus two tokens of each of the four hottest and four coldest non-empty experts."""
     T = cfg.T
     counts = np.bincount(idx.ravel(), minlength=cfg.E)
     order = np.argsort(-counts, kind="stable")
     nonempty = [int(e) for e in order if counts[e] > 0]
     if T >= 1024:
-        picks = set(range(0, T, max(8, T // 512)))
+        picks = set(range(0, T, max(8, T // max_sampled_tokens(cfg))))
         extremes = nonempty[:4] + nonempty[-4:]
     else:
         picks = set(np.linspace(0, T - 1, min(n_even, T)).astype(int).tolist())
@@ -377,15 +384,17 @@ def y_perm_rows_to_check(cfg, r_off, T):
     """Slots whose expert outputs are checked against the oracle: the last row of every routed
     expert that received tokens (each expert's weights, wherever they lie in HBM), the first and
     last rows of the shared segment, and from 1024 tokens every row of the four hottest and the
-    four coldest non-empty experts (their deepest and shallowest token tiles)."""
+    four coldest non-empty experts (their deepest and shallowest token tiles; for MXFP4 weights
+    the first 512 rows of each)."""
     counts = np.diff(r_off[: cfg.E + 1])
     rows = {int(r_off[e + 1]) - 1 for e in range(cfg.E) if counts[e] > 0}
     if cfg.n_shared and T > 0:
         rows.update({int(r_off[cfg.E]), int(r_off[cfg.E + 1]) - 1})
     if T >= 1024:
         order = [int(e) for e in np.argsort(-counts, kind="stable") if counts[e] > 0]
+        cap = 512 if cfg.wdtype == "mxfp4" else 1 << 30
         for e in order[:4] + order[-4:]:
-            rows.update(range(int(r_off[e]), int(r_off[e + 1])))
+            rows.update(range(int(r_off[e]), min(int(r_off[e + 1]), int(r_off[e]) + cap)))
     return sorted(rows)
 
 
