@@ -129,7 +129,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      const uint64_t pol_w = policy_evict_first();  // weights: streamed once per call
+      // weights: streamed once per call (evict first), unless the expert has several token
+      // tiles, whose tiles run at about the same time on other SMs and read them again
+      const uint64_t pol_once = policy_evict_first(), pol_again = policy_evict_normal();
       const uint64_t pol_b = policy_evict_last();   // token rows: reused by every weight tile
       const uint32_t full0 = PAIR ? mapa_shared(smem_u32(&full[0]), 0) : 0;
       uint32_t stage = 0, phase = 0;
@@ -151,6 +153,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         const bool sh = GATEUP && t.shared;
         const CUtensorMap* bmap = sh ? &tm_b1 : &tm_b0;
         const CUtensorMap* bmapw = sh ? &tm_b1w : &tm_b0w;
+        const uint64_t pol_w = t.multi ? pol_again : pol_once;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!wait_bar(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
           uint8_t* st = smem + stage * S::kStageBytes;

@@ -219,12 +219,15 @@ __global__ void __launch_bounds__(kThreadsW, 1)
   if (warp == 0) {
     // ---------------- TMA producer: E4M3 codes ----------------
     if (lane == 0) {
-      const uint64_t pol_w = policy_evict_first();
+      // codes: streamed once per call (evict first), unless the expert has several token
+      // tiles, whose tiles run at about the same time on other SMs and read them again
+      const uint64_t pol_once = policy_evict_first(), pol_again = policy_evict_normal();
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       for (int tile = tile0; ok && tile < total; tile += tstep) {
         Tile t;
         decode(tile, t);
+        const uint64_t pol_w = t.multi ? pol_again : pol_once;
         const int wrow = t.e * p.rows_per_expert + t.mt * (GATEUP ? kBM : kBM * KA);
         const int wrow1 = GATEUP ? wrow + p.f : wrow + kBM;
         for (int kb = 0; kb < kblocks; ++kb) {

@@ -37,6 +37,7 @@ struct TcParams {
 struct Tile {
   int e, mt, slot0, ntok, brow0;
   bool shared;
+  bool multi;  // the expert has more token tiles than this one: its weights are read again
 };
 
 // Token rows of the gate/up pass come from the gathered rows (routed experts) or straight from
@@ -59,6 +60,7 @@ __device__ __forceinline__ void decode_tile(const TcParams& p, int tile, Tile& t
   t.mt = mt;
   t.slot0 = seg0 + nt * NT;
   t.ntok = min(NT, cnt - nt * NT);
+  t.multi = ntn > 1;
   t.shared = (e == p.E);
   t.brow0 = (GATEUP && t.shared) ? t.slot0 - p.T * p.k : t.slot0;
 }
