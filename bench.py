@@ -63,6 +63,8 @@ def parse_args(argv=None):
     p.add_argument("--no-graph", action="store_true",
                    help="launch the layer eagerly each step instead of replaying a CUDA graph")
     p.add_argument("--e2e-steps", type=int, default=None)
+    p.add_argument("--graph-passes", type=int, default=1,
+                   help="layer passes captured back to back in the timed CUDA graph")
     p.add_argument("--T", type=int, default=None, help="override the token batch (profiling cases)")
     p.add_argument("--E", type=int, default=None, help="override the routed experts (profiling cases)")
     return p.parse_args(argv)
@@ -348,10 +350,13 @@ def load_config(name, T=None, E=None):
     return cfg
 
 
-def measure(cfg, steps, warmup, graph=True, e2e_steps=None, min_ms=None, keep_inputs=False):
+def measure(cfg, steps, warmup, graph=True, e2e_steps=None, min_ms=None, keep_inputs=False,
+            passes=1):
     """Times `steps` layer passes of one workload (CUDA events on the launching stream, inputs
     resident in HBM), then the gate/up and down phases averaged over as many replays, then the
-    end-to-end loop. With min_ms, steps grows until the timed region lasts about min_ms."""
+    end-to-end loop. With min_ms, steps grows until the timed region lasts about min_ms. With
+    passes > 1 the timed graph holds that many passes back to back (as a model's layers follow
+    one another in one graph)."""
     import torch
 
     import routed_expert_ffn_moe_gb300 as moe
@@ -369,19 +374,28 @@ def measure(cfg, steps, warmup, graph=True, e2e_steps=None, min_ms=None, keep_in
     torch.cuda.synchronize()
     moe.moe_check_device_status(layer.ws)
 
-    # One step = one layer pass (one moe_forward call), captured once into a CUDA graph (the
-    # library enqueues no synchronisation or allocation) and replayed. The timed graph holds the
-    # layer's kernels alone (an event recorded between two kernels would cut the programmatic
-    # launch overlap between them); a second graph, captured with the library's phase events,
-    # times the gate/up and down passes.
-    g = gp = None
+    # One step = one layer pass (one moe_forward call), captured into a CUDA graph (the library
+    # enqueues no synchronisation or allocation) and replayed; the graph holds `passes` of them.
+    # The timed graph holds the layer's kernels alone (an event recorded between two kernels
+    # would cut the programmatic launch overlap between them); a second graph of one pass,
+    # captured with the library's phase events, times the gate/up and down passes.
+    g = gp = g1 = None
+    passes = max(1, passes) if graph else 1
+    if graph and not min_ms and steps % passes:  # exactly `steps` passes
+        passes = max(p for p in range(1, passes + 1) if steps % p == 0)
     moe.moe_profile_enable(True)    # resets the launch counter
     moe.moe_profile_enable(False)   # no phase events; launches are still counted
     if graph:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            layer.forward(x)
-        launches_per_step = moe.moe_profile_read()["kernel_launches"]
+            for _ in range(passes):
+                layer.forward(x)
+        launches_per_step = moe.moe_profile_read()["kernel_launches"] // passes
+        g1 = g
+        if passes > 1:  # one pass a step for the end-to-end loop
+            g1 = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g1):
+                layer.forward(x)
         moe.moe_profile_enable(True)
         gp = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gp):
@@ -410,15 +424,17 @@ def measure(cfg, steps, warmup, graph=True, e2e_steps=None, min_ms=None, keep_in
             step()
         s1.record(stream)
         torch.cuda.synchronize()
-        est = s0.elapsed_time(s1) / 3
+        est = s0.elapsed_time(s1) / (3 * passes)
         steps = int(min(5000, max(steps, math.ceil(min_ms / max(est, 1e-3)))))
+    replays = -(-steps // passes)
+    steps = replays * passes
 
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(torch.cuda.current_device()) as clocks:
         torch.cuda.synchronize()
         t_host0 = time.time()
         start.record(stream)
-        for _ in range(steps):
+        for _ in range(replays):
             step()
         end.record(stream)
         torch.cuda.synchronize()
@@ -442,7 +458,8 @@ def measure(cfg, steps, warmup, graph=True, e2e_steps=None, min_ms=None, keep_in
         moe.moe_profile_enable(False)
         ms_up, ms_dn = up / steps, dn / steps
 
-        # End to end: pinned host x -> device, the layer, y -> pinned host, every step.
+        # End to end: pinned host x -> device, the layer, y -> pinned host, every step (one pass
+        # a step).
         e2e_steps = e2e_steps or max(3, steps // 4)
         x_host = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
         x_host.copy_(x)
@@ -452,7 +469,10 @@ def measure(cfg, steps, warmup, graph=True, e2e_steps=None, min_ms=None, keep_in
         e0.record(stream)
         for _ in range(e2e_steps):
             x.copy_(x_host, non_blocking=True)
-            step()
+            if g1 is not None:
+                g1.replay()
+            else:
+                layer.forward(x)
             y_host.copy_(layer.y, non_blocking=True)
         e1.record(stream)
         torch.cuda.synchronize()
@@ -497,7 +517,7 @@ def measure(cfg, steps, warmup, graph=True, e2e_steps=None, min_ms=None, keep_in
     res = {
         "cfg": cfg, "ms": ms, "ms_e2e": ms_e2e, "steps": steps, "e2e_steps": e2e_steps,
         "n_hit": n_hit, "launches_per_step": launches_per_step,
-        "graph": g is not None,
+        "graph": g is not None, "graph_passes": passes,
         "layer": {"us": ms * 1e3, "algorithmic_bytes": layer_bytes, "flops": layer_flops,
                   "achieved_GBps": layer_bytes / (ms * 1e-3) / 1e9,
                   "achieved_TFLOPs": layer_flops / (ms * 1e-3) / 1e12,
@@ -512,7 +532,7 @@ def measure(cfg, steps, warmup, graph=True, e2e_steps=None, min_ms=None, keep_in
     }
     if keep_inputs:
         res["dev"] = dev
-    del g, gp, layer, w, x, x_host, y_host
+    del g, gp, g1, layer, w, x, x_host, y_host
     if not keep_inputs:
         del dev
     torch.cuda.synchronize()
@@ -560,23 +580,24 @@ def main():
 
     want_cpu = not args.no_cpu_baseline
     r = measure(cfg, args.steps, args.warmup, graph=not args.no_graph, e2e_steps=args.e2e_steps,
-                keep_inputs=want_cpu)
+                keep_inputs=want_cpu, passes=args.graph_passes)
     roof = dict(r["roofline"])
     roof["traffic"] = ncu_traffic(cfg.name)
     out = {
         "metric": METRIC, "value": cfg.T / (r["ms"] * 1e-3), "unit": "tokens/s", "n_gpus": 1,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms"],
+        "steps": r["steps"], "warmup": args.warmup, "ms_per_step": r["ms"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": dtype_of(cfg), "data": "synthetic",
         "config": config_record(
             cfg,
-            launch="CUDA graph replay of one moe_forward call" if r["graph"] else "eager",
+            launch=(f"CUDA graph replay of {r['graph_passes']} moe_forward call(s) back to back"
+                    if r["graph"] else "eager"),
             l2="inputs larger than L2 (expert weights "
                f"{(cfg.E + cfg.n_shared) * moe_roofline_expert_bytes(cfg) / 1e9:.1f} GB), no flush",
             experts_hit=r["n_hit"], layer=r["layer"], phases_us=r["phases_us"]),
         "roofline": roof,
         "e2e": r["e2e"],
-        "gpu_launches": r["launches_per_step"] * args.steps,
+        "gpu_launches": r["launches_per_step"] * r["steps"],
         "clocks": r["clocks"],
     }
     if want_cpu:
@@ -587,7 +608,7 @@ def main():
     for name in SWEEPS[args.sweep]:
         sc = load_config(name)
         sweep.append(sweep_point(measure(sc, args.steps, args.warmup, graph=not args.no_graph,
-                                         min_ms=args.sweep_min_ms)))
+                                         min_ms=args.sweep_min_ms, passes=args.graph_passes)))
     out["sweep"] = sweep
     print(json.dumps(out), flush=True)
 

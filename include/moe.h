@@ -210,7 +210,8 @@ MOE_API moe_status moe_combine(const moe_shape* shape, const float* y_perm, cons
  * that one second stream. The overlap is used for prefill-sized batches (more than 32 routed
  * tokens per expert on average) with n_shared = 1; otherwise the four steps run in order on
  * `stream`. y_perm [T*k + n_shared*T, d] fp32 and y [T, d] bf16 as in moe_expert_ffn and
- * moe_combine. */
+ * moe_combine. The status word is cleared as the call starts (batches of at most 8 tokens: by
+ * the call's first kernel, so that a CUDA graph of consecutive calls holds no memset node). */
 MOE_API moe_status moe_forward(const moe_shape* shape, const void* x, const void* wg,
                                const float* bias, const void* w13, const void* s13,
                                const void* w2, const void* s2, int32_t* topk_idx, float* topk_w,

@@ -290,14 +290,16 @@ moe_status moe_forward(const moe_shape* shape, const void* x, const void* wg, co
   WsLayout L;
   if ((st = check_ws(shape, ws, ws_bytes, &L)) != MOE_OK) return st;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  // A layer starts here: clear the device status word.
-  cudaError_t e = cudaMemsetAsync(static_cast<char*>(ws) + L.status, 0, sizeof(int), cs);
-  if (e != cudaSuccess) return cuda_fail(e, "moe_forward status reset");
+  cudaError_t e;
   if (shape->T == 0) {  // no token: only the expert offsets are defined
+    // A layer starts here: clear the device status word.
+    e = cudaMemsetAsync(static_cast<char*>(ws) + L.status, 0, sizeof(int), cs);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_forward status reset");
     e = launch_permute(*shape, topk_idx, expert_offsets, perm_token, inv_slot,
                        static_cast<char*>(ws), L, cs);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_forward launch");
   }
+  // launch_forward clears the status word first (with a memset, or in its first kernel)
   e = launch_forward(*shape, static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(wg),
                      bias, w13, s13, w2, s2, topk_idx, topk_w, expert_offsets, perm_token,
                      inv_slot, y_perm, static_cast<uint16_t*>(y), static_cast<char*>(ws), L, cs);

@@ -233,16 +233,16 @@ __global__ void __launch_bounds__(256) k_plan_gather(const int32_t* __restrict__
 
 // Decode batches of at most 8 tokens (one permutation chunk), moe_forward only: after the
 // router logits, one launch does what k_router_topk, k_perm_small and k_plan_gather do. Every
-// block selects the top k of every token (warp_topk_token, the router's own selection) and
-// sorts the T*k (token, choice) pairs in shared memory exactly as k_perm_small sorts one chunk
-// (a lane per token, one 32-bit mask of tokens per expert, an exclusive scan of the mask
-// popcounts in expert order): at most 8 tokens (a warp each) x 1024 logits, a few
-// microseconds, repeated in every block so that no block waits for another. (At 32 tokens the
-// repeated selection made the front no faster than the three kernels it replaces: V4-Pro
-// decode 1576 us with it at 256 threads, 1559 us at 512, 1555 us without.) Block 0 then writes
-// the routing, the permutation and the tensor-core passes' tile prefixes; the other blocks
-// gather their share of the rows (GatherMode) with the permutation held in their own shared
-// memory.
+// block selects the top k of every token (warp_topk_token, the router's own selection, a warp
+// per token) and sorts the T*k (token, choice) pairs in shared memory as k_perm_small sorts one
+// chunk (one 32-bit mask of tokens per expert, an exclusive scan of the mask popcounts in
+// expert order, a pair's slot = its expert's offset + the number of its expert's tokens before
+// it), with a thread per pair and the slot offsets and both tile prefixes in one scan; this is
+// repeated in every block so that no block waits for another. (At 32 tokens the repeated
+// selection made the front no faster than the three kernels it replaces: V4-Pro decode 1576 us
+// with it at 256 threads, 1559 us at 512, 1555 us without.) Block 0 then writes the routing,
+// the permutation and the tensor-core passes' tile prefixes; the other blocks gather their
+// share of the rows (GatherMode) with the permutation held in their own shared memory.
 constexpr int kFrontMaxT = 8;
 
 __global__ void __launch_bounds__(256) k_route_front(
@@ -252,100 +252,100 @@ __global__ void __launch_bounds__(256) k_route_front(
     int32_t* __restrict__ plan, const uint16_t* __restrict__ x, long routed, int d,
     uint16_t* __restrict__ x_perm, int* status, mx::Planes xq, long nq, int mode) {
   extern __shared__ uint32_t fm[];
+  const int E1 = a.E + a.n_shared;
   uint32_t* sel = fm;                                               // [E] token masks
   int32_t* off_s = reinterpret_cast<int32_t*>(fm + E);              // [E + 2]
   int32_t* idx_s = off_s + (E + 2);                                 // [T * k]
   float* w_s = reinterpret_cast<float*>(idx_s + T * k);             // [T * k]
   int32_t* perm_s = reinterpret_cast<int32_t*>(w_s + T * k);        // [T * k]
   int32_t* inv_s = perm_s + T * k;                                  // [T * k]
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
   for (int e = threadIdx.x; e < E; e += blockDim.x) sel[e] = 0;
+  prefetch_l2_span(logits, (size_t)T * E * 4);
+  if (blockIdx.x > 0) prefetch_l2_span(x, (size_t)T * d * 2);
   pdl_wait_then_release();
   for (int t = warp; t < T; t += (int)(blockDim.x >> 5))
     warp_topk_token(logits + (size_t)t * E, E, k, idx_s + t * k, w_s + t * k);
   __syncthreads();
-  // the token masks of the one chunk (lane = token)
-  if (warp == 0 && lane < T) {
-    const int32_t* row = idx_s + lane * k;
-    for (int j = 0; j < k; ++j) {
-      const int e = row[j];
-      bool ok = (unsigned)e < (unsigned)E;
-      for (int j2 = 0; j2 < j && ok; ++j2) ok = row[j2] != e;
-      if (ok)
-        atomicOr(&sel[e], 1u << lane);
-      else if (blockIdx.x == 0)
-        record_error(status, MOE_ERR_DEVICE_BOUNDS);
-    }
+  // The token masks of the one chunk, a thread per (token, choice) pair. A pair whose expert is
+  // out of range or repeats an earlier choice of its token is dropped (and reported).
+  const int pairs = T * k;
+  for (int i = threadIdx.x; i < pairs; i += blockDim.x) {
+    const int t = i / k, j = i - t * k;
+    const int32_t* row = idx_s + t * k;
+    const int e = row[j];
+    bool ok = (unsigned)e < (unsigned)E;
+    for (int j2 = 0; j2 < j && ok; ++j2) ok = row[j2] != e;
+    if (ok)
+      atomicOr(&sel[e], 1u << t);
+    else if (blockIdx.x == 0)
+      record_error(status, MOE_ERR_DEVICE_BOUNDS);
   }
   __syncthreads();
-  // exclusive scan of the per-expert counts, each thread a run of consecutive experts
+  // One scan over the experts (the shared one last, T tokens): the slot offsets and, in block
+  // 0, the tile prefixes of the gate/up and the down pass (as plan_block writes them; every
+  // expert on the tensor cores, no split). Each thread takes a run of consecutive experts.
   {
-    const int per = (E + (int)blockDim.x - 1) / (int)blockDim.x;
-    const int e0 = min(E, (int)threadIdx.x * per), e1 = min(E, e0 + per);
-    int sum = 0;
-    for (int e = e0; e < e1; ++e) sum += __popc(sel[e]);
-    int total;
-    int run = block_exclusive_scan(sum, &total);
+    const int per = (E1 + (int)blockDim.x - 1) / (int)blockDim.x;
+    const int e0 = min(E1, (int)threadIdx.x * per), e1 = min(E1, e0 + per);
+    // plan units of an expert with cnt tokens (one token tile unless cnt exceeds it)
+    auto units = [](int cnt, int nt, int mt) {
+      return cnt <= 0 ? 0 : (cnt <= nt ? 1 : (cnt + nt - 1) / nt) * mt;
+    };
+    int3 sum = make_int3(0, 0, 0);
     for (int e = e0; e < e1; ++e) {
-      off_s[e] = run;
-      run += __popc(sel[e]);
+      const int cnt = e < E ? __popc(sel[e]) : T;
+      sum.x += e < E ? cnt : 0;
+      sum.y += units(cnt, a.nt_up, a.mt_up);
+      sum.z += units(cnt, a.nt_dn, a.mt_dn);
+    }
+    int3 tot;
+    int3 run = block_exclusive_scan3(sum, &tot);
+    for (int e = e0; e < e1; ++e) {
+      const int cnt = e < E ? __popc(sel[e]) : T;
+      if (e < E) off_s[e] = run.x;
+      if (blockIdx.x == 0) {
+        plan[kPlanTcUp * a.stride + e] = run.y;
+        plan[kPlanTcDown * a.stride + e] = run.z;
+      }
+      run.x += e < E ? cnt : 0;
+      run.y += units(cnt, a.nt_up, a.mt_up);
+      run.z += units(cnt, a.nt_dn, a.mt_dn);
     }
     if (threadIdx.x == 0) {
       off_s[E] = T * k;
       off_s[E + 1] = T * k + n_shared * T;
+      if (blockIdx.x == 0) {
+        plan[kPlanTcUp * a.stride + E1] = tot.y;
+        plan[kPlanTcDown * a.stride + E1] = tot.z;
+      }
     }
   }
   __syncthreads();
-  if (warp == 0 && lane < T) {
-    const int32_t* row = idx_s + lane * k;
-    const uint32_t below = (1u << lane) - 1u;
-    for (int j = 0; j < k; ++j) {
-      const int e = row[j];
-      bool ok = (unsigned)e < (unsigned)E;
-      for (int j2 = 0; j2 < j && ok; ++j2) ok = row[j2] != e;
-      if (!ok) {
-        inv_s[lane * k + j] = -1;
-        continue;
-      }
-      const int slot = off_s[e] + __popc(sel[e] & below);
-      perm_s[slot] = lane;
-      inv_s[lane * k + j] = slot;
+  // slots: expert offset + the pair's rank among its expert's tokens (token order)
+  for (int i = threadIdx.x; i < pairs; i += blockDim.x) {
+    const int t = i / k, j = i - t * k;
+    const int32_t* row = idx_s + t * k;
+    const int e = row[j];
+    bool ok = (unsigned)e < (unsigned)E;
+    for (int j2 = 0; j2 < j && ok; ++j2) ok = row[j2] != e;
+    if (!ok) {
+      inv_s[i] = -1;
+      continue;
     }
+    const int slot = off_s[e] + __popc(sel[e] & ((1u << t) - 1u));
+    perm_s[slot] = t;
+    inv_s[i] = slot;
   }
   __syncthreads();
   if (blockIdx.x == 0) {
-    for (int i = threadIdx.x; i < T * k; i += blockDim.x) {
+    for (int i = threadIdx.x; i < pairs; i += blockDim.x) {
       topk_idx[i] = idx_s[i];
       topk_w[i] = w_s[i];
       perm_token[i] = perm_s[i];
       inv_slot[i] = inv_s[i];
     }
     for (int e = threadIdx.x; e < E + 2; e += blockDim.x) offsets[e] = off_s[e];
-    // the plan rows the decode passes read (every expert on the tensor cores, no split): the
-    // tile prefixes of the gate/up and the down pass, as plan_block writes them
-    const int E1 = a.E + a.n_shared;
-    const int per = (E1 + (int)blockDim.x - 1) / (int)blockDim.x;
-    const int e0 = min(E1, (int)threadIdx.x * per), e1 = min(E1, e0 + per);
-    int su = 0, sd = 0;
-    for (int e = e0; e < e1; ++e) {
-      const int cnt = off_s[e + 1] - off_s[e];
-      su += cnt > 0 ? (cnt + a.nt_up - 1) / a.nt_up * a.mt_up : 0;
-      sd += cnt > 0 ? (cnt + a.nt_dn - 1) / a.nt_dn * a.mt_dn : 0;
-    }
-    int tot_u, tot_d;
-    int ru = block_exclusive_scan(su, &tot_u);
-    int rd = block_exclusive_scan(sd, &tot_d);
-    for (int e = e0; e < e1; ++e) {
-      const int cnt = off_s[e + 1] - off_s[e];
-      plan[kPlanTcUp * a.stride + e] = ru;
-      plan[kPlanTcDown * a.stride + e] = rd;
-      ru += cnt > 0 ? (cnt + a.nt_up - 1) / a.nt_up * a.mt_up : 0;
-      rd += cnt > 0 ? (cnt + a.nt_dn - 1) / a.nt_dn * a.mt_dn : 0;
-    }
-    if (threadIdx.x == 0) {
-      plan[kPlanTcUp * a.stride + E1] = tot_u;
-      plan[kPlanTcDown * a.stride + E1] = tot_d;
-    }
     return;
   }
   const long i = (long)(blockIdx.x - 1) * blockDim.x + threadIdx.x;
@@ -667,7 +667,9 @@ static cudaError_t launch_forward_front(const moe_shape& s, const uint16_t* x, c
                                         const WsLayout& L, cudaStream_t st) {
   int* status = reinterpret_cast<int*>(ws + L.status);
   float* logits = reinterpret_cast<float*>(ws + L.logits);
-  cudaError_t e = launch_router_logits(s, x, wg, bias, logits, st);
+  // the call's first kernel clears the status word (no memset node: it would end the
+  // programmatic launch overlap with the previous call's last kernel)
+  cudaError_t e = launch_router_logits(s, x, wg, bias, logits, st, status);
   if (e != cudaSuccess) return e;
   const FfnCall c = make_ffn_call(s, x, perm_token, offsets, w13, s13, w2, s2, y_perm, ws, L, true);
   e = launch_pdl(k_route_front, dim3((unsigned)(1 + (c.gather_n + 255) / 256)), dim3(256),
@@ -699,6 +701,8 @@ cudaError_t launch_forward(const moe_shape& s, const uint16_t* x, const uint16_t
   if (!overlap && front_applies(s) && !router_uses_tc(s))
     return launch_forward_front(s, x, wg, bias, w13, s13, w2, s2, topk_idx, topk_w, offsets,
                                 perm_token, inv_slot, y_perm, y, ws, L, st);
+  // A layer starts here: clear the device status word.
+  if ((e = cudaMemsetAsync(status, 0, sizeof(int), st)) != cudaSuccess) return e;
   if (!overlap) {
     if ((e = launch_route(s, x, wg, bias, topk_idx, topk_w, ws, L, st)) != cudaSuccess) return e;
     if ((e = launch_permute(s, topk_idx, offsets, perm_token, inv_slot, ws, L, st)) != cudaSuccess)

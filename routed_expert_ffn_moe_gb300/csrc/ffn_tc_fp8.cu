@@ -59,7 +59,7 @@ struct SmemQ {
   static constexpr uint32_t kCSlotBytes = kA * 2 * kBHalf;                 // scaled token tiles
   static constexpr uint32_t kTilesBytes = STAGES * kStageBytes + CSTAGES * kCSlotBytes;
   static constexpr uint32_t kBarBytes = 8 * (2 * STAGES + 2 * CSTAGES + 4) + 16;
-  static constexpr uint32_t kTotal = kTilesBytes + kBarBytes + 1024;
+  static constexpr uint32_t kTotal = kTilesBytes + kBarBytes + kTileListBytes + 1024;
   static constexpr uint32_t kAccCols = KA * NT;
   static constexpr uint32_t kAStageCols = kA * kACols;
   static constexpr uint32_t kUsedCols = 2 * kAccCols + CSTAGES * kAStageCols;
@@ -102,7 +102,7 @@ __device__ __forceinline__ void sts_u4(uint32_t addr, const uint4& v) {
 template <bool GATEUP, int NT, int STAGES, int CSTAGES, int KA>
 __global__ void __launch_bounds__(kThreadsQ, 1)
     k_tc_ffn_fp8(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b0,
-                 const __grid_constant__ CUtensorMap tm_b1, const TcParams p,
+                 const __grid_constant__ CUtensorMap tm_b1, TcParams p,
                  const float* __restrict__ scales) {
   using S = SmemQ<GATEUP, NT, STAGES, CSTAGES, KA>;
   static_assert(S::kUsedCols <= 512, "TMEM columns");
@@ -120,6 +120,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
   uint64_t* acc_empty = acc_full + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int32_t* list_s = reinterpret_cast<int32_t*>(smem + S::kTilesBytes + S::kBarBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E1 = p.E + p.n_shared;
@@ -152,38 +153,75 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-  // the tile list (prefix) is written by the previous kernel
+  // One stage of a tile: its weight boxes (KA tiles of 128 rows x 128 K), then its token rows
+  // (nbox boxes of 16 rows, two 64-wide K halves), all completing on the stage's full barrier.
+  const uint64_t pol_w = policy_evict_first();
+  const uint64_t pol_b = policy_evict_last();
+  auto stage_bytes = [&](const Tile& t) {
+    return S::kA * kQTileBytes + (uint32_t)((t.ntok + kBoxRows - 1) / kBoxRows) * 2 * kBBoxBytes;
+  };
+  auto load_weights = [&](const Tile& t, int kb, uint32_t stage) {
+    uint8_t* st = smem + stage * S::kStageBytes;
+    const int wrow = t.e * p.rows_per_expert + t.mt * kBM * (GATEUP ? 1 : KA);
+    tma_load_2d(st, &tm_w, &full[stage], kb * kQK, wrow, pol_w);
+    if (KA == 2)  // up rows of the same features, or the next 128 rows of W_d
+      tma_load_2d(st + kQTileBytes, &tm_w, &full[stage], kb * kQK, wrow + (GATEUP ? p.f : kBM),
+                  pol_w);
+  };
+  auto load_tokens = [&](const Tile& t, int kb, uint32_t stage) {
+    uint8_t* bt = smem + stage * S::kStageBytes + S::kA * kQTileBytes;
+    const CUtensorMap* bmap = (GATEUP && t.shared) ? &tm_b1 : &tm_b0;
+    const int nbox = (t.ntok + kBoxRows - 1) / kBoxRows;
+    for (int i = 0; i < nbox; ++i)
+      for (int hk = 0; hk < 2; ++hk)
+        tma_load_2d(bt + hk * S::kBHalf + i * kBBoxBytes, bmap, &full[stage],
+                    kb * kQK + hk * kBK, t.brow0 + i * kBoxRows, pol_b);
+  };
+  prefetch_l2_span(p.prefix, (size_t)(E1 + 1) * 4);
+  prefetch_l2_span(p.offsets, (size_t)(E1 + 1) * 4);
+  // The gate/up pass's tile list is written by the previous kernel. The down pass's was written
+  // two kernels back and its weights are constant: the list is read and the weights of the
+  // first tile's first stages are requested before the wait, which only the token rows (h, from
+  // the gate/up pass) need.
+  int pre = 0;  // stages whose weights went out before the wait
+  if constexpr (!GATEUP) {
+    stage_tile_list_early(p, list_s);
+    if (threadIdx.x == 0 && (int)blockIdx.x < p.prefix[E1]) {
+      Tile t;
+      decode_tile<GATEUP, NT>(p, blockIdx.x, t);
+      pre = min(STAGES, kblocks);
+      for (int kb = 0; kb < pre; ++kb) {
+        mbar_arrive_expect_tx(&full[kb], stage_bytes(t));
+        load_weights(t, kb, (uint32_t)kb);
+      }
+    }
+  }
   pdl_wait_then_release();
-  const int total = __ldg(p.prefix + E1);
+  if constexpr (GATEUP) stage_tile_list(p, list_s);
+  const int total = p.prefix[E1];
   const uint32_t acol0 = 2 * S::kAccCols;  // first TMEM column of the converted-weights ring
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      const uint64_t pol_w = policy_evict_first();
-      const uint64_t pol_b = policy_evict_last();
       uint32_t stage = 0, phase = 0;
       bool ok = true;
+      if (pre > 0) {  // the token rows of the stages requested before the wait
+        Tile t;
+        decode_tile<GATEUP, NT>(p, blockIdx.x, t);
+        for (int kb = 0; kb < pre; ++kb) load_tokens(t, kb, (uint32_t)kb);
+        stage = (uint32_t)(pre % STAGES);
+        phase = pre == STAGES ? 1u : 0u;
+      }
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
         Tile t;
         decode_tile<GATEUP, NT>(p, tile, t);
-        const int nbox = (t.ntok + kBoxRows - 1) / kBoxRows;
-        const uint32_t bytes = S::kA * kQTileBytes + (uint32_t)nbox * 2 * kBBoxBytes;
-        const int wrow = t.e * p.rows_per_expert + t.mt * kBM * (GATEUP ? 1 : KA);
-        const CUtensorMap* bmap = (GATEUP && t.shared) ? &tm_b1 : &tm_b0;
-        for (int kb = 0; kb < kblocks; ++kb) {
+        const uint32_t bytes = stage_bytes(t);
+        for (int kb = tile == (int)blockIdx.x ? pre : 0; kb < kblocks; ++kb) {
           if (!wait_bar(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
-          uint8_t* st = smem + stage * S::kStageBytes;
           mbar_arrive_expect_tx(&full[stage], bytes);
-          tma_load_2d(st, &tm_w, &full[stage], kb * kQK, wrow, pol_w);
-          if (KA == 2)  // up rows of the same features, or the next 128 rows of W_d
-            tma_load_2d(st + kQTileBytes, &tm_w, &full[stage], kb * kQK,
-                        wrow + (GATEUP ? p.f : kBM), pol_w);
-          uint8_t* bt = st + S::kA * kQTileBytes;
-          for (int i = 0; i < nbox; ++i)
-            for (int hk = 0; hk < 2; ++hk)
-              tma_load_2d(bt + hk * S::kBHalf + i * kBBoxBytes, bmap, &full[stage],
-                          kb * kQK + hk * kBK, t.brow0 + i * kBoxRows, pol_b);
+          load_weights(t, kb, stage);
+          load_tokens(t, kb, stage);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
       }

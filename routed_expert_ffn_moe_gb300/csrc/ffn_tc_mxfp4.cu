@@ -56,7 +56,10 @@ struct SmemMx {
   static constexpr uint32_t kStageBytes = SUB * kSliceBytes;
   static constexpr uint32_t kTilesBytes = STAGES * kStageBytes;
   static constexpr uint32_t kBarBytes = 8 * (2 * STAGES + 2 * ACCB) + 16;
-  static constexpr uint32_t kTotal = kTilesBytes + kBarBytes + 1024;
+  // the tile list goes to shared memory where it fits beside the ring
+  static constexpr bool kStageList = kTilesBytes + kBarBytes + kTileListBytes + 1024 <= 227 * 1024;
+  static constexpr uint32_t kTotal =
+      kTilesBytes + kBarBytes + (kStageList ? kTileListBytes : 0) + 1024;
   static constexpr uint32_t kAccN = 2 * NT;  // accumulator columns per weight tile: hi, then lo
   static constexpr uint32_t kAccCols = KA * kAccN;
   // scale words of the token B rows (hi rows, then lo rows): one 4-column group per 128 rows
@@ -188,7 +191,7 @@ __device__ __forceinline__ void down_epilogue(const TcParams& p, int total,
 template <bool GATEUP, int NT, int STAGES, int KA, int ACCB, int SUB>
 __global__ void __launch_bounds__(kThreadsMx, 1)
     k_tc_ffn_mx(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_hi,
-                const __grid_constant__ CUtensorMap tm_lo, const TcParams p, const MxParams q) {
+                const __grid_constant__ CUtensorMap tm_lo, TcParams p, const MxParams q) {
   using S = SmemMx<GATEUP, NT, STAGES, KA, ACCB, SUB>;
   static_assert(S::kUsedCols <= 512, "TMEM columns");
   static_assert(2 * NT <= 256, "MMA N");
@@ -203,6 +206,7 @@ __global__ void __launch_bounds__(kThreadsMx, 1)
   uint64_t* acc_empty = acc_full + ACCB;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + ACCB);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int32_t* list_s = reinterpret_cast<int32_t*>(smem + S::kTilesBytes + S::kBarBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E1 = p.E + p.n_shared;
@@ -232,44 +236,83 @@ __global__ void __launch_bounds__(kThreadsMx, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  // One stage of a tile: SUB K slices, each its weight boxes (KA tiles of 128 rows x 128 codes)
+  // and its token terms (nbox boxes of 16 hi rows, then as many lo rows), all completing on the
+  // stage's full barrier.
+  const uint64_t pol_w = policy_evict_first();
+  const uint64_t pol_b = policy_evict_last();
+  auto stage_bytes = [&](const Tile& t) {
+    return SUB * (KA * kWTx + (uint32_t)((t.ntok + kBoxRows - 1) / kBoxRows) * 2 * kTBox);
+  };
+  auto load_weights = [&](const Tile& t, int kb, uint32_t stage) {
+    const int wrow = t.e * p.rows_per_expert + t.mt * kBM * (GATEUP ? 1 : KA);
+#pragma unroll
+    for (int sb = 0; sb < SUB; ++sb) {
+      uint8_t* sl = smem + stage * S::kStageBytes + sb * S::kSliceBytes;
+      const int xk = (kb * SUB + sb) * kMxK;
+      tma_load_2d(sl, &tm_w, &full[stage], xk, wrow, pol_w);
+      if (KA == 2)  // up rows of the same features, or the next 128 rows of W_d
+        tma_load_2d(sl + kWSmem, &tm_w, &full[stage], xk, wrow + (GATEUP ? p.f : kBM), pol_w);
+    }
+  };
+  auto load_tokens = [&](const Tile& t, int kb, uint32_t stage) {
+    const int nbox = (t.ntok + kBoxRows - 1) / kBoxRows;
+#pragma unroll
+    for (int sb = 0; sb < SUB; ++sb) {
+      uint8_t* bt = smem + stage * S::kStageBytes + sb * S::kSliceBytes + KA * kWSmem;
+      const int xk = (kb * SUB + sb) * kMxK;
+      for (int i = 0; i < nbox; ++i) {
+        tma_load_2d(bt + i * kTBox, &tm_hi, &full[stage], xk, t.slot0 + i * kBoxRows, pol_b);
+        // the lo rows right after the tile's nbox boxes of hi rows
+        tma_load_2d(bt + (nbox + i) * kTBox, &tm_lo, &full[stage], xk, t.slot0 + i * kBoxRows,
+                    pol_b);
+      }
+    }
+  };
+  prefetch_l2_span(p.prefix, (size_t)(E1 + 1) * 4);
+  prefetch_l2_span(p.offsets, (size_t)(E1 + 1) * 4);
+  // As in the E4M3 decode tiles: the down pass reads its tile list (written two kernels back)
+  // and requests its first tile's first weight stages before the wait; the token terms of h come
+  // from the gate/up pass, after it.
+  int pre = 0;  // stages whose weights went out before the wait
+  if constexpr (!GATEUP && S::kStageList) {
+    stage_tile_list_early(p, list_s);
+    if (threadIdx.x == 0 && (int)blockIdx.x < p.prefix[E1]) {
+      Tile t;
+      decode_tile<GATEUP, NT>(p, blockIdx.x, t);
+      pre = min(STAGES, kblocks);
+      for (int kb = 0; kb < pre; ++kb) {
+        mbar_arrive_expect_tx(&full[kb], stage_bytes(t));
+        load_weights(t, kb, (uint32_t)kb);
+      }
+    }
+  }
   pdl_wait_then_release();  // tile list, token terms and (down pass) h come from earlier kernels
-  const int total = __ldg(p.prefix + E1);
+  if constexpr (GATEUP && S::kStageList) stage_tile_list(p, list_s);
+  const int total = p.prefix[E1];
   const uint32_t sf0 = ACCB * S::kAccCols;  // first TMEM column of the scale-word ring
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      const uint64_t pol_w = policy_evict_first();
-      const uint64_t pol_b = policy_evict_last();
       uint32_t stage = 0, phase = 0;
       bool ok = true;
+      if (pre > 0) {  // the token terms of the stages requested before the wait
+        Tile t;
+        decode_tile<GATEUP, NT>(p, blockIdx.x, t);
+        for (int kb = 0; kb < pre; ++kb) load_tokens(t, kb, (uint32_t)kb);
+        stage = (uint32_t)(pre % STAGES);
+        phase = pre == STAGES ? 1u : 0u;
+      }
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
         Tile t;
         decode_tile<GATEUP, NT>(p, tile, t);
-        const int nbox = (t.ntok + kBoxRows - 1) / kBoxRows;
-        const uint32_t bytes = SUB * (KA * kWTx + (uint32_t)nbox * 2 * kTBox);
-        const int wrow = t.e * p.rows_per_expert + t.mt * kBM * (GATEUP ? 1 : KA);
-        for (int kb = 0; kb < kblocks; ++kb) {
+        const uint32_t bytes = stage_bytes(t);
+        for (int kb = tile == (int)blockIdx.x ? pre : 0; kb < kblocks; ++kb) {
           if (!wait_bar(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
-          uint8_t* st = smem + stage * S::kStageBytes;
           mbar_arrive_expect_tx(&full[stage], bytes);
-#pragma unroll
-          for (int sb = 0; sb < SUB; ++sb) {
-            uint8_t* sl = st + sb * S::kSliceBytes;
-            const int xk = (kb * SUB + sb) * kMxK;
-            tma_load_2d(sl, &tm_w, &full[stage], xk, wrow, pol_w);
-            if (KA == 2)  // up rows of the same features, or the next 128 rows of W_d
-              tma_load_2d(sl + kWSmem, &tm_w, &full[stage], xk, wrow + (GATEUP ? p.f : kBM),
-                          pol_w);
-            uint8_t* bt = sl + KA * kWSmem;
-            for (int i = 0; i < nbox; ++i) {
-              tma_load_2d(bt + i * kTBox, &tm_hi, &full[stage], xk, t.slot0 + i * kBoxRows,
-                          pol_b);
-              // the lo rows right after the tile's nbox boxes of hi rows
-              tma_load_2d(bt + (nbox + i) * kTBox, &tm_lo,
-                          &full[stage], xk, t.slot0 + i * kBoxRows, pol_b);
-            }
-          }
+          load_weights(t, kb, stage);
+          load_tokens(t, kb, stage);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
       }

@@ -79,10 +79,12 @@ cudaError_t launch_route_hash(const moe_shape& s, const uint16_t* x, const uint1
                               const float* bias, const int32_t* token_ids,
                               const int32_t* tid2eid, int vocab, int32_t* topk_idx,
                               float* topk_w, char* ws, const WsLayout& L, cudaStream_t st);
-// the fp32 router's logits alone, in the defined order (router.cu); whether a batch takes the
-// tensor-core router instead
+// the fp32 router's logits alone, in the defined order (router.cu); with clear_status (batches
+// of at most 8 tokens), the kernel also zeroes that word after its wait, as the first kernel of
+// a call. Whether a batch takes the tensor-core router instead.
 cudaError_t launch_router_logits(const moe_shape& s, const uint16_t* x, const uint16_t* wg,
-                                 const float* bias, float* logits, cudaStream_t st);
+                                 const float* bias, float* logits, cudaStream_t st,
+                                 int* clear_status = nullptr);
 bool router_uses_tc(const moe_shape& s);
 cudaError_t launch_permute(const moe_shape& s, const int32_t* topk_idx, int32_t* offsets,
                            int32_t* perm_token, int32_t* inv_slot, char* ws, const WsLayout& L,
@@ -172,6 +174,27 @@ __device__ __forceinline__ void pdl_wait_then_release() {
 
 // ---- device helpers ------------------------------------------------------------------------
 #ifdef __CUDACC__
+// Hint: bring the 128-byte line holding p into L2. Issued before griddepcontrol.wait for data
+// the previous kernel may still be writing, it only warms the address translation and L2 (the
+// point of coherence): every value is still read after the wait.
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// prefetch_l2 over [p, p + bytes), the block's threads taking one line each in turn
+__device__ __forceinline__ void prefetch_l2_span(const void* p, size_t bytes) {
+  const char* c = static_cast<const char*>(p);
+  for (size_t o = (size_t)threadIdx.x * 128; o < bytes; o += (size_t)blockDim.x * 128)
+    prefetch_l2(c + o);
+}
+
+// One line every 64 KB of [p, p + bytes): the address translations of a larger buffer.
+__device__ __forceinline__ void prefetch_l2_pages(const void* p, size_t bytes) {
+  const char* c = static_cast<const char*>(p);
+  for (size_t o = (size_t)threadIdx.x << 16; o < bytes; o += (size_t)blockDim.x << 16)
+    prefetch_l2(c + o);
+}
+
 __device__ __forceinline__ void record_error(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
@@ -237,6 +260,47 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* total) {
   *total = warp_tot[((blockDim.x + 31) >> 5) - 1];
   __syncthreads();
   return warp_prefix + incl - v;
+}
+
+// Three exclusive scans in one pass (each component as block_exclusive_scan would give it).
+__device__ __forceinline__ int3 block_exclusive_scan3(int3 v, int3* total) {
+  __shared__ int3 warp_tot3[32];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int3 incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int nx = __shfl_up_sync(0xffffffffu, incl.x, o);
+    const int ny = __shfl_up_sync(0xffffffffu, incl.y, o);
+    const int nz = __shfl_up_sync(0xffffffffu, incl.z, o);
+    if (lane >= o) {
+      incl.x += nx;
+      incl.y += ny;
+      incl.z += nz;
+    }
+  }
+  if (lane == 31) warp_tot3[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    const int nw = (blockDim.x + 31) >> 5;
+    int3 w = lane < nw ? warp_tot3[lane] : make_int3(0, 0, 0);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int nx = __shfl_up_sync(0xffffffffu, w.x, o);
+      const int ny = __shfl_up_sync(0xffffffffu, w.y, o);
+      const int nz = __shfl_up_sync(0xffffffffu, w.z, o);
+      if (lane >= o) {
+        w.x += nx;
+        w.y += ny;
+        w.z += nz;
+      }
+    }
+    warp_tot3[lane] = w;  // inclusive prefix of warp totals
+  }
+  __syncthreads();
+  const int3 wp = wid ? warp_tot3[wid - 1] : make_int3(0, 0, 0);
+  *total = warp_tot3[((blockDim.x + 31) >> 5) - 1];
+  __syncthreads();
+  return make_int3(wp.x + incl.x - v.x, wp.y + incl.y - v.y, wp.z + incl.z - v.z);
 }
 #endif
 

@@ -25,8 +25,10 @@ template <int TT, int TE, int UNROLL = 4>
 __global__ void __launch_bounds__(128) k_router_logits(const uint16_t* __restrict__ x,
                                                        const uint16_t* __restrict__ wg,
                                                        const float* __restrict__ bias, int T,
-                                                       int d, int E, float* __restrict__ logits) {
+                                                       int d, int E, float* __restrict__ logits,
+                                                       int* clear) {
   pdl_wait_then_release();
+  if (clear && blockIdx.x == 0 && threadIdx.x == 0) *clear = 0;
   const int lane = threadIdx.x & 31;
   const int warp = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int n_et = (E + TE - 1) / TE;
@@ -160,26 +162,35 @@ __global__ void __launch_bounds__(128) k_router_logits_small(const uint16_t* __r
                                                              const uint16_t* __restrict__ wg,
                                                              const float* __restrict__ bias,
                                                              int T, int d, int E,
-                                                             float* __restrict__ logits) {
+                                                             float* __restrict__ logits,
+                                                             int* clear) {
   extern __shared__ uint4 xs[];  // [T][d / 8]
-  pdl_wait_then_release();
   const int lane = threadIdx.x & 31;
   const int chunks = d >> 3;
+  const int e = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const uint4* we = reinterpret_cast<const uint4*>(wg + (size_t)min(e, E - 1) * d);
+  const int mine = (chunks - lane + 31) / 32;  // chunks lane, lane + 32, ... below `chunks`
+  // The router row is a constant input: its first batch of chunks is requested before the wait
+  // for x (which the previous kernel may write).
+  uint4 w[kSmallBatch];
+#pragma unroll
+  for (int i = 0; i < kSmallBatch; ++i)
+    if (i < mine) w[i] = __ldg(we + lane + 32 * i);
+  pdl_wait_then_release();
+  if (clear && blockIdx.x == 0 && threadIdx.x == 0) *clear = 0;
   for (int i = threadIdx.x; i < T * chunks; i += blockDim.x)
     xs[i] = ldg_u4(reinterpret_cast<const uint4*>(x) + i);
   __syncthreads();
-  const int e = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (e >= E) return;
-  const uint4* we = reinterpret_cast<const uint4*>(wg + (size_t)e * d);
   float acc[kSmallT];
 #pragma unroll
   for (int t = 0; t < kSmallT; ++t) acc[t] = 0.f;
-  const int mine = (chunks - lane + 31) / 32;  // chunks lane, lane + 32, ... below `chunks`
   for (int b0 = 0; b0 < mine; b0 += kSmallBatch) {
-    uint4 w[kSmallBatch];
+    if (b0 > 0) {
 #pragma unroll
-    for (int i = 0; i < kSmallBatch; ++i)
-      if (b0 + i < mine) w[i] = __ldg(we + lane + 32 * (b0 + i));
+      for (int i = 0; i < kSmallBatch; ++i)
+        if (b0 + i < mine) w[i] = __ldg(we + lane + 32 * (b0 + i));
+    }
 #pragma unroll
     for (int i = 0; i < kSmallBatch; ++i) {
       if (b0 + i >= mine) break;
@@ -557,12 +568,12 @@ __global__ void __launch_bounds__(256, MAXM <= 8 ? 2 : 1) k_router_select(
 
 template <int TT, int TE, int UNROLL = 4>
 cudaError_t launch_logits(const uint16_t* x, const uint16_t* wg, const float* bias, int T, int d,
-                          int E, float* logits, cudaStream_t st) {
+                          int E, float* logits, cudaStream_t st, int* clear = nullptr) {
   const long warps = (long)((T + TT - 1) / TT) * ((E + TE - 1) / TE);
   const long blocks = (warps + 3) / 4;
   if constexpr (TT == 1) {
     return launch_pdl(k_router_logits<TT, TE, UNROLL>, dim3((unsigned)blocks), dim3(128), 0, st, x, wg,
-                      bias, T, d, E, logits);
+                      bias, T, d, E, logits, clear);
   } else {
     const long n_tt = (T + TT - 1) / TT, n_eb = ((E + TE - 1) / TE + 1) / 2;
     return launch_pdl(k_router_logits_x2<TT, TE>, dim3((unsigned)(((n_tt + 3) / 4) * n_eb)),
@@ -574,7 +585,8 @@ cudaError_t launch_logits(const uint16_t* x, const uint16_t* wg, const float* bi
 // Tile shape by batch: few tokens -> few experts per warp (more warps in flight for the
 // latency-bound case); 64+ tokens -> register-tiled packed-FMA kernel.
 cudaError_t launch_logits_for(const moe_shape& s, const uint16_t* x, const uint16_t* wg,
-                              const float* bias, float* logits, cudaStream_t st) {
+                              const float* bias, float* logits, cudaStream_t st,
+                              int* clear = nullptr) {
   // At these batch sizes the logits are latency-bound: one or two experts a warp (more warps in
   // flight) and eight chunk loads in flight a lane (measured: FP8 T=1 layer 127.7 -> 124.2 us,
   // MXFP4 T=8 272.9 -> 266.3 us).
@@ -585,9 +597,9 @@ cudaError_t launch_logits_for(const moe_shape& s, const uint16_t* x, const uint1
                              (int)smem) != cudaSuccess)
       return cudaGetLastError();
     return launch_pdl(k_router_logits_small, dim3((unsigned)((s.E + 3) / 4)), dim3(128), smem, st,
-                      x, wg, bias, s.T, s.d, s.E, logits);
+                      x, wg, bias, s.T, s.d, s.E, logits, clear);
   }
-  if (s.T <= 8) return launch_logits<1, 1, 8>(x, wg, bias, s.T, s.d, s.E, logits, st);
+  if (s.T <= 8) return launch_logits<1, 1, 8>(x, wg, bias, s.T, s.d, s.E, logits, st, clear);
   if (s.T <= 32) return launch_logits<1, 2, 8>(x, wg, bias, s.T, s.d, s.E, logits, st);
   if (s.T < 64) return launch_logits<1, 8>(x, wg, bias, s.T, s.d, s.E, logits, st);
   return launch_logits<4, 8>(x, wg, bias, s.T, s.d, s.E, logits, st);
@@ -648,9 +660,10 @@ bool router_uses_tc(const moe_shape& s) {
 }
 
 cudaError_t launch_router_logits(const moe_shape& s, const uint16_t* x, const uint16_t* wg,
-                                 const float* bias, float* logits, cudaStream_t st) {
+                                 const float* bias, float* logits, cudaStream_t st,
+                                 int* clear_status) {
   count_launches(1);
-  return launch_logits_for(s, x, wg, bias, logits, st);
+  return launch_logits_for(s, x, wg, bias, logits, st, clear_status);
 }
 
 template <int MAXM>

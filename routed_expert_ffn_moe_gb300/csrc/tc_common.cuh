@@ -24,8 +24,8 @@ struct TcParams {
   int mtiles;            // 128-row weight tiles per expert
   int rows_per_expert;   // rows of the weight map per expert: 2f (gate/up) or d (down)
   int f, d;
-  const int32_t* offsets;
-  const int32_t* prefix;  // [E1 + 1] tile prefix over experts
+  const int32_t* offsets;  // global memory, or a shared-memory copy (stage_tile_list)
+  const int32_t* prefix;   // [E1 + 1] tile prefix over experts (idem)
   uint16_t* h;
   float* y_perm;
   int* status;
@@ -40,6 +40,38 @@ struct Tile {
   bool multi;  // the expert has more token tiles than this one: its weights are read again
 };
 
+// Shared-memory copy of a tile list (prefix and offsets, E1 + 1 entries each; E1 <= 1025).
+constexpr uint32_t kTileListBytes = 2 * (1025 + 1) * 4;
+
+// All threads of the block copy the tile list into `sm` (kTileListBytes) and point p at the
+// copy, so that the roles decode their tiles from shared memory instead of a chain of dependent
+// global loads. Call after the wait for the kernel that wrote the list, with every thread.
+__device__ __forceinline__ void stage_tile_list(TcParams& p, int32_t* sm) {
+  const int E1 = p.E + p.n_shared;
+  for (int i = threadIdx.x; i <= E1; i += blockDim.x) {
+    sm[i] = p.prefix[i];
+    sm[E1 + 1 + i] = p.offsets[i];
+  }
+  __syncthreads();
+  p.prefix = sm;
+  p.offsets = sm + E1 + 1;
+}
+
+// stage_tile_list for a list written two or more kernels back, called BEFORE this kernel's
+// griddepcontrol.wait: the kernel that wrote the list completed before the previous kernel's
+// wait returned, and this kernel was launched after that, so the list is complete in L2; the
+// loads bypass L1 (ld.global.cg), whose lines may predate it.
+__device__ __forceinline__ void stage_tile_list_early(TcParams& p, int32_t* sm) {
+  const int E1 = p.E + p.n_shared;
+  for (int i = threadIdx.x; i <= E1; i += blockDim.x) {
+    sm[i] = __ldcg(p.prefix + i);
+    sm[E1 + 1 + i] = __ldcg(p.offsets + i);
+  }
+  __syncthreads();
+  p.prefix = sm;
+  p.offsets = sm + E1 + 1;
+}
+
 // Token rows of the gate/up pass come from the gathered rows (routed experts) or straight from
 // x (the shared expert, whose slot T*k + t is token t); the down pass reads h in slot order.
 template <bool GATEUP, int NT>
@@ -48,13 +80,13 @@ __device__ __forceinline__ void decode_tile(const TcParams& p, int tile, Tile& t
   int lo = 0, hi = E1;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (__ldg(p.prefix + mid) <= tile) lo = mid; else hi = mid;
+    if (p.prefix[mid] <= tile) lo = mid; else hi = mid;
   }
   const int e = lo;
-  const int seg0 = __ldg(p.offsets + e);
-  const int cnt = __ldg(p.offsets + e + 1) - seg0;
+  const int seg0 = p.offsets[e];
+  const int cnt = p.offsets[e + 1] - seg0;
   const int ntn = (cnt + NT - 1) / NT;
-  const int local = tile - __ldg(p.prefix + e);
+  const int local = tile - p.prefix[e];
   const int mt = local / ntn, nt = local - mt * ntn;
   t.e = e;
   t.mt = mt;
