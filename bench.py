@@ -63,8 +63,9 @@ def parse_args(argv=None):
     p.add_argument("--no-graph", action="store_true",
                    help="launch the layer eagerly each step instead of replaying a CUDA graph")
     p.add_argument("--e2e-steps", type=int, default=None)
-    p.add_argument("--graph-passes", type=int, default=1,
-                   help="layer passes captured back to back in the timed CUDA graph")
+    p.add_argument("--graph-passes", type=int, default=8,
+                   help="layer passes captured back to back in the timed CUDA graph (as a "
+                        "model's layers follow one another in one graph)")
     p.add_argument("--T", type=int, default=None, help="override the token batch (profiling cases)")
     p.add_argument("--E", type=int, default=None, help="override the routed experts (profiling cases)")
     return p.parse_args(argv)
