@@ -13,11 +13,13 @@ __global__ void __launch_bounds__(256) k_combine(const float* __restrict__ y_per
                                                  const float* __restrict__ topk_w, int T, int k,
                                                  int d, int n_shared, uint16_t* __restrict__ y,
                                                  int* status) {
-  if (blockIdx.x == 0) {
+  // small batches (a few blocks, latency-bound): warm L2 and this SM's address translations for
+  // what the block reads after the wait
+  if (T * k <= 256) {
     prefetch_l2_span(inv_slot, (size_t)T * k * 4);
     prefetch_l2_span(topk_w, (size_t)T * k * 4);
+    prefetch_l2_pages(y_perm, (size_t)T * (k + n_shared) * d * 4);
   }
-  prefetch_l2_pages(y_perm, (size_t)T * (k + n_shared) * d * 4);
   pdl_wait_then_release();
   const int d4 = d >> 2;
   const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
