@@ -207,6 +207,52 @@ enum GatherMode : int {
   kGatherF16 = 2,  // E4M3 and MXFP4 prefill tiles: the slot rows as f16 (x_perm)
 };
 
+// One warp copies slot row s (bf16, or converted to f16 as gather_f16_block does): the row's
+// token from one load, then 8 of the row's 16-byte chunks in flight a lane at a time (lane j
+// takes chunks j, j+32, ...). Slot s < routed holds token perm_token[s]; slot routed + t (the
+// shared expert's segment) holds token t.
+__device__ __forceinline__ void gather_row_warp(long s, const uint16_t* __restrict__ x,
+                                                const int32_t* __restrict__ perm_token, int T,
+                                                long routed, int d, uint16_t* __restrict__ out,
+                                                bool to_f16, int* status) {
+  const int lane = threadIdx.x & 31;
+  int t = s < routed ? perm_token[s] : (int)(s - routed);
+  if (t < 0 || t >= T) {
+    if (lane == 0) record_error(status, MOE_ERR_DEVICE_BOUNDS);
+    t = 0;
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(x + (long)t * d);
+  uint4* dst = reinterpret_cast<uint4*>(out + s * d);
+  const int n = d >> 3;
+  for (int c0 = lane; c0 < n; c0 += 32 * 8) {
+    uint4 v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (c0 + 32 * j < n) v[j] = __ldg(src + c0 + 32 * j);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (c0 + 32 * j >= n) break;
+      if (to_f16) {
+        uint32_t u[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+          asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;"
+              : "=r"(u[m])
+              : "f"(__uint_as_float(u[m] & 0xFFFF0000u)), "f"(__uint_as_float(u[m] << 16)));
+        v[j] = make_uint4(u[0], u[1], u[2], u[3]);
+      }
+      dst[c0 + 32 * j] = v[j];
+    }
+  }
+}
+
+// Blocks of the gather: the MXFP4 term encoding takes a thread per 32-element block, the row
+// copies a warp per row (8 rows a block of 256 threads).
+long gather_blocks(int mode, long nq, int d) {
+  if (nq <= 0) return 0;
+  return mode == kGatherMxTerms ? (nq * (d / 32) + 255) / 256 : (nq + 7) / 8;
+}
+
 // One launch for both: block 0 builds the plan from the expert offsets while the other blocks
 // gather the token rows the tensor-core passes read as contiguous TMA rows (GatherMode). Neither
 // needs the other.
@@ -222,13 +268,13 @@ __global__ void __launch_bounds__(256) k_plan_gather(const int32_t* __restrict__
     plan_block(offsets, a, plan);
     return;
   }
-  const long i = (long)(blockIdx.x - 1) * blockDim.x + threadIdx.x;
-  if (mode == kGatherMxTerms)
+  if (mode == kGatherMxTerms) {
+    const long i = (long)(blockIdx.x - 1) * blockDim.x + threadIdx.x;
     gather_encode_block(i, x, perm_token, T, routed, nq, d, xq, status);
-  else if (mode == kGatherF16)
-    gather_f16_block(i, x, perm_token, T, routed, nq, d, x_perm, status);
-  else
-    gather_row_chunks(i, x, perm_token, T, routed, d, x_perm, status);
+    return;
+  }
+  const long s = (long)(blockIdx.x - 1) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (s < nq) gather_row_warp(s, x, perm_token, T, routed, d, x_perm, mode == kGatherF16, status);
 }
 
 // Decode batches of at most 8 tokens (one permutation chunk), moe_forward only: after the
@@ -642,7 +688,8 @@ cudaError_t launch_expert_ffn(const moe_shape& s, const uint16_t* x, const int32
   if (s.T == 0) return cudaSuccess;
   const FfnCall c = make_ffn_call(s, x, perm_token, offsets, w13, s13, w2, s2, y_perm, ws, L,
                                   with_shared);
-  cudaError_t e = launch_pdl(k_plan_gather, dim3((unsigned)(1 + (c.gather_n + 255) / 256)),
+  const long gb = c.gather_n > 0 ? gather_blocks(c.mode, c.nq, s.d) : 0;
+  cudaError_t e = launch_pdl(k_plan_gather, dim3((unsigned)(1 + gb)),
                              dim3(256), 0, st, offsets, c.pa, c.plan, x, perm_token, s.T,
                              c.routed, s.d, c.a.x_perm, c.a.status, c.a.xq, c.nq, c.mode);
   count_launches(1);
