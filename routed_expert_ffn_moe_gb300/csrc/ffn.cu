@@ -296,7 +296,8 @@ __global__ void __launch_bounds__(256) k_route_front(
     int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int32_t* __restrict__ offsets,
     int32_t* __restrict__ perm_token, int32_t* __restrict__ inv_slot, PlanArgs a,
     int32_t* __restrict__ plan, const uint16_t* __restrict__ x, long routed, int d,
-    uint16_t* __restrict__ x_perm, int* status, mx::Planes xq, long nq, int mode) {
+    uint16_t* __restrict__ x_perm, int* status, mx::Planes xq, long nq, int mode,
+    int4* __restrict__ tile1, int n_ctas) {
   extern __shared__ uint32_t fm[];
   const int E1 = a.E + a.n_shared;
   uint32_t* sel = fm;                                               // [E] token masks
@@ -353,6 +354,11 @@ __global__ void __launch_bounds__(256) k_route_front(
       if (blockIdx.x == 0) {
         plan[kPlanTcUp * a.stride + e] = run.y;
         plan[kPlanTcDown * a.stride + e] = run.z;
+        // the gate/up CTAs' first tiles (one token tile an expert: weight tile = tile - prefix)
+        const int more = tot.y > n_ctas ? 1 << 16 : 0;
+        const int u = units(cnt, a.nt_up, a.mt_up);
+        for (int j = 0; tile1 && j < u && run.y + j < n_ctas; ++j)
+          tile1[run.y + j] = make_int4(e, j, e < E ? run.x : T * k, cnt | more);
       }
       run.x += e < E ? cnt : 0;
       run.y += units(cnt, a.nt_up, a.mt_up);
@@ -366,6 +372,9 @@ __global__ void __launch_bounds__(256) k_route_front(
         plan[kPlanTcDown * a.stride + E1] = tot.z;
       }
     }
+    if (blockIdx.x == 0 && tile1)  // CTAs without a tile
+      for (int c = tot.y + (int)threadIdx.x; c < n_ctas; c += blockDim.x)
+        tile1[c] = make_int4(-1, 0, 0, tot.y > n_ctas ? 1 << 16 : 0);
   }
   __syncthreads();
   // slots: expert offset + the pair's rank among its expert's tokens (token order)
@@ -718,11 +727,17 @@ static cudaError_t launch_forward_front(const moe_shape& s, const uint16_t* x, c
   // programmatic launch overlap with the previous call's last kernel)
   cudaError_t e = launch_router_logits(s, x, wg, bias, logits, st, status);
   if (e != cudaSuccess) return e;
-  const FfnCall c = make_ffn_call(s, x, perm_token, offsets, w13, s13, w2, s2, y_perm, ws, L, true);
+  FfnCall c = make_ffn_call(s, x, perm_token, offsets, w13, s13, w2, s2, y_perm, ws, L, true);
+  // E4M3 and MXFP4 decode tiles: the front also hands each gate/up CTA its first tile
+  int4* tile1 = nullptr;
+  if (c.decode && (c.fp8 || c.mxq) && c.pa.nt_up >= s.T && num_sms() <= kTile1Max) {
+    tile1 = reinterpret_cast<int4*>(ws + L.tile1);
+    c.a.tile1 = tile1;
+  }
   e = launch_pdl(k_route_front, dim3((unsigned)(1 + (c.gather_n + 255) / 256)), dim3(256),
                  front_smem_bytes(s.T, s.E, s.k), st, logits, s.T, s.E, s.k, s.n_shared, topk_idx,
                  topk_w, offsets, perm_token, inv_slot, c.pa, c.plan, x, c.routed, s.d,
-                 c.a.x_perm, status, c.a.xq, c.nq, c.mode);
+                 c.a.x_perm, status, c.a.xq, c.nq, c.mode, tile1, num_sms());
   count_launches(1);
   if (e != cudaSuccess) return e;
   if ((e = launch_passes(s, c, st)) != cudaSuccess) return e;

@@ -20,6 +20,9 @@ struct FfnArgs {
   float* y_perm;               // [slots, d] fp32
   int* status;                 // device error word
   mx::Planes xq, hq;           // MXFP4 weights: x and h as E4M3 terms (workspace), [slots, d|f]
+  // small-batch front: each gate/up CTA's first tile {e, m-tile, slot0, ntok | more << 16}
+  // (more: the pass has more tiles than CTAs), written by the front; or null
+  const int4* tile1;
 };
 
 // weight-streaming path (ffn_gemv.cu)

@@ -197,8 +197,12 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
     }
   }
   pdl_wait_then_release();
-  if constexpr (GATEUP) stage_tile_list(p, list_s);
-  const int total = p.prefix[E1];
+  int total = -1;
+  if constexpr (GATEUP) {
+    total = enter_one_tile(p);  // small batches: this CTA's tile from the front's descriptor
+    if (total < 0) stage_tile_list(p, list_s);
+  }
+  if (total < 0) total = p.prefix[E1];
   const uint32_t acol0 = 2 * S::kAccCols;  // first TMEM column of the converted-weights ring
 
   if (warp == 0) {
@@ -403,6 +407,7 @@ cudaError_t launch_tc_fp8(const FfnArgs& a, const int32_t* prefix, bool gateup, 
   p.h = a.h;
   p.y_perm = a.y_perm;
   p.status = a.status;
+  if (gateup) p.tile1 = a.tile1;
   const uint64_t E1 = (uint64_t)a.E + a.n_shared;
   const uint64_t routed = (uint64_t)a.T * a.k;
   const uint64_t slots = routed + (uint64_t)a.n_shared * a.T;

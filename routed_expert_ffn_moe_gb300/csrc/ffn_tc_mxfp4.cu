@@ -288,8 +288,12 @@ __global__ void __launch_bounds__(kThreadsMx, 1)
     }
   }
   pdl_wait_then_release();  // tile list, token terms and (down pass) h come from earlier kernels
-  if constexpr (GATEUP && S::kStageList) stage_tile_list(p, list_s);
-  const int total = p.prefix[E1];
+  int total = -1;
+  if constexpr (GATEUP) {
+    total = enter_one_tile(p);  // small batches: this CTA's tile from the front's descriptor
+    if (total < 0 && S::kStageList) stage_tile_list(p, list_s);
+  }
+  if (total < 0) total = p.prefix[E1];
   const uint32_t sf0 = ACCB * S::kAccCols;  // first TMEM column of the scale-word ring
 
   if (warp == 0) {
@@ -510,6 +514,7 @@ cudaError_t launch_tc_mx(const FfnArgs& a, const int32_t* prefix, bool gateup, b
   p.h = nullptr;
   p.y_perm = a.y_perm;
   p.status = a.status;
+  if (gateup) p.tile1 = a.tile1;
   const uint64_t E1 = (uint64_t)a.E + a.n_shared;
   const uint64_t routed = (uint64_t)a.T * a.k;
   const uint64_t slots = routed + (uint64_t)a.n_shared * a.T;

@@ -29,8 +29,11 @@ constexpr int kChunkTokens = 32;
 constexpr int kStatusRouterFull = 1, kStatusRouterBoundUse = 2;
 constexpr int kPlanRows = 8;
 
+// Most CTAs a small-batch gate/up pass may be launched with (its per-CTA tile descriptors).
+constexpr int kTile1Max = 1024;
+
 struct WsLayout {
-  size_t status, logits, hist, base, plan, x_perm, h, shared, xq, hq, rtc, total;
+  size_t status, logits, hist, base, plan, x_perm, h, shared, xq, hq, rtc, tile1, total;
   int nchunk;
 };
 
@@ -59,6 +62,7 @@ inline WsLayout ws_layout(const moe_shape& s) {
   L.xq = take(mxfp4 ? slots * (2 * (size_t)s.d + 2 * (size_t)(s.d / 32)) : 0);
   L.hq = take(mxfp4 ? slots * (2 * (size_t)s.f + 2 * (size_t)(s.f / 32)) : 0);
   L.rtc = take(16 + E * 4);
+  L.tile1 = take(kTile1Max * 16);  // small-batch gate/up: each CTA's first tile
   L.total = off;
   return L;
 }

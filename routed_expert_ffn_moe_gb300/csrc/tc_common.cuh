@@ -32,6 +32,12 @@ struct TcParams {
   // number of CTAs that take tiles (device memory, written by the plan kernel), or null for
   // all of them: the others leave at once
   const int32_t* active;
+  // small-batch gate/up pass: the front's per-CTA tile descriptors (enter_one_tile), or null
+  const int4* tile1;
+  // one-tile mode (single != 0): this CTA's only tile, {e, m-tile, slot0, ntok} (e < 0: none),
+  // read from the small-batch front's descriptors instead of decoding the tile list
+  int single;
+  int4 one;
 };
 
 struct Tile {
@@ -39,6 +45,18 @@ struct Tile {
   bool shared;
   bool multi;  // the expert has more token tiles than this one: its weights are read again
 };
+
+// Gate/up pass of the small-batch path: every thread reads this CTA's descriptor (after the
+// wait: the front writes it); if the pass has no more tiles than CTAs, the CTA runs in one-tile
+// mode (returns the tile count to loop to: blockIdx.x + 1, or 0 without a tile), else -1.
+__device__ __forceinline__ int enter_one_tile(TcParams& p) {
+  if (!p.tile1 || blockIdx.x >= (unsigned)kTile1Max) return -1;
+  const int4 q = p.tile1[blockIdx.x];
+  if (q.w >> 16) return -1;
+  p.single = 1;
+  p.one = q;
+  return q.x >= 0 ? (int)blockIdx.x + 1 : 0;
+}
 
 // Shared-memory copy of a tile list (prefix and offsets, E1 + 1 entries each; E1 <= 1025).
 constexpr uint32_t kTileListBytes = 2 * (1025 + 1) * 4;
@@ -76,6 +94,16 @@ __device__ __forceinline__ void stage_tile_list_early(TcParams& p, int32_t* sm) 
 // x (the shared expert, whose slot T*k + t is token t); the down pass reads h in slot order.
 template <bool GATEUP, int NT>
 __device__ __forceinline__ void decode_tile(const TcParams& p, int tile, Tile& t) {
+  if (p.single) {
+    t.e = p.one.x;
+    t.mt = p.one.y;
+    t.slot0 = p.one.z;
+    t.ntok = p.one.w & 0xFFFF;
+    t.multi = false;
+    t.shared = t.e == p.E;
+    t.brow0 = (GATEUP && t.shared) ? t.slot0 - p.T * p.k : t.slot0;
+    return;
+  }
   const int E1 = p.E + p.n_shared;
   int lo = 0, hi = E1;
   while (hi - lo > 1) {
