@@ -593,11 +593,12 @@ FfnCall make_ffn_call(const moe_shape& s, const uint16_t* x, const int32_t* perm
   // HBM-bound and the tensor-bound experts overlap instead of taking turns on every SM.
   c.split = s.wdtype == MOE_W_BF16 && !c.decode && c.use_tc && !c.use_gemv && c.routed > 0;
   if (c.split) {
-    // Measured rates on GB300 (one SM, fitted to split sweeps of the skewed prefill layer):
-    // decode tiles stream weights at ~78 GB/s in the gate/up pass and ~52 GB/s in the down pass
-    // (shorter tiles); prefill tiles run ~7.4 TFLOP/s (gate/up) and ~8.2 TFLOP/s (down).
+    // Rates on GB300 (one SM), fitted to split sweeps of the skewed prefill layer: decode tiles
+    // stream weights at ~68 GB/s in the gate/up pass and ~45 GB/s in the down pass (shorter
+    // tiles); prefill tiles run ~7.4 TFLOP/s (gate/up) and ~8.2 TFLOP/s (down). Only the ratio
+    // of the two sides matters for the split.
     const double bytes = s.d * (double)s.f * 2.0;       // one bf16 weight matrix of an expert
-    const double bw_up = 78e3, bw_dn = 52e3;            // bytes per microsecond
+    const double bw_up = 68e3, bw_dn = 45e3;            // bytes per microsecond
     const double tc_up = 7.4e6, tc_dn = 8.2e6;          // FLOP per microsecond
     pa.split = 1;
     pa.nt_c = tc_cold_tile_tokens();
