@@ -351,6 +351,17 @@ def load_config(name, T=None, E=None):
     return cfg
 
 
+def graph_passes(steps, passes, graph=True, exact=True) -> int:
+    """Layer passes per replay of the timed graph: 1 without a graph; with exact (the headline,
+    whose K passes are timed exactly), the largest divisor of steps up to the requested count."""
+    if not graph:
+        return 1
+    passes = max(1, passes)
+    if exact and steps % passes:
+        passes = max(p for p in range(1, passes + 1) if steps % p == 0)
+    return passes
+
+
 def measure(cfg, steps, warmup, graph=True, e2e_steps=None, min_ms=None, keep_inputs=False,
             passes=1):
     """Times `steps` layer passes of one workload (CUDA events on the launching stream, inputs
@@ -381,9 +392,7 @@ def measure(cfg, steps, warmup, graph=True, e2e_steps=None, min_ms=None, keep_in
     # would cut the programmatic launch overlap between them); a second graph of one pass,
     # captured with the library's phase events, times the gate/up and down passes.
     g = gp = g1 = None
-    passes = max(1, passes) if graph else 1
-    if graph and not min_ms and steps % passes:  # exactly `steps` passes
-        passes = max(p for p in range(1, passes + 1) if steps % p == 0)
+    passes = graph_passes(steps, passes, graph, exact=not min_ms)
     moe.moe_profile_enable(True)    # resets the launch counter
     moe.moe_profile_enable(False)   # no phase events; launches are still counted
     if graph:

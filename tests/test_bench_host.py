@@ -1,6 +1,7 @@
 """bench.py's host-side logic on CPU: it refuses more than one GPU before touching one, the
-reference arm (the CPU oracle) prints one line on rank 0 only, and the clock sampler reads
-nvidia-smi's lines and tells the samples inside the timed region from the rest."""
+reference arm (the CPU oracle) prints one line on rank 0 only, the clock sampler reads
+nvidia-smi's lines and tells the samples inside the timed region from the rest, and the timed
+graph's passes per replay keep the headline's pass count exact."""
 import datetime
 import json
 import os
@@ -62,3 +63,17 @@ def test_clock_summary_separates_the_timed_region():
     assert s["timed_region"]["sm_mhz"] == (2070 + 2055) / 2
     assert s["timed_region"]["reasons"] == ["sw_power_cap"]
     assert s["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"] and s["sm_max_mhz"] == 2070
+
+
+def test_graph_passes_keep_the_timed_pass_count_exact():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.graph_passes(200, 8) == 8
+    assert bench.graph_passes(20, 8) == 5        # 4 replays of 5 passes
+    assert bench.graph_passes(7, 8) == 7
+    assert bench.graph_passes(13, 8) == 1        # a prime above 8: one pass a replay
+    assert bench.graph_passes(12, 8, graph=False) == 1
+    assert bench.graph_passes(13, 8, exact=False) == 8   # sweep points round up instead
+    for k in range(1, 60):
+        p = bench.graph_passes(k, 8)
+        assert 1 <= p <= 8 and k % p == 0
